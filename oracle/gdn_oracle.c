@@ -22,8 +22,8 @@
  *  - "mstar PR #965" (mixed steps), section "What changed": dropped padding
  *    rows only ever address the null slot, so every real row's output and
  *    state is unchanged by them.
- *  The pages print no formula for the rule.  The formulas below are the
- *  standard gated delta rule of the benchmark spec:
+ *  The pages name the rule but print no formula for it.  The formulas below
+ *  are the standard gated delta rule of Gated DeltaNet:
  *      alpha = exp(-exp(A_log) * softplus(a + dt_bias)),   beta = sigmoid(b)
  *      q^ = q / sqrt(sum q^2 + eps) / sqrt(dk),            k^ = k / sqrt(sum k^2 + eps)
  *      S' = alpha * S * (I - beta * k^ k^T) + beta * v k^T,   o = S' q^
@@ -185,8 +185,9 @@ void gdn_oracle_head(int dk, int dv, const double *S, const double *q, const dou
  * Row r is padding when read_slot[r] == 0: out[r] = 0, nothing else.
  * Otherwise the state is read from read_slot[r] and written to write_slot[r]
  * (twin) or back to read_slot[r] (keep_in_place).  A slot outside
- * [0, num_slots), or a twin write to slot 0, makes the row count as bad: its
- * output is zero and nothing is written.  Returns the number of bad rows.
+ * [0, num_slots), a twin write to slot 0, or a twin write slot equal to the
+ * read slot (a twin step writes the other slot) makes the row count as bad:
+ * its output is zero and nothing is written.  Returns the number of bad rows.
  * Rows must name distinct slots (a precondition of the method).
  */
 int gdn_oracle_step(int rows, int hk, int hv, int dk, int dv, int num_slots,
@@ -205,7 +206,8 @@ int gdn_oracle_step(int rows, int hk, int hv, int dk, int dv, int num_slots,
         int ws = keep_in_place ? rs : write_slot[r];
         if (rs == 0) {
             row_ok[r] = 0;
-        } else if (rs < 0 || rs >= num_slots || ws <= 0 || ws >= num_slots) {
+        } else if (rs < 0 || rs >= num_slots || ws <= 0 || ws >= num_slots ||
+                   (!keep_in_place && ws == rs)) {
             row_ok[r] = 0;
             ++bad;
         } else {
@@ -274,7 +276,8 @@ void gdn_oracle_conv_row(int C, int W, const double *win, const double *x, const
  * Conv decode over a slot-indexed conv pool [num_slots][W-1][C].
  * x: [rows][C], y: [rows][C].  write_slot == NULL means in place.
  * Padding rows (read slot 0) give y = 0 and touch no slot.  Bad slots as in
- * gdn_oracle_step.  Returns the number of bad rows.
+ * gdn_oracle_step (with a write slot given, it must differ from the read
+ * slot).  Returns the number of bad rows.
  */
 int gdn_oracle_conv_step(int rows, int C, int W, int num_slots, const double *x,
                          double *conv_pool, const int32_t *read_slot, const int32_t *write_slot,
@@ -287,7 +290,8 @@ int gdn_oracle_conv_step(int rows, int C, int W, int num_slots, const double *x,
         int rs = read_slot[r];
         int ws = write_slot ? write_slot[r] : rs;
         double *yr = y + (size_t)r * C;
-        if (rs == 0 || rs < 0 || rs >= num_slots || ws <= 0 || ws >= num_slots) {
+        if (rs == 0 || rs < 0 || rs >= num_slots || ws <= 0 || ws >= num_slots ||
+            (write_slot && ws == rs)) {
             if (rs != 0)
                 ++bad;
             for (int c = 0; c < C; ++c)

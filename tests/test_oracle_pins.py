@@ -371,6 +371,25 @@ def test_step_bad_slots_are_reported(orc):
     assert np.array_equal(p[0], pool[0]) and np.array_equal(p[4], pool[4])
 
 
+def test_twin_write_must_name_the_other_slot(orc):
+    """A twin step writes the next state to the request's other slot; a twin
+    row naming its read slot as write slot is rejected, in the rule and the conv."""
+    rng = np.random.default_rng(26)
+    pool, q, k, v, a, b, A_log, dt_bias = _pool_case(rng, rows=2)
+    rs = np.array([2, 3], dtype=np.int32)
+    ws = np.array([2, 4], dtype=np.int32)
+    p = pool.copy()
+    out, bad = orc.step(q, k, v, a, b, A_log, dt_bias, p, rs, ws)
+    assert bad == 1 and np.all(out[0] == 0.0) and np.array_equal(p[2], pool[2])
+    assert not np.array_equal(p[4], pool[4])
+    p = pool.copy()
+    _, bad = orc.step(q, k, v, a, b, A_log, dt_bias, p, rs, ws, keep_in_place=True)
+    assert bad == 0
+    cp = rng.standard_normal((6, 3, 8))
+    y, bad = orc.conv_step(rng.standard_normal((2, 8)), cp, rs, ws, rng.standard_normal((8, 4)), None)
+    assert bad == 1 and np.all(y[0] == 0.0)
+
+
 def test_commit_swaps(orc):
     rs = np.array([1, 0, 5], dtype=np.int32)
     ws = np.array([2, 0, 6], dtype=np.int32)
