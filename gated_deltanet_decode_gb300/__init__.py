@@ -1,0 +1,283 @@
+"""GB300 (sm_103a) Gated DeltaNet decode: Python binding of the C ABI.
+
+The functions here only marshal torch tensors (device pointers, sizes, the
+current CUDA stream) into calls of ``libgdn_decode.so``; every step of the
+decode path runs in the library's CUDA kernels.  The names follow the C ABI
+(``include/gdn_decode.h``):
+
+  GDNStatePool / ConvStatePool   slot-indexed pools (slot 0 = null slot)
+  causal_conv1d_decode           depthwise causal conv, one token a row
+  gdn_decode_step                gated delta rule per row and value head
+  gdn_layer_decode               both in one kernel
+  gdn_commit                     twin-slot commit (swap read/write slots)
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import (GDN_BF16, GDN_DEVERR_BAD_SLOT, GDN_DEVERR_NONE, GDN_F32, GDN_PROBE_INPLACE,
+                   GDN_PROBE_READ, GDN_PROBE_TWIN, GDN_PROBE_WRITE, gdn_dims)
+
+__all__ = [
+    "GDNError", "load", "lib_path", "GDNStatePool", "ConvStatePool", "causal_conv1d_decode",
+    "gdn_decode_step", "gdn_layer_decode", "gdn_commit", "gdn_validate_slots",
+    "get_device_error", "probe_traffic", "GDN_F32", "GDN_BF16", "GDN_DEVERR_NONE",
+    "GDN_DEVERR_BAD_SLOT", "GDN_PROBE_TWIN", "GDN_PROBE_INPLACE", "GDN_PROBE_READ",
+    "GDN_PROBE_WRITE",
+]
+
+
+class GDNError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[gdn status {code}] {msg}")
+        self.code = code
+
+
+def load():
+    return _lib.load()
+
+
+def lib_path() -> str:
+    return _lib.lib_path()
+
+
+def _check(rc: int):
+    if rc != 0:
+        msg = _lib.load().gdn_last_error().decode(errors="replace")
+        raise GDNError(rc, msg)
+
+
+_DTYPES = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16}
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t not in _DTYPES:
+        raise TypeError(f"activation dtype must be float32 or bfloat16, got {t}")
+    return _DTYPES[t]
+
+
+def _stream(dev: torch.device) -> int:
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor], what: str, dtype=None, device=None, contiguous=True):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{what} is on {t.device}, expected {device}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{what} must be {dtype}, got {t.dtype}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    return t.data_ptr()
+
+
+def _numel(t: torch.Tensor, n: int, what: str):
+    if t.numel() != n:
+        raise ValueError(f"{what} has {t.numel()} elements, expected {n}")
+
+
+class GDNStatePool:
+    """Recurrent state pool [num_slots][hv][dv][dk] fp32 in torch-owned memory.
+
+    The library wraps the tensor (it never frees it).  Slot 0 is the null slot.
+    """
+
+    def __init__(self, num_slots: int, hk: int, hv: int, dk: int, dv: int, device=None,
+                 tensor: Optional[torch.Tensor] = None):
+        L = _lib.load()
+        device = torch.device(device if device is not None else "cuda")
+        if tensor is None:
+            tensor = torch.zeros((num_slots, hv, dv, dk), dtype=torch.float32, device=device)
+        if tuple(tensor.shape) != (num_slots, hv, dv, dk) or tensor.dtype != torch.float32:
+            raise ValueError("state tensor must be float32 [num_slots][hv][dv][dk]")
+        self.tensor = tensor
+        self.num_slots, self.hk, self.hv, self.dk, self.dv = num_slots, hk, hv, dk, dv
+        h = ctypes.c_void_p()
+        _check(L.gdn_state_pool_wrap(_ptr(tensor, "state"), num_slots, gdn_dims(hk, hv, dk, dv),
+                                     ctypes.byref(h)))
+        self._h = h
+
+    @property
+    def handle(self):
+        return self._h
+
+    def zero_slots(self, slots: torch.Tensor):
+        _check(_lib.load().gdn_pool_zero_slots(self._h, _ptr(slots, "slots", torch.int32),
+                                               slots.numel(), _stream(self.tensor.device)))
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            try:
+                _lib.load().gdn_state_pool_destroy(h)
+            except Exception:
+                pass
+            self._h = None
+
+
+class ConvStatePool:
+    """Conv window pool [num_slots][width-1][channels] in the activation dtype."""
+
+    def __init__(self, num_slots: int, channels: int, width: int, dtype=torch.bfloat16, device=None,
+                 tensor: Optional[torch.Tensor] = None):
+        L = _lib.load()
+        device = torch.device(device if device is not None else "cuda")
+        if tensor is None:
+            tensor = torch.zeros((num_slots, width - 1, channels), dtype=dtype, device=device)
+        if tuple(tensor.shape) != (num_slots, width - 1, channels) or tensor.dtype != dtype:
+            raise ValueError("conv tensor must be [num_slots][width-1][channels] of the given dtype")
+        self.tensor = tensor
+        self.num_slots, self.channels, self.width, self.dtype = num_slots, channels, width, dtype
+        h = ctypes.c_void_p()
+        _check(L.conv_state_pool_wrap(_ptr(tensor, "conv state"), num_slots, channels, width,
+                                      _dtype_code(dtype), ctypes.byref(h)))
+        self._h = h
+
+    @property
+    def handle(self):
+        return self._h
+
+    def zero_slots(self, slots: torch.Tensor):
+        _check(_lib.load().conv_pool_zero_slots(self._h, _ptr(slots, "slots", torch.int32),
+                                                slots.numel(), _stream(self.tensor.device)))
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            try:
+                _lib.load().conv_state_pool_destroy(h)
+            except Exception:
+                pass
+            self._h = None
+
+
+def causal_conv1d_decode(x: torch.Tensor, conv_pool: ConvStatePool, slot_idx: torch.Tensor,
+                         w: torch.Tensor, bias: Optional[torch.Tensor] = None,
+                         out: Optional[torch.Tensor] = None, write_slot: Optional[torch.Tensor] = None,
+                         silu: bool = True) -> torch.Tensor:
+    """Conv state update for one token a row. x: [rows][C] (row stride allowed)."""
+    rows, C = x.shape
+    dt = conv_pool.dtype
+    dev = x.device
+    if x.stride(1) != 1:
+        raise ValueError("x rows must be contiguous")
+    if out is None:
+        out = torch.empty((rows, C), dtype=dt, device=dev)
+    _numel(slot_idx, rows, "slot_idx")
+    if write_slot is not None:
+        _numel(write_slot, rows, "write_slot")
+    _numel(w, C * conv_pool.width, "w")
+    if bias is not None:
+        _numel(bias, C, "bias")
+    _check(_lib.load().causal_conv1d_decode(
+        _ptr(x, "x", dt, dev, contiguous=False), x.stride(0), conv_pool.handle,
+        _ptr(slot_idx, "slot_idx", torch.int32, dev), _ptr(write_slot, "write_slot", torch.int32, dev),
+        _ptr(w, "w", dt, dev), _ptr(bias, "bias", dt, dev), int(bool(silu)),
+        _ptr(out, "out", dt, dev), rows, _dtype_code(dt), _stream(dev)))
+    return out
+
+
+def gdn_decode_step(q, k, v, a, b, A_log, dt_bias, pool: GDNStatePool, read_slot, write_slot=None,
+                    out: Optional[torch.Tensor] = None, keep_in_place: bool = False) -> torch.Tensor:
+    """Gated delta rule for one token a row. q,k: [rows][hk][dk]; v: [rows][hv][dv]; a,b: [rows][hv]."""
+    rows = q.shape[0]
+    dt = q.dtype
+    dev = q.device
+    _numel(q, rows * pool.hk * pool.dk, "q")
+    _numel(k, rows * pool.hk * pool.dk, "k")
+    _numel(v, rows * pool.hv * pool.dv, "v")
+    _numel(a, rows * pool.hv, "a")
+    _numel(b, rows * pool.hv, "b")
+    _numel(A_log, pool.hv, "A_log")
+    _numel(dt_bias, pool.hv, "dt_bias")
+    _numel(read_slot, rows, "read_slot")
+    if write_slot is not None:
+        _numel(write_slot, rows, "write_slot")
+    if out is None:
+        out = torch.empty((rows, pool.hv, pool.dv), dtype=dt, device=dev)
+    _numel(out, rows * pool.hv * pool.dv, "out")
+    _check(_lib.load().gdn_decode_step(
+        _ptr(q, "q", dt, dev), _ptr(k, "k", dt, dev), _ptr(v, "v", dt, dev), _ptr(a, "a", dt, dev),
+        _ptr(b, "b", dt, dev), _ptr(A_log, "A_log", torch.float32, dev),
+        _ptr(dt_bias, "dt_bias", torch.float32, dev), pool.handle,
+        _ptr(read_slot, "read_slot", torch.int32, dev), _ptr(write_slot, "write_slot", torch.int32, dev),
+        _ptr(out, "out", dt, dev), rows, pool.hv, int(bool(keep_in_place)), _dtype_code(dt),
+        _stream(dev)))
+    return out
+
+
+def gdn_layer_decode(x, conv_pool: ConvStatePool, w, bias, A_log, dt_bias, a, b, pool: GDNStatePool,
+                     read_slot, write_slot=None, out: Optional[torch.Tensor] = None,
+                     keep_in_place: bool = False, silu: bool = True) -> torch.Tensor:
+    """Fused conv + gated delta rule. x: [rows][2*hk*dk + hv*dv] packed q|k|v."""
+    rows = x.shape[0]
+    dt = x.dtype
+    dev = x.device
+    C = 2 * pool.hk * pool.dk + pool.hv * pool.dv
+    _numel(x, rows * C, "x")
+    _numel(w, C * conv_pool.width, "w")
+    if bias is not None:
+        _numel(bias, C, "bias")
+    _numel(a, rows * pool.hv, "a")
+    _numel(b, rows * pool.hv, "b")
+    _numel(A_log, pool.hv, "A_log")
+    _numel(dt_bias, pool.hv, "dt_bias")
+    _numel(read_slot, rows, "read_slot")
+    if write_slot is not None:
+        _numel(write_slot, rows, "write_slot")
+    if out is None:
+        out = torch.empty((rows, pool.hv, pool.dv), dtype=dt, device=dev)
+    _numel(out, rows * pool.hv * pool.dv, "out")
+    _check(_lib.load().gdn_layer_decode(
+        _ptr(x, "x", dt, dev), conv_pool.handle, _ptr(w, "w", dt, dev), _ptr(bias, "bias", dt, dev),
+        int(bool(silu)), _ptr(A_log, "A_log", torch.float32, dev),
+        _ptr(dt_bias, "dt_bias", torch.float32, dev), _ptr(a, "a", dt, dev), _ptr(b, "b", dt, dev),
+        pool.handle, _ptr(read_slot, "read_slot", torch.int32, dev),
+        _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev), rows,
+        int(bool(keep_in_place)), _dtype_code(dt), _stream(dev)))
+    return out
+
+
+def gdn_commit(read_slot: torch.Tensor, write_slot: torch.Tensor) -> None:
+    """Swap the read and write slot tables on the device (twin-slot commit)."""
+    n = read_slot.numel()
+    _numel(write_slot, n, "write_slot")
+    dev = read_slot.device
+    _check(_lib.load().gdn_commit(_ptr(read_slot, "read_slot", torch.int32, dev),
+                                  _ptr(write_slot, "write_slot", torch.int32, dev), n, _stream(dev)))
+
+
+def gdn_validate_slots(read_slot: torch.Tensor, write_slot: Optional[torch.Tensor], num_slots: int,
+                       keep_in_place: bool = False) -> None:
+    """Debug check of the slot tables (synchronises). Raises GDNError on a violation."""
+    dev = read_slot.device
+    _check(_lib.load().gdn_validate_slots(_ptr(read_slot, "read_slot", torch.int32, dev),
+                                          _ptr(write_slot, "write_slot", torch.int32, dev),
+                                          read_slot.numel(), num_slots, int(bool(keep_in_place)),
+                                          _stream(dev)))
+
+
+def get_device_error(device=None) -> int:
+    """Read and clear the sticky device error word of `device` (synchronises)."""
+    device = torch.device(device if device is not None else "cuda")
+    code = ctypes.c_int(0)
+    with torch.cuda.device(device):
+        _check(_lib.load().gdn_get_device_error(ctypes.byref(code), _stream(device)))
+    return code.value
+
+
+def probe_traffic(pool: GDNStatePool, read_slot: torch.Tensor, write_slot: Optional[torch.Tensor],
+                  mode: int, sink: Optional[torch.Tensor] = None) -> None:
+    """Move a step's state bytes with no arithmetic (roofline probe)."""
+    dev = read_slot.device
+    _check(_lib.load().gdn_probe_traffic(pool.handle, _ptr(read_slot, "read_slot", torch.int32, dev),
+                                         _ptr(write_slot, "write_slot", torch.int32, dev),
+                                         read_slot.numel(), mode,
+                                         _ptr(sink, "sink", torch.float32, dev), _stream(dev)))

@@ -1,0 +1,112 @@
+// Device-side helpers shared by the GDN decode kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+// ---------------------------------------------------------------------------
+// Activation types: fp32 or bf16, converted to fp32 for all arithmetic.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x)
+{
+    return __float2bfloat16_rn(x);
+}
+
+// Round an fp32 value to the activation type and back (the value a separate
+// kernel would have stored and the next one would have read).
+template <typename T> __device__ __forceinline__ float round_act(float x)
+{
+    return to_f(from_f<T>(x));
+}
+
+// ---------------------------------------------------------------------------
+// State stream: 16-byte loads that skip L1 (each byte is touched once), and
+// plain 16-byte stores.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float4 ld_state(const float *p)
+{
+    float4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_state(float *p, float4 v)
+{
+    asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Gates (fp32, with CUDA's expf / log1pf).
+//   alpha = exp(-exp(A_log) * softplus(a + dt_bias)),  softplus(x) = x above 20
+//   beta  = 1 / (1 + exp(-b))
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float softplus_f(float x)
+{
+    return x > 20.0f ? x : log1pf(expf(x));
+}
+__device__ __forceinline__ float gate_alpha(float A_log, float a, float dt_bias)
+{
+    float rate = expf(A_log);
+    float g = rate == 0.0f ? 0.0f : rate * softplus_f(a + dt_bias);
+    return expf(-g);
+}
+__device__ __forceinline__ float gate_beta(float b)
+{
+    return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-b)));
+}
+
+// ---------------------------------------------------------------------------
+// Depthwise causal conv of one channel for one token.  win[j] are the
+// previous W-1 inputs (oldest first); tap W-1 multiplies x.  The same routine
+// serves the standalone conv and the fused layer, so both round identically.
+// ---------------------------------------------------------------------------
+template <int W>
+__device__ __forceinline__ float conv_channel(const float (&win)[W - 1], float x, const float (&w)[W],
+                                              float bias, bool silu)
+{
+    float pre = bias;
+#pragma unroll
+    for (int j = 0; j < W - 1; ++j)
+        pre = __fmaf_rn(w[j], win[j], pre);
+    pre = __fmaf_rn(w[W - 1], x, pre);
+    if (silu)
+        pre = __fdiv_rn(pre, __fadd_rn(1.0f, expf(-pre)));
+    return pre;
+}
+
+// Sticky device error word: the first error code wins.
+__device__ __forceinline__ void report(int *err, int code)
+{
+    if (err)
+        atomicCAS(err, 0, code);
+}
+
+// Row classification shared by every slot-indexed kernel.
+//   0 = padding (read slot 0), 1 = real, -1 = bad (reported by the caller).
+// A twin step writes the request's other slot, so a twin write slot equal to
+// the read slot is bad.
+__device__ __forceinline__ int classify_row(int rs, int ws, int num_slots, bool in_place)
+{
+    if (rs == 0)
+        return 0;
+    if (rs < 0 || rs >= num_slots)
+        return -1;
+    if (in_place)
+        return 1;
+    if (ws <= 0 || ws >= num_slots || ws == rs)
+        return -1;
+    return 1;
+}
+
+} // namespace gdn

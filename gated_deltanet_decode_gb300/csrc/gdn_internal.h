@@ -1,0 +1,78 @@
+// Host-side interface between the C ABI (gdn_api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdn_decode.h"
+
+struct gdn_pool {
+    float *data;
+    int num_slots;
+    gdn_dims dims;
+    bool owned;
+};
+
+struct conv_pool {
+    void *data;
+    int num_slots;
+    int channels;
+    int width;
+    int dtype;
+    bool owned;
+};
+
+namespace gdn {
+
+// Everything one launch of the state kernels needs.  Pointers are device
+// pointers; layouts as in gdn_decode.h.
+struct StepArgs {
+    // gdn_decode_step inputs (unused by the fused layer)
+    const void *q, *k, *v;
+    // shared
+    const void *a, *b;
+    const float *A_log, *dt_bias;
+    float *pool;
+    int num_slots;
+    const int32_t *read_slot, *write_slot;
+    int in_place;
+    void *out;
+    int rows, hk, hv, dk, dv;
+    int *err;
+    // fused layer only
+    const void *x;
+    void *conv;        // conv pool data
+    const void *w;     // [C][W]
+    const void *bias;  // [C] or null
+    int silu;
+    int width;
+    int channels;
+};
+
+struct ConvArgs {
+    const void *x;
+    int x_stride;
+    void *conv;
+    int num_slots;
+    const int32_t *read_slot, *write_slot;
+    const void *w, *bias;
+    int silu;
+    void *out;
+    int rows, channels, width;
+    int *err;
+};
+
+// Launchers return cudaSuccess or the launch error.  Shapes were validated by
+// the caller.
+cudaError_t launch_gdn_step(const StepArgs &a, int dtype, cudaStream_t s);
+cudaError_t launch_gdn_layer(const StepArgs &a, int dtype, cudaStream_t s);
+cudaError_t launch_conv(const ConvArgs &a, int dtype, cudaStream_t s);
+
+// True when the state kernels are built for (dk, dv).
+bool step_shape_supported(int dk, int dv);
+// True when the fused layer can run this shape; in place it needs every block
+// of a qk group (group value heads x row chunks) in one portable cluster.
+bool layer_shape_supported(int dk, int dv, int group, bool in_place);
+
+} // namespace gdn

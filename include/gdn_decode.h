@@ -1,0 +1,220 @@
+/*
+ * gdn_decode.h -- C ABI of the GB300 (sm_103a) Gated DeltaNet decode library.
+ *
+ * One decode step of a Gated DeltaNet (GDN) linear-attention layer, one token
+ * a row, over slot-indexed state pools:
+ *
+ *   causal_conv1d_decode   depthwise width-W causal conv (+ SiLU) over the
+ *                          packed q|k|v channels, rolling a per-slot conv
+ *                          window.  "mstar PR #1139", section "What changed"
+ *                          (the decode-only conv: the conv state update for one
+ *                          token a row, with null slots, strided rows, optional
+ *                          bias and activation, and a write slot).
+ *   gdn_decode_step        the gated delta rule per row and value head:
+ *                            alpha = exp(-exp(A_log) * softplus(a + dt_bias))
+ *                            beta  = sigmoid(b)
+ *                            q^ = q / sqrt(|q|^2 + 1e-6) / sqrt(dk)
+ *                            k^ = k / sqrt(|k|^2 + 1e-6)
+ *                            S' = alpha * S * (I - beta k^ k^T) + beta v k^T
+ *                            o  = S' q^
+ *                          "mstar PR #1139", section "Why" (the GDN rule, the
+ *                          recurrent state update, is state traffic) and
+ *                          "What changed" (twin slots: read one slot, write the
+ *                          other, commit swaps them; in place for other walks).
+ *   gdn_layer_decode       both of the above in one kernel.
+ *   gdn_commit             the twin-slot commit (swap read and write slots).
+ *
+ * Conventions
+ *  - Every function returns a status (GDN_OK = 0).  On failure a message is
+ *    left in a thread-local buffer read by gdn_last_error().
+ *  - Tensor arguments are DEVICE pointers unless stated otherwise; rows are
+ *    contiguous and densely packed unless a row stride is given.  The caller
+ *    owns every activation buffer.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Compute
+ *    calls only enqueue work: no host synchronisation and no allocation.  The
+ *    first call on a device looks up the library's device error word, so
+ *    make one call on each device before capturing a CUDA graph.  Pool
+ *    create/destroy and gdn_validate_slots / gdn_get_device_error synchronise.
+ *  - Activation dtype: GDN_F32 or GDN_BF16 (q, k, v, a, b, x, conv weights and
+ *    bias, conv pool, outputs).  The recurrent state is always fp32, and
+ *    A_log and dt_bias are always fp32.
+ *  - Slot 0 of every pool is the null slot.  A row whose read slot is 0 is a
+ *    padding row: it reads and writes no slot and its outputs are written as
+ *    zeros ("mstar PR #1127", "What changed": padding rows sit on slot 0,
+ *    which stays zero; "mstar PR #965", "What changed": rows on the null slot
+ *    change no real row's result).
+ *  - Bad slots found on the device (a read or write slot outside
+ *    [0, num_slots), a real row whose write slot is 0, or a twin row whose
+ *    write slot equals its read slot) skip that row, zero its outputs and set
+ *    a sticky per-device error word, read and cleared by
+ *    gdn_get_device_error().  Kernels never trap, assert or spin-wait.
+ *  - Preconditions not checked on the fast path: real rows name distinct
+ *    write slots, and no row writes a slot another row reads.
+ *    gdn_validate_slots() checks them (it synchronises).
+ */
+#ifndef GDN_DECODE_H
+#define GDN_DECODE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define GDN_OK 0
+#define GDN_EINVAL 1       /* bad argument: null pointer, bad size, bad dtype */
+#define GDN_ENOMEM 2       /* device allocation failed (pool create only) */
+#define GDN_ECUDA 3        /* a CUDA runtime call failed (message has details) */
+#define GDN_EUNSUPPORTED 4 /* a shape the kernels are not built for */
+#define GDN_ESLOTS 5       /* gdn_validate_slots found a violation */
+
+/* ---- device error word values (gdn_get_device_error) ------------------ */
+#define GDN_DEVERR_NONE 0
+#define GDN_DEVERR_BAD_SLOT 1 /* some row named a slot outside the pool */
+
+/* ---- activation dtypes ------------------------------------------------ */
+#define GDN_F32 0
+#define GDN_BF16 1
+
+/* Head geometry of one GDN layer.  hv % hk == 0: value head h reads qk head
+ * h / (hv / hk) (consecutive value heads share a qk head).  dk is one of
+ * 16, 32, 64, 128, 256; dv is a multiple of 8, at most 512. */
+typedef struct gdn_dims {
+    int hk;
+    int hv;
+    int dk;
+    int dv;
+} gdn_dims;
+
+typedef struct gdn_pool gdn_pool;   /* recurrent state pool (opaque) */
+typedef struct conv_pool conv_pool; /* conv window pool (opaque) */
+
+/* Message for the last failing call on this thread ("" if none). */
+const char *gdn_last_error(void);
+
+/* Library ABI version (increases when a signature changes). */
+int gdn_abi_version(void);
+
+/* ---- recurrent state pool -------------------------------------------- *
+ * Layout: [num_slots][hv][dv][dk] fp32, dk contiguous; S[i][j] maps key
+ * component j to value component i.  One slot is one request's state for
+ * this layer; with twin slots a request holds two ("mstar PR #1139", "What
+ * changed").  Slot 0 is the null slot.
+ *
+ * gdn_state_pool_create allocates and zero-fills (on `stream`, then waits
+ * for it); the library owns the memory and frees it in
+ * gdn_state_pool_destroy.  Returns GDN_ENOMEM when the device is full.
+ * gdn_state_pool_wrap adopts caller memory (e.g. a torch tensor) of exactly
+ * num_slots*hv*dv*dk floats, 16-byte aligned; destroy then frees only the
+ * handle.  num_slots >= 1. */
+int gdn_state_pool_create(int num_slots, gdn_dims dims, void *stream, gdn_pool **out);
+int gdn_state_pool_wrap(void *dev_ptr, int num_slots, gdn_dims dims, gdn_pool **out);
+int gdn_state_pool_destroy(gdn_pool *pool);
+void *gdn_pool_data(const gdn_pool *pool);
+int gdn_pool_num_slots(const gdn_pool *pool);
+gdn_dims gdn_pool_dims(const gdn_pool *pool);
+
+/* Zero the n slots listed in the device array `slots` (a request's release
+ * or rollback zeroes both of its slots: "mstar PR #1139", "Tests").  Slots
+ * outside [0, num_slots) are skipped and set the device error word.  n may
+ * be 0. */
+int gdn_pool_zero_slots(gdn_pool *pool, const int32_t *slots, int n, void *stream);
+
+/* ---- conv window pool ------------------------------------------------- *
+ * Layout: [num_slots][width-1][channels] in the activation dtype, channel
+ * contiguous, oldest input first.  width is 2..4; channels a multiple of 8.
+ * Create/wrap/destroy/zero as for the state pool (wrap needs 16-byte
+ * alignment). */
+int conv_state_pool_create(int num_slots, int channels, int width, int dtype, void *stream,
+                           conv_pool **out);
+int conv_state_pool_wrap(void *dev_ptr, int num_slots, int channels, int width, int dtype,
+                         conv_pool **out);
+int conv_state_pool_destroy(conv_pool *pool);
+void *conv_pool_data(const conv_pool *pool);
+int conv_pool_num_slots(const conv_pool *pool);
+int conv_pool_zero_slots(conv_pool *pool, const int32_t *slots, int n, void *stream);
+
+/* ---- causal_conv1d_decode --------------------------------------------- *
+ * For each row r with s = slot_idx[r] != 0 and each channel c:
+ *   pre      = bias[c] + sum_{j<W-1} w[c][j] * win_s[j][c] + w[c][W-1] * x[r][c]
+ *   out[r][c]= silu ? pre / (1 + exp(-pre)) : pre        (fp32, rounded once)
+ *   window of write_slot[r] (or of s when write_slot == NULL) = [win_s[1..], x[r]]
+ * Rows with slot 0 write out[r] = 0 and touch no slot.
+ *   x          [rows] x channels, row stride x_row_stride elements (>= channels,
+ *              multiple of 8); x, w, bias and out 16-byte aligned
+ *   w          [channels][W];  bias [channels] or NULL
+ *   out        [rows][channels], dense
+ *   slot_idx   [rows] int32 read slots;  write_slot [rows] int32 or NULL
+ * "mstar PR #1139", "What changed" and "Tests" (null slots, strided rows, no
+ * bias or activation, a write slot leaving the read slot alone). */
+int causal_conv1d_decode(const void *x, int x_row_stride, conv_pool *cp, const int32_t *slot_idx,
+                         const int32_t *write_slot, const void *w, const void *bias, int silu,
+                         void *out, int rows, int dtype, void *stream);
+
+/* ---- gdn_decode_step --------------------------------------------------- *
+ *   q, k   [rows][hk][dk]     v, out [rows][hv][dv]     a, b [rows][hv]
+ *   A_log, dt_bias [hv] fp32
+ *   read_slot [rows] int32; write_slot [rows] int32 (ignored when
+ *   keep_in_place != 0, and may then be NULL)
+ * For every real row and value head: S = pool[read_slot[r]][h]; the updated
+ * state goes to write_slot[r] (twin) or back to read_slot[r] (in place); out
+ * receives o.  `heads` must equal the pool's hv.  Twin and in-place calls
+ * produce bit-identical values ("mstar PR #1139", "What changed": same
+ * kernel, same values). */
+int gdn_decode_step(const void *q, const void *k, const void *v, const void *a, const void *b,
+                    const float *A_log, const float *dt_bias, gdn_pool *pool,
+                    const int32_t *read_slot, const int32_t *write_slot, void *out, int rows,
+                    int heads, int keep_in_place, int dtype, void *stream);
+
+/* ---- gdn_layer_decode -------------------------------------------------- *
+ * causal_conv1d_decode (SiLU on when silu != 0) followed by gdn_decode_step,
+ * in one kernel.  x is [rows][C], C = 2*hk*dk + hv*dv packed [q | k | v],
+ * head-major; the conv pool must have C channels.  Both pools use the same
+ * read/write slots.  The conv output is rounded to the activation dtype
+ * before the rule, exactly as between the two separate calls, so the result
+ * is bit-identical to causal_conv1d_decode + gdn_decode_step. */
+int gdn_layer_decode(const void *x, conv_pool *cp, const void *w, const void *bias, int silu,
+                     const float *A_log, const float *dt_bias, const void *a, const void *b,
+                     gdn_pool *pool, const int32_t *read_slot, const int32_t *write_slot,
+                     void *out, int rows, int keep_in_place, int dtype, void *stream);
+
+/* ---- gdn_commit -------------------------------------------------------- *
+ * Twin-slot commit: swap read_slot[r] and write_slot[r] for every row, on the
+ * device ("mstar PR #1139", "What changed": commit swaps them). */
+int gdn_commit(int32_t *read_slot, int32_t *write_slot, int rows, void *stream);
+
+/* ---- debugging --------------------------------------------------------- *
+ * gdn_validate_slots copies the tables to the host (synchronising `stream`)
+ * and returns GDN_ESLOTS with a message if a slot is out of range, a real
+ * row writes the null slot, two real rows read or write one slot, a twin row
+ * writes its own read slot, or a row writes a slot another row reads.
+ * write_slot may be NULL when keep_in_place != 0. */
+int gdn_validate_slots(const int32_t *read_slot, const int32_t *write_slot, int rows,
+                       int num_slots, int keep_in_place, void *stream);
+
+/* Synchronise `stream`, return the current device's error word in *code and
+ * clear it. */
+int gdn_get_device_error(int *code, void *stream);
+
+/* ---- roofline probes --------------------------------------------------- *
+ * Move the state bytes of a step with no arithmetic, over the same pool
+ * geometry and slot tables ("mstar PR #1139", "Numbers": the same reads and
+ * writes with no math; read-only plus write-only).  mode:
+ *   GDN_PROBE_TWIN     read the read slot, write the write slot
+ *   GDN_PROBE_INPLACE  read and write back the read slot
+ *   GDN_PROBE_READ     read only (sink may be NULL; it only keeps the loads
+ *                      alive and is practically never written)
+ *   GDN_PROBE_WRITE    write only (the write slot receives zeros) */
+#define GDN_PROBE_TWIN 0
+#define GDN_PROBE_INPLACE 1
+#define GDN_PROBE_READ 2
+#define GDN_PROBE_WRITE 3
+int gdn_probe_traffic(gdn_pool *pool, const int32_t *read_slot, const int32_t *write_slot,
+                      int rows, int mode, float *sink, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_DECODE_H */

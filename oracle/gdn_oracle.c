@@ -98,6 +98,13 @@ double gdn_oracle_round_bf16(double x)
     return r;
 }
 
+/* Elementwise gdn_oracle_round_bf16 over n values. */
+void gdn_oracle_round_bf16_array(const double *x, double *y, long n)
+{
+    for (long i = 0; i < n; ++i)
+        y[i] = gdn_oracle_round_bf16(x[i]);
+}
+
 /* Round a double to the nearest binary32 value. */
 double gdn_oracle_round_f32(double x)
 {

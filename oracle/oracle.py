@@ -63,6 +63,8 @@ def lib():
             L.gdn_oracle_beta.argtypes = [_D]
             L.gdn_oracle_round_bf16.restype = _D
             L.gdn_oracle_round_bf16.argtypes = [_D]
+            L.gdn_oracle_round_bf16_array.restype = None
+            L.gdn_oracle_round_bf16_array.argtypes = [_P, _P, ctypes.c_long]
             L.gdn_oracle_round_f32.restype = _D
             L.gdn_oracle_round_f32.argtypes = [_D]
             L.gdn_oracle_l2norm.restype = None
@@ -114,9 +116,10 @@ def beta(b: float) -> float:
 
 
 def round_bf16(x) -> np.ndarray:
-    f = lib().gdn_oracle_round_bf16
     x = _f64(x)
-    return np.array([f(float(t)) for t in x.ravel()], dtype=np.float64).reshape(x.shape)
+    y = np.empty_like(x)
+    lib().gdn_oracle_round_bf16_array(_ptr(x), _ptr(y), x.size)
+    return y
 
 
 def l2norm(x, eps: float = 1e-6, scale: float = 1.0) -> np.ndarray:

@@ -1,0 +1,163 @@
+"""CPU-only checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments on the host before touching CUDA.
+
+No call here reaches the GPU: every call either fails validation or has
+nothing to launch (rows == 0), and pools wrap fake (never dereferenced)
+addresses.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn_decode.h")
+
+EINVAL, EUNSUPPORTED = 1, 4
+FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
+
+
+@pytest.fixture(scope="module")
+def L():
+    from gated_deltanet_decode_gb300 import _lib
+    return _lib.load()
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*([a-z_][a-z0-9_]*)\s*\(", src, re.M)
+    return sorted(set(n for n in names if not n.startswith("_")))
+
+
+def test_header_declarations_are_exported(L):
+    from gated_deltanet_decode_gb300 import _lib
+    declared = _declared()
+    assert len(declared) >= 20
+    assert sorted(_lib.EXPORTS) == declared
+    for name in declared:
+        assert hasattr(L, name), f"{name} not exported"
+    assert L.gdn_abi_version() >= 1
+
+
+def _dims(hk=2, hv=2, dk=16, dv=16):
+    from gated_deltanet_decode_gb300._lib import gdn_dims
+    return gdn_dims(hk, hv, dk, dv)
+
+
+def _wrap(L, num_slots=9, **kw):
+    h = ctypes.c_void_p()
+    rc = L.gdn_state_pool_wrap(FAKE, num_slots, _dims(**kw), ctypes.byref(h))
+    return rc, h
+
+
+def test_state_pool_wrap_validation(L):
+    h = ctypes.c_void_p()
+    assert L.gdn_state_pool_wrap(None, 9, _dims(), ctypes.byref(h)) == EINVAL
+    assert b"NULL" in L.gdn_last_error()
+    assert L.gdn_state_pool_wrap(FAKE + 4, 9, _dims(), ctypes.byref(h)) == EINVAL  # misaligned
+    assert _wrap(L, num_slots=0)[0] == EINVAL
+    assert _wrap(L, hk=3, hv=4)[0] == EINVAL          # hv % hk != 0
+    assert _wrap(L, dk=48)[0] == EUNSUPPORTED
+    assert _wrap(L, dv=12)[0] == EUNSUPPORTED          # dv % 8
+    rc, h = _wrap(L, num_slots=5, hk=2, hv=4, dk=64, dv=32)
+    assert rc == 0 and h.value
+    assert L.gdn_pool_num_slots(h) == 5
+    d = L.gdn_pool_dims(h)
+    assert (d.hk, d.hv, d.dk, d.dv) == (2, 4, 64, 32)
+    assert L.gdn_pool_data(h) == FAKE
+    assert L.gdn_state_pool_destroy(h) == 0            # wrapped: frees the handle only
+    assert L.gdn_state_pool_destroy(None) == 0
+
+
+def test_conv_pool_wrap_validation(L):
+    h = ctypes.c_void_p()
+    assert L.conv_state_pool_wrap(FAKE, 9, 96, 5, 0, ctypes.byref(h)) == EUNSUPPORTED  # width
+    assert L.conv_state_pool_wrap(FAKE, 9, 100, 4, 0, ctypes.byref(h)) == EINVAL       # channels % 8
+    assert L.conv_state_pool_wrap(FAKE, 9, 96, 4, 7, ctypes.byref(h)) == EINVAL        # dtype
+    assert L.conv_state_pool_wrap(FAKE, 9, 96, 4, 1, ctypes.byref(h)) == 0
+    assert L.conv_pool_num_slots(h) == 9 and L.conv_pool_data(h) == FAKE
+    assert L.conv_state_pool_destroy(h) == 0
+
+
+def test_step_argument_checks(L):
+    rc, pool = _wrap(L)
+    assert rc == 0
+    P = FAKE
+    args = dict(q=P, k=P, v=P, a=P, b=P, A_log=P, dt_bias=P, pool=pool, rs=P, ws=P, out=P,
+                rows=4, heads=2, inplace=0, dtype=0)
+
+    def call(**over):
+        x = dict(args, **over)
+        return L.gdn_decode_step(x["q"], x["k"], x["v"], x["a"], x["b"], x["A_log"], x["dt_bias"],
+                                 x["pool"], x["rs"], x["ws"], x["out"], x["rows"], x["heads"],
+                                 x["inplace"], x["dtype"], None)
+
+    assert call(pool=None) == EINVAL
+    assert call(rows=-1) == EINVAL
+    assert call(dtype=5) == EINVAL
+    assert call(heads=3) == EINVAL and b"heads" in L.gdn_last_error()
+    assert call(q=None) == EINVAL
+    assert call(ws=None) == EINVAL                      # twin needs a write table
+    assert call(a=None) == EINVAL
+    assert call(rows=0) == 0                            # nothing to launch
+    assert call(rows=0, ws=None, inplace=1) == 0
+    L.gdn_state_pool_destroy(pool)
+
+
+def test_layer_and_conv_argument_checks(L):
+    rc, pool = _wrap(L, hk=2, hv=2, dk=16, dv=16)
+    cp = ctypes.c_void_p()
+    assert L.conv_state_pool_wrap(FAKE, 9, 96, 4, 0, ctypes.byref(cp)) == 0
+    bad_cp = ctypes.c_void_p()
+    assert L.conv_state_pool_wrap(FAKE, 9, 88, 4, 0, ctypes.byref(bad_cp)) == 0
+    P = FAKE
+
+    def layer(cpool, rows=4, inplace=0, dtype=0, x=P, w=P, pool_=pool):
+        return L.gdn_layer_decode(x, cpool, w, None, 1, P, P, P, P, pool_, P, P, P, rows, inplace,
+                                  dtype, None)
+
+    assert layer(None) == EINVAL
+    assert layer(bad_cp) == EINVAL and b"channels" in L.gdn_last_error()
+    assert layer(cp, dtype=1) == EINVAL                 # dtype differs from the conv pool's
+    assert layer(cp, x=None) == EINVAL
+    assert layer(cp, rows=0) == 0
+    # in place, a qk group that cannot fit one 8-block cluster is refused
+    rc, big = _wrap(L, num_slots=3, hk=1, hv=16, dk=16, dv=512)
+    assert rc == 0
+    cbig = ctypes.c_void_p()
+    assert L.conv_state_pool_wrap(FAKE, 3, 2 * 16 + 16 * 512, 4, 0, ctypes.byref(cbig)) == 0
+    assert layer(cbig, rows=1, inplace=1, pool_=big) == EUNSUPPORTED
+    assert layer(cbig, rows=0, inplace=0, pool_=big) == 0
+
+    def conv(stride=96, x=P, out=P, rows=2, dtype=0):
+        return L.causal_conv1d_decode(x, stride, cp, P, None, P, None, 1, out, rows, dtype, None)
+
+    assert conv(stride=90) == EINVAL                    # shorter than a row
+    assert conv(stride=100) == EINVAL                   # not a multiple of 8
+    assert conv(x=P + 8) == EINVAL                      # misaligned
+    assert conv(out=None) == EINVAL
+    assert conv(dtype=1) == EINVAL
+    assert conv(rows=0) == 0
+    for h in (cp, bad_cp, cbig):
+        L.conv_state_pool_destroy(h)
+    L.gdn_state_pool_destroy(pool)
+    L.gdn_state_pool_destroy(big)
+
+
+def test_small_entry_points_checks(L):
+    assert L.gdn_commit(None, None, 0, None) == 0
+    assert L.gdn_commit(None, FAKE, 3, None) == EINVAL
+    assert L.gdn_commit(FAKE, FAKE, -1, None) == EINVAL
+    assert L.gdn_validate_slots(FAKE, None, 0, 9, 0, None) == 0
+    assert L.gdn_validate_slots(FAKE, None, 2, 9, 0, None) == EINVAL
+    assert L.gdn_get_device_error(None, None) == EINVAL
+    rc, pool = _wrap(L)
+    assert L.gdn_probe_traffic(pool, FAKE, FAKE, 4, 9, None, None) == EINVAL
+    assert L.gdn_probe_traffic(pool, FAKE, None, 4, 0, None, None) == EINVAL
+    assert L.gdn_probe_traffic(pool, FAKE, FAKE, 0, 0, None, None) == 0
+    assert L.gdn_pool_zero_slots(pool, None, 0, None) == 0
+    assert L.gdn_pool_zero_slots(pool, None, 2, None) == EINVAL
+    assert L.gdn_pool_zero_slots(None, FAKE, 2, None) == EINVAL
+    L.gdn_state_pool_destroy(pool)
