@@ -1,0 +1,476 @@
+#!/usr/bin/env python
+"""Benchmark of the GDN decode layer on GB300.
+
+Workload (default): the 0.8B-shaped single layer -- 64 rows, 16 qk / 16 value
+heads, dk = dv = 128, 6144 conv channels of width 4, bf16 activations, fp32
+state, 129-slot pools, twin slots.  One step is one fused conv + GDN layer
+decode (gdn_layer_decode) followed by the twin commit (gdn_commit), through
+the C ABI.  Four independent layer instances (pools, parameters, inputs) are
+used in rotation, so that a step never finds the state it reads in L2 (the
+four state pools hold 4 x 135 MB against a 126 MB L2).
+
+Prints one JSON line: whole-job GB/s of algorithmic bytes, µs per layer,
+the roofline of the layer kernel, an end-to-end figure through host buffers,
+the clocks seen during the timed region and the fp64 oracle timed on the
+host cores.  `--impl reference` times the oracle itself on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN decode layer: achieved HBM GB/s (% of 8 TB/s) and µs/layer at 64 rows"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+NSETS = 4
+KERNEL_SOURCES = ["gated_deltanet_decode_gb300/csrc/gdn_step.cu",
+                  "gated_deltanet_decode_gb300/csrc/gdn_device.cuh"]
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "gdn_layer_decode_qwen08b_rows64.md")
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes
+# ---------------------------------------------------------------------------
+
+def layer_bytes(s, real_rows: int) -> int:
+    """Bytes one gdn_layer_decode launch must move at least.
+
+    Per real row: the state read and written (2 * hv * dv * dk * 4), the conv
+    window read and written (2 * (W-1) * C * e), the token x (C * e), the gates'
+    inputs a and b (2 * hv * e).  Per row: the output (hv * dv * e) and two slot
+    ids.  Per launch: conv taps and bias ((W + 1) * C * e), A_log and dt_bias.
+    """
+    e = 2 if s.dtype == "bf16" else 4
+    C = s.channels
+    per_real = (2 * s.hv * s.dv * s.dk * 4 + 2 * (s.width - 1) * C * e + C * e + 2 * s.hv * e)
+    per_row = s.hv * s.dv * e + 2 * 4
+    per_launch = (s.width + 1) * C * e + 2 * s.hv * 4
+    return real_rows * per_real + s.rows * per_row + per_launch
+
+
+def commit_bytes(rows: int) -> int:
+    return rows * 4 * 4  # read and write both tables
+
+
+# ---------------------------------------------------------------------------
+# peaks, traffic, clocks
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the layer kernel from the committed ncu summary,
+    or None when the summary is missing or the kernel changed since."""
+    try:
+        fields = {}
+        with open(TRAFFIC_SUMMARY) as f:
+            for line in f:
+                if ":" in line and line.strip().startswith(("traffic_per_launch_bytes", "source_sha256")):
+                    k, v = line.split(":", 1)
+                    fields[k.strip().strip("-* `")] = v.strip().strip("` ")
+        if fields.get("source_sha256") != kernel_source_sha():
+            return None
+        return int(fields["traffic_per_launch_bytes"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.idx)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def build_sets(G, I, s, device, nsets):
+    import torch
+    sets = []
+    for i in range(nsets):
+        gen = I.Gen(1000 + i)
+        prm = gen.params(s)
+        inp = gen.layer_inputs(s)
+        dt = s.dtype
+        st = {
+            "pool": G.GDNStatePool(s.num_slots, s.hk, s.hv, s.dk, s.dv, device=device,
+                                   tensor=torch.from_numpy(gen.state_pool(s)).to(device)),
+            "cp": G.ConvStatePool(s.num_slots, s.channels, s.width, dtype=I.torch_dtype(dt), device=device,
+                                  tensor=I.to_torch(gen.conv_pool(s), dt, device)),
+            "w": I.to_torch(prm["w"], dt, device),
+            "bias": I.to_torch(prm["bias"], dt, device),
+            "A_log": I.to_torch(prm["A_log"], "f32", device),
+            "dt_bias": I.to_torch(prm["dt_bias"], "f32", device),
+            "x": I.to_torch(inp["x"], dt, device),
+            "a": I.to_torch(inp["a"], dt, device),
+            "b": I.to_torch(inp["b"], dt, device),
+            "out": torch.empty((s.rows, s.hv, s.dv), dtype=I.torch_dtype(dt), device=device),
+        }
+        rs, ws = gen.slot_tables(s.rows, s.num_slots)
+        st["rs"] = torch.from_numpy(rs).to(device)
+        st["ws"] = torch.from_numpy(ws).to(device)
+        st["layer"] = G.prepare_layer_decode(st["x"], st["cp"], st["w"], st["bias"], st["A_log"],
+                                             st["dt_bias"], st["a"], st["b"], st["pool"], st["rs"], st["ws"],
+                                             st["out"])
+        st["commit"] = G.prepare_commit(st["rs"], st["ws"])
+        sets.append(st)
+    return sets
+
+
+def run_ours(args, rank, world, device):
+    import torch
+    import gated_deltanet_decode_gb300 as G
+    from gated_deltanet_decode_gb300 import inputs as I
+
+    s = I.QWEN_08B
+    G.load()
+    sets = build_sets(G, I, s, device, NSETS)
+    stream = torch.cuda.current_stream(device)
+    real_rows = s.rows
+    lb = layer_bytes(s, real_rows)
+    step_bytes = lb + commit_bytes(s.rows)
+
+    for i in range(args.warmup):
+        st = sets[i % NSETS]
+        st["layer"]()
+        st["commit"]()
+    torch.cuda.synchronize(device)
+    if G.get_device_error(device) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    K = args.steps
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(device.index if device.index is not None else 0)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    host0 = time.perf_counter()
+    t0.record(stream)
+    for i in range(K):
+        st = sets[i % NSETS]
+        ev_a[i].record(stream)
+        st["layer"]()
+        ev_b[i].record(stream)
+        st["commit"]()
+    t1.record(stream)
+    host_enqueue_s = time.perf_counter() - host0
+    torch.cuda.synchronize(device)
+    clk = clocks.stop()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    total_ms = t0.elapsed_time(t1)
+    layer_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
+    if G.get_device_error(device) != 0:
+        raise RuntimeError("device error during the timed region")
+
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    ms_per_step = total_ms / K
+    value = world * step_bytes * K / (total_ms * 1e-3) / 1e9
+    layer_mean_ms = statistics.fmean(layer_ms)
+    achieved = lb / (layer_mean_ms * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+
+    # end to end through host buffers: inputs in pinned memory, output read back
+    e2e = run_e2e(G, I, s, sets, device, min(K, 2000), step_bytes)
+
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": "0.8B-shaped GDN decode layer: fused conv+rule, 64 rows, 16 qk/16 v heads, "
+                        "dk=dv=128, 6144 conv channels width 4, bf16 activations, fp32 state, "
+                        "129-slot pools, twin slots, commit each step",
+            "rows": s.rows, "hk": s.hk, "hv": s.hv, "dk": s.dk, "dv": s.dv, "conv_width": s.width,
+            "activations": s.dtype, "num_slots": s.num_slots, "mode": "twin",
+            "l2": f"inputs larger than L2: {NSETS} layer instances in rotation "
+                  f"({NSETS} x {s.num_slots * s.hv * s.dv * s.dk * 4 / 1e6:.0f} MB of state)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "us_per_layer": round(layer_mean_ms * 1e3, 3),
+        "us_per_step": round(ms_per_step * 1e3, 3),
+        "pct_of_8TBps": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
+        "rows_heads_per_s": round(world * s.rows * s.hv * K / (total_ms * 1e-3), 1),
+        "algorithmic_bytes_per_step": step_bytes,
+        "host_enqueue_s": round(host_enqueue_s, 4),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "gdn_layer_decode (gdn_state_kernel, fused layer, twin)",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": recorded_traffic(),
+            "algorithmic_bytes_per_launch": lb,
+        },
+        "e2e": e2e,
+        "gpu_launches": 2 * K,
+        "clocks": clk,
+    }
+    return res
+
+
+def run_e2e(G, I, s, sets, device, K, step_bytes):
+    """Same step through host buffers: per step, copy x, a, b from pinned host
+    memory, run the layer and the commit, read the output back."""
+    import torch
+    stream = torch.cuda.current_stream(device)
+    hosts = []
+    for st in sets:
+        hosts.append({k: st[k].cpu().pin_memory() for k in ("x", "a", "b")})
+        hosts[-1]["out"] = torch.empty(st["out"].shape, dtype=st["out"].dtype).pin_memory()
+    for i in range(8):
+        st, h = sets[i % NSETS], hosts[i % NSETS]
+        for k in ("x", "a", "b"):
+            st[k].copy_(h[k], non_blocking=True)
+        st["layer"]()
+        st["commit"]()
+        h["out"].copy_(st["out"], non_blocking=True)
+    torch.cuda.synchronize(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(K):
+        st, h = sets[i % NSETS], hosts[i % NSETS]
+        for k in ("x", "a", "b"):
+            st[k].copy_(h[k], non_blocking=True)
+        st["layer"]()
+        st["commit"]()
+        h["out"].copy_(st["out"], non_blocking=True)
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = t0.elapsed_time(t1) / K
+    h2d = sum(hosts[0][k].numel() * hosts[0][k].element_size() for k in ("x", "a", "b"))
+    d2h = hosts[0]["out"].numel() * hosts[0]["out"].element_size()
+    return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 6),
+            "steps": K}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def oracle_layer_sample(s, rows: int, seed: int = 7):
+    """Inputs for the oracle on `rows` rows of the workload (fp64, rounded to
+    the activation dtype like the GPU's)."""
+    import numpy as np
+    from gated_deltanet_decode_gb300 import inputs as I
+    sub = s.with_(rows=rows, num_slots=2 * rows + 1)
+    gen = I.Gen(seed)
+    prm = gen.params(sub)
+    inp = gen.layer_inputs(sub)
+    rnd = lambda a: I.as_f64(I.to_torch(a, sub.dtype, "cpu"))  # noqa: E731
+    rs, ws = gen.slot_tables(rows, sub.num_slots)
+    return {
+        "s": sub, "w": rnd(prm["w"]), "bias": rnd(prm["bias"]), "A_log": prm["A_log"].astype(np.float64),
+        "dt_bias": prm["dt_bias"].astype(np.float64), "x": rnd(inp["x"]), "a": rnd(inp["a"]),
+        "b": rnd(inp["b"]), "pool": gen.state_pool(sub).astype(np.float64),
+        "cp": rnd(gen.conv_pool(sub)), "rs": rs, "ws": ws,
+    }
+
+
+def time_oracle_step(orc, d, nthreads: int) -> float:
+    t = time.perf_counter()
+    orc.layer(d["x"], d["cp"], d["w"], d["bias"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["pool"],
+              d["rs"], d["ws"], hk=d["s"].hk, act_bf16=d["s"].dtype == "bf16", nthreads=nthreads)
+    orc.commit(d["rs"], d["ws"])
+    return time.perf_counter() - t
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(budget_s: float = 12.0):
+    """The oracle as it stands, on all host cores, over the full 64-row step of
+    the workload, repeated while the budget lasts (at least once)."""
+    import oracle as orc
+    from gated_deltanet_decode_gb300 import inputs as I
+    s = I.QWEN_08B
+    cores = host_cores()
+    d = oracle_layer_sample(s, s.rows)
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while not times or time.perf_counter() < t_end:
+        times.append(time_oracle_step(orc, d, cores))
+    per = statistics.median(times)
+    return {"value": round(layer_bytes(s, s.rows) / per / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{len(times)} full 64-row steps of the workload (fp64 oracle layer + commit), "
+                      f"median {per * 1e3:.1f} ms per step"}
+
+
+def run_reference(args):
+    """--impl reference: the oracle itself; each step is a bounded sample of the
+    workload -- one row and 4 of its 16 head pairs -- so that the default
+    step count finishes in well under a minute."""
+    import oracle as orc
+    from gated_deltanet_decode_gb300 import inputs as I
+    s = I.QWEN_08B.with_(hk=4, hv=4)
+    cores = host_cores()
+    d = oracle_layer_sample(s, 1)
+    for _ in range(args.warmup):
+        time_oracle_step(orc, d, cores)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        time_oracle_step(orc, d, cores)
+    el = time.perf_counter() - t
+    bytes_per = layer_bytes(s.with_(rows=1), 1) + commit_bytes(1)
+    value = bytes_per * args.steps / el / 1e9
+    sample = ("one row and 4 of the 16 qk/v head pairs of the 64-row workload per step "
+              "(fp64 oracle layer + commit)")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "0.8B-shaped GDN decode layer (fused conv+rule), sampled: one row "
+                               "and 4 head pairs a step",
+                   "rows": 1, "hk": s.hk, "hv": s.hv, "dk": s.dk, "dv": s.dv},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import torch
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    res = run_ours(args, rank, world, device)
+    if rank == 0:
+        if world == 1:
+            res["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

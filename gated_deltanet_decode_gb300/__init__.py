@@ -281,3 +281,67 @@ def probe_traffic(pool: GDNStatePool, read_slot: torch.Tensor, write_slot: Optio
                                          _ptr(write_slot, "write_slot", torch.int32, dev),
                                          read_slot.numel(), mode,
                                          _ptr(sink, "sink", torch.float32, dev), _stream(dev)))
+
+
+class PreparedCall:
+    """A validated C-ABI call with its pointer arguments bound once.
+
+    Calling it launches the same entry point again on the same buffers and
+    stream, without re-marshalling the tensors: a decode loop (or a graph
+    capture) then costs one ctypes call per launch.  The tensors must stay
+    alive and keep their addresses while the call is used.
+    """
+
+    def __init__(self, fn_name: str, args: tuple, keep: tuple):
+        self._fn = getattr(_lib.load(), fn_name)
+        self._args = args
+        self._keep = keep  # hold references to the tensors whose pointers are bound
+
+    def __call__(self) -> None:
+        rc = self._fn(*self._args)
+        if rc:
+            _check(rc)
+
+
+def prepare_layer_decode(x, conv_pool: ConvStatePool, w, bias, A_log, dt_bias, a, b, pool: GDNStatePool,
+                         read_slot, write_slot, out, keep_in_place: bool = False, silu: bool = True,
+                         stream: Optional[torch.cuda.Stream] = None) -> PreparedCall:
+    """gdn_layer_decode bound to fixed buffers (validated here, once)."""
+    rows = x.shape[0]
+    dt = x.dtype
+    dev = x.device
+    C = 2 * pool.hk * pool.dk + pool.hv * pool.dv
+    _numel(x, rows * C, "x")
+    _numel(w, C * conv_pool.width, "w")
+    if bias is not None:
+        _numel(bias, C, "bias")
+    for tname, tt, n in (("a", a, rows * pool.hv), ("b", b, rows * pool.hv), ("A_log", A_log, pool.hv),
+                         ("dt_bias", dt_bias, pool.hv), ("read_slot", read_slot, rows),
+                         ("out", out, rows * pool.hv * pool.dv)):
+        _numel(tt, n, tname)
+    if write_slot is not None:
+        _numel(write_slot, rows, "write_slot")
+    s = (stream or torch.cuda.current_stream(dev)).cuda_stream
+    args = (_ptr(x, "x", dt, dev), conv_pool.handle, _ptr(w, "w", dt, dev), _ptr(bias, "bias", dt, dev),
+            int(bool(silu)), _ptr(A_log, "A_log", torch.float32, dev),
+            _ptr(dt_bias, "dt_bias", torch.float32, dev), _ptr(a, "a", dt, dev), _ptr(b, "b", dt, dev),
+            pool.handle, _ptr(read_slot, "read_slot", torch.int32, dev),
+            _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev), rows,
+            int(bool(keep_in_place)), _dtype_code(dt), s)
+    return PreparedCall("gdn_layer_decode", args,
+                        (x, conv_pool, w, bias, A_log, dt_bias, a, b, pool, read_slot, write_slot, out))
+
+
+def prepare_commit(read_slot: torch.Tensor, write_slot: torch.Tensor,
+                   stream: Optional[torch.cuda.Stream] = None) -> PreparedCall:
+    """gdn_commit bound to fixed slot tables."""
+    n = read_slot.numel()
+    _numel(write_slot, n, "write_slot")
+    dev = read_slot.device
+    s = (stream or torch.cuda.current_stream(dev)).cuda_stream
+    args = (_ptr(read_slot, "read_slot", torch.int32, dev), _ptr(write_slot, "write_slot", torch.int32, dev),
+            n, s)
+    return PreparedCall("gdn_commit", args, (read_slot, write_slot))
+
+
+__all__ += ["PreparedCall", "prepare_layer_decode", "prepare_commit"]
