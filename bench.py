@@ -160,6 +160,15 @@ class ClockSampler:
 # our arm
 # ---------------------------------------------------------------------------
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def build_sets(G, I, s, device, nsets):
     import torch
     sets = []
@@ -247,10 +256,7 @@ def run_ours(args, rank, world, device):
         raise RuntimeError("device error during the timed region")
 
     if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([total_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+        total_ms = max_over_ranks(total_ms, device)
 
     ms_per_step = total_ms / K
     value = world * step_bytes * K / (total_ms * 1e-3) / 1e9

@@ -1,0 +1,55 @@
+"""Host logic of the multi-rank benchmark, on CPU with gloo: every rank
+reports the slowest rank's time (world size 2)."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    import sys
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    import bench
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    try:
+        q.put((rank, bench.max_over_ranks(10.0 + 5.0 * rank)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = dict(q.get(timeout=10) for _ in range(2))
+    assert got == {0: 15.0, 1: 15.0}
+
+
+def test_bench_byte_model():
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    from gated_deltanet_decode_gb300 import inputs as I
+    s = I.QWEN_08B
+    b = bench.layer_bytes(s, s.rows)
+    state = 64 * 16 * 128 * 128 * 4 * 2
+    assert state == 134217728
+    assert state < b < state * 1.06          # conv, vectors and parameters add under 6%
+    assert bench.layer_bytes(s, 0) < 0.01 * state   # padding rows move no state
