@@ -34,7 +34,7 @@ METRIC = "GDN decode layer: achieved HBM GB/s (% of 8 TB/s) and µs/layer at 64 
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 NSETS = 4
-KERNEL_SOURCES = ["gated_deltanet_decode_gb300/csrc/gdn_step.cu",
+KERNEL_SOURCES = ["gated_deltanet_decode_gb300/csrc/gdn_stream.cu",
                   "gated_deltanet_decode_gb300/csrc/gdn_device.cuh"]
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "gdn_layer_decode_qwen08b_rows64.md")
 
@@ -266,6 +266,7 @@ def run_ours(args, rank, world, device):
 
     # end to end through host buffers: inputs in pinned memory, output read back
     e2e = run_e2e(G, I, s, sets, device, min(K, 2000), step_bytes)
+    probes = run_probes(G, s, sets, device, min(K, 2000))
 
     res = {
         "metric": METRIC,
@@ -298,7 +299,7 @@ def run_ours(args, rank, world, device):
         "host_enqueue_s": round(host_enqueue_s, 4),
         "roofline": {
             "bound": "hbm",
-            "kernel": "gdn_layer_decode (gdn_state_kernel, fused layer, twin)",
+            "kernel": "gdn_layer_decode (gdn_stream_kernel, fused layer, twin)",
             "achieved": round(achieved, 2),
             "peak": peak,
             "peak_kind": peak_kind,
@@ -308,9 +309,44 @@ def run_ours(args, rank, world, device):
             "algorithmic_bytes_per_launch": lb,
         },
         "e2e": e2e,
+        "probes": probes,
         "gpu_launches": 2 * K,
         "clocks": clk,
     }
+    return res
+
+
+def run_probes(G, s, sets, device, K):
+    """GB/s of the traffic probes over the same rotation: the state bytes of a
+    step moved with no arithmetic (twin copy, in-place read-modify-write,
+    read only, write only)."""
+    import torch
+    stream = torch.cuda.current_stream(device)
+    state = s.rows * s.hv * s.dv * s.dk * 4
+    res = {}
+    for name, mode, nbytes in (("twin_copy", G.GDN_PROBE_TWIN, 2 * state),
+                               ("in_place_rmw", G.GDN_PROBE_INPLACE, 2 * state),
+                               ("read_only", G.GDN_PROBE_READ, state),
+                               ("write_only", G.GDN_PROBE_WRITE, state)):
+        calls = [G.PreparedCall("gdn_probe_traffic",
+                                (st["pool"].handle, st["rs"].data_ptr(), st["ws"].data_ptr(), s.rows, mode,
+                                 None, stream.cuda_stream), (st,)) for st in sets]
+
+        def go(i):
+            calls[i % NSETS]()
+        for i in range(8):
+            go(i)
+        torch.cuda.synchronize(device)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(K):
+            go(i)
+        t1.record(stream)
+        torch.cuda.synchronize(device)
+        us = t0.elapsed_time(t1) * 1e3 / K
+        res[name] = {"us": round(us, 3), "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1)}
+    # the probes wrote the pools; the layer kernel's values are not reused after this
     return res
 
 

@@ -20,6 +20,7 @@ GDN_ESLOTS = 5
 
 GDN_DEVERR_NONE = 0
 GDN_DEVERR_BAD_SLOT = 1
+GDN_DEVERR_TIMEOUT = 2
 
 GDN_F32 = 0
 GDN_BF16 = 1

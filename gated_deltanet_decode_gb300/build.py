@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libgdn_decode.so")
-SOURCES = ["gdn_api.cu", "gdn_step.cu", "gdn_conv.cu"]
+SOURCES = ["gdn_api.cu", "gdn_stream.cu", "gdn_conv.cu"]
 HEADERS = [os.path.join(CSRC, "gdn_device.cuh"), os.path.join(CSRC, "gdn_internal.h"),
            os.path.join(ROOT, "include", "gdn_decode.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,6 +1,6 @@
 // C ABI of the GDN decode library: argument checks, pools, the sticky device
 // error word, and the small kernels (commit, slot zeroing, traffic probes).
-// The heavy kernels live in gdn_step.cu and gdn_conv.cu.
+// The heavy kernels live in gdn_stream.cu and gdn_conv.cu.
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -467,6 +467,8 @@ int gdn_decode_step(const void *q, const void *k, const void *v, const void *a, 
         return ok();
     if (!q || !k || !v)
         return fail(GDN_EINVAL, "q, k and v must be non-NULL");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v))
+        return fail(GDN_EINVAL, "q, k and v must be 16-byte aligned");
     int *err = nullptr;
     rc = device_error_ptr(&err);
     if (rc)
@@ -516,14 +518,14 @@ int gdn_layer_decode(const void *x, conv_pool *cp, const void *w, const void *bi
     if (cp->dtype != dtype)
         return fail(GDN_EINVAL, "dtype %d does not match the conv pool's %d", dtype, cp->dtype);
     if (!gdn::layer_shape_supported(d.dk, d.dv, d.hv / d.hk, keep_in_place != 0))
-        return fail(GDN_EUNSUPPORTED,
-                    "in-place fused layer needs a qk group (hv/hk=%d value heads of dv=%d) to fit "
-                    "one 8-block cluster",
-                    d.hv / d.hk, d.dv);
+        return fail(GDN_EUNSUPPORTED, "unsupported layer shape (hv/hk=%d, dk=%d, dv=%d)", d.hv / d.hk,
+                    d.dk, d.dv);
     if (rows == 0)
         return ok();
     if (!x || !w)
         return fail(GDN_EINVAL, "x and w must be non-NULL");
+    if (!aligned16(x) || !aligned16(w) || (bias && !aligned16(bias)))
+        return fail(GDN_EINVAL, "x, w and bias must be 16-byte aligned");
     int *err = nullptr;
     rc = device_error_ptr(&err);
     if (rc)

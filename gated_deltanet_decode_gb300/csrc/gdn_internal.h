@@ -71,8 +71,7 @@ cudaError_t launch_conv(const ConvArgs &a, int dtype, cudaStream_t s);
 
 // True when the state kernels are built for (dk, dv).
 bool step_shape_supported(int dk, int dv);
-// True when the fused layer can run this shape; in place it needs every block
-// of a qk group (group value heads x row chunks) in one portable cluster.
+// True when the fused layer can run this shape.
 bool layer_shape_supported(int dk, int dv, int group, bool in_place);
 
 } // namespace gdn

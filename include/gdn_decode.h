@@ -47,7 +47,8 @@
  *    [0, num_slots), a real row whose write slot is 0, or a twin row whose
  *    write slot equals its read slot) skip that row, zero its outputs and set
  *    a sticky per-device error word, read and cleared by
- *    gdn_get_device_error().  Kernels never trap, assert or spin-wait.
+ *    gdn_get_device_error().  Kernels never trap or assert; their waits on
+ *    shared-memory barriers are bounded and report GDN_DEVERR_TIMEOUT.
  *  - Preconditions not checked on the fast path: real rows name distinct
  *    write slots, and no row writes a slot another row reads.
  *    gdn_validate_slots() checks them (it synchronises).
@@ -72,6 +73,7 @@ extern "C" {
 /* ---- device error word values (gdn_get_device_error) ------------------ */
 #define GDN_DEVERR_NONE 0
 #define GDN_DEVERR_BAD_SLOT 1 /* some row named a slot outside the pool */
+#define GDN_DEVERR_TIMEOUT 2  /* a bounded wait inside a kernel ran out; its CTA stopped */
 
 /* ---- activation dtypes ------------------------------------------------ */
 #define GDN_F32 0
@@ -157,6 +159,8 @@ int causal_conv1d_decode(const void *x, int x_row_stride, conv_pool *cp, const i
  *   A_log, dt_bias [hv] fp32
  *   read_slot [rows] int32; write_slot [rows] int32 (ignored when
  *   keep_in_place != 0, and may then be NULL)
+ *   q, k and v are copied by the bulk-copy engine: each must be 16-byte
+ *   aligned (GDN_EINVAL otherwise). 
  * For every real row and value head: S = pool[read_slot[r]][h]; the updated
  * state goes to write_slot[r] (twin) or back to read_slot[r] (in place); out
  * receives o.  `heads` must equal the pool's hv.  Twin and in-place calls
@@ -173,7 +177,8 @@ int gdn_decode_step(const void *q, const void *k, const void *v, const void *a, 
  * head-major; the conv pool must have C channels.  Both pools use the same
  * read/write slots.  The conv output is rounded to the activation dtype
  * before the rule, exactly as between the two separate calls, so the result
- * is bit-identical to causal_conv1d_decode + gdn_decode_step. */
+ * is bit-identical to causal_conv1d_decode + gdn_decode_step.  x, w and bias
+ * must be 16-byte aligned. */
 int gdn_layer_decode(const void *x, conv_pool *cp, const void *w, const void *bias, int silu,
                      const float *A_log, const float *dt_bias, const void *a, const void *b,
                      gdn_pool *pool, const int32_t *read_slot, const int32_t *write_slot,

@@ -101,6 +101,7 @@ def test_step_argument_checks(L):
     assert call(q=None) == EINVAL
     assert call(ws=None) == EINVAL                      # twin needs a write table
     assert call(a=None) == EINVAL
+    assert call(q=P + 8) == EINVAL and b"aligned" in L.gdn_last_error()
     assert call(rows=0) == 0                            # nothing to launch
     assert call(rows=0, ws=None, inplace=1) == 0
     L.gdn_state_pool_destroy(pool)
@@ -123,13 +124,14 @@ def test_layer_and_conv_argument_checks(L):
     assert layer(cp, dtype=1) == EINVAL                 # dtype differs from the conv pool's
     assert layer(cp, x=None) == EINVAL
     assert layer(cp, rows=0) == 0
-    # in place, a qk group that cannot fit one 8-block cluster is refused
+    assert layer(cp, x=P + 8) == EINVAL                 # bulk-copy sources must be 16-byte aligned
+    assert layer(cp, w=P + 4) == EINVAL
+    # a wide qk group (16 value heads of dv = 512 sharing one qk head) is accepted
     rc, big = _wrap(L, num_slots=3, hk=1, hv=16, dk=16, dv=512)
     assert rc == 0
     cbig = ctypes.c_void_p()
     assert L.conv_state_pool_wrap(FAKE, 3, 2 * 16 + 16 * 512, 4, 0, ctypes.byref(cbig)) == 0
-    assert layer(cbig, rows=1, inplace=1, pool_=big) == EUNSUPPORTED
-    assert layer(cbig, rows=0, inplace=0, pool_=big) == 0
+    assert layer(cbig, rows=0, inplace=1, pool_=big) == 0
 
     def conv(stride=96, x=P, out=P, rows=2, dtype=0):
         return L.causal_conv1d_decode(x, stride, cp, P, None, P, None, 1, out, rows, dtype, None)
