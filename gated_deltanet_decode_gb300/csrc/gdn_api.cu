@@ -89,6 +89,7 @@ namespace {
 
 __global__ void commit_kernel(int32_t *rs, int32_t *ws, int rows)
 {
+    gdn::wait_prior_grid();
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r < rows) {
         const int32_t t = rs[r];
@@ -570,9 +571,8 @@ int gdn_commit(int32_t *read_slot, int32_t *write_slot, int rows, void *stream)
         return ok();
     if (!read_slot || !write_slot)
         return fail(GDN_EINVAL, "slot tables must be non-NULL");
-    commit_kernel<<<(rows + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(read_slot,
-                                                                                     write_slot, rows);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = gdn::launch_pdl(commit_kernel, dim3((rows + 255) / 256), dim3(256), 0,
+                                    static_cast<cudaStream_t>(stream), read_slot, write_slot, rows);
     if (e != cudaSuccess)
         return cuda_fail(e, "gdn_commit launch");
     return ok();

@@ -59,6 +59,7 @@ template <> struct Vec8<__nv_bfloat16> {
 template <typename T, int W>
 __global__ void __launch_bounds__(kThreads) conv_decode_kernel(const ConvArgs p, int groups_per_row)
 {
+    wait_prior_grid();
     const long long gid = (long long)blockIdx.x * kThreads + threadIdx.x;
     const int r = (int)(gid / groups_per_row);
     const int c0 = (int)(gid % groups_per_row) * kVec;
@@ -130,8 +131,7 @@ cudaError_t launch_w(const ConvArgs &a, cudaStream_t s)
     if (threads == 0)
         return cudaSuccess;
     const long long blocks = (threads + kThreads - 1) / kThreads;
-    conv_decode_kernel<T, W><<<(unsigned)blocks, kThreads, 0, s>>>(a, groups);
-    return cudaGetLastError();
+    return launch_pdl(conv_decode_kernel<T, W>, dim3((unsigned)blocks), dim3(kThreads), 0, s, a, groups);
 }
 
 template <typename T>

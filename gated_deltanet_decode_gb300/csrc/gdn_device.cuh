@@ -85,6 +85,34 @@ __device__ __forceinline__ float conv_channel(const float (&win)[W - 1], float x
     return pre;
 }
 
+// Programmatic dependent launch: kernels are launched with the PDL attribute,
+// so a kernel's CTAs may be scheduled while the previous kernel on the stream
+// drains.  Every kernel calls this before its first global-memory access; it
+// returns once the previous grid has completed and its writes are visible
+// (at once when there is no such dependency), so stream order is preserved.
+__device__ __forceinline__ void wait_prior_grid()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Launch `kern` on `s` with the programmatic-stream-serialization attribute.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Sticky device error word: the first error code wins.
 __device__ __forceinline__ void report(int *err, int code)
 {

@@ -5,39 +5,48 @@
 // The step is state traffic: every real (row, value head) reads a dv x dk
 // fp32 state and writes the next one, with a few multiply-adds per element
 // ("mstar PR #1139", section "Why": a kernel with the same reads and writes
-// and no math takes 45.2 of the rule's 46.1 us).  The kernel therefore keeps
-// as many bytes in flight as shared memory allows and spends as few
-// instructions as possible per byte:
+// and no math takes 45.2 of the rule's 46.1 us).  The kernel keeps as many
+// bytes in flight as shared memory allows and spends as few instructions as
+// it can per byte, since with the memory stream saturated the SMs' issue
+// rate is the next limit:
 //
 //  * Work item = RB consecutive value rows of one (row, value head): 16 KiB of
-//    fp32 state (RB = 4096 / dk), contiguous in the pool.  Items are dealt
-//    round-robin to two CTAs per SM (persistent grid), so every CTA gets the
-//    same number of items to within one.
+//    fp32 state (RB = 4096 / dk), contiguous in the pool.  A persistent grid
+//    (three CTAs per SM for the fused layer, two for the plain step) splits
+//    the items into contiguous ranges, equal to within one item.
+//  * Chains: consecutive items of a CTA that share a row and qk head form a
+//    chain.  Only a chain's first item copies q and k (or their conv inputs)
+//    and computes the q/k values, their norms and k^ . q^; the rest of the
+//    chain reuses them (values in a double-buffered shared buffer, norms in
+//    registers).
 //  * Producer warp: prepares items 32 at a time (each lane loads one item's
 //    slots and gate inputs and computes its gates), then one lane copies each
 //    item's metadata into a free stage and issues cp.async.bulk copies of the
-//    state chunk and
-//    of the item's small inputs (q, k, v -- or, in the fused layer, the conv
-//    windows, tokens, taps and bias of the item's channels) into a ring of
-//    shared-memory stages, completing on the stage's "full" mbarrier.
-//  * Consumer warps (8): per item, the prologue computes the q/k/v values
-//    (the conv in the fused layer) and the L2 norms by a block reduction among
-//    consumers; then each lane owns 16 floats of one state row
-//    (dk/16 lanes a row, 16-byte vectors interleaved so a warp store covers
-//    whole 128-byte lines), forms u = S k^ and w = S q^ in one butterfly, and
-//    stores S' = alpha S + c k^ (c = beta (v - alpha u)) straight to HBM with
-//    o = alpha w + c (k^ . q^).  Then the warps release the stage ("empty").
-//  * Every wait is bounded: a wait that runs out reports GDN_DEVERR_TIMEOUT,
-//    the consumers agree on it through a barrier reduction, and the CTA stops
-//    after the producer has waited (bounded) for its copies still in flight.
+//    state chunk and of the item's small inputs into a ring of shared-memory
+//    stages, completing on the stage's "full" mbarrier.
+//  * v warp (fused layer): computes the item's v channels (conv, one channel
+//    a lane) and writes their windows, then signals the stage's "vready".
+//  * Consumer warps (8): on a chain's first item, one q or k channel a thread
+//    (the conv in the fused layer) and a CTA-wide sum of squares, synchronised
+//    by an mbarrier.  Then each lane owns 16 floats of one state row (dk/16
+//    lanes a row, 16-byte vectors interleaved so a warp store covers whole
+//    128-byte lines), forms u = S k and w = S q with packed f32x2 FMAs and one
+//    butterfly, and stores S' = alpha S + c k^ (c = beta (v - alpha u k^))
+//    straight to HBM, with o = alpha w + c (k^ . q^).  Then the warps release
+//    the stage ("empty").
+//  * Every wait is bounded: a wait that runs out reports GDN_DEVERR_TIMEOUT
+//    and its warp leaves the loop (no hardware barrier inside the loop can be
+//    left waiting); the CTA stops after the producer has waited (bounded) for
+//    its copies still in flight.
 //
-// Fused layer, in place: the q/k conv window of a qk group is read by every
-// item of the group and must be written once, after all of them read it.
-// In-place launches deal whole groups (all value heads and row chunks sharing
-// the qk head) to one CTA, in order, and the group's last item writes the
-// window.  Twin launches write another slot, so the chunk-0 item of the
-// group's first value head writes it at once.  The arithmetic per row is the
-// same in every schedule, so twin and in place give bit-identical values.
+// Fused layer, in place: the q/k conv window of a qk group must be written
+// once, after every reader has read it.  In-place launches split the items
+// into ranges of whole groups (all value heads and row chunks sharing the qk
+// head), so a group's items run in order on one CTA and only the first of
+// them copies and reads the window; it writes the new window right after.
+// Twin launches write another slot, so the chunk-0 item of the group's first
+// value head writes it.  The arithmetic per row is the same in every
+// schedule, so twin and in place give bit-identical values.
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
 
@@ -47,11 +56,16 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32; // + one producer warp
 constexpr float kL2Eps = 1e-6f;
-constexpr int kBarId = 1;                 // named barrier among the consumers
 constexpr long long kWaitLimit = 1ll << 20;
-constexpr int kCtasPerSm = 2;
+constexpr uint32_t kSuspendHintNs = 1000;
+constexpr int kMaxStages = 8;
+
+// warps 0-7 consume, warp 8 produces, warp 9 computes v (fused layer only)
+template <bool LAYER> constexpr int threads_for() { return kConsumers + 32 + (LAYER ? 32 : 0); }
+// CTAs per SM: the fused layer's conv work hides better with more warps; the
+// plain step streams better with deeper rings (measured).
+template <bool LAYER> constexpr int ctas_per_sm() { return LAYER ? 3 : 2; }
 
 template <int DK> struct Geo {
     static_assert(DK >= 16 && DK <= 256 && DK % 16 == 0, "dk");
@@ -61,7 +75,7 @@ template <int DK> struct Geo {
 };
 
 // ---------------------------------------------------------------------------
-// PTX wrappers: mbarrier, bulk copy, named barrier with an OR reduction
+// PTX wrappers: mbarrier, bulk copy, packed fp32 arithmetic
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t sm_addr(const void *p)
 {
@@ -80,14 +94,16 @@ __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes)
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
+// try_wait suspends the thread until the phase completes or the hint (ns)
+// runs out, so waiting warps do not take issue slots from working ones.
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok)
-                 : "r"(bar), "r"(parity)
+                 : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
                  : "memory");
     return ok != 0;
 }
@@ -105,18 +121,23 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
                  ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
-// Named barrier over the consumer warps that also ORs a predicate across them.
-__device__ __forceinline__ bool consumers_sync_or(bool pred)
+// Two-wide fp32 FMA and multiply: each half rounds exactly like the scalar op.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
 {
-    uint32_t r;
-    asm volatile("{\n\t.reg .pred p, q;\n\t"
-                 "setp.ne.u32 p, %1, 0;\n\t"
-                 "bar.red.or.pred q, %2, %3, p;\n\t"
-                 "selp.u32 %0, 1, 0, q;\n\t}"
-                 : "=r"(r)
-                 : "r"((uint32_t)pred), "n"(kBarId), "n"(kConsumers)
-                 : "memory");
-    return r != 0;
+    unsigned long long A = *reinterpret_cast<unsigned long long *>(&a);
+    unsigned long long B = *reinterpret_cast<unsigned long long *>(&b);
+    unsigned long long Cc = *reinterpret_cast<unsigned long long *>(&c);
+    unsigned long long D;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(D) : "l"(A), "l"(B), "l"(Cc));
+    return *reinterpret_cast<float2 *>(&D);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b)
+{
+    unsigned long long A = *reinterpret_cast<unsigned long long *>(&a);
+    unsigned long long B = *reinterpret_cast<unsigned long long *>(&b);
+    unsigned long long D;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(D) : "l"(A), "l"(B));
+    return *reinterpret_cast<float2 *>(&D);
 }
 
 template <typename T>
@@ -140,68 +161,65 @@ template <typename T, int DK, bool LAYER, int W> struct Stage {
     static constexpr int align16(int x) { return (x + 15) & ~15; }
     static constexpr int STATE = 0;
     static constexpr int STATE_BYTES = RB * DK * 4;
-    // raw inputs (TMA destinations)
-    static constexpr int RAW = STATE + STATE_BYTES;
+    // raw inputs (bulk-copy destinations)
     // step:  q[DK] | k[DK] | v[RB]
     // layer: win[W-1][NCH] | x[NCH] | w[NCH][W] | bias[NCH], each [q | k | v]
+    static constexpr int RAW = STATE + STATE_BYTES;
     static constexpr int WIN = RAW;
     static constexpr int XS = LAYER ? WIN + (W - 1) * NCH * E : RAW;
     static constexpr int WS = XS + NCH * E;
     static constexpr int BS = WS + NCH * W * E;
     static constexpr int RAW_END = LAYER ? BS + NCH * E : RAW + NCH * E;
-    // computed by the consumers
-    static constexpr int QN = align16(RAW_END);        // q values (fp32) [DK]
-    static constexpr int KN = QN + DK * 4;             // k values (fp32) [DK]
-    static constexpr int VN = KN + DK * 4;             // v values (fp32) [RB]
-    static constexpr int PART = VN + RB * 4;           // block-reduction partials [3][8]
-    static constexpr int META = align16(PART + 3 * kConsumerWarps * 4); // Meta, by the producer
-    static constexpr int BYTES = (META + 48 + 127) & ~127;
+    static constexpr int VN = align16(RAW_END);                  // v values (fp32) [RB], layer only
+    static constexpr int META = align16(VN + (LAYER ? RB * 4 : 0)); // Meta, by the producer
+    static constexpr int BYTES = (META + 64 + 127) & ~127;
 };
 
 struct Meta {
-    int r, h, chunk, rs, ws, live, last, rows;
+    int r, h, chunk, rs, ws, live, rows;
+    int reuse; // same row and qk head as the previous item: q/k values reused
     float alpha, beta;
 };
 
-// The item sequence of one CTA.  Fine: items dealt round-robin.  Coarse:
-// whole qk groups dealt round-robin, the items of a group in order.
+// Contiguous ranges: CTA b of g takes units [first(b), first(b + 1)),
+// balanced to within one unit.  Fine: a unit is an item.  Coarse: a unit is
+// a whole qk group (group value heads x row chunks), its items in order.
 struct Sched {
     int hv, group, chunks;
-    int n_units;     // items (fine) or groups (coarse)
+    int n_units;
     int per_unit;    // 1 (fine) or group * chunks (coarse)
     int coarse;
 
-    // number of items CTA b of a grid of g CTAs processes
+    __device__ __forceinline__ int first(int b, int g) const
+    {
+        return (int)(((long long)n_units * b) / g);
+    }
     __device__ __forceinline__ int count(int b, int g) const
     {
-        if (b >= n_units)
-            return 0;
-        return ((n_units - 1 - b) / g + 1) * per_unit;
+        return (first(b + 1, g) - first(b, g)) * per_unit;
     }
-
     // k-th item of CTA b in a grid of g CTAs (k < count(b, g))
-    __device__ __forceinline__ void item(int b, int g, int k, int &r, int &h, int &chunk, bool &last) const
+    __device__ __forceinline__ void item(int b, int g, int k, int &r, int &h, int &chunk) const
     {
-        const int unit = b + (k / per_unit) * g;
+        const int unit = first(b, g) + k / per_unit;
         if (!coarse) {
             chunk = unit % chunks;
             const int rh = unit / chunks;
             h = rh % hv;
             r = rh / hv;
-            last = false;
         } else {
             const int j = k % per_unit;
             const int hk = hv / group;
             r = unit / hk;
             h = (unit % hk) * group + j / chunks;
             chunk = j % chunks;
-            last = j == per_unit - 1;
         }
     }
 };
 
 template <typename T, int DK, bool LAYER, int W>
-__global__ void __launch_bounds__(kThreads, 2) gdn_stream_kernel(const StepArgs p, const Sched sc, int nstages)
+__global__ void __launch_bounds__(threads_for<LAYER>(), ctas_per_sm<LAYER>())
+gdn_stream_kernel(const StepArgs p, const Sched sc, int nst)
 {
     using G = Geo<DK>;
     using L = Stage<T, DK, LAYER, W>;
@@ -209,30 +227,44 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_stream_kernel(const StepArgs 
     constexpr int E = L::E;
 
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ __align__(8) unsigned long long bars[2 * 8]; // full[s], empty[s]
+    __shared__ __align__(8) unsigned long long bars[3 * kMaxStages + 1]; // full, empty, vready, qk
+    __shared__ __align__(16) float qkbuf[2][2 * DK];         // a chain's q | k values, double-buffered
+    __shared__ float part[2][kConsumerWarps][2];             // per-warp sums of q^2 and k^2
+    __shared__ Meta table[32];                               // the producer's batch
     __shared__ int abort_flag;
     __shared__ int issued_n, consumed_n;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int nst = nstages;
     auto full_bar = [&](int s) { return sm_addr(&bars[s]); };
-    auto empty_bar = [&](int s) { return sm_addr(&bars[8 + s]); };
+    auto empty_bar = [&](int s) { return sm_addr(&bars[kMaxStages + s]); };
+    auto vready_bar = [&](int s) { return sm_addr(&bars[2 * kMaxStages + s]); };
+    const uint32_t qk_bar = sm_addr(&bars[3 * kMaxStages]);
     auto stage = [&](int s) { return smem + (size_t)s * L::BYTES; };
+    auto timeout = [&]() {
+        report(p.err, GDN_DEVERR_TIMEOUT);
+        atomicExch(&abort_flag, 1);
+    };
 
     if (tid == 0) {
         for (int s = 0; s < nst; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), kConsumerWarps);
+            mbar_init(empty_bar(s), kConsumerWarps + (LAYER ? 1 : 0));
+            mbar_init(vready_bar(s), 1);
         }
+        mbar_init(qk_bar, kConsumerWarps);
         abort_flag = 0;
         issued_n = 0;
         consumed_n = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    wait_prior_grid(); // barrier set-up overlapped the previous kernel's tail
 
     const int C = p.channels;
+    const int group = p.hv / p.hk;
+    const int n_items = sc.count(blockIdx.x, gridDim.x);
+
     if (warp == kConsumerWarps) {
         // =========================== producer ===========================
         // The warp prepares items 32 at a time: lane j loads item j's slots
@@ -240,16 +272,12 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_stream_kernel(const StepArgs 
         // computes its gates into a shared table; lane 0 then streams the
         // batch: wait for a free stage, copy the item's metadata into it, issue
         // the bulk copies.
-        __shared__ Meta table[32];
-        const int n_items = sc.count(blockIdx.x, gridDim.x);
         bool stop = false;
         for (int base = 0; base < n_items && !stop; base += 32) {
             const int kk = base + lane;
             if (kk < n_items) {
                 Meta q;
-                bool last;
-                sc.item(blockIdx.x, gridDim.x, kk, q.r, q.h, q.chunk, last);
-                q.last = last;
+                sc.item(blockIdx.x, gridDim.x, kk, q.r, q.h, q.chunk);
                 q.rs = p.read_slot[q.r];
                 q.ws = p.in_place ? q.rs : p.write_slot[q.r];
                 const float av = ld_act<T>(p.a, (size_t)q.r * p.hv + q.h);
@@ -262,6 +290,12 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_stream_kernel(const StepArgs 
                 q.rows = min(RB, p.dv - q.chunk * RB);
                 q.alpha = q.live ? gate_alpha(al, av, dt) : 0.f;
                 q.beta = q.live ? gate_beta(bv) : 0.f;
+                q.reuse = 0;
+                if (kk > 0) {
+                    int r0, h0, c0;
+                    sc.item(blockIdx.x, gridDim.x, kk - 1, r0, h0, c0);
+                    q.reuse = q.live && r0 == q.r && h0 / group == q.h / group;
+                }
                 table[lane] = q;
             }
             __syncwarp();
@@ -270,10 +304,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_stream_kernel(const StepArgs 
                 for (int j = 0; j < nb; ++j) {
                     const int k = base + j;
                     const int s = k % nst;
-                    const uint32_t par = (uint32_t)((k / nst) & 1);
-                    if (!mbar_wait(empty_bar(s), par ^ 1u)) {
-                        report(p.err, GDN_DEVERR_TIMEOUT);
-                        atomicExch(&abort_flag, 1);
+                    if (!mbar_wait(empty_bar(s), (uint32_t)((k / nst) & 1) ^ 1u)) {
+                        timeout();
                         stop = true;
                         break;
                     }
@@ -287,14 +319,15 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_stream_kernel(const StepArgs 
                     const uint32_t fb = full_bar(s);
                     if (q.live) {
                         const int r = q.r, h = q.h, chunk = q.chunk, rows = q.rows;
-                        const int g = h / (p.hv / p.hk);
+                        const int g = h / group;
                         const int cq = g * DK, ck = p.hk * DK + g * DK;
                         const int cv = 2 * p.hk * DK + h * p.dv + chunk * RB;
+                        const int nqk = q.reuse ? 0 : 2 * DK; // q/k channels to copy
                         uint32_t bytes = (uint32_t)(rows * DK * 4);
                         if constexpr (LAYER)
-                            bytes += (uint32_t)(((W - 1) + 1 + W + (p.bias ? 1 : 0)) * (2 * DK + rows) * E);
+                            bytes += (uint32_t)(((W - 1) + 1 + W + (p.bias ? 1 : 0)) * (nqk + rows) * E);
                         else
-                            bytes += (uint32_t)((2 * DK + rows) * E);
+                            bytes += (uint32_t)((nqk + rows) * E);
                         mbar_arrive_tx(fb, bytes);
                         const float *src =
                             p.pool + (((size_t)q.rs * p.hv + h) * p.dv + (size_t)chunk * RB) * DK;
@@ -309,6 +342,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_stream_kernel(const StepArgs 
                             const int n[3] = {DK, DK, rows};
 #pragma unroll
                             for (int sgm = 0; sgm < 3; ++sgm) {
+                                if (sgm < 2 && q.reuse)
+                                    continue;
 #pragma unroll
                                 for (int jj = 0; jj < W - 1; ++jj)
                                     bulk_load(sm_addr(st + L::WIN + (jj * L::NCH + off[sgm]) * E),
@@ -326,9 +361,11 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_stream_kernel(const StepArgs 
                             const unsigned char *qp = reinterpret_cast<const unsigned char *>(p.q);
                             const unsigned char *kp = reinterpret_cast<const unsigned char *>(p.k);
                             const unsigned char *vp = reinterpret_cast<const unsigned char *>(p.v);
-                            bulk_load(sm_addr(st + L::RAW), qp + ((size_t)r * p.hk + g) * DK * E, DK * E, fb);
-                            bulk_load(sm_addr(st + L::RAW + DK * E), kp + ((size_t)r * p.hk + g) * DK * E,
-                                      DK * E, fb);
+                            if (!q.reuse) {
+                                bulk_load(sm_addr(st + L::RAW), qp + ((size_t)r * p.hk + g) * DK * E, DK * E, fb);
+                                bulk_load(sm_addr(st + L::RAW + DK * E), kp + ((size_t)r * p.hk + g) * DK * E,
+                                          DK * E, fb);
+                            }
                             bulk_load(sm_addr(st + L::RAW + 2 * DK * E),
                                       vp + (((size_t)r * p.hv + h) * p.dv + (size_t)chunk * RB) * E,
                                       (uint32_t)(rows * E), fb);
@@ -342,189 +379,203 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_stream_kernel(const StepArgs 
             stop = __shfl_sync(0xffffffffu, stop, 0);
             __syncwarp();
         }
-    } else {
-        // =========================== consumers ==========================
-        const int lrow = lane / G::LPR, lcol = lane % G::LPR;
-        const int t = tid; // consumer index 0..255
-        const int n_items = sc.count(blockIdx.x, gridDim.x);
-        for (int k = 0; k < n_items; ++k) {
-            const int s = (int)(k % nst);
-            const uint32_t par = (uint32_t)((k / nst) & 1);
-            const bool got = mbar_wait(full_bar(s), par);
-            unsigned char *st = stage(s);
-            const Meta m = *reinterpret_cast<const Meta *>(st + L::META);
-            const bool live = got && m.live;
-            float *qn = reinterpret_cast<float *>(st + L::QN);
-            float *kn = reinterpret_cast<float *>(st + L::KN);
-            float *vn = reinterpret_cast<float *>(st + L::VN);
-            float *part = reinterpret_cast<float *>(st + L::PART);
-            T *out = reinterpret_cast<T *>(p.out) + ((size_t)m.r * p.hv + m.h) * p.dv + (size_t)m.chunk * RB;
-
-            // ---- prologue: q, k, v values, norms' partial sums, gates -------
-            float pqq = 0.f, pkk = 0.f, pqk = 0.f;
-            if (live) {
-                const int group = p.hv / p.hk;
-                const int g = m.h / group;
-                if (t < DK) {
-                    float qv, kv;
-                    if constexpr (LAYER) {
-                        float wq[W], wk[W], winq[W - 1], wink[W - 1];
-#pragma unroll
-                        for (int j = 0; j < W; ++j) {
-                            wq[j] = sh_act<T>(st + L::WS, t * W + j);
-                            wk[j] = sh_act<T>(st + L::WS, (DK + t) * W + j);
-                        }
-#pragma unroll
-                        for (int j = 0; j < W - 1; ++j) {
-                            winq[j] = sh_act<T>(st + L::WIN, j * L::NCH + t);
-                            wink[j] = sh_act<T>(st + L::WIN, j * L::NCH + DK + t);
-                        }
-                        const float xq = sh_act<T>(st + L::XS, t);
-                        const float xk = sh_act<T>(st + L::XS, DK + t);
-                        const float bq = p.bias ? sh_act<T>(st + L::BS, t) : 0.f;
-                        const float bk = p.bias ? sh_act<T>(st + L::BS, DK + t) : 0.f;
-                        qv = round_act<T>(conv_channel<W>(winq, xq, wq, bq, p.silu != 0));
-                        kv = round_act<T>(conv_channel<W>(wink, xk, wk, bk, p.silu != 0));
-                        // the q/k window is written once per group: by the chunk-0 item
-                        // of its first value head (twin), or by its last item (in place)
-                        const bool writer = p.in_place ? m.last : (m.h % group == 0 && m.chunk == 0);
-                        if (writer) {
-                            T *wout = reinterpret_cast<T *>(p.conv) + (size_t)m.ws * (W - 1) * C;
-                            const int cq = g * DK + t, ck = p.hk * DK + g * DK + t;
-#pragma unroll
-                            for (int j = 0; j + 1 < W - 1; ++j) {
-                                wout[(size_t)j * C + cq] = from_f<T>(winq[j + 1]);
-                                wout[(size_t)j * C + ck] = from_f<T>(wink[j + 1]);
-                            }
-                            wout[(size_t)(W - 2) * C + cq] = from_f<T>(xq);
-                            wout[(size_t)(W - 2) * C + ck] = from_f<T>(xk);
-                        }
-                    } else {
-                        qv = sh_act<T>(st + L::RAW, t);
-                        kv = sh_act<T>(st + L::RAW, DK + t);
-                    }
-                    qn[t] = qv;
-                    kn[t] = kv;
-                    pqq = qv * qv;
-                    pkk = kv * kv;
-                    pqk = qv * kv;
+    } else if (LAYER && warp == kConsumerWarps + 1) {
+        // =========================== v warp =============================
+        if constexpr (LAYER) {
+            for (int k = 0; k < n_items; ++k) {
+                const int s = k % nst;
+                if (!mbar_wait(full_bar(s), (uint32_t)((k / nst) & 1))) {
+                    timeout();
+                    break;
                 }
-                if (t < m.rows) {
-                    float vv;
-                    if constexpr (LAYER) {
+                unsigned char *st = stage(s);
+                const Meta m = *reinterpret_cast<const Meta *>(st + L::META);
+                if (m.live) {
+                    float *vn = reinterpret_cast<float *>(st + L::VN);
+                    T *wout = reinterpret_cast<T *>(p.conv) + (size_t)m.ws * (W - 1) * C;
+                    for (int c = lane; c < m.rows; c += 32) {
                         float wv[W], winv[W - 1];
 #pragma unroll
                         for (int j = 0; j < W; ++j)
-                            wv[j] = sh_act<T>(st + L::WS, (2 * DK + t) * W + j);
+                            wv[j] = sh_act<T>(st + L::WS, (2 * DK + c) * W + j);
 #pragma unroll
                         for (int j = 0; j < W - 1; ++j)
-                            winv[j] = sh_act<T>(st + L::WIN, j * L::NCH + 2 * DK + t);
-                        const float xv = sh_act<T>(st + L::XS, 2 * DK + t);
-                        const float bv = p.bias ? sh_act<T>(st + L::BS, 2 * DK + t) : 0.f;
-                        vv = round_act<T>(conv_channel<W>(winv, xv, wv, bv, p.silu != 0));
+                            winv[j] = sh_act<T>(st + L::WIN, j * L::NCH + 2 * DK + c);
+                        const float xv = sh_act<T>(st + L::XS, 2 * DK + c);
+                        const float bv = p.bias ? sh_act<T>(st + L::BS, 2 * DK + c) : 0.f;
+                        vn[c] = round_act<T>(conv_channel<W>(winv, xv, wv, bv, p.silu != 0));
                         // this item is the only reader and writer of its v channels
-                        T *wout = reinterpret_cast<T *>(p.conv) + (size_t)m.ws * (W - 1) * C;
-                        const int cv = 2 * p.hk * DK + m.h * p.dv + m.chunk * RB + t;
+                        const int cv = 2 * p.hk * DK + m.h * p.dv + m.chunk * RB + c;
 #pragma unroll
                         for (int j = 0; j + 1 < W - 1; ++j)
                             wout[(size_t)j * C + cv] = from_f<T>(winv[j + 1]);
                         wout[(size_t)(W - 2) * C + cv] = from_f<T>(xv);
-                    } else {
-                        vv = sh_act<T>(st + L::RAW, 2 * DK + t);
                     }
-                    vn[t] = vv;
                 }
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) {
-                    pqq += __shfl_xor_sync(0xffffffffu, pqq, off);
-                    pkk += __shfl_xor_sync(0xffffffffu, pkk, off);
-                    pqk += __shfl_xor_sync(0xffffffffu, pqk, off);
-                }
+                __syncwarp();
                 if (lane == 0) {
-                    part[0 * kConsumerWarps + warp] = pqq;
-                    part[1 * kConsumerWarps + warp] = pkk;
-                    part[2 * kConsumerWarps + warp] = pqk;
+                    mbar_arrive(vready_bar(s));
+                    mbar_arrive(empty_bar(s));
                 }
             }
-            // every consumer learns whether any consumer's wait ran out
-            if (consumers_sync_or(!got)) {
-                if (t == 0) {
-                    report(p.err, GDN_DEVERR_TIMEOUT);
-                    atomicExch(&abort_flag, 1);
-                }
+        }
+    } else if (warp < kConsumerWarps) {
+        // =========================== consumers ==========================
+        const int lrow = lane / G::LPR, lcol = lane % G::LPR;
+        const int t = tid; // consumer index 0..255
+        const int row = warp * G::RPW + lrow;
+        int chains = 0;                // chains started so far
+        int qkb = 0;                   // buffer of the current chain
+        float inv_q = 0.f, inv_k = 0.f, kappa = 0.f;
+        for (int k = 0; k < n_items; ++k) {
+            const int s = k % nst;
+            const uint32_t par = (uint32_t)((k / nst) & 1);
+            if (!mbar_wait(full_bar(s), par)) {
+                timeout();
                 break;
             }
-
-            if (live) {
-                // ---- norms and gates --------------------------------------------
-                float qq = 0.f, kk = 0.f, qk = 0.f;
-                constexpr int kRedWarps = (DK + 31) / 32;
+            unsigned char *st = stage(s);
+            const Meta m = *reinterpret_cast<const Meta *>(st + L::META);
+            T *out = reinterpret_cast<T *>(p.out) + ((size_t)m.r * p.hv + m.h) * p.dv + (size_t)m.chunk * RB;
+            if (m.live) {
+                if (!m.reuse) {
+                    // ---- a chain starts: q/k values, norms, k^ . q^ -----------------
+                    qkb = chains & 1;
+                    float *qk = qkbuf[qkb];
+                    const int g = m.h / group;
+                    float psq = 0.f, psk = 0.f;
+                    for (int c = t; c < 2 * DK; c += kConsumers) {
+                        const bool isq = c < DK;
+                        float val;
+                        if constexpr (LAYER) {
+                            float wq[W], winq[W - 1];
 #pragma unroll
-                for (int wi = 0; wi < kRedWarps; ++wi) {
-                    qq += part[0 * kConsumerWarps + wi];
-                    kk += part[1 * kConsumerWarps + wi];
-                    qk += part[2 * kConsumerWarps + wi];
-                }
-                const float inv_q = __fdiv_rn(1.0f, sqrtf(qq + kL2Eps)) * rsqrtf((float)DK);
-                const float inv_k = __fdiv_rn(1.0f, sqrtf(kk + kL2Eps));
-                const float kappa = qk * inv_q * inv_k;
-                const float alpha = m.alpha;
-                const float beta = m.beta;
-
-                // ---- the state rows ---------------------------------------------
-                // every lane runs the reductions (the shuffles need the whole
-                // warp); only rows inside the chunk are stored
-                const int row = warp * G::RPW + lrow;
-                {
-                    float4 kh[4], qh[4], sv[4];
-                    const float *srow = reinterpret_cast<const float *>(st + L::STATE) + row * DK + 4 * lcol;
+                            for (int j = 0; j < W; ++j)
+                                wq[j] = sh_act<T>(st + L::WS, c * W + j);
 #pragma unroll
-                    for (int mm = 0; mm < 4; ++mm) {
-                        const int j = 4 * (lcol + G::LPR * mm);
-                        const float4 kr = *reinterpret_cast<const float4 *>(&kn[j]);
-                        const float4 qr = *reinterpret_cast<const float4 *>(&qn[j]);
-                        kh[mm] = make_float4(kr.x * inv_k, kr.y * inv_k, kr.z * inv_k, kr.w * inv_k);
-                        qh[mm] = make_float4(qr.x * inv_q, qr.y * inv_q, qr.z * inv_q, qr.w * inv_q);
-                        sv[mm] = *reinterpret_cast<const float4 *>(srow + 4 * G::LPR * mm);
-                    }
-                    float u = 0.f, wd = 0.f;
+                            for (int j = 0; j < W - 1; ++j)
+                                winq[j] = sh_act<T>(st + L::WIN, j * L::NCH + c);
+                            const float xq = sh_act<T>(st + L::XS, c);
+                            const float bq = p.bias ? sh_act<T>(st + L::BS, c) : 0.f;
+                            val = round_act<T>(conv_channel<W>(winq, xq, wq, bq, p.silu != 0));
+                            // The q/k window is written once per group.  Twin: by the chunk-0
+                            // item of the group's first value head (it writes another slot).
+                            // In place: a group lies within one CTA and only its first item
+                            // copies the window (the rest reuse its q/k), so that item writes
+                            // the window as soon as its own copy has landed.
+                            const bool writer = p.in_place ? true : (m.h % group == 0 && m.chunk == 0);
+                            if (writer) {
+                                T *wout = reinterpret_cast<T *>(p.conv) + (size_t)m.ws * (W - 1) * C;
+                                const int gc = isq ? g * DK + c : p.hk * DK + g * DK + (c - DK);
 #pragma unroll
-                    for (int mm = 0; mm < 4; ++mm) {
-                        u = __fmaf_rn(sv[mm].x, kh[mm].x, u);
-                        u = __fmaf_rn(sv[mm].y, kh[mm].y, u);
-                        u = __fmaf_rn(sv[mm].z, kh[mm].z, u);
-                        u = __fmaf_rn(sv[mm].w, kh[mm].w, u);
-                        wd = __fmaf_rn(sv[mm].x, qh[mm].x, wd);
-                        wd = __fmaf_rn(sv[mm].y, qh[mm].y, wd);
-                        wd = __fmaf_rn(sv[mm].z, qh[mm].z, wd);
-                        wd = __fmaf_rn(sv[mm].w, qh[mm].w, wd);
-                    }
-#pragma unroll
-                    for (int off = G::LPR / 2; off >= 1; off >>= 1) {
-                        u += __shfl_xor_sync(0xffffffffu, u, off, G::LPR);
-                        wd += __shfl_xor_sync(0xffffffffu, wd, off, G::LPR);
-                    }
-                    if (row < m.rows) {
-                        const float vi = vn[row];
-                        const float c = beta * __fmaf_rn(-alpha, u, vi);
-                        const float o = __fmaf_rn(c, kappa, alpha * wd);
-                        float *dst = p.pool +
-                                     (((size_t)m.ws * p.hv + m.h) * p.dv + (size_t)m.chunk * RB + row) * DK +
-                                     4 * lcol;
-#pragma unroll
-                        for (int mm = 0; mm < 4; ++mm) {
-                            float4 nv;
-                            nv.x = __fmaf_rn(c, kh[mm].x, alpha * sv[mm].x);
-                            nv.y = __fmaf_rn(c, kh[mm].y, alpha * sv[mm].y);
-                            nv.z = __fmaf_rn(c, kh[mm].z, alpha * sv[mm].z);
-                            nv.w = __fmaf_rn(c, kh[mm].w, alpha * sv[mm].w);
-                            st_state(dst + 4 * G::LPR * mm, nv);
+                                for (int j = 0; j + 1 < W - 1; ++j)
+                                    wout[(size_t)j * C + gc] = from_f<T>(winq[j + 1]);
+                                wout[(size_t)(W - 2) * C + gc] = from_f<T>(xq);
+                            }
+                        } else {
+                            val = sh_act<T>(st + L::RAW, c);
                         }
-                        if (lcol == 0)
-                            out[row] = from_f<T>(o);
+                        qk[c] = val;
+                        if (isq)
+                            psq = __fmaf_rn(val, val, psq);
+                        else
+                            psk = __fmaf_rn(val, val, psk);
                     }
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) {
+                        psq += __shfl_xor_sync(0xffffffffu, psq, off);
+                        psk += __shfl_xor_sync(0xffffffffu, psk, off);
+                    }
+                    if (lane == 0) {
+                        part[qkb][warp][0] = psq;
+                        part[qkb][warp][1] = psk;
+                    }
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(qk_bar);
+                    if (!mbar_wait(qk_bar, (uint32_t)(chains & 1))) {
+                        timeout();
+                        break;
+                    }
+                    ++chains;
+                    float qq = 0.f, kk2 = 0.f;
+#pragma unroll
+                    for (int wi = 0; wi < kConsumerWarps; ++wi) {
+                        qq += part[qkb][wi][0];
+                        kk2 += part[qkb][wi][1];
+                    }
+                    inv_q = __fdiv_rn(1.0f, sqrtf(qq + kL2Eps)) * rsqrtf((float)DK);
+                    inv_k = __fdiv_rn(1.0f, sqrtf(kk2 + kL2Eps));
+                    float pqk = 0.f;
+                    for (int i = lane; i < DK; i += 32)
+                        pqk = __fmaf_rn(qk[i], qk[DK + i], pqk);
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1)
+                        pqk += __shfl_xor_sync(0xffffffffu, pqk, off);
+                    kappa = pqk * inv_q * inv_k; // k^ . q^
                 }
-            } else if (got) {
+
+                // ---- this lane's state row ---------------------------------------
+                float vi = 0.f;
+                if constexpr (LAYER) {
+                    if (!mbar_wait(vready_bar(s), par)) {
+                        timeout();
+                        break;
+                    }
+                    if (row < m.rows)
+                        vi = reinterpret_cast<const float *>(st + L::VN)[row];
+                } else {
+                    if (row < m.rows)
+                        vi = sh_act<T>(st + L::RAW, 2 * DK + row);
+                }
+                const float *kq = qkbuf[qkb];
+                const float *srow = reinterpret_cast<const float *>(st + L::STATE) + row * DK + 4 * lcol;
+                float4 kh[4], qh[4], sv[4];
+#pragma unroll
+                for (int mm = 0; mm < 4; ++mm) {
+                    const int j = 4 * (lcol + G::LPR * mm);
+                    qh[mm] = *reinterpret_cast<const float4 *>(&kq[j]);
+                    kh[mm] = *reinterpret_cast<const float4 *>(&kq[DK + j]);
+                    sv[mm] = *reinterpret_cast<const float4 *>(srow + 4 * G::LPR * mm);
+                }
+                // u = S . k and w = S . q on the raw values; the shuffles need the
+                // whole warp, so every lane reduces and only real rows are stored
+                float2 u2 = make_float2(0.f, 0.f), w2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int mm = 0; mm < 4; ++mm) {
+                    u2 = fma2(make_float2(sv[mm].x, sv[mm].y), make_float2(kh[mm].x, kh[mm].y), u2);
+                    u2 = fma2(make_float2(sv[mm].z, sv[mm].w), make_float2(kh[mm].z, kh[mm].w), u2);
+                    w2 = fma2(make_float2(sv[mm].x, sv[mm].y), make_float2(qh[mm].x, qh[mm].y), w2);
+                    w2 = fma2(make_float2(sv[mm].z, sv[mm].w), make_float2(qh[mm].z, qh[mm].w), w2);
+                }
+                float u = u2.x + u2.y, wd = w2.x + w2.y;
+#pragma unroll
+                for (int off = G::LPR / 2; off >= 1; off >>= 1) {
+                    u += __shfl_xor_sync(0xffffffffu, u, off);
+                    wd += __shfl_xor_sync(0xffffffffu, wd, off);
+                }
+                u *= inv_k;  // S . k^
+                wd *= inv_q; // S . q^
+                if (row < m.rows) {
+                    const float alpha = m.alpha, beta = m.beta;
+                    const float c = beta * __fmaf_rn(-alpha, u, vi);
+                    const float o = __fmaf_rn(c, kappa, alpha * wd);
+                    const float ck = c * inv_k; // S' = alpha S + c k^ = alpha S + (c / |k|) k
+                    const float2 a2 = make_float2(alpha, alpha), c2 = make_float2(ck, ck);
+                    float *dst = p.pool +
+                                 (((size_t)m.ws * p.hv + m.h) * p.dv + (size_t)m.chunk * RB + row) * DK + 4 * lcol;
+#pragma unroll
+                    for (int mm = 0; mm < 4; ++mm) {
+                        const float2 lo = fma2(c2, make_float2(kh[mm].x, kh[mm].y),
+                                               mul2(a2, make_float2(sv[mm].x, sv[mm].y)));
+                        const float2 hi = fma2(c2, make_float2(kh[mm].z, kh[mm].w),
+                                               mul2(a2, make_float2(sv[mm].z, sv[mm].w)));
+                        st_state(dst + 4 * G::LPR * mm, make_float4(lo.x, lo.y, hi.x, hi.y));
+                    }
+                    if (lcol == 0)
+                        out[row] = from_f<T>(o);
+                }
+            } else {
                 // padding or bad row: zero outputs, no slot touched
                 if (t < m.rows)
                     out[t] = from_f<T>(0.f);
@@ -539,10 +590,10 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_stream_kernel(const StepArgs 
 
     // A CTA whose waits ran out leaves no copy in flight: the producer waits
     // (bounded) for every stage it filled that was not consumed.
-    asm volatile("barrier.sync 0;" ::: "memory"); // the producer warp arrives divergently
+    asm volatile("barrier.sync 0;" ::: "memory"); // warps arrive here at different times
     if (abort_flag && tid == kConsumers) {
         for (int k = consumed_n; k < issued_n; ++k)
-            mbar_wait(full_bar((int)(k % nst)), (uint32_t)((k / nst) & 1));
+            mbar_wait(full_bar(k % nst), (uint32_t)((k / nst) & 1));
     }
 }
 
@@ -582,10 +633,11 @@ cudaError_t launch_stream(const StepArgs &a, bool coarse, cudaStream_t s)
     sc.n_units = (int)(items / sc.per_unit);
     if (sc.n_units == 0)
         return cudaSuccess;
-    // two CTAs per SM, each with as many stages as fit (at most 8)
-    const int max_smem = (227 * 1024) / kCtasPerSm - 2048;
+    // ctas_per_sm CTAs per SM, each with as many stages as fit
+    constexpr int kCtas = ctas_per_sm<LAYER>();
+    const int max_smem = (227 * 1024) / kCtas - 4096;
     int nst = max_smem / L::BYTES;
-    nst = nst > 8 ? 8 : nst;
+    nst = nst > kMaxStages ? kMaxStages : nst;
     if (nst < 2)
         return cudaErrorInvalidConfiguration;
     const size_t smem = (size_t)nst * L::BYTES;
@@ -600,10 +652,9 @@ cudaError_t launch_stream(const StepArgs &a, bool coarse, cudaStream_t s)
             return e;
         configured |= bit;
     }
-    const int slots = kCtasPerSm * num_sms();
+    const int slots = kCtas * num_sms();
     const int grid = (int)(sc.n_units < slots ? sc.n_units : slots);
-    kern<<<grid, kThreads, smem, s>>>(a, sc, nst);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(threads_for<LAYER>()), smem, s, a, sc, nst);
 }
 
 template <typename T, bool LAYER, int W>
