@@ -19,11 +19,12 @@
 //    and computes the q/k values, their norms and k^ . q^; the rest of the
 //    chain reuses them (values in a double-buffered shared buffer, norms in
 //    registers).
-//  * Producer warp: prepares items 32 at a time (each lane loads one item's
-//    slots and gate inputs and computes its gates), then one lane copies each
-//    item's metadata into a free stage and issues cp.async.bulk copies of the
-//    state chunk and of the item's small inputs into a ring of shared-memory
-//    stages, completing on the stage's "full" mbarrier.
+//  * Producer warp: prepares items 32 at a time (one lane each: slots, gate
+//    inputs, gates); one lane streams them: it waits for the item's stage,
+//    issues cp.async.bulk copies of the state chunk and of the item's small
+//    inputs with their byte count (the first of two arrivals on the stage's
+//    "full" mbarrier) and writes the item's metadata (the second).  The first
+//    stages' copies leave before the gates are even computed.
 //  * v warp (fused layer): computes the item's v channels (conv, one channel
 //    a lane) and writes their windows, then signals the stage's "vready".
 //  * Consumer warps (8): on a chain's first item, one q or k channel a thread
@@ -198,10 +199,10 @@ struct Sched {
     {
         return (first(b + 1, g) - first(b, g)) * per_unit;
     }
-    // k-th item of CTA b in a grid of g CTAs (k < count(b, g))
-    __device__ __forceinline__ void item(int b, int g, int k, int &r, int &h, int &chunk) const
+    // k-th item of the CTA whose range starts at unit `first_unit`
+    __device__ __forceinline__ void item_at(int first_unit, int k, int &r, int &h, int &chunk) const
     {
-        const int unit = first(b, g) + k / per_unit;
+        const int unit = first_unit + k / per_unit;
         if (!coarse) {
             chunk = unit % chunks;
             const int rh = unit / chunks;
@@ -248,7 +249,7 @@ gdn_stream_kernel(const StepArgs p, const Sched sc, int nst)
 
     if (tid == 0) {
         for (int s = 0; s < nst; ++s) {
-            mbar_init(full_bar(s), 1);
+            mbar_init(full_bar(s), 2); // copies + metadata
             mbar_init(empty_bar(s), kConsumerWarps + (LAYER ? 1 : 0));
             mbar_init(vready_bar(s), 1);
         }
@@ -267,113 +268,150 @@ gdn_stream_kernel(const StepArgs p, const Sched sc, int nst)
 
     if (warp == kConsumerWarps) {
         // =========================== producer ===========================
-        // The warp prepares items 32 at a time: lane j loads item j's slots
-        // and gate inputs (independent loads, all in flight together) and
-        // computes its gates into a shared table; lane 0 then streams the
-        // batch: wait for a free stage, copy the item's metadata into it, issue
-        // the bulk copies.
+        // Items are prepared 32 at a time, one per lane: its slots and gate
+        // inputs (independent loads, in flight together) and then its gates.
+        // One lane streams the batch: for each item it waits for the item's
+        // stage, issues the bulk copies with their byte count (the first of two
+        // arrivals on "full") and writes the item's metadata (the second).  At
+        // the start the first nst items' copies go out as soon as their slots
+        // are known, before the gates are computed.
+        const int first_b = sc.first(blockIdx.x, gridDim.x);
+        int prev_r = -1, prev_g = -1; // the item before the batch
         bool stop = false;
+
+        // issue item k's copies into its stage (first arrival on "full")
+        auto issue = [&](int k, const Meta &q) -> bool {
+            const int s = k % nst;
+            if (!mbar_wait(empty_bar(s), (uint32_t)((k / nst) & 1) ^ 1u)) {
+                timeout();
+                return false;
+            }
+            if (*(volatile int *)&abort_flag)
+                return false;
+            unsigned char *st = stage(s);
+            const uint32_t fb = full_bar(s);
+            if (!q.live) {
+                mbar_arrive(fb);
+                return true;
+            }
+            const int r = q.r, h = q.h, chunk = q.chunk, rows = q.rows;
+            const int g = h / group;
+            const int cq = g * DK, ck = p.hk * DK + g * DK;
+            const int cv = 2 * p.hk * DK + h * p.dv + chunk * RB;
+            const int nqk = q.reuse ? 0 : 2 * DK; // q/k channels to copy
+            uint32_t bytes = (uint32_t)(rows * DK * 4);
+            if constexpr (LAYER)
+                bytes += (uint32_t)(((W - 1) + 1 + W + (p.bias ? 1 : 0)) * (nqk + rows) * E);
+            else
+                bytes += (uint32_t)((nqk + rows) * E);
+            mbar_arrive_tx(fb, bytes);
+            const float *src = p.pool + (((size_t)q.rs * p.hv + h) * p.dv + (size_t)chunk * RB) * DK;
+            bulk_load(sm_addr(st + L::STATE), src, (uint32_t)(rows * DK * 4), fb);
+            if constexpr (LAYER) {
+                const unsigned char *conv = reinterpret_cast<const unsigned char *>(p.conv);
+                const unsigned char *x = reinterpret_cast<const unsigned char *>(p.x);
+                const unsigned char *w = reinterpret_cast<const unsigned char *>(p.w);
+                const unsigned char *bias = reinterpret_cast<const unsigned char *>(p.bias);
+                const int off[3] = {0, DK, 2 * DK};
+                const int ch[3] = {cq, ck, cv};
+                const int n[3] = {DK, DK, rows};
+#pragma unroll
+                for (int sgm = 0; sgm < 3; ++sgm) {
+                    if (sgm < 2 && q.reuse)
+                        continue;
+#pragma unroll
+                    for (int jj = 0; jj < W - 1; ++jj)
+                        bulk_load(sm_addr(st + L::WIN + (jj * L::NCH + off[sgm]) * E),
+                                  conv + (((size_t)q.rs * (W - 1) + jj) * C + ch[sgm]) * E,
+                                  (uint32_t)(n[sgm] * E), fb);
+                    bulk_load(sm_addr(st + L::XS + off[sgm] * E), x + ((size_t)r * C + ch[sgm]) * E,
+                              (uint32_t)(n[sgm] * E), fb);
+                    bulk_load(sm_addr(st + L::WS + off[sgm] * W * E), w + (size_t)ch[sgm] * W * E,
+                              (uint32_t)(n[sgm] * W * E), fb);
+                    if (bias)
+                        bulk_load(sm_addr(st + L::BS + off[sgm] * E), bias + (size_t)ch[sgm] * E,
+                                  (uint32_t)(n[sgm] * E), fb);
+                }
+            } else {
+                const unsigned char *qp = reinterpret_cast<const unsigned char *>(p.q);
+                const unsigned char *kp = reinterpret_cast<const unsigned char *>(p.k);
+                const unsigned char *vp = reinterpret_cast<const unsigned char *>(p.v);
+                if (!q.reuse) {
+                    bulk_load(sm_addr(st + L::RAW), qp + ((size_t)r * p.hk + g) * DK * E, DK * E, fb);
+                    bulk_load(sm_addr(st + L::RAW + DK * E), kp + ((size_t)r * p.hk + g) * DK * E, DK * E, fb);
+                }
+                bulk_load(sm_addr(st + L::RAW + 2 * DK * E),
+                          vp + (((size_t)r * p.hv + h) * p.dv + (size_t)chunk * RB) * E, (uint32_t)(rows * E), fb);
+            }
+            return true;
+        };
+        // write item k's metadata (second arrival on "full")
+        auto publish = [&](int k, const Meta &q) {
+            unsigned char *st = stage(k % nst);
+            *reinterpret_cast<Meta *>(st + L::META) = q;
+            mbar_arrive(full_bar(k % nst));
+            issued_n = k + 1;
+        };
+
         for (int base = 0; base < n_items && !stop; base += 32) {
             const int kk = base + lane;
+            Meta q;
+            q.r = q.h = q.chunk = q.rs = q.ws = q.live = q.rows = q.reuse = 0;
+            q.alpha = q.beta = 0.f;
+            float av = 0.f, bv = 0.f, al = 0.f, dt = 0.f;
             if (kk < n_items) {
-                Meta q;
-                sc.item(blockIdx.x, gridDim.x, kk, q.r, q.h, q.chunk);
+                sc.item_at(first_b, kk, q.r, q.h, q.chunk);
                 q.rs = p.read_slot[q.r];
                 q.ws = p.in_place ? q.rs : p.write_slot[q.r];
-                const float av = ld_act<T>(p.a, (size_t)q.r * p.hv + q.h);
-                const float bv = ld_act<T>(p.b, (size_t)q.r * p.hv + q.h);
-                const float al = p.A_log[q.h], dt = p.dt_bias[q.h];
+                av = ld_act<T>(p.a, (size_t)q.r * p.hv + q.h);
+                bv = ld_act<T>(p.b, (size_t)q.r * p.hv + q.h);
+                al = p.A_log[q.h];
+                dt = p.dt_bias[q.h];
+            }
+            const int g = q.h / group;
+            int pr = __shfl_up_sync(0xffffffffu, q.r, 1), pg = __shfl_up_sync(0xffffffffu, g, 1);
+            if (lane == 0) {
+                pr = prev_r;
+                pg = prev_g;
+            }
+            prev_r = __shfl_sync(0xffffffffu, q.r, 31);
+            prev_g = __shfl_sync(0xffffffffu, g, 31);
+            if (kk < n_items) {
                 const int cls = classify_row(q.rs, q.ws, p.num_slots, p.in_place != 0);
                 if (cls < 0)
                     report(p.err, GDN_DEVERR_BAD_SLOT);
                 q.live = cls == 1;
                 q.rows = min(RB, p.dv - q.chunk * RB);
-                q.alpha = q.live ? gate_alpha(al, av, dt) : 0.f;
-                q.beta = q.live ? gate_beta(bv) : 0.f;
-                q.reuse = 0;
-                if (kk > 0) {
-                    int r0, h0, c0;
-                    sc.item(blockIdx.x, gridDim.x, kk - 1, r0, h0, c0);
-                    q.reuse = q.live && r0 == q.r && h0 / group == q.h / group;
-                }
-                table[lane] = q;
+                // a chain continues only through live items (liveness is per row)
+                q.reuse = q.live && kk > 0 && pr == q.r && pg == g;
+            }
+            const int nb = min(32, n_items - base);
+            table[lane] = q; // everything but the gates
+            __syncwarp();
+            // start-up: the first stages' copies go out before the gates are computed
+            const int early = base == 0 ? min(nst, nb) : 0;
+            if (lane == 0) {
+                for (int j = 0; j < early; ++j)
+                    if (!issue(j, table[j])) {
+                        stop = true;
+                        break;
+                    }
+            }
+            if (q.live) {
+                table[lane].alpha = gate_alpha(al, av, dt);
+                table[lane].beta = gate_beta(bv);
             }
             __syncwarp();
-            if (lane == 0) {
-                const int nb = min(32, n_items - base);
-                for (int j = 0; j < nb; ++j) {
-                    const int k = base + j;
-                    const int s = k % nst;
-                    if (!mbar_wait(empty_bar(s), (uint32_t)((k / nst) & 1) ^ 1u)) {
-                        timeout();
+            if (lane == 0 && !stop) {
+                for (int j = 0; j < early; ++j)
+                    publish(base + j, table[j]);
+                for (int j = early; j < nb; ++j) {
+                    const Meta qq = table[j];
+                    if (!issue(base + j, qq)) {
                         stop = true;
                         break;
                     }
-                    if (*(volatile int *)&abort_flag) {
-                        stop = true;
-                        break;
-                    }
-                    const Meta q = table[j];
-                    unsigned char *st = stage(s);
-                    *reinterpret_cast<Meta *>(st + L::META) = q;
-                    const uint32_t fb = full_bar(s);
-                    if (q.live) {
-                        const int r = q.r, h = q.h, chunk = q.chunk, rows = q.rows;
-                        const int g = h / group;
-                        const int cq = g * DK, ck = p.hk * DK + g * DK;
-                        const int cv = 2 * p.hk * DK + h * p.dv + chunk * RB;
-                        const int nqk = q.reuse ? 0 : 2 * DK; // q/k channels to copy
-                        uint32_t bytes = (uint32_t)(rows * DK * 4);
-                        if constexpr (LAYER)
-                            bytes += (uint32_t)(((W - 1) + 1 + W + (p.bias ? 1 : 0)) * (nqk + rows) * E);
-                        else
-                            bytes += (uint32_t)((nqk + rows) * E);
-                        mbar_arrive_tx(fb, bytes);
-                        const float *src =
-                            p.pool + (((size_t)q.rs * p.hv + h) * p.dv + (size_t)chunk * RB) * DK;
-                        bulk_load(sm_addr(st + L::STATE), src, (uint32_t)(rows * DK * 4), fb);
-                        if constexpr (LAYER) {
-                            const unsigned char *conv = reinterpret_cast<const unsigned char *>(p.conv);
-                            const unsigned char *x = reinterpret_cast<const unsigned char *>(p.x);
-                            const unsigned char *w = reinterpret_cast<const unsigned char *>(p.w);
-                            const unsigned char *bias = reinterpret_cast<const unsigned char *>(p.bias);
-                            const int off[3] = {0, DK, 2 * DK};
-                            const int ch[3] = {cq, ck, cv};
-                            const int n[3] = {DK, DK, rows};
-#pragma unroll
-                            for (int sgm = 0; sgm < 3; ++sgm) {
-                                if (sgm < 2 && q.reuse)
-                                    continue;
-#pragma unroll
-                                for (int jj = 0; jj < W - 1; ++jj)
-                                    bulk_load(sm_addr(st + L::WIN + (jj * L::NCH + off[sgm]) * E),
-                                              conv + (((size_t)q.rs * (W - 1) + jj) * C + ch[sgm]) * E,
-                                              (uint32_t)(n[sgm] * E), fb);
-                                bulk_load(sm_addr(st + L::XS + off[sgm] * E), x + ((size_t)r * C + ch[sgm]) * E,
-                                          (uint32_t)(n[sgm] * E), fb);
-                                bulk_load(sm_addr(st + L::WS + off[sgm] * W * E), w + (size_t)ch[sgm] * W * E,
-                                          (uint32_t)(n[sgm] * W * E), fb);
-                                if (bias)
-                                    bulk_load(sm_addr(st + L::BS + off[sgm] * E), bias + (size_t)ch[sgm] * E,
-                                              (uint32_t)(n[sgm] * E), fb);
-                            }
-                        } else {
-                            const unsigned char *qp = reinterpret_cast<const unsigned char *>(p.q);
-                            const unsigned char *kp = reinterpret_cast<const unsigned char *>(p.k);
-                            const unsigned char *vp = reinterpret_cast<const unsigned char *>(p.v);
-                            if (!q.reuse) {
-                                bulk_load(sm_addr(st + L::RAW), qp + ((size_t)r * p.hk + g) * DK * E, DK * E, fb);
-                                bulk_load(sm_addr(st + L::RAW + DK * E), kp + ((size_t)r * p.hk + g) * DK * E,
-                                          DK * E, fb);
-                            }
-                            bulk_load(sm_addr(st + L::RAW + 2 * DK * E),
-                                      vp + (((size_t)r * p.hv + h) * p.dv + (size_t)chunk * RB) * E,
-                                      (uint32_t)(rows * E), fb);
-                        }
-                    } else {
-                        mbar_arrive(fb);
-                    }
-                    issued_n = k + 1;
+                    publish(base + j, qq);
                 }
             }
             stop = __shfl_sync(0xffffffffu, stop, 0);
