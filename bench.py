@@ -169,7 +169,7 @@ def max_over_ranks(x: float, device=None) -> float:
     return float(t.item())
 
 
-def build_sets(G, I, s, device, nsets):
+def build_sets(G, I, s, device, nsets, pad_frac=0.0):
     import torch
     sets = []
     for i in range(nsets):
@@ -191,15 +191,166 @@ def build_sets(G, I, s, device, nsets):
             "b": I.to_torch(inp["b"], dt, device),
             "out": torch.empty((s.rows, s.hv, s.dv), dtype=I.torch_dtype(dt), device=device),
         }
-        rs, ws = gen.slot_tables(s.rows, s.num_slots)
+        rs, ws = gen.slot_tables(s.rows, s.num_slots, pad_frac)
         st["rs"] = torch.from_numpy(rs).to(device)
         st["ws"] = torch.from_numpy(ws).to(device)
         st["layer"] = G.prepare_layer_decode(st["x"], st["cp"], st["w"], st["bias"], st["A_log"],
                                              st["dt_bias"], st["a"], st["b"], st["pool"], st["rs"], st["ws"],
                                              st["out"])
+        st["layer_ip"] = G.prepare_layer_decode(st["x"], st["cp"], st["w"], st["bias"], st["A_log"],
+                                                st["dt_bias"], st["a"], st["b"], st["pool"], st["rs"], None,
+                                                st["out"], keep_in_place=True)
         st["commit"] = G.prepare_commit(st["rs"], st["ws"])
         sets.append(st)
     return sets
+
+
+def time_calls(calls, n, device):
+    """Mean µs per call of `n` back-to-back calls cycling through `calls`."""
+    import torch
+    stream = torch.cuda.current_stream(device)
+    for i in range(2 * len(calls)):
+        calls[i % len(calls)]()
+    torch.cuda.synchronize(device)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(n):
+        calls[i % len(calls)]()
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    return a.elapsed_time(b) * 1e3 / n
+
+
+def run_extras(G, I, device, n=400):
+    """The other workloads, timed on the same terms (four instances in rotation,
+    back-to-back launches): the rows x write-mode sweep, the 9B-shaped GQA layer
+    and the 18-layer decode stack (eager and CUDA-graph replay)."""
+    import torch
+    res = {}
+    sweep = {}
+    for rows in I.SWEEP_ROWS:
+        sh = I.QWEN_08B.with_(rows=rows, num_slots=I.SWEEP_SLOTS)
+        sets = build_sets(G, I, sh, device, NSETS, pad_frac=0.25)
+        real = rows - int(math.floor(0.25 * rows))
+        nb = layer_bytes(sh, real)
+        tw = time_calls([st["layer"] for st in sets], n, device)
+        ip = time_calls([st["layer_ip"] for st in sets], n, device)
+        sweep[str(rows)] = {"real_rows": real, "twin_us": round(tw, 2), "in_place_us": round(ip, 2),
+                            "twin_GBs": round(nb / tw / 1e3, 1), "in_place_GBs": round(nb / ip / 1e3, 1)}
+        del sets
+        torch.cuda.empty_cache()
+    res["sweep_rows_write_mode"] = {"workload": "0.8B-shaped fused layer, 25% padding rows on the null "
+                                                "slot, 513-slot pools, twin vs in place", "rows": sweep}
+    gqa = {}
+    for rows in (64, 256):
+        sh = I.QWEN_9B.with_(rows=rows, num_slots=2 * rows + 1)
+        sets = build_sets(G, I, sh, device, NSETS)
+        nb = layer_bytes(sh, rows)
+        tw = time_calls([st["layer"] for st in sets], n // 2, device)
+        gqa[str(rows)] = {"twin_us": round(tw, 2), "GBs": round(nb / tw / 1e3, 1),
+                          "frac_of_measured_peak": round(nb / tw / 1e3 / hbm_peak()[0], 4)}
+        del sets
+        torch.cuda.empty_cache()
+    res["qwen9b_gqa"] = {"workload": "9B-shaped fused layer: 16 qk / 32 v heads, 2R+1 slots, twin",
+                         "rows": gqa}
+    res["decode_stack"] = run_stack(G, I, device)
+    return res
+
+
+def run_stack(G, I, device, layers=18, steps=64):
+    """18 fused layers of the 0.8B shape per step, 128 rows with 10% padding,
+    257-slot pools per layer, one commit per step, the rows' request order
+    re-permuted (a 1 KB host-to-device table copy) every 16 steps."""
+    import numpy as np
+    import torch
+    s = I.STACK
+    gen = I.Gen(77)
+    # everything runs on one stream, which the graph capture also uses (the
+    # prepared calls are bound to the stream current when they are prepared)
+    stream = torch.cuda.Stream(device)
+    stream.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(stream):
+        return _run_stack(G, I, device, s, gen, stream, layers, steps)
+
+
+def _run_stack(G, I, device, s, gen, stream, layers, steps):
+    import numpy as np
+    import torch
+    dt = s.dtype
+    Ls = []
+    for _ in range(layers):
+        prm = gen.params(s)
+        inp = gen.layer_inputs(s)
+        Ls.append({
+            "pool": G.GDNStatePool(s.num_slots, s.hk, s.hv, s.dk, s.dv, device=device,
+                                   tensor=torch.from_numpy(gen.state_pool(s)).to(device)),
+            "cp": G.ConvStatePool(s.num_slots, s.channels, s.width, dtype=I.torch_dtype(dt), device=device,
+                                  tensor=I.to_torch(gen.conv_pool(s), dt, device)),
+            "w": I.to_torch(prm["w"], dt, device), "bias": I.to_torch(prm["bias"], dt, device),
+            "A_log": I.to_torch(prm["A_log"], "f32", device), "dt_bias": I.to_torch(prm["dt_bias"], "f32", device),
+            "x": I.to_torch(inp["x"], dt, device), "a": I.to_torch(inp["a"], dt, device),
+            "b": I.to_torch(inp["b"], dt, device),
+            "out": torch.empty((s.rows, s.hv, s.dv), dtype=I.torch_dtype(dt), device=device)})
+    n_real = s.rows - int(0.10 * s.rows)
+    perm = gen.rng.permutation(np.arange(1, s.num_slots, dtype=np.int32))
+    req = [perm[:n_real].copy(), perm[n_real:2 * n_real].copy()]
+    rs = torch.zeros(s.rows, dtype=torch.int32, device=device)
+    ws = torch.zeros(s.rows, dtype=torch.int32, device=device)
+    tables = []
+    for k in range(steps // 16 + 1):  # pinned host tables for each re-permutation
+        pos = gen.rng.permutation(s.rows)[:n_real]
+        order = gen.rng.permutation(n_real)
+        tr = np.zeros(s.rows, np.int32)
+        tw = np.zeros(s.rows, np.int32)
+        # after 16 steps (an even number of commits) every request is back on its first slot
+        tr[pos] = req[0][order]
+        tw[pos] = req[1][order]
+        tables.append((torch.from_numpy(tr).pin_memory(), torch.from_numpy(tw).pin_memory()))
+    calls = [G.prepare_layer_decode(L["x"], L["cp"], L["w"], L["bias"], L["A_log"], L["dt_bias"], L["a"], L["b"],
+                                    L["pool"], rs, ws, L["out"]) for L in Ls]
+    commit = G.prepare_commit(rs, ws)
+
+    def one_step():
+        for c in calls:
+            c()
+        commit()
+
+    def run(replay):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(steps):
+            if i % 16 == 0:
+                tr, tw = tables[i // 16]
+                rs.copy_(tr, non_blocking=True)
+                ws.copy_(tw, non_blocking=True)
+            replay()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        return a.elapsed_time(b) * 1e3 / steps
+
+    rs.copy_(tables[0][0])
+    ws.copy_(tables[0][1])
+    one_step()
+    torch.cuda.synchronize(device)
+    eager_us = run(one_step)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        one_step()
+    torch.cuda.synchronize(device)
+    graph_us = run(g.replay)
+    step_bytes = layers * layer_bytes(s, n_real) + commit_bytes(s.rows)
+    if G.get_device_error(device) != 0:
+        raise RuntimeError("device error in the decode stack")
+    res = {"workload": f"{layers} fused layers (0.8B shape) per step, {s.rows} rows with 10% padding, "
+                       f"{s.num_slots}-slot pools, commit per step, re-permuted every 16 steps, {steps} steps",
+           "eager_us_per_step": round(eager_us, 1), "graph_us_per_step": round(graph_us, 1),
+           "eager_GBs": round(step_bytes / eager_us / 1e3, 1), "graph_GBs": round(step_bytes / graph_us / 1e3, 1),
+           "us_per_layer_graph": round(graph_us / layers, 2)}
+    del Ls, calls, g
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_ours(args, rank, world, device):
@@ -274,6 +425,9 @@ def run_ours(args, rank, world, device):
     # end to end through host buffers: inputs in pinned memory, output read back
     e2e = run_e2e(G, I, s, sets, device, min(K, 2000), step_bytes)
     probes = run_probes(G, s, sets, device, min(K, 2000))
+    del sets
+    torch.cuda.empty_cache()
+    extras = run_extras(G, I, device) if not args.no_extras else {}
 
     res = {
         "metric": METRIC,
@@ -319,6 +473,7 @@ def run_ours(args, rank, world, device):
         },
         "e2e": e2e,
         "probes": probes,
+        **extras,
         "gpu_launches": 2 * K,
         "clocks": clk,
     }
@@ -494,6 +649,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=100)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="omit the sweep, 9B and decode-stack workloads (reported beside the headline)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
