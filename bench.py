@@ -90,9 +90,10 @@ def recorded_traffic():
         fields = {}
         with open(TRAFFIC_SUMMARY) as f:
             for line in f:
-                if ":" in line and line.strip().startswith(("traffic_per_launch_bytes", "source_sha256")):
-                    k, v = line.split(":", 1)
-                    fields[k.strip().strip("-* `")] = v.strip().strip("` ")
+                key = line.strip().lstrip("-* `")
+                if ":" in key and key.startswith(("traffic_per_launch_bytes", "source_sha256")):
+                    k, v = key.split(":", 1)
+                    fields[k.strip().strip("`")] = v.strip().strip("` ")
         if fields.get("source_sha256") != kernel_source_sha():
             return None
         return int(fields["traffic_per_launch_bytes"])

@@ -53,3 +53,18 @@ def test_bench_byte_model():
     assert state == 134217728
     assert state < b < state * 1.06          # conv, vectors and parameters add under 6%
     assert bench.layer_bytes(s, 0) < 0.01 * state   # padding rows move no state
+
+
+def test_recorded_traffic_follows_kernel_source(tmp_path, monkeypatch):
+    """The roofline's traffic figure is read from the ncu summary only while
+    the summary's source hash matches the kernel sources."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    sha = bench.kernel_source_sha()
+    p = tmp_path / "summary.md"
+    p.write_text(f"text\n\n- traffic_per_launch_bytes: 1234\n- source_sha256: {sha}\n")
+    monkeypatch.setattr(bench, "TRAFFIC_SUMMARY", str(p))
+    assert bench.recorded_traffic() == 1234
+    p.write_text("- traffic_per_launch_bytes: 1234\n- source_sha256: " + "0" * 64 + "\n")
+    assert bench.recorded_traffic() is None
