@@ -30,6 +30,8 @@ GDN_PROBE_INPLACE = 1
 GDN_PROBE_READ = 2
 GDN_PROBE_WRITE = 3
 
+GDN_MAX_POOLS = 4096
+
 # Every symbol the header declares (the export test checks this list against
 # include/gdn_decode.h).
 EXPORTS = [

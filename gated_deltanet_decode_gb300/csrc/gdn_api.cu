@@ -83,6 +83,65 @@ int device_error_ptr(int **out)
 } // namespace
 
 // ---------------------------------------------------------------------------
+// Work counters of the state kernels.  Each state pool handle holds one pair
+// (the next unit to claim, producers done) in this table, handed out on the
+// host when the handle is made, so no call allocates device memory for it.
+// The kernels leave a pair at zero when their launch ends; the table starts
+// at zero when the module loads.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned int g_work[GDN_MAX_POOLS][2];
+
+namespace {
+
+std::mutex g_work_mu;
+std::vector<int> g_work_free;
+int g_work_next = 0;
+unsigned int *g_work_addr[kMaxDevices] = {};
+
+int work_index_take(int *index)
+{
+    std::lock_guard<std::mutex> lk(g_work_mu);
+    if (!g_work_free.empty()) {
+        *index = g_work_free.back();
+        g_work_free.pop_back();
+        return GDN_OK;
+    }
+    if (g_work_next >= GDN_MAX_POOLS)
+        return fail(GDN_ENOMEM, "more than %d state pools alive at once", GDN_MAX_POOLS);
+    *index = g_work_next++;
+    return GDN_OK;
+}
+
+void work_index_give(int index)
+{
+    std::lock_guard<std::mutex> lk(g_work_mu);
+    g_work_free.push_back(index);
+}
+
+// Device address of the pool's counter pair on the current device.
+int work_ptr(const gdn_pool *pool, unsigned int **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(GDN_EUNSUPPORTED, "device ordinal %d beyond %d", dev, kMaxDevices);
+    std::lock_guard<std::mutex> lk(g_work_mu);
+    if (!g_work_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_work);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress(work counters)");
+        g_work_addr[dev] = static_cast<unsigned int *>(p);
+    }
+    *out = g_work_addr[dev] + 2 * (size_t)pool->work_index;
+    return GDN_OK;
+}
+
+} // namespace
+
+// ---------------------------------------------------------------------------
 // small kernels
 // ---------------------------------------------------------------------------
 namespace {
@@ -224,7 +283,13 @@ int gdn_state_pool_create(int num_slots, gdn_dims dims, void *stream, gdn_pool *
         cudaFree(p);
         return cuda_fail(e, "zero-filling the state pool");
     }
-    *out = new gdn_pool{static_cast<float *>(p), num_slots, dims, true};
+    int wi = 0;
+    rc = work_index_take(&wi);
+    if (rc) {
+        cudaFree(p);
+        return rc;
+    }
+    *out = new gdn_pool{static_cast<float *>(p), num_slots, dims, true, wi};
     return ok();
 }
 
@@ -242,7 +307,11 @@ int gdn_state_pool_wrap(void *dev_ptr, int num_slots, gdn_dims dims, gdn_pool **
     int rc = check_dims(dims);
     if (rc)
         return rc;
-    *out = new gdn_pool{static_cast<float *>(dev_ptr), num_slots, dims, false};
+    int wi = 0;
+    rc = work_index_take(&wi);
+    if (rc)
+        return rc;
+    *out = new gdn_pool{static_cast<float *>(dev_ptr), num_slots, dims, false, wi};
     return ok();
 }
 
@@ -253,6 +322,7 @@ int gdn_state_pool_destroy(gdn_pool *pool)
     cudaError_t e = cudaSuccess;
     if (pool->owned)
         e = cudaFree(pool->data);
+    work_index_give(pool->work_index);
     delete pool;
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaFree(state pool)");
@@ -494,6 +564,9 @@ int gdn_decode_step(const void *q, const void *k, const void *v, const void *a, 
     s.dk = pool->dims.dk;
     s.dv = pool->dims.dv;
     s.err = err;
+    rc = work_ptr(pool, &s.work);
+    if (rc)
+        return rc;
     cudaError_t e = gdn::launch_gdn_step(s, dtype, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "gdn_decode_step launch");
@@ -555,6 +628,9 @@ int gdn_layer_decode(const void *x, conv_pool *cp, const void *w, const void *bi
     s.silu = silu ? 1 : 0;
     s.width = cp->width;
     s.channels = C;
+    rc = work_ptr(pool, &s.work);
+    if (rc)
+        return rc;
     cudaError_t e = gdn::launch_gdn_layer(s, dtype, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "gdn_layer_decode launch");

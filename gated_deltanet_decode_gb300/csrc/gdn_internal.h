@@ -12,6 +12,7 @@ struct gdn_pool {
     int num_slots;
     gdn_dims dims;
     bool owned;
+    int work_index; // this pool's pair of work counters in the library's table
 };
 
 struct conv_pool {
@@ -40,6 +41,7 @@ struct StepArgs {
     void *out;
     int rows, hk, hv, dk, dv;
     int *err;
+    unsigned int *work; // the pool's two work counters (claim, producers done), zero between launches
     // fused layer only
     const void *x;
     void *conv;        // conv pool data

@@ -61,6 +61,7 @@ constexpr float kL2Eps = 1e-6f;
 constexpr long long kWaitLimit = 1ll << 20;
 constexpr uint32_t kSuspendHintNs = 1000;
 constexpr int kMaxStages = 8;
+constexpr int kClaimMinItemsPerCta = 12;
 
 // warps 0-7 consume, warp 8 produces, warp 9 computes v (fused layer only)
 template <bool LAYER> constexpr int threads_for() { return kConsumers + 32 + (LAYER ? 32 : 0); }
@@ -182,34 +183,36 @@ struct Meta {
     float alpha, beta;
 };
 
-// Contiguous ranges: CTA b of g takes units [first(b), first(b + 1)),
-// balanced to within one unit.  Fine: a unit is an item.  Coarse: a unit is
-// a whole qk group (group value heads x row chunks), its items in order.
+// Work units, in (row, value head, chunk) order.  Fine: a unit is an item.
+// Coarse: a unit is a whole qk group (group value heads x row chunks), its
+// items in order.  The first n_static units are split into contiguous ranges,
+// CTA b of g taking [first(b), first(b + 1)) (equal to within one unit); the
+// rest are claimed `claim` units at a time from the pool's work counter by
+// whichever CTA runs out first, so that CTAs that stream slower take less of
+// the tail.
 struct Sched {
     int hv, group, chunks;
     int n_units;
     int per_unit;    // 1 (fine) or group * chunks (coarse)
     int coarse;
+    int n_static;    // units split statically (n_units: no claims)
+    int claim;       // units per claim
 
     __device__ __forceinline__ int first(int b, int g) const
     {
-        return (int)(((long long)n_units * b) / g);
+        return (int)(((long long)n_static * b) / g);
     }
-    __device__ __forceinline__ int count(int b, int g) const
+    // item i of the whole launch
+    __device__ __forceinline__ void item_at(int i, int &r, int &h, int &chunk) const
     {
-        return (first(b + 1, g) - first(b, g)) * per_unit;
-    }
-    // k-th item of the CTA whose range starts at unit `first_unit`
-    __device__ __forceinline__ void item_at(int first_unit, int k, int &r, int &h, int &chunk) const
-    {
-        const int unit = first_unit + k / per_unit;
+        const int unit = i / per_unit;
         if (!coarse) {
             chunk = unit % chunks;
             const int rh = unit / chunks;
             h = rh % hv;
             r = rh / hv;
         } else {
-            const int j = k % per_unit;
+            const int j = i % per_unit;
             const int hk = hv / group;
             r = unit / hk;
             h = (unit % hk) * group + j / chunks;
@@ -218,12 +221,20 @@ struct Sched {
     }
 };
 
+// Stages a CTA holds: as many as fit beside the other CTAs of its SM.
+template <typename T, int DK, bool LAYER, int W> struct Stages {
+    static constexpr int fit = ((227 * 1024) / ctas_per_sm<LAYER>() - 4096) / Stage<T, DK, LAYER, W>::BYTES;
+    static constexpr int value = fit > kMaxStages ? kMaxStages : fit;
+    static_assert(value >= 2, "a stage ring needs two stages");
+};
+
 template <typename T, int DK, bool LAYER, int W>
 __global__ void __launch_bounds__(threads_for<LAYER>(), ctas_per_sm<LAYER>())
-gdn_stream_kernel(const StepArgs p, const Sched sc, int nst)
+gdn_stream_kernel(const StepArgs p, const Sched sc)
 {
     using G = Geo<DK>;
     using L = Stage<T, DK, LAYER, W>;
+    constexpr int nst = Stages<T, DK, LAYER, W>::value;
     constexpr int RB = G::RB;
     constexpr int E = L::E;
 
@@ -264,18 +275,22 @@ gdn_stream_kernel(const StepArgs p, const Sched sc, int nst)
 
     const int C = p.channels;
     const int group = p.hv / p.hk;
-    const int n_items = sc.count(blockIdx.x, gridDim.x);
 
     if (warp == kConsumerWarps) {
         // =========================== producer ===========================
-        // Items are prepared 32 at a time, one per lane: its slots and gate
-        // inputs (independent loads, in flight together) and then its gates.
-        // One lane streams the batch: for each item it waits for the item's
-        // stage, issues the bulk copies with their byte count (the first of two
-        // arrivals on "full") and writes the item's metadata (the second).  At
-        // the start the first nst items' copies go out as soon as their slots
-        // are known, before the gates are computed.
-        const int first_b = sc.first(blockIdx.x, gridDim.x);
+        // Items are prepared up to 32 at a time, one per lane: its slots and
+        // gate inputs (independent loads, in flight together) and then its
+        // gates.  One lane streams the batch: for each item it waits for the
+        // item's stage, issues the bulk copies with their byte count (the
+        // first of two arrivals on "full") and writes the item's metadata (the
+        // second).  At the start the first nst items' copies go out as soon as
+        // their slots are known, before the gates are computed.  The CTA's
+        // static range comes first, then claimed ranges; a metadata-only
+        // stage with live = -1 ends the stream.
+        int lo = sc.first(blockIdx.x, gridDim.x) * sc.per_unit; // items [lo, hi) to do next
+        int hi = sc.first(blockIdx.x + 1, gridDim.x) * sc.per_unit;
+        const bool claims = sc.n_static < sc.n_units;
+        int kdone = 0;                // items issued so far
         int prev_r = -1, prev_g = -1; // the item before the batch
         bool stop = false;
 
@@ -353,14 +368,28 @@ gdn_stream_kernel(const StepArgs p, const Sched sc, int nst)
             issued_n = k + 1;
         };
 
-        for (int base = 0; base < n_items && !stop; base += 32) {
-            const int kk = base + lane;
+        while (!stop) {
+            if (lo >= hi) {
+                if (!claims)
+                    break;
+                int u = 0;
+                if (lane == 0)
+                    u = (int)atomicAdd(p.work, (unsigned)sc.claim);
+                u = __shfl_sync(0xffffffffu, u, 0) + sc.n_static;
+                if (u >= sc.n_units)
+                    break;
+                lo = u * sc.per_unit;
+                hi = min(u + sc.claim, sc.n_units) * sc.per_unit;
+            }
+            const int nb = min(32, hi - lo);
+            const int base = kdone;
+            const bool valid = lane < nb;
             Meta q;
             q.r = q.h = q.chunk = q.rs = q.ws = q.live = q.rows = q.reuse = 0;
             q.alpha = q.beta = 0.f;
             float av = 0.f, bv = 0.f, al = 0.f, dt = 0.f;
-            if (kk < n_items) {
-                sc.item_at(first_b, kk, q.r, q.h, q.chunk);
+            if (valid) {
+                sc.item_at(lo + lane, q.r, q.h, q.chunk);
                 q.rs = p.read_slot[q.r];
                 q.ws = p.in_place ? q.rs : p.write_slot[q.r];
                 av = ld_act<T>(p.a, (size_t)q.r * p.hv + q.h);
@@ -374,18 +403,17 @@ gdn_stream_kernel(const StepArgs p, const Sched sc, int nst)
                 pr = prev_r;
                 pg = prev_g;
             }
-            prev_r = __shfl_sync(0xffffffffu, q.r, 31);
-            prev_g = __shfl_sync(0xffffffffu, g, 31);
-            if (kk < n_items) {
+            prev_r = __shfl_sync(0xffffffffu, q.r, nb - 1);
+            prev_g = __shfl_sync(0xffffffffu, g, nb - 1);
+            if (valid) {
                 const int cls = classify_row(q.rs, q.ws, p.num_slots, p.in_place != 0);
                 if (cls < 0)
                     report(p.err, GDN_DEVERR_BAD_SLOT);
                 q.live = cls == 1;
                 q.rows = min(RB, p.dv - q.chunk * RB);
                 // a chain continues only through live items (liveness is per row)
-                q.reuse = q.live && kk > 0 && pr == q.r && pg == g;
+                q.reuse = q.live && pr == q.r && pg == g;
             }
-            const int nb = min(32, n_items - base);
             table[lane] = q; // everything but the gates
             __syncwarp();
             // start-up: the first stages' copies go out before the gates are computed
@@ -416,11 +444,39 @@ gdn_stream_kernel(const StepArgs p, const Sched sc, int nst)
             }
             stop = __shfl_sync(0xffffffffu, stop, 0);
             __syncwarp();
+            kdone += nb;
+            lo += nb;
+        }
+        // This CTA makes no more claims.  The last CTA to get here resets the
+        // counters for the pool's next launch: every other CTA has counted
+        // itself done after its last claim.
+        if (claims && lane == 0) {
+            __threadfence();
+            if (atomicAdd(p.work + 1, 1u) == gridDim.x - 1) {
+                atomicExch(p.work, 0u);
+                atomicExch(p.work + 1, 0u);
+            }
+        }
+        // end of the stream
+        if (lane == 0 && !stop) {
+            const int s = kdone % nst;
+            if (!mbar_wait(empty_bar(s), (uint32_t)((kdone / nst) & 1) ^ 1u)) {
+                timeout();
+            } else {
+                Meta e;
+                e.r = e.h = e.chunk = e.rs = e.ws = e.rows = e.reuse = 0;
+                e.live = -1;
+                e.alpha = e.beta = 0.f;
+                *reinterpret_cast<Meta *>(stage(s) + L::META) = e;
+                mbar_arrive(full_bar(s)); // both arrivals: no copies
+                mbar_arrive(full_bar(s));
+                issued_n = kdone + 1;
+            }
         }
     } else if (LAYER && warp == kConsumerWarps + 1) {
         // =========================== v warp =============================
         if constexpr (LAYER) {
-            for (int k = 0; k < n_items; ++k) {
+            for (int k = 0;; ++k) {
                 const int s = k % nst;
                 if (!mbar_wait(full_bar(s), (uint32_t)((k / nst) & 1))) {
                     timeout();
@@ -428,6 +484,8 @@ gdn_stream_kernel(const StepArgs p, const Sched sc, int nst)
                 }
                 unsigned char *st = stage(s);
                 const Meta m = *reinterpret_cast<const Meta *>(st + L::META);
+                if (m.live < 0)
+                    break; // end of the stream
                 if (m.live) {
                     float *vn = reinterpret_cast<float *>(st + L::VN);
                     T *wout = reinterpret_cast<T *>(p.conv) + (size_t)m.ws * (W - 1) * C;
@@ -465,7 +523,7 @@ gdn_stream_kernel(const StepArgs p, const Sched sc, int nst)
         int chains = 0;                // chains started so far
         int qkb = 0;                   // buffer of the current chain
         float inv_q = 0.f, inv_k = 0.f, kappa = 0.f;
-        for (int k = 0; k < n_items; ++k) {
+        for (int k = 0;; ++k) {
             const int s = k % nst;
             const uint32_t par = (uint32_t)((k / nst) & 1);
             if (!mbar_wait(full_bar(s), par)) {
@@ -474,6 +532,8 @@ gdn_stream_kernel(const StepArgs p, const Sched sc, int nst)
             }
             unsigned char *st = stage(s);
             const Meta m = *reinterpret_cast<const Meta *>(st + L::META);
+            if (m.live < 0)
+                break; // end of the stream
             T *out = reinterpret_cast<T *>(p.out) + ((size_t)m.r * p.hv + m.h) * p.dv + (size_t)m.chunk * RB;
             if (m.live) {
                 if (!m.reuse) {
@@ -570,11 +630,19 @@ gdn_stream_kernel(const StepArgs p, const Sched sc, int nst)
                 const float *srow = reinterpret_cast<const float *>(st + L::STATE) + row * DK + 4 * lcol;
                 float4 kh[4], qh[4], sv[4];
 #pragma unroll
+                for (int mm = 0; mm < 4; ++mm)
+                    sv[mm] = *reinterpret_cast<const float4 *>(srow + 4 * G::LPR * mm);
+                // The warp has all it needs from the stage (state row, v, metadata;
+                // q/k values live outside the stages): release it before the math and
+                // the stores, so its next copy starts sooner.
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(empty_bar(s));
+#pragma unroll
                 for (int mm = 0; mm < 4; ++mm) {
                     const int j = 4 * (lcol + G::LPR * mm);
                     qh[mm] = *reinterpret_cast<const float4 *>(&kq[j]);
                     kh[mm] = *reinterpret_cast<const float4 *>(&kq[DK + j]);
-                    sv[mm] = *reinterpret_cast<const float4 *>(srow + 4 * G::LPR * mm);
                 }
                 // u = S . k and w = S . q on the raw values; the shuffles need the
                 // whole warp, so every lane reduces and only real rows are stored
@@ -617,10 +685,10 @@ gdn_stream_kernel(const StepArgs p, const Sched sc, int nst)
                 // padding or bad row: zero outputs, no slot touched
                 if (t < m.rows)
                     out[t] = from_f<T>(0.f);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(empty_bar(s));
             }
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(empty_bar(s));
             if (t == 0)
                 consumed_n = k + 1;
         }
@@ -673,12 +741,7 @@ cudaError_t launch_stream(const StepArgs &a, bool coarse, cudaStream_t s)
         return cudaSuccess;
     // ctas_per_sm CTAs per SM, each with as many stages as fit
     constexpr int kCtas = ctas_per_sm<LAYER>();
-    const int max_smem = (227 * 1024) / kCtas - 4096;
-    int nst = max_smem / L::BYTES;
-    nst = nst > kMaxStages ? kMaxStages : nst;
-    if (nst < 2)
-        return cudaErrorInvalidConfiguration;
-    const size_t smem = (size_t)nst * L::BYTES;
+    const size_t smem = (size_t)Stages<T, DK, LAYER, W>::value * L::BYTES;
     auto kern = gdn_stream_kernel<T, DK, LAYER, W>;
     static unsigned long long configured = 0; // one bit per device, per instantiation
     int dev = 0;
@@ -692,7 +755,15 @@ cudaError_t launch_stream(const StepArgs &a, bool coarse, cudaStream_t s)
     }
     const int slots = kCtas * num_sms();
     const int grid = (int)(sc.n_units < slots ? sc.n_units : slots);
-    return launch_pdl(kern, dim3(grid), dim3(threads_for<LAYER>()), smem, s, a, sc, nst);
+    // With a dozen or more items a CTA, half of the units are claimed at run
+    // time, a (row, value head) of fine items (or one coarse unit) a claim;
+    // with fewer, the claims' latency costs more than the balance they buy
+    // (measured on the 0.8B and 9B layer shapes at 16 to 256 rows).
+    sc.claim = coarse ? 1 : (sc.chunks < 4 ? sc.chunks : 4);
+    sc.n_static = sc.n_units;
+    if (items >= (long long)kClaimMinItemsPerCta * grid && a.work)
+        sc.n_static = sc.n_units / 2 / sc.claim * sc.claim;
+    return launch_pdl(kern, dim3(grid), dim3(threads_for<LAYER>()), smem, s, a, sc);
 }
 
 template <typename T, bool LAYER, int W>

@@ -52,6 +52,12 @@
  *  - Preconditions not checked on the fast path: real rows name distinct
  *    write slots, and no row writes a slot another row reads.
  *    gdn_validate_slots() checks them (it synchronises).
+ *  - Launches of gdn_decode_step / gdn_layer_decode that use the same state
+ *    pool must not overlap on the GPU: issue them on one stream, or order
+ *    them with events.  Each pool handle owns a pair of work counters that
+ *    its launches share (the kernels hand out the tail of their work through
+ *    them and leave them at zero when they end); overlapping launches on one
+ *    pool race on that pair.  Launches on different pools may overlap.
  */
 #ifndef GDN_DECODE_H
 #define GDN_DECODE_H
@@ -74,6 +80,9 @@ extern "C" {
 #define GDN_DEVERR_NONE 0
 #define GDN_DEVERR_BAD_SLOT 1 /* some row named a slot outside the pool */
 #define GDN_DEVERR_TIMEOUT 2  /* a bounded wait inside a kernel ran out; its CTA stopped */
+
+/* ---- limits ------------------------------------------------------------ */
+#define GDN_MAX_POOLS 4096 /* state pool handles alive at once, per process */
 
 /* ---- activation dtypes ------------------------------------------------ */
 #define GDN_F32 0
@@ -108,8 +117,12 @@ int gdn_abi_version(void);
  * for it); the library owns the memory and frees it in
  * gdn_state_pool_destroy.  Returns GDN_ENOMEM when the device is full.
  * gdn_state_pool_wrap adopts caller memory (e.g. a torch tensor) of exactly
- * num_slots*hv*dv*dk floats, 16-byte aligned; destroy then frees only the
- * handle.  num_slots >= 1. */
+ * num_slots*hv*dv*dk floats, 16-byte aligned; it makes no CUDA call, and
+ * destroy then frees only the handle.  num_slots >= 1.  Every handle also
+ * takes one pair of work counters from a fixed table in the library's device
+ * memory (GDN_MAX_POOLS pairs; GDN_ENOMEM once all are taken) and returns it
+ * in gdn_state_pool_destroy, which must come after the pool's last launch has
+ * finished. */
 int gdn_state_pool_create(int num_slots, gdn_dims dims, void *stream, gdn_pool **out);
 int gdn_state_pool_wrap(void *dev_ptr, int num_slots, gdn_dims dims, gdn_pool **out);
 int gdn_state_pool_destroy(gdn_pool *pool);

@@ -14,7 +14,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gdn_decode.h")
 
-EINVAL, EUNSUPPORTED = 1, 4
+EINVAL, ENOMEM, EUNSUPPORTED = 1, 2, 4
 FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
 
 
@@ -69,6 +69,31 @@ def test_state_pool_wrap_validation(L):
     assert L.gdn_pool_data(h) == FAKE
     assert L.gdn_state_pool_destroy(h) == 0            # wrapped: frees the handle only
     assert L.gdn_state_pool_destroy(None) == 0
+
+
+def test_state_pool_handle_limit(L):
+    """Every state pool handle holds one pair of work counters from a fixed
+    table; handles beyond GDN_MAX_POOLS fail with GDN_ENOMEM and destroyed
+    handles give their pair back."""
+    from gated_deltanet_decode_gb300._lib import GDN_MAX_POOLS
+    handles = []
+    try:
+        while len(handles) <= GDN_MAX_POOLS:
+            rc, h = _wrap(L)
+            if rc:
+                break
+            handles.append(h)
+        assert rc == ENOMEM and b"state pools" in L.gdn_last_error()
+        assert GDN_MAX_POOLS - 64 <= len(handles) <= GDN_MAX_POOLS
+        assert L.gdn_state_pool_destroy(handles.pop()) == 0
+        rc, h = _wrap(L)
+        assert rc == 0
+        handles.append(h)
+    finally:
+        for h in handles:
+            assert L.gdn_state_pool_destroy(h) == 0
+    rc, h = _wrap(L)
+    assert rc == 0 and L.gdn_state_pool_destroy(h) == 0
 
 
 def test_conv_pool_wrap_validation(L):

@@ -173,3 +173,34 @@ def test_fused_tiny_chained_vs_oracle(gdn, orc):
     assert state_rel_err(pool_gpu[rs], p_ref[rs]).max() <= 8 * STATE_TOL_ONE
     # fp32 windows: the shift copies values, so they match the oracle's exactly
     assert np.array_equal(f64(c.cp.tensor), cp_ref)
+
+
+def test_repeated_launches_reuse_the_work_counters(gdn):
+    """With many items a CTA the kernels hand out the tail of their work
+    through the pool's pair of work counters and leave it at zero when they
+    end: launch after launch on one pool (twin, in place, twin, fused and
+    unfused) writes every output and gives identical values."""
+    s = I.QWEN_08B.with_(rows=256)
+    c = LayerCase(gdn, s, seed=33, num_slots=2 * s.rows + 1, pad_frac=0.1)
+    xd, _ = c.draw()
+    out = torch.empty((s.rows, s.hv, s.dv), dtype=I.torch_dtype(s.dtype), device="cuda")
+    runs = []
+    for keep_in_place in (False, True, False, False):
+        c.reset()
+        out.fill_(float("nan"))
+        gdn.gdn_layer_decode(xd["x"], c.cp, c.w, c.bias, c.A_log, c.dt_bias, xd["a"], xd["b"], c.pool,
+                             c.rs, None if keep_in_place else c.ws, out=out, keep_in_place=keep_in_place)
+        torch.cuda.synchronize()
+        runs.append((keep_in_place, out.clone(), c.pool.tensor.clone()))
+    for _ in range(2):
+        c.reset()
+        o_u, _ = c.unfused(xd)
+        torch.cuda.synchronize()
+        runs.append((False, o_u.clone(), c.pool.tensor.clone()))
+    o0, p0 = runs[0][1], runs[0][2]
+    assert not torch.isnan(o0.float()).any()
+    for keep_in_place, o, p in runs[1:]:
+        assert torch.equal(o, o0)
+        if not keep_in_place:
+            assert torch.equal(p, p0)
+    assert gdn.get_device_error() == 0
