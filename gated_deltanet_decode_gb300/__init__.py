@@ -24,7 +24,7 @@ from ._lib import (GDN_BF16, GDN_DEVERR_BAD_SLOT, GDN_DEVERR_NONE, GDN_F32, GDN_
 
 __all__ = [
     "GDNError", "load", "lib_path", "GDNStatePool", "ConvStatePool", "causal_conv1d_decode",
-    "gdn_decode_step", "gdn_layer_decode", "gdn_commit", "gdn_validate_slots",
+    "gdn_decode_step", "gdn_layer_decode", "gdn_layer_decode_noalloc", "gdn_commit", "gdn_validate_slots",
     "get_device_error", "probe_traffic", "GDN_F32", "GDN_BF16", "GDN_DEVERR_NONE",
     "GDN_DEVERR_BAD_SLOT", "GDN_PROBE_TWIN", "GDN_PROBE_INPLACE", "GDN_PROBE_READ",
     "GDN_PROBE_WRITE",
@@ -242,6 +242,39 @@ def gdn_layer_decode(x, conv_pool: ConvStatePool, w, bias, A_log, dt_bias, a, b,
         pool.handle, _ptr(read_slot, "read_slot", torch.int32, dev),
         _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev), rows,
         int(bool(keep_in_place)), _dtype_code(dt), _stream(dev)))
+    return out
+
+
+def gdn_layer_decode_noalloc(x, conv_pool: ConvStatePool, w, bias, A_log, dt_bias, a, b,
+                             pool: GDNStatePool, read_slot, write_slot, out: torch.Tensor,
+                             keep_in_place: bool = False, silu: bool = True,
+                             scratch_slot: int = 0) -> torch.Tensor:
+    """gdn_layer_decode with its work counters in the library's fixed scratch
+    slot `scratch_slot` instead of the pool's; allocates nothing, so `out`
+    is required."""
+    rows = x.shape[0]
+    dt = x.dtype
+    dev = x.device
+    C = 2 * pool.hk * pool.dk + pool.hv * pool.dv
+    _numel(x, rows * C, "x")
+    _numel(w, C * conv_pool.width, "w")
+    if bias is not None:
+        _numel(bias, C, "bias")
+    _numel(a, rows * pool.hv, "a")
+    _numel(b, rows * pool.hv, "b")
+    _numel(A_log, pool.hv, "A_log")
+    _numel(dt_bias, pool.hv, "dt_bias")
+    _numel(read_slot, rows, "read_slot")
+    if write_slot is not None:
+        _numel(write_slot, rows, "write_slot")
+    _numel(out, rows * pool.hv * pool.dv, "out")
+    _check(_lib.load().gdn_layer_decode_noalloc(
+        _ptr(x, "x", dt, dev), conv_pool.handle, _ptr(w, "w", dt, dev), _ptr(bias, "bias", dt, dev),
+        int(bool(silu)), _ptr(A_log, "A_log", torch.float32, dev),
+        _ptr(dt_bias, "dt_bias", torch.float32, dev), _ptr(a, "a", dt, dev), _ptr(b, "b", dt, dev),
+        pool.handle, _ptr(read_slot, "read_slot", torch.int32, dev),
+        _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev), rows,
+        int(bool(keep_in_place)), int(scratch_slot), _dtype_code(dt), _stream(dev)))
     return out
 
 

@@ -573,11 +573,14 @@ int gdn_decode_step(const void *q, const void *k, const void *v, const void *a, 
     return ok();
 }
 
-int gdn_layer_decode(const void *x, conv_pool *cp, const void *w, const void *bias, int silu,
-                     const float *A_log, const float *dt_bias, const void *a, const void *b,
-                     gdn_pool *pool, const int32_t *read_slot, const int32_t *write_slot,
-                     void *out, int rows, int keep_in_place, int dtype, void *stream)
+// Checks a fused layer call and fills its launch arguments, all but the work
+// counters.  *none is set when there is nothing to launch (rows == 0).
+static int layer_args(const void *x, conv_pool *cp, const void *w, const void *bias, int silu,
+                      const float *A_log, const float *dt_bias, const void *a, const void *b,
+                      gdn_pool *pool, const int32_t *read_slot, const int32_t *write_slot, void *out,
+                      int rows, int keep_in_place, int dtype, gdn::StepArgs *s, bool *none)
 {
+    *none = true;
     int rc = check_state_common(pool, a, b, A_log, dt_bias, read_slot, write_slot, out, rows,
                                 keep_in_place, dtype);
     if (rc)
@@ -604,36 +607,113 @@ int gdn_layer_decode(const void *x, conv_pool *cp, const void *w, const void *bi
     rc = device_error_ptr(&err);
     if (rc)
         return rc;
-    gdn::StepArgs s = {};
-    s.a = a;
-    s.b = b;
-    s.A_log = A_log;
-    s.dt_bias = dt_bias;
-    s.pool = pool->data;
-    s.num_slots = pool->num_slots < cp->num_slots ? pool->num_slots : cp->num_slots;
-    s.read_slot = read_slot;
-    s.write_slot = write_slot;
-    s.in_place = keep_in_place ? 1 : 0;
-    s.out = out;
-    s.rows = rows;
-    s.hk = d.hk;
-    s.hv = d.hv;
-    s.dk = d.dk;
-    s.dv = d.dv;
-    s.err = err;
-    s.x = x;
-    s.conv = cp->data;
-    s.w = w;
-    s.bias = bias;
-    s.silu = silu ? 1 : 0;
-    s.width = cp->width;
-    s.channels = C;
+    *s = gdn::StepArgs{};
+    s->a = a;
+    s->b = b;
+    s->A_log = A_log;
+    s->dt_bias = dt_bias;
+    s->pool = pool->data;
+    s->num_slots = pool->num_slots < cp->num_slots ? pool->num_slots : cp->num_slots;
+    s->read_slot = read_slot;
+    s->write_slot = write_slot;
+    s->in_place = keep_in_place ? 1 : 0;
+    s->out = out;
+    s->rows = rows;
+    s->hk = d.hk;
+    s->hv = d.hv;
+    s->dk = d.dk;
+    s->dv = d.dv;
+    s->err = err;
+    s->x = x;
+    s->conv = cp->data;
+    s->w = w;
+    s->bias = bias;
+    s->silu = silu ? 1 : 0;
+    s->width = cp->width;
+    s->channels = C;
+    *none = false;
+    return GDN_OK;
+}
+
+int gdn_layer_decode(const void *x, conv_pool *cp, const void *w, const void *bias, int silu,
+                     const float *A_log, const float *dt_bias, const void *a, const void *b,
+                     gdn_pool *pool, const int32_t *read_slot, const int32_t *write_slot,
+                     void *out, int rows, int keep_in_place, int dtype, void *stream)
+{
+    gdn::StepArgs s;
+    bool none = true;
+    int rc = layer_args(x, cp, w, bias, silu, A_log, dt_bias, a, b, pool, read_slot, write_slot, out,
+                        rows, keep_in_place, dtype, &s, &none);
+    if (rc || none)
+        return rc;
     rc = work_ptr(pool, &s.work);
     if (rc)
         return rc;
     cudaError_t e = gdn::launch_gdn_layer(s, dtype, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "gdn_layer_decode launch");
+    return ok();
+}
+
+// ---- gdn_layer_decode_noalloc ------------------------------------------------
+// gdn_layer_decode for callers that cannot allocate device memory: the work
+// counters of the launch come from a fixed array of this file, looked up once
+// per device, instead of the state pool's pair.
+
+static __device__ __align__(256) unsigned int g_noalloc_scratch[GDN_NOALLOC_SCRATCH_SLOTS][2];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+unsigned int *g_noalloc_addr[kMaxDevices] = {};
+
+int noalloc_scratch_ptr(unsigned int **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(GDN_EUNSUPPORTED, "device ordinal %d beyond %d", dev, kMaxDevices);
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        unsigned int *p = nullptr;
+        e = cudaGetSymbolAddress((void **)&p, g_noalloc_scratch);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return GDN_OK;
+}
+
+} // namespace
+
+int gdn_layer_decode_noalloc(const void *x, conv_pool *cp, const void *w, const void *bias, int silu,
+                             const float *A_log, const float *dt_bias, const void *a, const void *b,
+                             gdn_pool *pool, const int32_t *read_slot, const int32_t *write_slot,
+                             void *out, int rows, int keep_in_place, int scratch_slot, int dtype,
+                             void *stream)
+{
+    if (scratch_slot < 0 || scratch_slot >= GDN_NOALLOC_SCRATCH_SLOTS)
+        return fail(GDN_EINVAL,
+                    "scratch_slot=%d: the no-allocation scratch holds %d slots of %d bytes (%d bytes)",
+                    scratch_slot, GDN_NOALLOC_SCRATCH_SLOTS, (int)(2 * sizeof(unsigned int)),
+                    (int)sizeof(g_noalloc_scratch));
+    gdn::StepArgs s;
+    bool none = true;
+    int rc = layer_args(x, cp, w, bias, silu, A_log, dt_bias, a, b, pool, read_slot, write_slot, out,
+                        rows, keep_in_place, dtype, &s, &none);
+    if (rc || none)
+        return rc;
+    unsigned int *scratch = nullptr;
+    rc = noalloc_scratch_ptr(&scratch);
+    if (rc)
+        return rc;
+    s.work = scratch + 2 * (size_t)scratch_slot;
+    cudaError_t e = gdn::launch_gdn_layer(s, dtype, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "gdn_layer_decode_noalloc launch");
     return ok();
 }
 

@@ -197,6 +197,28 @@ int gdn_layer_decode(const void *x, conv_pool *cp, const void *w, const void *bi
                      gdn_pool *pool, const int32_t *read_slot, const int32_t *write_slot,
                      void *out, int rows, int keep_in_place, int dtype, void *stream);
 
+/* ---- gdn_layer_decode_noalloc ------------------------------------------ *
+ * gdn_layer_decode for callers that cannot allocate device memory; the pages
+ * have no counterpart (it is an interface matter, not part of the method).
+ * Same arguments, checks and results, bit for bit, as gdn_layer_decode, plus
+ * scratch_slot.  The call allocates nothing (no cudaMalloc, no allocating
+ * library routine): the kernel's scratch, two 32-bit work counters, is slot
+ * `scratch_slot` of a fixed array in the library's device memory of
+ * GDN_NOALLOC_SCRATCH_SLOTS slots (8 bytes each, 512 bytes in all), whose
+ * device address is looked up once per device.  A slot outside
+ * [0, GDN_NOALLOC_SCRATCH_SLOTS) is rejected with GDN_EINVAL.  Both counters
+ * of the slot must be zero when a launch starts: the array is zero when the
+ * library loads and every launch leaves its slot at zero when it ends.
+ * Calls that overlap on the GPU and use the same scratch slot race on it and
+ * give wrong results; give concurrent calls different slots.  The state
+ * pool's own work counters are not used by this call. */
+#define GDN_NOALLOC_SCRATCH_SLOTS 64
+int gdn_layer_decode_noalloc(const void *x, conv_pool *cp, const void *w, const void *bias, int silu,
+                             const float *A_log, const float *dt_bias, const void *a, const void *b,
+                             gdn_pool *pool, const int32_t *read_slot, const int32_t *write_slot,
+                             void *out, int rows, int keep_in_place, int scratch_slot, int dtype,
+                             void *stream);
+
 /* ---- gdn_commit -------------------------------------------------------- *
  * Twin-slot commit: swap read_slot[r] and write_slot[r] for every row, on the
  * device ("mstar PR #1139", "What changed": commit swaps them). */

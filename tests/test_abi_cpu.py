@@ -167,6 +167,18 @@ def test_layer_and_conv_argument_checks(L):
     assert conv(out=None) == EINVAL
     assert conv(dtype=1) == EINVAL
     assert conv(rows=0) == 0
+    # the no-allocation variant: same checks, plus its scratch slot
+    from gated_deltanet_decode_gb300._lib import GDN_NOALLOC_SCRATCH_SLOTS
+
+    def layer_na(cpool, slot, rows=4, x=P):
+        return L.gdn_layer_decode_noalloc(x, cpool, P, None, 1, P, P, P, P, pool, P, P, P, rows, 0, slot,
+                                          0, None)
+
+    assert layer_na(cp, GDN_NOALLOC_SCRATCH_SLOTS) == EINVAL and b"scratch" in L.gdn_last_error()
+    assert layer_na(cp, -1) == EINVAL
+    assert layer_na(bad_cp, 0) == EINVAL and b"channels" in L.gdn_last_error()
+    assert layer_na(cp, 0, x=P + 8) == EINVAL
+    assert layer_na(cp, GDN_NOALLOC_SCRATCH_SLOTS - 1, rows=0) == 0
     for h in (cp, bad_cp, cbig):
         L.conv_state_pool_destroy(h)
     L.gdn_state_pool_destroy(pool)

@@ -1,0 +1,74 @@
+"""gdn_layer_decode_noalloc through the C ABI: the same results as
+gdn_layer_decode, bit for bit, on two calls in a row.
+
+The shapes give the kernel a dozen or more items a CTA, so the launch hands
+out the tail of its work through the scratch counters; the second call only
+gets every item if the first left its scratch slot at zero.
+"""
+import ctypes
+
+import pytest
+import torch
+
+from gated_deltanet_decode_gb300 import inputs as I
+from gpu_helpers import pair, t, ti
+
+pytestmark = pytest.mark.gpu
+
+
+def _call(L, name, c, xd, out, keep_in_place, extra=()):
+    P = lambda v: ctypes.c_void_p(v.data_ptr()) if v is not None else None
+    args = [P(xd["x"]), c["cp"].handle, P(c["w"]), P(c["bias"]), 1, P(c["A_log"]), P(c["dt_bias"]),
+            P(xd["a"]), P(xd["b"]), c["pool"].handle, P(c["rs"]), None if keep_in_place else P(c["ws"]),
+            P(out), xd["x"].shape[0], int(keep_in_place), *extra, c["dtype_code"],
+            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)]
+    rc = getattr(L, name)(*args)
+    assert rc == 0, L.gdn_last_error()
+
+
+def _case(gdn, s, seed):
+    gen = I.Gen(seed)
+    num_slots = 2 * s.rows + 1
+    prm = gen.params(s)
+    c = {"dtype_code": gdn.GDN_BF16 if s.dtype == "bf16" else gdn.GDN_F32}
+    c["w"], _ = pair(prm["w"], s.dtype)
+    c["bias"], _ = pair(prm["bias"], s.dtype)
+    c["A_log"], c["dt_bias"] = t(prm["A_log"]), t(prm["dt_bias"])
+    c["pool0"] = torch.from_numpy(gen.state_pool(s, num_slots)).cuda()
+    c["cp0"], _ = pair(gen.conv_pool(s, num_slots), s.dtype)
+    c["pool"] = gdn.GDNStatePool(num_slots, s.hk, s.hv, s.dk, s.dv, device="cuda", tensor=c["pool0"].clone())
+    c["cp"] = gdn.ConvStatePool(num_slots, s.channels, s.width, dtype=c["cp0"].dtype, device="cuda",
+                                tensor=c["cp0"].clone())
+    rs, ws = gen.slot_tables(s.rows, num_slots, 0.25)
+    c["rs"], c["ws"] = ti(rs), ti(ws)
+    xd = {k: pair(v, s.dtype)[0] for k, v in gen.layer_inputs(s).items()}
+    return c, xd
+
+
+def _reset(c):
+    c["pool"].tensor.copy_(c["pool0"])
+    c["cp"].tensor.copy_(c["cp0"])
+
+
+@pytest.mark.parametrize("shape", [I.QWEN_08B.with_(rows=256), I.QWEN_9B], ids=["0.8b-256rows", "9b-64rows"])
+@pytest.mark.parametrize("keep_in_place", [False, True], ids=["twin", "in_place"])
+def test_noalloc_equals_layer_decode_twice(gdn, shape, keep_in_place):
+    L = gdn.load()
+    c, xd = _case(gdn, shape, seed=50)
+    s = shape
+    ref = torch.empty((s.rows, s.hv, s.dv), dtype=I.torch_dtype(s.dtype), device="cuda")
+    _reset(c)
+    _call(L, "gdn_layer_decode", c, xd, ref, keep_in_place)
+    torch.cuda.synchronize()
+    ref_pool, ref_cp = c["pool"].tensor.clone(), c["cp"].tensor.clone()
+    for call in range(2):
+        out = torch.full_like(ref, float("nan"))
+        _reset(c)
+        _call(L, "gdn_layer_decode_noalloc", c, xd, out, keep_in_place, extra=(3,))
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), f"call {call}: outputs differ"
+        assert torch.equal(c["pool"].tensor, ref_pool), f"call {call}: state pools differ"
+        assert torch.equal(c["cp"].tensor, ref_cp), f"call {call}: conv pools differ"
+    code = ctypes.c_int(-1)
+    assert L.gdn_get_device_error(ctypes.byref(code), None) == 0
+    assert code.value == 0
