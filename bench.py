@@ -4,8 +4,8 @@
 Workload (default): the 0.8B-shaped single layer -- 64 rows, 16 qk / 16 value
 heads, dk = dv = 128, 6144 conv channels of width 4, bf16 activations, fp32
 state, 129-slot pools, twin slots.  One step is one fused conv + GDN layer
-decode (gdn_layer_decode) followed by the twin commit (gdn_commit), through
-the C ABI.  Four independent layer instances (pools, parameters, inputs) are
+decode with the twin commit folded into the same launch
+(gdn_layer_decode_commit), through the C ABI.  Four independent layer instances (pools, parameters, inputs) are
 used in rotation, so that a step never finds the state it reads in L2 (the
 four state pools hold 4 x 135 MB against a 126 MB L2).
 
@@ -202,6 +202,9 @@ def build_sets(G, I, s, device, nsets, pad_frac=0.0):
                                                 st["dt_bias"], st["a"], st["b"], st["pool"], st["rs"], None,
                                                 st["out"], keep_in_place=True)
         st["commit"] = G.prepare_commit(st["rs"], st["ws"])
+        st["layer_commit"] = G.prepare_layer_decode(st["x"], st["cp"], st["w"], st["bias"], st["A_log"],
+                                                    st["dt_bias"], st["a"], st["b"], st["pool"], st["rs"],
+                                                    st["ws"], st["out"], commit=True)
         sets.append(st)
     return sets
 
@@ -261,7 +264,7 @@ def run_extras(G, I, device, n=400):
 
 def run_stack(G, I, device, layers=18, steps=64):
     """18 fused layers of the 0.8B shape per step, 128 rows with 10% padding,
-    257-slot pools per layer, one commit per step, the rows' request order
+    257-slot pools per layer, one commit per step (in the last layer's launch), the rows' request order
     re-permuted (a 1 KB host-to-device table copy) every 16 steps."""
     import numpy as np
     import torch
@@ -308,14 +311,14 @@ def _run_stack(G, I, device, s, gen, stream, layers, steps):
         tr[pos] = req[0][order]
         tw[pos] = req[1][order]
         tables.append((torch.from_numpy(tr).pin_memory(), torch.from_numpy(tw).pin_memory()))
+    # the last layer of the step commits the shared slot tables in its own launch
     calls = [G.prepare_layer_decode(L["x"], L["cp"], L["w"], L["bias"], L["A_log"], L["dt_bias"], L["a"], L["b"],
-                                    L["pool"], rs, ws, L["out"]) for L in Ls]
-    commit = G.prepare_commit(rs, ws)
+                                    L["pool"], rs, ws, L["out"], commit=li == len(Ls) - 1)
+             for li, L in enumerate(Ls)]
 
     def one_step():
         for c in calls:
             c()
-        commit()
 
     def run(replay):
         a = torch.cuda.Event(enable_timing=True)
@@ -369,6 +372,7 @@ def run_ours(args, rank, world, device):
 
     for i in range(args.warmup):
         st = sets[i % NSETS]
+        st["layer_commit"]()
         st["layer"]()
         st["commit"]()
     torch.cuda.synchronize(device)
@@ -386,13 +390,12 @@ def run_ours(args, rank, world, device):
     clocks.start()
     time.sleep(0.3)  # let the sampler start before the timed region
     host0 = time.perf_counter()
-    # timed region: K steps of (fused layer, commit), events only at the ends
-    # so consecutive kernels keep their programmatic-launch overlap
+    # timed region: K steps (fused layer with the commit in the same launch),
+    # events only at the ends so consecutive kernels keep their
+    # programmatic-launch overlap
     t0.record(stream)
     for i in range(K):
-        st = sets[i % NSETS]
-        st["layer"]()
-        st["commit"]()
+        sets[i % NSETS]["layer_commit"]()
     t1.record(stream)
     host_enqueue_s = time.perf_counter() - host0
     torch.cuda.synchronize(device)
@@ -405,6 +408,17 @@ def run_ours(args, rank, world, device):
     for i in range(KL):
         sets[i % NSETS]["layer"]()
     l1.record(stream)
+    torch.cuda.synchronize(device)
+    # the same step as two launches (gdn_layer_decode, then gdn_commit), for comparison
+    KS = max(K // 4, 100)
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for i in range(KS):
+        st = sets[i % NSETS]
+        st["layer"]()
+        st["commit"]()
+    s1.record(stream)
     torch.cuda.synchronize(device)
     clk = clocks.stop()
     if world > 1:
@@ -446,7 +460,7 @@ def run_ours(args, rank, world, device):
         "config": {
             "workload": "0.8B-shaped GDN decode layer: fused conv+rule, 64 rows, 16 qk/16 v heads, "
                         "dk=dv=128, 6144 conv channels width 4, bf16 activations, fp32 state, "
-                        "129-slot pools, twin slots, commit each step",
+                        "129-slot pools, twin slots, commit each step (in the layer's launch)",
             "rows": s.rows, "hk": s.hk, "hv": s.hv, "dk": s.dk, "dv": s.dv, "conv_width": s.width,
             "activations": s.dtype, "num_slots": s.num_slots, "mode": "twin",
             "l2": f"inputs larger than L2: {NSETS} layer instances in rotation "
@@ -457,6 +471,7 @@ def run_ours(args, rank, world, device):
         "layer_timing": f"{KL} back-to-back gdn_layer_decode launches over the {NSETS} instances, "
                         "CUDA events at both ends",
         "us_per_step": round(ms_per_step * 1e3, 3),
+        "us_per_step_two_launches": round(s0.elapsed_time(s1) * 1e3 / KS, 3),
         "pct_of_8TBps": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
         "rows_heads_per_s": round(world * s.rows * s.hv * K / (total_ms * 1e-3), 1),
         "algorithmic_bytes_per_step": step_bytes,
@@ -475,7 +490,7 @@ def run_ours(args, rank, world, device):
         "e2e": e2e,
         "probes": probes,
         **extras,
-        "gpu_launches": 2 * K,
+        "gpu_launches": K,
         "clocks": clk,
     }
     return res
@@ -517,7 +532,7 @@ def run_probes(G, s, sets, device, K):
 
 def run_e2e(G, I, s, sets, device, K, step_bytes):
     """Same step through host buffers: per step, copy x, a, b from pinned host
-    memory, run the layer and the commit, read the output back."""
+    memory, run the layer with its commit, read the output back."""
     import torch
     stream = torch.cuda.current_stream(device)
     hosts = []
@@ -528,8 +543,7 @@ def run_e2e(G, I, s, sets, device, K, step_bytes):
         st, h = sets[i % NSETS], hosts[i % NSETS]
         for k in ("x", "a", "b"):
             st[k].copy_(h[k], non_blocking=True)
-        st["layer"]()
-        st["commit"]()
+        st["layer_commit"]()
         h["out"].copy_(st["out"], non_blocking=True)
     torch.cuda.synchronize(device)
     t0 = torch.cuda.Event(enable_timing=True)
@@ -539,8 +553,7 @@ def run_e2e(G, I, s, sets, device, K, step_bytes):
         st, h = sets[i % NSETS], hosts[i % NSETS]
         for k in ("x", "a", "b"):
             st[k].copy_(h[k], non_blocking=True)
-        st["layer"]()
-        st["commit"]()
+        st["layer_commit"]()
         h["out"].copy_(st["out"], non_blocking=True)
     t1.record(stream)
     torch.cuda.synchronize(device)

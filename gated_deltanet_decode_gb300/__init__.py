@@ -215,8 +215,12 @@ def gdn_decode_step(q, k, v, a, b, A_log, dt_bias, pool: GDNStatePool, read_slot
 
 def gdn_layer_decode(x, conv_pool: ConvStatePool, w, bias, A_log, dt_bias, a, b, pool: GDNStatePool,
                      read_slot, write_slot=None, out: Optional[torch.Tensor] = None,
-                     keep_in_place: bool = False, silu: bool = True) -> torch.Tensor:
-    """Fused conv + gated delta rule. x: [rows][2*hk*dk + hv*dv] packed q|k|v."""
+                     keep_in_place: bool = False, silu: bool = True, commit: bool = False) -> torch.Tensor:
+    """Fused conv + gated delta rule. x: [rows][2*hk*dk + hv*dv] packed q|k|v.
+    With commit (twin only) the slot tables are swapped in the same launch
+    (gdn_layer_decode_commit)."""
+    if commit and (keep_in_place or write_slot is None):
+        raise ValueError("commit needs twin slots (a write_slot table, keep_in_place False)")
     rows = x.shape[0]
     dt = x.dtype
     dev = x.device
@@ -235,13 +239,15 @@ def gdn_layer_decode(x, conv_pool: ConvStatePool, w, bias, A_log, dt_bias, a, b,
     if out is None:
         out = torch.empty((rows, pool.hv, pool.dv), dtype=dt, device=dev)
     _numel(out, rows * pool.hv * pool.dv, "out")
-    _check(_lib.load().gdn_layer_decode(
-        _ptr(x, "x", dt, dev), conv_pool.handle, _ptr(w, "w", dt, dev), _ptr(bias, "bias", dt, dev),
-        int(bool(silu)), _ptr(A_log, "A_log", torch.float32, dev),
-        _ptr(dt_bias, "dt_bias", torch.float32, dev), _ptr(a, "a", dt, dev), _ptr(b, "b", dt, dev),
-        pool.handle, _ptr(read_slot, "read_slot", torch.int32, dev),
-        _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev), rows,
-        int(bool(keep_in_place)), _dtype_code(dt), _stream(dev)))
+    args = (_ptr(x, "x", dt, dev), conv_pool.handle, _ptr(w, "w", dt, dev), _ptr(bias, "bias", dt, dev),
+            int(bool(silu)), _ptr(A_log, "A_log", torch.float32, dev),
+            _ptr(dt_bias, "dt_bias", torch.float32, dev), _ptr(a, "a", dt, dev), _ptr(b, "b", dt, dev),
+            pool.handle, _ptr(read_slot, "read_slot", torch.int32, dev),
+            _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev), rows)
+    if commit:
+        _check(_lib.load().gdn_layer_decode_commit(*args, _dtype_code(dt), _stream(dev)))
+    else:
+        _check(_lib.load().gdn_layer_decode(*args, int(bool(keep_in_place)), _dtype_code(dt), _stream(dev)))
     return out
 
 
@@ -338,8 +344,11 @@ class PreparedCall:
 
 def prepare_layer_decode(x, conv_pool: ConvStatePool, w, bias, A_log, dt_bias, a, b, pool: GDNStatePool,
                          read_slot, write_slot, out, keep_in_place: bool = False, silu: bool = True,
-                         stream: Optional[torch.cuda.Stream] = None) -> PreparedCall:
-    """gdn_layer_decode bound to fixed buffers (validated here, once)."""
+                         stream: Optional[torch.cuda.Stream] = None, commit: bool = False) -> PreparedCall:
+    """gdn_layer_decode (or, with commit, gdn_layer_decode_commit) bound to
+    fixed buffers (validated here, once)."""
+    if commit and (keep_in_place or write_slot is None):
+        raise ValueError("commit needs twin slots (a write_slot table, keep_in_place False)")
     rows = x.shape[0]
     dt = x.dtype
     dev = x.device
@@ -359,9 +368,12 @@ def prepare_layer_decode(x, conv_pool: ConvStatePool, w, bias, A_log, dt_bias, a
             int(bool(silu)), _ptr(A_log, "A_log", torch.float32, dev),
             _ptr(dt_bias, "dt_bias", torch.float32, dev), _ptr(a, "a", dt, dev), _ptr(b, "b", dt, dev),
             pool.handle, _ptr(read_slot, "read_slot", torch.int32, dev),
-            _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev), rows,
-            int(bool(keep_in_place)), _dtype_code(dt), s)
-    return PreparedCall("gdn_layer_decode", args,
+            _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev), rows)
+    if commit:
+        args += (_dtype_code(dt), s)
+    else:
+        args += (int(bool(keep_in_place)), _dtype_code(dt), s)
+    return PreparedCall("gdn_layer_decode_commit" if commit else "gdn_layer_decode", args,
                         (x, conv_pool, w, bias, A_log, dt_bias, a, b, pool, read_slot, write_slot, out))
 
 

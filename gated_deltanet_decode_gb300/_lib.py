@@ -41,7 +41,8 @@ EXPORTS = [
     "gdn_pool_num_slots", "gdn_pool_dims", "gdn_pool_zero_slots",
     "conv_state_pool_create", "conv_state_pool_wrap", "conv_state_pool_destroy", "conv_pool_data",
     "conv_pool_num_slots", "conv_pool_zero_slots",
-    "causal_conv1d_decode", "gdn_decode_step", "gdn_layer_decode", "gdn_layer_decode_noalloc",
+    "causal_conv1d_decode", "gdn_decode_step", "gdn_layer_decode", "gdn_layer_decode_commit",
+    "gdn_layer_decode_noalloc",
     "gdn_commit", "gdn_validate_slots", "gdn_get_device_error", "gdn_probe_traffic",
 ]
 
@@ -73,6 +74,7 @@ _SIGS = {
     "causal_conv1d_decode": (_I, [_P, _I, _P, _P, _P, _P, _P, _I, _P, _I, _I, _P]),
     "gdn_decode_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "gdn_layer_decode": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    "gdn_layer_decode_commit": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P]),
     "gdn_layer_decode_noalloc": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                                       _P]),
     "gdn_commit": (_I, [_P, _P, _I, _P]),

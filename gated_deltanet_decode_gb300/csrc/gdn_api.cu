@@ -655,6 +655,27 @@ int gdn_layer_decode(const void *x, conv_pool *cp, const void *w, const void *bi
     return ok();
 }
 
+int gdn_layer_decode_commit(const void *x, conv_pool *cp, const void *w, const void *bias, int silu,
+                            const float *A_log, const float *dt_bias, const void *a, const void *b,
+                            gdn_pool *pool, int32_t *read_slot, int32_t *write_slot, void *out,
+                            int rows, int dtype, void *stream)
+{
+    gdn::StepArgs s;
+    bool none = true;
+    int rc = layer_args(x, cp, w, bias, silu, A_log, dt_bias, a, b, pool, read_slot, write_slot, out,
+                        rows, 0, dtype, &s, &none);
+    if (rc || none)
+        return rc;
+    rc = work_ptr(pool, &s.work);
+    if (rc)
+        return rc;
+    s.commit = 1;
+    cudaError_t e = gdn::launch_gdn_layer(s, dtype, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "gdn_layer_decode_commit launch");
+    return ok();
+}
+
 // ---- gdn_layer_decode_noalloc ------------------------------------------------
 // gdn_layer_decode for callers that cannot allocate device memory: the work
 // counters of the launch come from a fixed array of this file, looked up once

@@ -42,6 +42,7 @@ struct StepArgs {
     int rows, hk, hv, dk, dv;
     int *err;
     unsigned int *work; // the pool's two work counters (claim, producers done), zero between launches
+    int commit;         // twin only: swap read_slot and write_slot once every producer has read them
     // fused layer only
     const void *x;
     void *conv;        // conv pool data

@@ -290,6 +290,7 @@ gdn_stream_kernel(const StepArgs p, const Sched sc)
         int lo = sc.first(blockIdx.x, gridDim.x) * sc.per_unit; // items [lo, hi) to do next
         int hi = sc.first(blockIdx.x + 1, gridDim.x) * sc.per_unit;
         const bool claims = sc.n_static < sc.n_units;
+        const bool counted = claims || p.commit; // producers count themselves done
         int kdone = 0;                // items issued so far
         int prev_r = -1, prev_g = -1; // the item before the batch
         bool stop = false;
@@ -447,14 +448,47 @@ gdn_stream_kernel(const StepArgs p, const Sched sc)
             kdone += nb;
             lo += nb;
         }
-        // This CTA makes no more claims.  The last CTA to get here resets the
-        // counters for the pool's next launch: every other CTA has counted
-        // itself done after its last claim.
-        if (claims && lane == 0) {
-            __threadfence();
-            if (atomicAdd(p.work + 1, 1u) == gridDim.x - 1) {
-                atomicExch(p.work, 0u);
-                atomicExch(p.work + 1, 0u);
+        // This CTA makes no more claims and reads no more slots.  The last CTA
+        // to get here (every other one has counted itself done after its last
+        // claim and its last slot load) commits the slot tables if asked and
+        // resets the counters for the pool's next launch.
+        if (counted) {
+            int last = 0;
+            if (lane == 0) {
+                __threadfence();
+                last = atomicAdd(p.work + 1, 1u) == gridDim.x - 1;
+            }
+            if (__shfl_sync(0xffffffffu, last, 0)) {
+                __threadfence();
+                if (p.commit) {
+                    // the whole warp swaps the tables, 256 rows a round, loads first
+                    int32_t *rs = const_cast<int32_t *>(p.read_slot);
+                    int32_t *ws = const_cast<int32_t *>(p.write_slot);
+                    for (int r0 = 0; r0 < p.rows; r0 += 256) {
+                        int32_t vr[8], vw[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int r = r0 + 32 * j + lane;
+                            if (r < p.rows) {
+                                vr[j] = rs[r];
+                                vw[j] = ws[r];
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int r = r0 + 32 * j + lane;
+                            if (r < p.rows) {
+                                rs[r] = vw[j];
+                                ws[r] = vr[j];
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    atomicExch(p.work, 0u);
+                    atomicExch(p.work + 1, 0u);
+                }
             }
         }
         // end of the stream

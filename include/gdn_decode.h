@@ -197,6 +197,18 @@ int gdn_layer_decode(const void *x, conv_pool *cp, const void *w, const void *bi
                      gdn_pool *pool, const int32_t *read_slot, const int32_t *write_slot,
                      void *out, int rows, int keep_in_place, int dtype, void *stream);
 
+/* ---- gdn_layer_decode_commit ------------------------------------------- *
+ * gdn_layer_decode in twin mode followed by gdn_commit, in one launch: the
+ * same values, then read_slot[r] and write_slot[r] swapped for every row
+ * ("mstar PR #1139", "What changed": twin slots, the commit swaps them).  For
+ * the last layer of a step whose layers share one slot table; the kernel
+ * swaps the tables once no CTA of the launch reads them any more, so the next
+ * launch on the stream sees the committed tables. */
+int gdn_layer_decode_commit(const void *x, conv_pool *cp, const void *w, const void *bias, int silu,
+                            const float *A_log, const float *dt_bias, const void *a, const void *b,
+                            gdn_pool *pool, int32_t *read_slot, int32_t *write_slot, void *out,
+                            int rows, int dtype, void *stream);
+
 /* ---- gdn_layer_decode_noalloc ------------------------------------------ *
  * gdn_layer_decode for callers that cannot allocate device memory; the pages
  * have no counterpart (it is an interface matter, not part of the method).

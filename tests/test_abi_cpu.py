@@ -167,6 +167,13 @@ def test_layer_and_conv_argument_checks(L):
     assert conv(out=None) == EINVAL
     assert conv(dtype=1) == EINVAL
     assert conv(rows=0) == 0
+    # layer + commit in one launch: twin only, so the write table is required
+    def layer_c(cpool, rows=4, ws=P):
+        return L.gdn_layer_decode_commit(P, cpool, P, None, 1, P, P, P, P, pool, P, ws, P, rows, 0, None)
+
+    assert layer_c(cp, ws=None) == EINVAL
+    assert layer_c(bad_cp) == EINVAL and b"channels" in L.gdn_last_error()
+    assert layer_c(cp, rows=0) == 0
     # the no-allocation variant: same checks, plus its scratch slot
     from gated_deltanet_decode_gb300._lib import GDN_NOALLOC_SCRATCH_SLOTS
 

@@ -204,3 +204,33 @@ def test_repeated_launches_reuse_the_work_counters(gdn):
         if not keep_in_place:
             assert torch.equal(p, p0)
     assert gdn.get_device_error() == 0
+
+
+@pytest.mark.parametrize("shape", [I.TINY, I.QWEN_08B, I.QWEN_08B.with_(rows=256), I.QWEN_9B],
+                         ids=["tiny", "0.8b", "0.8b-256rows", "9b"])
+def test_fused_commit_equals_layer_then_commit(gdn, shape):
+    """gdn_layer_decode_commit gives the values of gdn_layer_decode followed by
+    gdn_commit, bit for bit, and leaves the slot tables swapped; two steps in
+    a row read the committed tables."""
+    c = LayerCase(gdn, shape, seed=34, num_slots=2 * shape.rows + 1, pad_frac=0.25)
+    steps = [c.draw()[0] for _ in range(2)]
+    rs0, ws0 = c.rs.clone(), c.ws.clone()
+    ref = []
+    for xd in steps:
+        o = c.fused(xd).clone()
+        gdn.gdn_commit(c.rs, c.ws)
+        torch.cuda.synchronize()
+        ref.append((o, c.rs.clone(), c.ws.clone()))
+    ref_pool, ref_cp = c.pool.tensor.clone(), c.cp.tensor.clone()
+    c.reset()
+    c.rs.copy_(rs0)
+    c.ws.copy_(ws0)
+    for (o_ref, rs_ref, ws_ref), xd in zip(ref, steps):
+        o = gdn.gdn_layer_decode(xd["x"], c.cp, c.w, c.bias, c.A_log, c.dt_bias, xd["a"], xd["b"], c.pool,
+                                 c.rs, c.ws, commit=True).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_ref)
+        assert torch.equal(c.rs, rs_ref) and torch.equal(c.ws, ws_ref)
+    assert torch.equal(c.pool.tensor, ref_pool)
+    assert torch.equal(c.cp.tensor, ref_cp)
+    assert gdn.get_device_error() == 0

@@ -82,16 +82,24 @@ class Stack:
             ex.append(d)
         return ex
 
-    def step(self):
+    def step(self, fused_commit=False):
+        """All layers, then the commit (with fused_commit, inside the last
+        layer's launch)."""
+        n = len(self.layers)
         for li, L in enumerate(self.layers):
             self.gdn.gdn_layer_decode(self.x[li], L["cp"], L["w"], L["bias"], L["A_log"], L["dt_bias"],
-                                      self.a[li], self.b[li], L["pool"], self.rs, self.ws, out=L["out"])
-        self.gdn.gdn_commit(self.rs, self.ws)
+                                      self.a[li], self.b[li], L["pool"], self.rs, self.ws, out=L["out"],
+                                      commit=fused_commit and li == n - 1)
+        if not fused_commit:
+            self.gdn.gdn_commit(self.rs, self.ws)
         # the commit swaps every request's two slots; keep the host copy in step
         self.req_rs, self.req_ws = self.req_ws, self.req_rs
 
 
-def test_stack_graph_replay_equals_eager(gdn):
+@pytest.mark.parametrize("fused_commit", [False, True], ids=["commit_kernel", "commit_in_last_layer"])
+def test_stack_graph_replay_equals_eager(gdn, fused_commit):
+    """Eager steps (separate commit) against graph replays of steps whose
+    commit is a separate kernel or folded into the last layer's launch."""
     torch.manual_seed(0)
     st = Stack(gdn, layers=18, dtype="bf16", seed=40)
     st.place()
@@ -108,7 +116,7 @@ def test_stack_graph_replay_equals_eager(gdn):
         L["cp"].tensor.copy_(c0)
     st.rs.copy_(rs0)
     st.ws.copy_(ws0)
-    st.step()  # warm-up of every launch path before capture (error word lookup, attributes)
+    st.step(fused_commit)  # warm-up of every launch path before capture (error word lookup, attributes)
     for (p0, c0), L in zip(snap0, st.layers):
         L["pool"].tensor.copy_(p0)
         L["cp"].tensor.copy_(c0)
@@ -120,7 +128,7 @@ def test_stack_graph_replay_equals_eager(gdn):
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
         with torch.cuda.graph(g, stream=side):
-            st.step()
+            st.step(fused_commit)
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
     for _ in range(4):
