@@ -360,6 +360,143 @@ int gdn_oracle_layer(int rows, int hk, int hv, int dk, int dv, int W, int num_sl
     return bad > bad2 ? bad : bad2;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Many tokens a row: prefill and speculative verification                   */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Sequence r holds tokens [cu_seqlens[r], cu_seqlens[r+1]) of the packed
+ * inputs q, k: [T][hk][dk]   v: [T][hv][dv]   a, b: [T][hv]   out: [T][hv][dv].
+ * For each real sequence and value head the decode rule is applied token
+ * after token, in order, starting from the state in read_slot[r]; o_t comes
+ * from the state after token t ("mstar PR #1139", "Why": prefill keeps the
+ * state in place; the rule is the recurrent update of one token).  The final
+ * state goes to write_slot[r] (twin), or back to read_slot[r] when write_slot
+ * is NULL (in place).  When token_slot ([T]) is given, the state after token t
+ * goes to token_slot[t] instead: a state a token, as speculative verification
+ * keeps them ("mstar PR #1139", "What changed": speculative decoding holds a
+ * state per token); write_slot is then ignored and the read slot left alone.
+ * Padding (read slot 0): outputs zero, nothing written.  Bad: a slot outside
+ * [0, num_slots), a write or token slot 0, a twin write slot equal to the read
+ * slot, a token slot equal to the read slot; outputs zero, nothing written.
+ * Returns the number of bad sequences.  Sequences must name distinct slots.
+ */
+static int prefill_seq_ok(int r, int num_slots, const int32_t *cu_seqlens, const int32_t *read_slot,
+                          const int32_t *write_slot, const int32_t *token_slot, int *bad)
+{
+    int rs = read_slot[r];
+    if (rs == 0)
+        return 0;
+    int ok = rs > 0 && rs < num_slots;
+    if (token_slot) {
+        for (int t = cu_seqlens[r]; t < cu_seqlens[r + 1]; ++t)
+            if (token_slot[t] <= 0 || token_slot[t] >= num_slots || token_slot[t] == rs)
+                ok = 0;
+    } else if (write_slot) {
+        int ws = write_slot[r];
+        if (ws <= 0 || ws >= num_slots || ws == rs)
+            ok = 0;
+    }
+    if (!ok)
+        ++*bad;
+    return ok;
+}
+
+int gdn_oracle_prefill(int nseq, int hk, int hv, int dk, int dv, int num_slots,
+                       const int32_t *cu_seqlens, const double *q, const double *k, const double *v,
+                       const double *a, const double *b, const double *A_log, const double *dt_bias,
+                       double *pool, const int32_t *read_slot, const int32_t *write_slot,
+                       const int32_t *token_slot, double *out, int nthreads)
+{
+    const int group = hv / hk;
+    const size_t head_elems = (size_t)dv * dk;
+    const size_t slot_elems = (size_t)hv * head_elems;
+    int bad = 0;
+    int *seq_ok = (int *)malloc(sizeof(int) * (size_t)(nseq > 0 ? nseq : 1));
+    for (int r = 0; r < nseq; ++r)
+        seq_ok[r] = prefill_seq_ok(r, num_slots, cu_seqlens, read_slot, write_slot, token_slot, &bad);
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (long u = 0; u < (long)nseq * hv; ++u) {
+        int r = (int)(u / hv);
+        int h = (int)(u % hv);
+        int g = h / group;
+        if (!seq_ok[r]) {
+            for (int t = cu_seqlens[r]; t < cu_seqlens[r + 1]; ++t)
+                for (int i = 0; i < dv; ++i)
+                    out[((size_t)t * hv + h) * dv + i] = 0.0;
+            continue;
+        }
+        int rs = read_slot[r];
+        double *S = (double *)malloc(sizeof(double) * head_elems);
+        double *S_new = (double *)malloc(sizeof(double) * head_elems);
+        memcpy(S, pool + (size_t)rs * slot_elems + (size_t)h * head_elems, sizeof(double) * head_elems);
+        for (int t = cu_seqlens[r]; t < cu_seqlens[r + 1]; ++t) {
+            gdn_oracle_head(dk, dv, S, q + ((size_t)t * hk + g) * dk, k + ((size_t)t * hk + g) * dk,
+                            v + ((size_t)t * hv + h) * dv, a[(size_t)t * hv + h], b[(size_t)t * hv + h],
+                            A_log[h], dt_bias[h], S_new, out + ((size_t)t * hv + h) * dv);
+            memcpy(S, S_new, sizeof(double) * head_elems);
+            if (token_slot)
+                memcpy(pool + (size_t)token_slot[t] * slot_elems + (size_t)h * head_elems, S,
+                       sizeof(double) * head_elems);
+        }
+        if (!token_slot) {
+            int ws = write_slot ? write_slot[r] : rs;
+            memcpy(pool + (size_t)ws * slot_elems + (size_t)h * head_elems, S, sizeof(double) * head_elems);
+        }
+        free(S);
+        free(S_new);
+    }
+    free(seq_ok);
+    return bad;
+}
+
+/*
+ * The depthwise causal conv over many tokens a row.  Sequence r's tokens
+ * x[cu_seqlens[r] .. cu_seqlens[r+1]) ([T][C]) continue the window held in
+ * read_slot[r]: each token sees the W-1 inputs before it, from the window and
+ * then from the sequence itself; y: [T][C].  The window after the last token
+ * goes to write_slot[r] (NULL: in place), or, with token_slot ([T]), the
+ * window after token t goes to token_slot[t].  Padding and bad sequences as
+ * in gdn_oracle_prefill.  Returns the number of bad sequences.
+ */
+int gdn_oracle_conv_prefill(int nseq, int C, int W, int num_slots, const int32_t *cu_seqlens,
+                            const double *x, double *conv_pool, const int32_t *read_slot,
+                            const int32_t *write_slot, const int32_t *token_slot, const double *w,
+                            const double *bias, int silu, double *y)
+{
+    const size_t slot_elems = (size_t)(W - 1) * C;
+    double *win = (double *)malloc(sizeof(double) * (slot_elems > 0 ? slot_elems : 1));
+    double *new_win = (double *)malloc(sizeof(double) * (slot_elems > 0 ? slot_elems : 1));
+    int bad = 0;
+    for (int r = 0; r < nseq; ++r) {
+        if (!prefill_seq_ok(r, num_slots, cu_seqlens, read_slot, write_slot, token_slot, &bad)) {
+            for (int t = cu_seqlens[r]; t < cu_seqlens[r + 1]; ++t)
+                for (int c = 0; c < C; ++c)
+                    y[(size_t)t * C + c] = 0.0;
+            continue;
+        }
+        int rs = read_slot[r];
+        memcpy(win, conv_pool + (size_t)rs * slot_elems, sizeof(double) * slot_elems);
+        for (int t = cu_seqlens[r]; t < cu_seqlens[r + 1]; ++t) {
+            gdn_oracle_conv_row(C, W, win, x + (size_t)t * C, w, bias, silu, y + (size_t)t * C, new_win);
+            memcpy(win, new_win, sizeof(double) * slot_elems);
+            if (token_slot)
+                memcpy(conv_pool + (size_t)token_slot[t] * slot_elems, win, sizeof(double) * slot_elems);
+        }
+        if (!token_slot) {
+            int ws = write_slot ? write_slot[r] : rs;
+            memcpy(conv_pool + (size_t)ws * slot_elems, win, sizeof(double) * slot_elems);
+        }
+    }
+    free(win);
+    free(new_win);
+    return bad;
+}
+
 /* Commit of a twin step: the read and write slot of every row trade places. */
 void gdn_oracle_commit(int rows, int32_t *read_slot, int32_t *write_slot)
 {

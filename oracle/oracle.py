@@ -7,7 +7,10 @@ path; arrays go in and out as float64 numpy arrays (int32 for slot tables).
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 against closed forms, special cases, a hand-worked example
 (``tests/golden/rule_2x2.json``), an unrolled product of transition matrices
-and brute force on tiny inputs.
+and brute force on tiny inputs; ``prefill`` and ``conv_prefill`` by
+``tests/test_oracle_prefill_pins.py`` (the unrolled product per token, the
+pinned one-token step token by token, numpy's convolution).  Planted mistakes
+in ``tests/test_oracle_mutations.py`` show the pins are sharp.
 """
 from __future__ import annotations
 
@@ -26,7 +29,7 @@ _lib = None
 
 __all__ = [
     "build", "lib", "softplus", "alpha", "beta", "round_bf16", "l2norm", "rule", "head",
-    "conv_row", "step", "conv_step", "layer", "commit", "max_threads",
+    "conv_row", "step", "conv_step", "layer", "prefill", "conv_prefill", "commit", "max_threads",
 ]
 
 
@@ -83,6 +86,12 @@ def lib():
             L.gdn_oracle_layer.restype = _I
             L.gdn_oracle_layer.argtypes = [_I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P,
                                            _P, _P, _P, _P, _P, _P, _I, _I, _P, _I]
+            L.gdn_oracle_prefill.restype = _I
+            L.gdn_oracle_prefill.argtypes = [_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P,
+                                             _P, _P, _P, _P, _P, _I]
+            L.gdn_oracle_conv_prefill.restype = _I
+            L.gdn_oracle_conv_prefill.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I,
+                                                  _P]
             L.gdn_oracle_commit.restype = None
             L.gdn_oracle_commit.argtypes = [_I, _P, _P]
             L.gdn_oracle_max_threads.restype = _I
@@ -230,6 +239,55 @@ def layer(x, conv_pool, w, bias, a, b, A_log, dt_bias, pool, read_slot, write_sl
                                  int(bool(keep_in_place)), int(bool(act_bf16)), _ptr(out),
                                  int(nthreads))
     return out, bad
+
+
+def prefill(cu_seqlens, q, k, v, a, b, A_log, dt_bias, pool, read_slot, write_slot=None,
+            token_slot=None, nthreads: int = 0):
+    """Many tokens a sequence over an fp64 pool [num_slots][hv][dv][dk],
+    updated in place.  q, k: [T][hk][dk]; v: [T][hv][dv]; a, b: [T][hv].
+    write_slot None: in place; token_slot ([T]): a state a token (verify).
+
+    Returns (out [T][hv][dv], bad_sequences).
+    """
+    q, k, v, a, b = _f64(q), _f64(k), _f64(v), _f64(a), _f64(b)
+    A_log, dt_bias = _f64(A_log), _f64(dt_bias)
+    assert pool.dtype == np.float64 and pool.flags.c_contiguous
+    num_slots, hv, dv, dk = pool.shape
+    T, hk = q.shape[0], q.shape[1]
+    cu = _i32(cu_seqlens)
+    nseq = cu.shape[0] - 1
+    assert cu[0] == 0 and cu[-1] == T
+    rs = _i32(read_slot)
+    ws = None if write_slot is None else _i32(write_slot)
+    ts = None if token_slot is None else _i32(token_slot)
+    out = np.empty((T, hv, dv))
+    bad = lib().gdn_oracle_prefill(nseq, hk, hv, dk, dv, num_slots, _ptr(cu), _ptr(q), _ptr(k), _ptr(v),
+                                   _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(pool), _ptr(rs),
+                                   _ptr(ws), _ptr(ts), _ptr(out), int(nthreads))
+    return out, bad
+
+
+def conv_prefill(cu_seqlens, x, conv_pool, read_slot, write_slot, w, bias, token_slot=None,
+                 silu: bool = True):
+    """Causal conv over many tokens a sequence, on an fp64 conv pool
+    [num_slots][W-1][C] updated in place.  x: [T][C].  write_slot None: in
+    place; token_slot ([T]): a window a token.  Returns (y [T][C], bad)."""
+    x, w = _f64(x), _f64(w)
+    assert conv_pool.dtype == np.float64 and conv_pool.flags.c_contiguous
+    num_slots = conv_pool.shape[0]
+    T, C = x.shape
+    W = w.shape[1]
+    bias = None if bias is None else _f64(bias)
+    cu = _i32(cu_seqlens)
+    nseq = cu.shape[0] - 1
+    assert cu[0] == 0 and cu[-1] == T
+    rs = _i32(read_slot)
+    ws = None if write_slot is None else _i32(write_slot)
+    ts = None if token_slot is None else _i32(token_slot)
+    y = np.empty((T, C))
+    bad = lib().gdn_oracle_conv_prefill(nseq, C, W, num_slots, _ptr(cu), _ptr(x), _ptr(conv_pool), _ptr(rs),
+                                        _ptr(ws), _ptr(ts), _ptr(w), _ptr(bias), int(bool(silu)), _ptr(y))
+    return y, bad
 
 
 def commit(read_slot: np.ndarray, write_slot: np.ndarray) -> None:

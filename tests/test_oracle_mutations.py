@@ -32,7 +32,15 @@ MUTATIONS = {
     "bf16_truncates": ("nearbyint(x / spacing)", "trunc(x / spacing)"),
     "padding_writes_null": ("if (rs == 0) {\n            row_ok[r] = 0;",
                             "if (0) {\n            row_ok[r] = 0;"),
+    # many tokens a sequence
+    "prefill_state_not_carried": ("memcpy(S, S_new, sizeof(double) * head_elems);", ""),
+    "prefill_tokens_reversed": ("for (int t = cu_seqlens[r]; t < cu_seqlens[r + 1]; ++t) {\n            gdn_oracle_head(",
+                                "for (int t = cu_seqlens[r + 1] - 1; t >= cu_seqlens[r]; --t) {\n            gdn_oracle_head("),
+    "verify_one_token_slot": ("pool + (size_t)token_slot[t] * slot_elems", "pool + (size_t)token_slot[cu_seqlens[r]] * slot_elems"),
+    "prefill_twin_writes_read_slot": ("int ws = write_slot ? write_slot[r] : rs;", "int ws = rs;"),
+    "conv_prefill_window_not_carried": ("memcpy(win, new_win, sizeof(double) * slot_elems);", ""),
 }
+PIN_FILES = ["test_oracle_pins.py", "test_oracle_prefill_pins.py"]
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
@@ -47,6 +55,6 @@ def test_pins_catch_planted_mistake(name, tmp_path):
                     str(cfile), "-lm"], check=True)
     env = dict(os.environ, GDN_ORACLE_LIB=str(so))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        *[os.path.join(ROOT, "tests", f) for f in PIN_FILES]],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins did not catch {name}:\n{r.stdout[-2000:]}"
