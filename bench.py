@@ -35,7 +35,8 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 NSETS = 4
 KERNEL_SOURCES = ["gated_deltanet_decode_gb300/csrc/gdn_stream.cu",
-                  "gated_deltanet_decode_gb300/csrc/gdn_device.cuh"]
+                  "gated_deltanet_decode_gb300/csrc/gdn_device.cuh",
+                  "gated_deltanet_decode_gb300/csrc/gdn_ptx.cuh"]
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "gdn_layer_decode_qwen08b_rows64.md")
 
 
@@ -259,6 +260,106 @@ def run_extras(G, I, device, n=400):
     res["qwen9b_gqa"] = {"workload": "9B-shaped fused layer: 16 qk / 32 v heads, 2R+1 slots, twin",
                          "rows": gqa}
     res["decode_stack"] = run_stack(G, I, device)
+    res["many_tokens"] = run_many_tokens(G, I, device)
+    return res
+
+
+def fp32_alu_peak_tflops() -> float:
+    """FP32 FMA rate from the unit counts and the SM clock: 128 FP32 lanes an
+    SM, 2 flops an FMA, at the measured maximum SM clock."""
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    mhz = 2070.0
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", mhz))
+    except (OSError, ValueError):
+        pass
+    return sms * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def run_many_tokens(G, I, device, n=20):
+    """Prefill (the rule over many tokens, in place), verification (a state a
+    token) and the conv over a sequence, 0.8B-shaped, bf16 activations."""
+    import torch
+    res = {}
+    s = I.QWEN_08B
+    sets = []
+    for i, (nseq, tok) in enumerate([(8, 512)] * 2):
+        gen = I.Gen(2000 + i)
+        lens = [tok] * nseq
+        T = nseq * tok
+        cu, rs, ws, _ = gen.seq_tables(lens, 2 * nseq + 1)
+        prm = gen.params(s)
+        inp = gen.step_inputs(s.with_(rows=T))
+        st = {k: I.to_torch(v, s.dtype, device) for k, v in inp.items()}
+        st["x"] = I.to_torch(gen.layer_inputs(s.with_(rows=T))["x"], s.dtype, device)
+        st["w"] = I.to_torch(prm["w"], s.dtype, device)
+        st["bias"] = I.to_torch(prm["bias"], s.dtype, device)
+        st["A_log"] = I.to_torch(prm["A_log"], "f32", device)
+        st["dt_bias"] = I.to_torch(prm["dt_bias"], "f32", device)
+        st["pool"] = G.GDNStatePool(2 * nseq + 1, s.hk, s.hv, s.dk, s.dv, device=device,
+                                    tensor=torch.from_numpy(gen.state_pool(s, 2 * nseq + 1)).to(device))
+        st["cp"] = G.ConvStatePool(2 * nseq + 1, s.channels, s.width, dtype=I.torch_dtype(s.dtype),
+                                   device=device, tensor=I.to_torch(gen.conv_pool(s, 2 * nseq + 1), s.dtype, device))
+        st["cu"], st["rs"] = torch.from_numpy(cu).to(device), torch.from_numpy(rs).to(device)
+        st["out"] = torch.empty((T, s.hv, s.dv), dtype=I.torch_dtype(s.dtype), device=device)
+        st["y"] = torch.empty((T, s.channels), dtype=I.torch_dtype(s.dtype), device=device)
+        sets.append(st)
+    nseq, tok = 8, 512
+    T = nseq * tok
+
+    def prefill(st):
+        G.gdn_prefill(st["q"], st["k"], st["v"], st["a"], st["b"], st["A_log"], st["dt_bias"], st["pool"],
+                      st["cu"], st["rs"], None, out=st["out"], keep_in_place=True)
+
+    def conv(st):
+        G.causal_conv1d_prefill(st["x"], st["cp"], st["cu"], st["rs"], st["w"], st["bias"], out=st["y"])
+
+    us = time_calls([lambda st=st: prefill(st) for st in sets], n, device)
+    flops = 6.0 * s.dk * s.dv * s.hv * T  # per token and head: S.k, S.q, the update
+    peak = fp32_alu_peak_tflops()
+    res["prefill"] = {"workload": f"0.8B-shaped rule, {nseq} sequences x {tok} tokens, in place",
+                      "us": round(us, 1), "tokens_per_s": round(T / (us * 1e-6), 1),
+                      "roofline": {"bound": "alu", "achieved": round(flops / (us * 1e-6) / 1e12, 3),
+                                   "peak": round(peak, 1), "unit": "TFLOP/s",
+                                   "frac": round(flops / (us * 1e-6) / 1e12 / peak, 4),
+                                   "peak_kind": "fp32 FMA lanes x 2 x max SM clock"}}
+    cb = 2.0 * T * s.channels * 2 + 2 * nseq * (s.width - 1) * s.channels * 2
+    us = time_calls([lambda st=st: conv(st) for st in sets], n, device)
+    res["conv_prefill"] = {"workload": f"0.8B-shaped conv, {nseq} sequences x {tok} tokens, in place",
+                           "us": round(us, 1), "GBs": round(cb / us / 1e3, 1)}
+    del sets
+    torch.cuda.empty_cache()
+    # verification: 64 rows, 4 draft tokens each, a state a token
+    rows, tok = 64, 4
+    vsets = []
+    for i in range(NSETS):
+        gen = I.Gen(3000 + i)
+        T = rows * tok
+        num_slots = 2 * rows + T + 1
+        cu, rs, _, ts = gen.seq_tables([tok] * rows, num_slots)
+        prm = gen.params(s)
+        st = {k: I.to_torch(v, s.dtype, device) for k, v in gen.step_inputs(s.with_(rows=T)).items()}
+        st["A_log"] = I.to_torch(prm["A_log"], "f32", device)
+        st["dt_bias"] = I.to_torch(prm["dt_bias"], "f32", device)
+        st["pool"] = G.GDNStatePool(num_slots, s.hk, s.hv, s.dk, s.dv, device=device,
+                                    tensor=torch.from_numpy(gen.state_pool(s, num_slots)).to(device))
+        st["cu"], st["rs"], st["ts"] = (torch.from_numpy(a).to(device) for a in (cu, rs, ts))
+        st["out"] = torch.empty((T, s.hv, s.dv), dtype=I.torch_dtype(s.dtype), device=device)
+        vsets.append(st)
+
+    def verify(st):
+        G.gdn_verify(st["q"], st["k"], st["v"], st["a"], st["b"], st["A_log"], st["dt_bias"], st["pool"],
+                     st["cu"], st["rs"], st["ts"], out=st["out"])
+
+    us = time_calls([lambda st=st: verify(st) for st in vsets], 200, device)
+    vb = rows * s.hv * s.dv * s.dk * 4 * (1 + tok)  # one state read, one state written a token
+    res["verify"] = {"workload": f"0.8B-shaped rule, {rows} rows x {tok} draft tokens, a state a token",
+                     "us": round(us, 2), "GBs": round(vb / us / 1e3, 1),
+                     "frac_of_measured_peak": round(vb / us / 1e3 / hbm_peak()[0], 4)}
+    del vsets
+    torch.cuda.empty_cache()
     return res
 
 

@@ -25,6 +25,7 @@ from ._lib import (GDN_BF16, GDN_DEVERR_BAD_SLOT, GDN_DEVERR_NONE, GDN_F32, GDN_
 __all__ = [
     "GDNError", "load", "lib_path", "GDNStatePool", "ConvStatePool", "causal_conv1d_decode",
     "gdn_decode_step", "gdn_layer_decode", "gdn_layer_decode_noalloc", "gdn_commit", "gdn_validate_slots",
+    "gdn_prefill", "gdn_verify", "causal_conv1d_prefill",
     "get_device_error", "probe_traffic", "GDN_F32", "GDN_BF16", "GDN_DEVERR_NONE",
     "GDN_DEVERR_BAD_SLOT", "GDN_PROBE_TWIN", "GDN_PROBE_INPLACE", "GDN_PROBE_READ",
     "GDN_PROBE_WRITE",
@@ -210,6 +211,93 @@ def gdn_decode_step(q, k, v, a, b, A_log, dt_bias, pool: GDNStatePool, read_slot
         _ptr(read_slot, "read_slot", torch.int32, dev), _ptr(write_slot, "write_slot", torch.int32, dev),
         _ptr(out, "out", dt, dev), rows, pool.hv, int(bool(keep_in_place)), _dtype_code(dt),
         _stream(dev)))
+    return out
+
+
+def _prefill_checks(q, k, v, a, b, A_log, dt_bias, pool, cu_seqlens, read_slot):
+    T = q.shape[0]
+    nseq = cu_seqlens.numel() - 1
+    if nseq < 0:
+        raise ValueError("cu_seqlens needs nseq + 1 entries")
+    _numel(q, T * pool.hk * pool.dk, "q")
+    _numel(k, T * pool.hk * pool.dk, "k")
+    _numel(v, T * pool.hv * pool.dv, "v")
+    _numel(a, T * pool.hv, "a")
+    _numel(b, T * pool.hv, "b")
+    _numel(A_log, pool.hv, "A_log")
+    _numel(dt_bias, pool.hv, "dt_bias")
+    _numel(read_slot, nseq, "read_slot")
+    return T, nseq
+
+
+def gdn_prefill(q, k, v, a, b, A_log, dt_bias, pool: GDNStatePool, cu_seqlens, read_slot, write_slot=None,
+                out: Optional[torch.Tensor] = None, keep_in_place: bool = False) -> torch.Tensor:
+    """The rule over many tokens a sequence (packed, token-major: q,k [T][hk][dk],
+    v [T][hv][dv], a,b [T][hv]; sequence r is tokens cu_seqlens[r]..cu_seqlens[r+1]).
+    The final state goes to write_slot (twin) or back to read_slot (in place)."""
+    T, nseq = _prefill_checks(q, k, v, a, b, A_log, dt_bias, pool, cu_seqlens, read_slot)
+    dt, dev = q.dtype, q.device
+    if write_slot is not None:
+        _numel(write_slot, nseq, "write_slot")
+    if out is None:
+        out = torch.empty((T, pool.hv, pool.dv), dtype=dt, device=dev)
+    _numel(out, T * pool.hv * pool.dv, "out")
+    _check(_lib.load().gdn_prefill(
+        _ptr(q, "q", dt, dev), _ptr(k, "k", dt, dev), _ptr(v, "v", dt, dev), _ptr(a, "a", dt, dev),
+        _ptr(b, "b", dt, dev), _ptr(A_log, "A_log", torch.float32, dev),
+        _ptr(dt_bias, "dt_bias", torch.float32, dev), pool.handle,
+        _ptr(cu_seqlens, "cu_seqlens", torch.int32, dev), _ptr(read_slot, "read_slot", torch.int32, dev),
+        _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev), nseq, T,
+        int(bool(keep_in_place)), _dtype_code(dt), _stream(dev)))
+    return out
+
+
+def gdn_verify(q, k, v, a, b, A_log, dt_bias, pool: GDNStatePool, cu_seqlens, read_slot, token_slot,
+               out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """As gdn_prefill, but the state after token t goes to token_slot[t] (a
+    state a token) and the read slot is left alone."""
+    T, nseq = _prefill_checks(q, k, v, a, b, A_log, dt_bias, pool, cu_seqlens, read_slot)
+    dt, dev = q.dtype, q.device
+    _numel(token_slot, T, "token_slot")
+    if out is None:
+        out = torch.empty((T, pool.hv, pool.dv), dtype=dt, device=dev)
+    _numel(out, T * pool.hv * pool.dv, "out")
+    _check(_lib.load().gdn_verify(
+        _ptr(q, "q", dt, dev), _ptr(k, "k", dt, dev), _ptr(v, "v", dt, dev), _ptr(a, "a", dt, dev),
+        _ptr(b, "b", dt, dev), _ptr(A_log, "A_log", torch.float32, dev),
+        _ptr(dt_bias, "dt_bias", torch.float32, dev), pool.handle,
+        _ptr(cu_seqlens, "cu_seqlens", torch.int32, dev), _ptr(read_slot, "read_slot", torch.int32, dev),
+        _ptr(token_slot, "token_slot", torch.int32, dev), _ptr(out, "out", dt, dev), nseq, T,
+        _dtype_code(dt), _stream(dev)))
+    return out
+
+
+def causal_conv1d_prefill(x, conv_pool: ConvStatePool, cu_seqlens, read_slot, w, bias, write_slot=None,
+                          token_slot=None, out: Optional[torch.Tensor] = None, silu: bool = True) -> torch.Tensor:
+    """The conv over many tokens a sequence: x [T][C] packed token-major; the
+    window continues from read_slot and ends in write_slot (None: in place), or
+    with token_slot [T] the window after each token goes to its slot."""
+    T = x.shape[0]
+    C = conv_pool.channels
+    nseq = cu_seqlens.numel() - 1
+    dt, dev = x.dtype, x.device
+    _numel(x, T * C, "x")
+    _numel(w, C * conv_pool.width, "w")
+    if bias is not None:
+        _numel(bias, C, "bias")
+    _numel(read_slot, nseq, "read_slot")
+    if write_slot is not None:
+        _numel(write_slot, nseq, "write_slot")
+    if token_slot is not None:
+        _numel(token_slot, T, "token_slot")
+    if out is None:
+        out = torch.empty((T, C), dtype=dt, device=dev)
+    _numel(out, T * C, "out")
+    _check(_lib.load().causal_conv1d_prefill(
+        _ptr(x, "x", dt, dev), conv_pool.handle, _ptr(cu_seqlens, "cu_seqlens", torch.int32, dev),
+        _ptr(read_slot, "read_slot", torch.int32, dev), _ptr(write_slot, "write_slot", torch.int32, dev),
+        _ptr(token_slot, "token_slot", torch.int32, dev), _ptr(w, "w", dt, dev), _ptr(bias, "bias", dt, dev),
+        int(bool(silu)), _ptr(out, "out", dt, dev), nseq, T, _dtype_code(dt), _stream(dev)))
     return out
 
 

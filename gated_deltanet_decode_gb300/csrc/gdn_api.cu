@@ -676,6 +676,145 @@ int gdn_layer_decode_commit(const void *x, conv_pool *cp, const void *w, const v
     return ok();
 }
 
+// ---- many tokens a sequence: gdn_prefill, gdn_verify, causal_conv1d_prefill ------
+
+static int check_tokens(int nseq, int total_tokens, const int32_t *cu_seqlens, const int32_t *read_slot,
+                        int dtype)
+{
+    if (nseq < 0 || total_tokens < 0)
+        return fail(GDN_EINVAL, "nseq=%d and total_tokens=%d must be >= 0", nseq, total_tokens);
+    if (!dtype_ok(dtype))
+        return fail(GDN_EINVAL, "bad dtype %d", dtype);
+    if (nseq > 0 && (!cu_seqlens || !read_slot))
+        return fail(GDN_EINVAL, "cu_seqlens and read_slot must be non-NULL");
+    return GDN_OK;
+}
+
+static int prefill_launch(const void *q, const void *k, const void *v, const void *a, const void *b,
+                          const float *A_log, const float *dt_bias, gdn_pool *pool, const int32_t *cu_seqlens,
+                          const int32_t *read_slot, const int32_t *write_slot, const int32_t *token_slot,
+                          void *out, int nseq, int total_tokens, int dtype, void *stream, const char *what)
+{
+    if (!pool)
+        return fail(GDN_EINVAL, "state pool is NULL");
+    int rc = check_tokens(nseq, total_tokens, cu_seqlens, read_slot, dtype);
+    if (rc)
+        return rc;
+    if (nseq == 0)
+        return ok();
+    if (total_tokens > 0) {
+        if (!q || !k || !v || !a || !b || !A_log || !dt_bias || !out)
+            return fail(GDN_EINVAL, "q, k, v, a, b, A_log, dt_bias and out must be non-NULL");
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v))
+            return fail(GDN_EINVAL, "q, k and v must be 16-byte aligned");
+    }
+    int *err = nullptr;
+    rc = device_error_ptr(&err);
+    if (rc)
+        return rc;
+    gdn::PrefillArgs s = {};
+    s.q = q;
+    s.k = k;
+    s.v = v;
+    s.a = a;
+    s.b = b;
+    s.A_log = A_log;
+    s.dt_bias = dt_bias;
+    s.pool = pool->data;
+    s.num_slots = pool->num_slots;
+    s.cu_seqlens = cu_seqlens;
+    s.read_slot = read_slot;
+    s.write_slot = write_slot;
+    s.token_slot = token_slot;
+    s.out = out;
+    s.nseq = nseq;
+    s.total_tokens = total_tokens;
+    s.hk = pool->dims.hk;
+    s.hv = pool->dims.hv;
+    s.dk = pool->dims.dk;
+    s.dv = pool->dims.dv;
+    s.err = err;
+    cudaError_t e = gdn::launch_gdn_prefill(s, dtype, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, what);
+    return ok();
+}
+
+int gdn_prefill(const void *q, const void *k, const void *v, const void *a, const void *b,
+                const float *A_log, const float *dt_bias, gdn_pool *pool, const int32_t *cu_seqlens,
+                const int32_t *read_slot, const int32_t *write_slot, void *out, int nseq, int total_tokens,
+                int keep_in_place, int dtype, void *stream)
+{
+    if (!keep_in_place && nseq > 0 && !write_slot)
+        return fail(GDN_EINVAL, "write_slot is NULL in twin mode");
+    return prefill_launch(q, k, v, a, b, A_log, dt_bias, pool, cu_seqlens, read_slot,
+                          keep_in_place ? nullptr : write_slot, nullptr, out, nseq, total_tokens, dtype,
+                          stream, "gdn_prefill launch");
+}
+
+int gdn_verify(const void *q, const void *k, const void *v, const void *a, const void *b,
+               const float *A_log, const float *dt_bias, gdn_pool *pool, const int32_t *cu_seqlens,
+               const int32_t *read_slot, const int32_t *token_slot, void *out, int nseq, int total_tokens,
+               int dtype, void *stream)
+{
+    if (!pool)
+        return fail(GDN_EINVAL, "state pool is NULL");
+    int rc = check_tokens(nseq, total_tokens, cu_seqlens, read_slot, dtype);
+    if (rc)
+        return rc;
+    if (nseq == 0 || total_tokens == 0)
+        return ok(); // no token, no state to keep
+    if (!token_slot)
+        return fail(GDN_EINVAL, "token_slot must be non-NULL");
+    return prefill_launch(q, k, v, a, b, A_log, dt_bias, pool, cu_seqlens, read_slot, nullptr, token_slot,
+                          out, nseq, total_tokens, dtype, stream, "gdn_verify launch");
+}
+
+int causal_conv1d_prefill(const void *x, conv_pool *cp, const int32_t *cu_seqlens, const int32_t *read_slot,
+                          const int32_t *write_slot, const int32_t *token_slot, const void *w,
+                          const void *bias, int silu, void *out, int nseq, int total_tokens, int dtype,
+                          void *stream)
+{
+    if (!cp)
+        return fail(GDN_EINVAL, "conv pool is NULL");
+    int rc = check_tokens(nseq, total_tokens, cu_seqlens, read_slot, dtype);
+    if (rc)
+        return rc;
+    if (dtype != cp->dtype)
+        return fail(GDN_EINVAL, "dtype %d does not match the conv pool's %d", dtype, cp->dtype);
+    if (nseq == 0)
+        return ok();
+    if (!w || (total_tokens > 0 && (!x || !out)))
+        return fail(GDN_EINVAL, "x, w and out must be non-NULL");
+    if ((x && !aligned16(x)) || !aligned16(w) || (out && !aligned16(out)) || (bias && !aligned16(bias)))
+        return fail(GDN_EINVAL, "x, w, bias and out must be 16-byte aligned");
+    int *err = nullptr;
+    rc = device_error_ptr(&err);
+    if (rc)
+        return rc;
+    gdn::ConvPrefillArgs s = {};
+    s.x = x;
+    s.conv = cp->data;
+    s.num_slots = cp->num_slots;
+    s.cu_seqlens = cu_seqlens;
+    s.read_slot = read_slot;
+    s.write_slot = write_slot;
+    s.token_slot = token_slot;
+    s.w = w;
+    s.bias = bias;
+    s.silu = silu ? 1 : 0;
+    s.out = out;
+    s.nseq = nseq;
+    s.total_tokens = total_tokens;
+    s.channels = cp->channels;
+    s.width = cp->width;
+    s.err = err;
+    cudaError_t e = gdn::launch_conv_prefill(s, dtype, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "causal_conv1d_prefill launch");
+    return ok();
+}
+
 // ---- gdn_layer_decode_noalloc ------------------------------------------------
 // gdn_layer_decode for callers that cannot allocate device memory: the work
 // counters of the launch come from a fixed array of this file, looked up once

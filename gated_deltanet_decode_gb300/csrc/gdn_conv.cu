@@ -123,6 +123,119 @@ __global__ void __launch_bounds__(kThreads) conv_decode_kernel(const ConvArgs p,
     Vec8<T>::store(conv_out + (size_t)(W - 2) * C, x);
 }
 
+// The conv over many tokens a sequence ("mstar PR #1139", section "Why":
+// prefill keeps the state in place): a thread owns 8 channels of one
+// sequence, keeps their window in registers and walks the tokens in order,
+// so each token's output equals one causal_conv1d_decode call.  The window
+// after the last token goes to the write slot (or back in place); with token
+// slots, the window after every token goes to that token's slot.
+template <typename T, int W>
+__global__ void __launch_bounds__(kThreads) conv_prefill_kernel(const ConvPrefillArgs p, int groups_per_row)
+{
+    wait_prior_grid();
+    const long long gid = (long long)blockIdx.x * kThreads + threadIdx.x;
+    const int r = (int)(gid / groups_per_row);
+    const int c0 = (int)(gid % groups_per_row) * kVec;
+    if (r >= p.nseq)
+        return;
+    const int C = p.channels;
+    const int t0 = p.cu_seqlens[r], t1 = p.cu_seqlens[r + 1];
+    const int rs = p.read_slot[r];
+    const bool in_place = p.write_slot == nullptr || p.token_slot != nullptr;
+    const int ws = in_place ? rs : p.write_slot[r];
+    const int cls = classify_seq(rs, ws, in_place, p.token_slot, t0, t1, p.total_tokens, p.num_slots);
+    T *out = reinterpret_cast<T *>(p.out) + c0;
+    if (cls != 1) {
+        if (cls < 0 && c0 == 0)
+            report(p.err, GDN_DEVERR_BAD_SLOT);
+        if (t0 >= 0 && t1 >= t0 && t1 <= p.total_tokens) {
+            float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int t = t0; t < t1; ++t)
+                Vec8<T>::store(out + (size_t)t * C, z);
+        }
+        return;
+    }
+    T *conv = reinterpret_cast<T *>(p.conv);
+    float win[W - 1][8];
+#pragma unroll
+    for (int j = 0; j < W - 1; ++j)
+        Vec8<T>::load(conv + ((size_t)rs * (W - 1) + j) * C + c0, win[j]);
+    float taps[8 * W];
+    {
+        const T *wp = reinterpret_cast<const T *>(p.w) + (size_t)c0 * W;
+#pragma unroll
+        for (int t = 0; t < W; ++t) {
+            float tmp[8];
+            Vec8<T>::load(wp + 8 * t, tmp);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                taps[8 * t + i] = tmp[i];
+        }
+    }
+    float bias[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (p.bias)
+        Vec8<T>::load(reinterpret_cast<const T *>(p.bias) + c0, bias);
+    const T *xp = reinterpret_cast<const T *>(p.x) + c0;
+    for (int t = t0; t < t1; ++t) {
+        float x[8], y[8];
+        Vec8<T>::load(xp + (size_t)t * C, x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float wi[W], wn[W - 1];
+#pragma unroll
+            for (int j = 0; j < W; ++j)
+                wi[j] = taps[i * W + j];
+#pragma unroll
+            for (int j = 0; j < W - 1; ++j)
+                wn[j] = win[j][i];
+            y[i] = conv_channel<W>(wn, x[i], wi, bias[i], p.silu != 0);
+        }
+        Vec8<T>::store(out + (size_t)t * C, y);
+        // the window moves on by one token; values stay in the activation type
+#pragma unroll
+        for (int j = 0; j + 1 < W - 1; ++j)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                win[j][i] = win[j + 1][i];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            win[W - 2][i] = x[i];
+        if (p.token_slot) {
+            const int ts = p.token_slot[t];
+#pragma unroll
+            for (int j = 0; j < W - 1; ++j)
+                Vec8<T>::store(conv + ((size_t)ts * (W - 1) + j) * C + c0, win[j]);
+        }
+    }
+    if (!p.token_slot) {
+#pragma unroll
+        for (int j = 0; j < W - 1; ++j)
+            Vec8<T>::store(conv + ((size_t)ws * (W - 1) + j) * C + c0, win[j]);
+    }
+}
+
+template <typename T, int W>
+cudaError_t launch_prefill_w(const ConvPrefillArgs &a, cudaStream_t s)
+{
+    const int groups = a.channels / kVec;
+    const long long threads = (long long)a.nseq * groups;
+    if (threads == 0)
+        return cudaSuccess;
+    const long long blocks = (threads + kThreads - 1) / kThreads;
+    return launch_pdl(conv_prefill_kernel<T, W>, dim3((unsigned)blocks), dim3(kThreads), 0, s, a, groups);
+}
+
+template <typename T>
+cudaError_t launch_prefill_t(const ConvPrefillArgs &a, cudaStream_t s)
+{
+    switch (a.width) {
+    case 2: return launch_prefill_w<T, 2>(a, s);
+    case 3: return launch_prefill_w<T, 3>(a, s);
+    case 4: return launch_prefill_w<T, 4>(a, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 template <typename T, int W>
 cudaError_t launch_w(const ConvArgs &a, cudaStream_t s)
 {
@@ -150,6 +263,11 @@ cudaError_t launch_t(const ConvArgs &a, cudaStream_t s)
 cudaError_t launch_conv(const ConvArgs &a, int dtype, cudaStream_t s)
 {
     return dtype == GDN_BF16 ? launch_t<__nv_bfloat16>(a, s) : launch_t<float>(a, s);
+}
+
+cudaError_t launch_conv_prefill(const ConvPrefillArgs &a, int dtype, cudaStream_t s)
+{
+    return dtype == GDN_BF16 ? launch_prefill_t<__nv_bfloat16>(a, s) : launch_prefill_t<float>(a, s);
 }
 
 } // namespace gdn

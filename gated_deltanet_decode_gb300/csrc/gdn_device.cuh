@@ -137,4 +137,27 @@ __device__ __forceinline__ int classify_row(int rs, int ws, int num_slots, bool 
     return 1;
 }
 
+// Sequence classification of the many-token kernels (0 padding, 1 real,
+// -1 bad): a token range outside [0, total_tokens) is bad; with token slots
+// every token's slot must be a real slot other than the read slot; otherwise
+// as classify_row.
+__device__ __forceinline__ int classify_seq(int rs, int ws, bool in_place, const int32_t *token_slot,
+                                            int t0, int t1, int total_tokens, int num_slots)
+{
+    if (t0 < 0 || t1 < t0 || t1 > total_tokens)
+        return -1;
+    if (token_slot) {
+        const int cls = classify_row(rs, rs, num_slots, true);
+        if (cls != 1)
+            return cls;
+        for (int t = t0; t < t1; ++t) {
+            const int s = token_slot[t];
+            if (s <= 0 || s >= num_slots || s == rs)
+                return -1;
+        }
+        return 1;
+    }
+    return classify_row(rs, ws, num_slots, in_place);
+}
+
 } // namespace gdn

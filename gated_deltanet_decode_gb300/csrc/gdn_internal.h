@@ -66,11 +66,40 @@ struct ConvArgs {
     int *err;
 };
 
+// Many tokens a sequence (prefill, verification).  Sequence r holds tokens
+// [cu_seqlens[r], cu_seqlens[r+1]) of the packed token-major inputs.
+struct PrefillArgs {
+    const void *q, *k, *v, *a, *b;
+    const float *A_log, *dt_bias;
+    float *pool;
+    int num_slots;
+    const int32_t *cu_seqlens, *read_slot;
+    const int32_t *write_slot; // NULL: in place
+    const int32_t *token_slot; // non-NULL: the state after each token goes to token_slot[t]
+    void *out;
+    int nseq, total_tokens, hk, hv, dk, dv;
+    int *err;
+};
+
+struct ConvPrefillArgs {
+    const void *x; // [T][C]
+    void *conv;
+    int num_slots;
+    const int32_t *cu_seqlens, *read_slot, *write_slot, *token_slot;
+    const void *w, *bias;
+    int silu;
+    void *out;
+    int nseq, total_tokens, channels, width;
+    int *err;
+};
+
 // Launchers return cudaSuccess or the launch error.  Shapes were validated by
 // the caller.
 cudaError_t launch_gdn_step(const StepArgs &a, int dtype, cudaStream_t s);
 cudaError_t launch_gdn_layer(const StepArgs &a, int dtype, cudaStream_t s);
 cudaError_t launch_conv(const ConvArgs &a, int dtype, cudaStream_t s);
+cudaError_t launch_gdn_prefill(const PrefillArgs &a, int dtype, cudaStream_t s);
+cudaError_t launch_conv_prefill(const ConvPrefillArgs &a, int dtype, cudaStream_t s);
 
 // True when the state kernels are built for (dk, dv).
 bool step_shape_supported(int dk, int dv);

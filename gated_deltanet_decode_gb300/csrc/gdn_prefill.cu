@@ -1,0 +1,380 @@
+// gdn_prefill / gdn_verify: the gated delta rule over many tokens a sequence,
+// sm_103a.
+//
+// A prefill is the decode rule applied token after token, keeping the state
+// ("mstar PR #1139", section "Why": the rule is the recurrent state update,
+// and prefill keeps the state in place); verification keeps the state after
+// every token in a slot of its own (section "What changed": speculative
+// decoding holds a state per token, so twin slots do not apply to it).
+//
+// A CTA owns RB = 4096 / dk value rows of one (sequence, value head): 16 KiB
+// of fp32 state, read once into registers (16 floats a lane, the decode
+// kernel's geometry) and written once at the end (or once a token when
+// verifying).  The tokens stream through a ring of shared-memory stages: a
+// loader warp computes the gates 32 tokens at a time and bulk-copies each
+// token's raw q, k and v chunk; the 8 consumer warps normalise q and k (one
+// channel a thread, a CTA-wide sum through an mbarrier) and update the state
+// rows exactly as the decode kernel does, with the same operations in the
+// same order, so T tokens of a prefill equal T decode steps bit for bit.
+//
+// The rule is sequential in the tokens: a CTA's work is one token after the
+// other, and the launch has nseq * hv * (dv / RB) CTAs.  (The chunked form,
+// which turns runs of tokens into dense products for the tensor cores, is a
+// different kernel; this one is exact with respect to the decode step.)
+#include "gdn_device.cuh"
+#include "gdn_internal.h"
+#include "gdn_ptx.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kWarps = 8;                    // consumer warps
+constexpr int kConsumerThreads = kWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32; // + the loader warp
+constexpr int kStages = 8;                   // token ring depth
+constexpr float kL2Eps = 1e-6f;
+
+template <int DK> struct PGeo {
+    static_assert(DK >= 16 && DK <= 256 && DK % 16 == 0, "dk");
+    static constexpr int LPR = DK / 16;      // lanes per state row
+    static constexpr int RPW = 32 / LPR;     // state rows per warp
+    static constexpr int RB = RPW * kWarps;  // state rows per CTA (4096 / DK)
+};
+
+// One token's raw inputs: q[DK] | k[DK] | v[RB], activation type.
+template <typename T, int DK> struct PStage {
+    static constexpr int E = sizeof(T);
+    static constexpr int QK = 0;
+    static constexpr int V = 2 * DK * E;
+    static constexpr int BYTES = (V + PGeo<DK>::RB * E + 15) & ~15;
+};
+
+template <typename T>
+__device__ __forceinline__ float sh_val(const unsigned char *base, int idx)
+{
+    return to_f(reinterpret_cast<const T *>(base)[idx]);
+}
+template <typename T>
+__device__ __forceinline__ float gl_val(const void *base, size_t idx)
+{
+    return to_f(reinterpret_cast<const T *>(base)[idx]);
+}
+
+template <typename T, int DK>
+__global__ void __launch_bounds__(kThreads, 2) gdn_prefill_kernel(const PrefillArgs p)
+{
+    using G = PGeo<DK>;
+    using L = PStage<T, DK>;
+    constexpr int RB = G::RB;
+    constexpr int E = L::E;
+
+    __shared__ __align__(128) unsigned char ring[kStages * L::BYTES];
+    __shared__ __align__(8) unsigned long long bars[2 * kStages + 1]; // full, empty, qk
+    __shared__ __align__(16) float qkbuf[2][2 * DK];                 // a token's q | k values
+    __shared__ float part[2][kWarps][2];
+    __shared__ float gate_a[kStages], gate_b[kStages];
+    __shared__ float tab_a[32], tab_b[32];
+    __shared__ int s_cls, s_t0, s_t1, s_rs, s_ws;
+    __shared__ int abort_flag, issued_n, consumed_n;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int chunks = (p.dv + RB - 1) / RB;
+    const int chunk = blockIdx.x % chunks;
+    const int rh = blockIdx.x / chunks;
+    const int h = rh % p.hv, r = rh / p.hv;
+    const int g = h / (p.hv / p.hk);
+    const int rows = min(RB, p.dv - chunk * RB);
+    const bool verify = p.token_slot != nullptr;
+    auto full_bar = [&](int s) { return sm_addr(&bars[s]); };
+    auto empty_bar = [&](int s) { return sm_addr(&bars[kStages + s]); };
+    const uint32_t qk_bar = sm_addr(&bars[2 * kStages]);
+    auto timeout = [&]() {
+        report(p.err, GDN_DEVERR_TIMEOUT);
+        atomicExch(&abort_flag, 1);
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 2); // copies + gates
+            mbar_init(empty_bar(s), kWarps);
+        }
+        mbar_init(qk_bar, kWarps);
+        abort_flag = 0;
+        issued_n = 0;
+        consumed_n = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    wait_prior_grid();
+
+    // the sequence: its tokens, its slots, and whether it is real
+    if (warp == kWarps) {
+        const int t0 = p.cu_seqlens[r], t1 = p.cu_seqlens[r + 1];
+        const int rs = p.read_slot[r];
+        const bool in_place = p.write_slot == nullptr || verify;
+        const int ws = in_place ? rs : p.write_slot[r];
+        int cls;
+        if (t0 < 0 || t1 < t0 || t1 > p.total_tokens)
+            cls = -1;
+        else
+            cls = classify_row(rs, ws, p.num_slots, in_place);
+        if (cls == 1 && verify) {
+            bool bad = false;
+            for (int t = t0 + lane; t < t1; t += 32) {
+                const int s = p.token_slot[t];
+                bad |= s <= 0 || s >= p.num_slots || s == rs;
+            }
+            if (__any_sync(0xffffffffu, bad))
+                cls = -1;
+        }
+        if (lane == 0) {
+            if (cls < 0 && h == 0 && chunk == 0)
+                report(p.err, GDN_DEVERR_BAD_SLOT);
+            s_cls = cls;
+            s_t0 = t0;
+            s_t1 = t1;
+            s_rs = rs;
+            s_ws = ws;
+        }
+    }
+    __syncthreads();
+    const int cls = s_cls, t0 = s_t0, t1 = s_t1;
+    const size_t out_tok = (size_t)p.hv * p.dv; // output elements a token
+    T *outb = reinterpret_cast<T *>(p.out) + (size_t)h * p.dv + (size_t)chunk * RB;
+    if (cls != 1) {
+        // padding or bad: zero outputs (when the token range is sane), no slot touched
+        if (t0 >= 0 && t1 >= t0 && t1 <= p.total_tokens) {
+            const long long n_out = (long long)(t1 - t0) * rows;
+            for (long long e = tid; e < n_out; e += kThreads)
+                outb[(size_t)(t0 + e / rows) * out_tok + (size_t)(e % rows)] = from_f<T>(0.f);
+        }
+        return;
+    }
+    const int n = t1 - t0;
+    const int rs = s_rs, ws = s_ws;
+
+    if (warp == kWarps) {
+        // ============================ loader ============================
+        // Gates 32 tokens at a time, one a lane; then one lane streams the
+        // tokens' raw q, k and v chunk into the ring: copies with their byte
+        // count (first arrival on "full"), gates (second arrival).
+        const unsigned char *qp = reinterpret_cast<const unsigned char *>(p.q);
+        const unsigned char *kp = reinterpret_cast<const unsigned char *>(p.k);
+        const unsigned char *vp = reinterpret_cast<const unsigned char *>(p.v);
+        const float al = p.A_log[h], dt = p.dt_bias[h];
+        bool stop = false;
+        for (int base = 0; base < n && !stop; base += 32) {
+            const int kk = base + lane;
+            float ga = 0.f, gb = 0.f;
+            if (kk < n) {
+                const size_t t = (size_t)(t0 + kk);
+                ga = gate_alpha(al, gl_val<T>(p.a, t * p.hv + h), dt);
+                gb = gate_beta(gl_val<T>(p.b, t * p.hv + h));
+            }
+            tab_a[lane] = ga;
+            tab_b[lane] = gb;
+            __syncwarp();
+            if (lane == 0) {
+                const int nb = min(32, n - base);
+                for (int j = 0; j < nb; ++j) {
+                    const int k = base + j, s = k % kStages;
+                    if (!mbar_wait(empty_bar(s), (uint32_t)((k / kStages) & 1) ^ 1u)) {
+                        timeout();
+                        stop = true;
+                        break;
+                    }
+                    if (*(volatile int *)&abort_flag) {
+                        stop = true;
+                        break;
+                    }
+                    const size_t t = (size_t)(t0 + k);
+                    unsigned char *st = ring + (size_t)s * L::BYTES;
+                    const uint32_t fb = full_bar(s);
+                    mbar_arrive_tx(fb, (uint32_t)((2 * DK + rows) * E));
+                    bulk_load(sm_addr(st + L::QK), qp + (t * p.hk + g) * DK * E, DK * E, fb);
+                    bulk_load(sm_addr(st + L::QK + DK * E), kp + (t * p.hk + g) * DK * E, DK * E, fb);
+                    bulk_load(sm_addr(st + L::V), vp + ((t * p.hv + h) * p.dv + (size_t)chunk * RB) * E,
+                              (uint32_t)(rows * E), fb);
+                    gate_a[s] = tab_a[j];
+                    gate_b[s] = tab_b[j];
+                    mbar_arrive(fb);
+                    issued_n = k + 1;
+                }
+            }
+            stop = __shfl_sync(0xffffffffu, stop, 0);
+            __syncwarp();
+        }
+    } else {
+        // =========================== consumers ==========================
+        const int lrow = lane / G::LPR, lcol = lane % G::LPR;
+        const int t = tid; // consumer index 0..255
+        const int row = warp * G::RPW + lrow;
+        const bool live_row = row < rows;
+        const size_t row_off = ((size_t)h * p.dv + (size_t)chunk * RB + row) * DK + 4 * lcol;
+        const size_t slot_floats = (size_t)p.hv * p.dv * DK;
+        float4 sv[4];
+#pragma unroll
+        for (int mm = 0; mm < 4; ++mm)
+            sv[mm] = live_row ? ld_state(p.pool + (size_t)rs * slot_floats + row_off + 4 * G::LPR * mm)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        bool ok = true;
+        for (int k = 0; k < n; ++k) {
+            const int s = k % kStages;
+            if (!mbar_wait(full_bar(s), (uint32_t)((k / kStages) & 1))) {
+                timeout();
+                ok = false;
+                break;
+            }
+            const unsigned char *st = ring + (size_t)s * L::BYTES;
+            const int qb = k & 1;
+            float *qk = qkbuf[qb];
+            // q and k values, their norms, k^ . q^ (as at a decode chain's start)
+            float psq = 0.f, psk = 0.f;
+            for (int c = t; c < 2 * DK; c += kConsumerThreads) {
+                const float val = sh_val<T>(st + L::QK, c);
+                qk[c] = val;
+                if (c < DK)
+                    psq = __fmaf_rn(val, val, psq);
+                else
+                    psk = __fmaf_rn(val, val, psk);
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) {
+                psq += __shfl_xor_sync(0xffffffffu, psq, off);
+                psk += __shfl_xor_sync(0xffffffffu, psk, off);
+            }
+            if (lane == 0) {
+                part[qb][warp][0] = psq;
+                part[qb][warp][1] = psk;
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(qk_bar);
+            if (!mbar_wait(qk_bar, (uint32_t)(k & 1))) {
+                timeout();
+                ok = false;
+                break;
+            }
+            float qq = 0.f, kk2 = 0.f;
+#pragma unroll
+            for (int wi = 0; wi < kWarps; ++wi) {
+                qq += part[qb][wi][0];
+                kk2 += part[qb][wi][1];
+            }
+            const float inv_q = __fdiv_rn(1.0f, sqrtf(qq + kL2Eps)) * rsqrtf((float)DK);
+            const float inv_k = __fdiv_rn(1.0f, sqrtf(kk2 + kL2Eps));
+            float pqk = 0.f;
+            for (int i = lane; i < DK; i += 32)
+                pqk = __fmaf_rn(qk[i], qk[DK + i], pqk);
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1)
+                pqk += __shfl_xor_sync(0xffffffffu, pqk, off);
+            const float kappa = pqk * inv_q * inv_k;
+            const float vi = live_row ? sh_val<T>(st + L::V, row) : 0.f;
+            const float alpha = gate_a[s], beta = gate_b[s];
+            // the stage is no longer needed: its q/k values are in qkbuf
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(empty_bar(s));
+            float4 kh[4], qh[4];
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) {
+                const int j = 4 * (lcol + G::LPR * mm);
+                qh[mm] = *reinterpret_cast<const float4 *>(&qk[j]);
+                kh[mm] = *reinterpret_cast<const float4 *>(&qk[DK + j]);
+            }
+            float2 u2 = make_float2(0.f, 0.f), w2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) {
+                u2 = fma2(make_float2(sv[mm].x, sv[mm].y), make_float2(kh[mm].x, kh[mm].y), u2);
+                u2 = fma2(make_float2(sv[mm].z, sv[mm].w), make_float2(kh[mm].z, kh[mm].w), u2);
+                w2 = fma2(make_float2(sv[mm].x, sv[mm].y), make_float2(qh[mm].x, qh[mm].y), w2);
+                w2 = fma2(make_float2(sv[mm].z, sv[mm].w), make_float2(qh[mm].z, qh[mm].w), w2);
+            }
+            float u = u2.x + u2.y, wd = w2.x + w2.y;
+#pragma unroll
+            for (int off = G::LPR / 2; off >= 1; off >>= 1) {
+                u += __shfl_xor_sync(0xffffffffu, u, off);
+                wd += __shfl_xor_sync(0xffffffffu, wd, off);
+            }
+            u *= inv_k;  // S . k^
+            wd *= inv_q; // S . q^
+            if (live_row) {
+                const float c = beta * __fmaf_rn(-alpha, u, vi);
+                const float o = __fmaf_rn(c, kappa, alpha * wd);
+                const float ck = c * inv_k;
+                const float2 a2 = make_float2(alpha, alpha), c2 = make_float2(ck, ck);
+#pragma unroll
+                for (int mm = 0; mm < 4; ++mm) {
+                    const float2 lo = fma2(c2, make_float2(kh[mm].x, kh[mm].y),
+                                           mul2(a2, make_float2(sv[mm].x, sv[mm].y)));
+                    const float2 hi = fma2(c2, make_float2(kh[mm].z, kh[mm].w),
+                                           mul2(a2, make_float2(sv[mm].z, sv[mm].w)));
+                    sv[mm] = make_float4(lo.x, lo.y, hi.x, hi.y);
+                }
+                const size_t tok = (size_t)(t0 + k);
+                if (lcol == 0)
+                    outb[tok * out_tok + row] = from_f<T>(o);
+                if (verify) {
+                    float *dst = p.pool + (size_t)p.token_slot[tok] * slot_floats + row_off;
+#pragma unroll
+                    for (int mm = 0; mm < 4; ++mm)
+                        st_state(dst + 4 * G::LPR * mm, sv[mm]);
+                }
+            }
+            if (t == 0)
+                consumed_n = k + 1;
+        }
+        if (ok && !verify && live_row) {
+            float *dst = p.pool + (size_t)ws * slot_floats + row_off;
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm)
+                st_state(dst + 4 * G::LPR * mm, sv[mm]);
+        }
+    }
+
+    // A CTA whose waits ran out leaves no copy in flight: the loader waits
+    // (bounded) for every stage it filled that was not consumed.
+    asm volatile("barrier.sync 0;" ::: "memory");
+    if (abort_flag && tid == kConsumerThreads) {
+        for (int k = consumed_n; k < issued_n; ++k)
+            mbar_wait(full_bar(k % kStages), (uint32_t)((k / kStages) & 1));
+    }
+}
+
+template <typename T, int DK>
+cudaError_t launch_dk(const PrefillArgs &a, cudaStream_t s)
+{
+    constexpr int RB = PGeo<DK>::RB;
+    const long long chunks = (a.dv + RB - 1) / RB;
+    const long long ctas = (long long)a.nseq * a.hv * chunks;
+    if (ctas == 0)
+        return cudaSuccess;
+    if (ctas > 0x7fffffffll)
+        return cudaErrorInvalidValue;
+    return launch_pdl(gdn_prefill_kernel<T, DK>, dim3((unsigned)ctas), dim3(kThreads), 0, s, a);
+}
+
+template <typename T>
+cudaError_t launch_t(const PrefillArgs &a, cudaStream_t s)
+{
+    switch (a.dk) {
+    case 16: return launch_dk<T, 16>(a, s);
+    case 32: return launch_dk<T, 32>(a, s);
+    case 64: return launch_dk<T, 64>(a, s);
+    case 128: return launch_dk<T, 128>(a, s);
+    case 256: return launch_dk<T, 256>(a, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+} // namespace
+
+cudaError_t launch_gdn_prefill(const PrefillArgs &a, int dtype, cudaStream_t s)
+{
+    return dtype == GDN_BF16 ? launch_t<__nv_bfloat16>(a, s) : launch_t<float>(a, s);
+}
+
+} // namespace gdn

@@ -49,6 +49,7 @@
 // value head writes it.  The arithmetic per row is the same in every
 // schedule, so twin and in place give bit-identical values.
 #include "gdn_device.cuh"
+#include "gdn_ptx.cuh"
 #include "gdn_internal.h"
 
 namespace gdn {
@@ -58,8 +59,6 @@ namespace {
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr float kL2Eps = 1e-6f;
-constexpr long long kWaitLimit = 1ll << 20;
-constexpr uint32_t kSuspendHintNs = 1000;
 constexpr int kMaxStages = 8;
 constexpr int kClaimMinItemsPerCta = 12;
 
@@ -75,72 +74,6 @@ template <int DK> struct Geo {
     static constexpr int RPW = 32 / LPR;             // state rows per warp
     static constexpr int RB = RPW * kConsumerWarps;  // state rows per item (4096 / DK)
 };
-
-// ---------------------------------------------------------------------------
-// PTX wrappers: mbarrier, bulk copy, packed fp32 arithmetic
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t sm_addr(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-// try_wait suspends the thread until the phase completes or the hint (ns)
-// runs out, so waiting warps do not take issue slots from working ones.
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok)
-                 : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
-                 : "memory");
-    return ok != 0;
-}
-// Bounded wait for the phase of `parity` to complete; false when it ran out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
-{
-    for (long long i = 0; i < kWaitLimit; ++i)
-        if (mbar_try(bar, parity))
-            return true;
-    return false;
-}
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-// Two-wide fp32 FMA and multiply: each half rounds exactly like the scalar op.
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
-{
-    unsigned long long A = *reinterpret_cast<unsigned long long *>(&a);
-    unsigned long long B = *reinterpret_cast<unsigned long long *>(&b);
-    unsigned long long Cc = *reinterpret_cast<unsigned long long *>(&c);
-    unsigned long long D;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(D) : "l"(A), "l"(B), "l"(Cc));
-    return *reinterpret_cast<float2 *>(&D);
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b)
-{
-    unsigned long long A = *reinterpret_cast<unsigned long long *>(&a);
-    unsigned long long B = *reinterpret_cast<unsigned long long *>(&b);
-    unsigned long long D;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(D) : "l"(A), "l"(B));
-    return *reinterpret_cast<float2 *>(&D);
-}
 
 template <typename T>
 __device__ __forceinline__ float ld_act(const void *base, size_t idx)
@@ -455,11 +388,16 @@ gdn_stream_kernel(const StepArgs p, const Sched sc)
         if (counted) {
             int last = 0;
             if (lane == 0) {
-                __threadfence();
-                last = atomicAdd(p.work + 1, 1u) == gridDim.x - 1;
+                // release: this producer's slot loads come before its count;
+                // acquire: the last one's writes come after every other's loads
+                unsigned done;
+                asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                             : "=r"(done)
+                             : "l"(p.work + 1)
+                             : "memory");
+                last = done == gridDim.x - 1;
             }
             if (__shfl_sync(0xffffffffu, last, 0)) {
-                __threadfence();
                 if (p.commit) {
                     // the whole warp swaps the tables, 256 rows a round, loads first
                     int32_t *rs = const_cast<int32_t *>(p.read_slot);

@@ -124,6 +124,40 @@ class Gen:
         ws[real] = perm[n_real:2 * n_real] if twin else perm[:n_real]
         return rs, ws
 
+    def seq_tables(self, lens, num_slots: int, n_pad: int = 0):
+        """Packed sequences of the given lengths for the many-token calls:
+        (cu_seqlens [nseq+1], read_slot [nseq], write_slot [nseq],
+        token_slot [T]), int32.
+
+        n_pad sequences, at random positions, are padding (slots 0, token
+        slots 0).  Real sequences take distinct slots from a random
+        permutation of 1..num_slots-1: reads first, then writes, then one slot
+        a token of the real sequences (for a state a token)."""
+        lens = np.asarray(lens, dtype=np.int64)
+        nseq = len(lens)
+        cu = np.zeros(nseq + 1, dtype=np.int32)
+        cu[1:] = np.cumsum(lens)
+        pad = np.zeros(nseq, dtype=bool)
+        if n_pad:
+            pad[self.rng.choice(nseq, size=n_pad, replace=False)] = True
+        n_real = int((~pad).sum())
+        n_tok = int(lens[~pad].sum())
+        need = 2 * n_real + n_tok
+        if need > num_slots - 1:
+            raise ValueError(f"the sequences need {need} slots, the pool has {num_slots - 1}")
+        perm = self.rng.permutation(np.arange(1, num_slots, dtype=np.int32))
+        rs = np.zeros(nseq, dtype=np.int32)
+        ws = np.zeros(nseq, dtype=np.int32)
+        rs[~pad] = perm[:n_real]
+        ws[~pad] = perm[n_real:2 * n_real]
+        ts = np.zeros(int(cu[-1]), dtype=np.int32)
+        nxt = 2 * n_real
+        for r in range(nseq):
+            if not pad[r]:
+                ts[cu[r]:cu[r + 1]] = perm[nxt:nxt + lens[r]]
+                nxt += int(lens[r])
+        return cu, rs, ws, ts
+
 
 # ---------------------------------------------------------------------------
 # torch helpers (plumbing only)

@@ -197,6 +197,48 @@ int gdn_layer_decode(const void *x, conv_pool *cp, const void *w, const void *bi
                      gdn_pool *pool, const int32_t *read_slot, const int32_t *write_slot,
                      void *out, int rows, int keep_in_place, int dtype, void *stream);
 
+/* ---- many tokens a sequence -------------------------------------------- *
+ * Packed sequences: sequence r holds tokens [cu_seqlens[r], cu_seqlens[r+1])
+ * of the token-major inputs (cu_seqlens [nseq+1] int32 on the device,
+ * cu_seqlens[0] = 0, non-decreasing, cu_seqlens[nseq] = total_tokens; a
+ * range outside [0, total_tokens] makes the sequence bad).  read_slot,
+ * write_slot [nseq]; token_slot [total_tokens].  A sequence whose read slot
+ * is 0 is padding (outputs zero, no slot touched); bad slots skip the
+ * sequence, zero its outputs and set the device error word.
+ *
+ * gdn_prefill: the rule applied token after token, from the state in
+ * read_slot[r]; the final state goes to write_slot[r] (twin) or back to
+ * read_slot[r] (keep_in_place != 0, write_slot may be NULL).  ("mstar PR
+ * #1139", "Why": the rule is the recurrent state update of one token, and
+ * prefill keeps the state in place.)  Each token's output and every state
+ * equal, bit for bit, the same tokens fed one decode step at a time
+ * (gdn_decode_step, in place or twin).
+ *   q, k [T][hk][dk]   v, out [T][hv][dv]   a, b [T][hv]   A_log, dt_bias [hv]
+ *   q, k and v are bulk-copied: 16-byte aligned.
+ * gdn_verify: as gdn_prefill, but the state after token t goes to
+ * token_slot[t] and the read slot is left alone: a state a token, for
+ * speculative decoding ("mstar PR #1139", "What changed": speculative
+ * decoding holds a state per token).  Token slots must be real slots other
+ * than the sequence's read slot.
+ * causal_conv1d_prefill: the conv over a sequence, continuing the window in
+ * read_slot[r]: x, out [T][C] (rows packed, C the pool's channels); the
+ * window after the last token goes to write_slot[r] (NULL: in place), or,
+ * when token_slot is given, the window after token t goes to token_slot[t].
+ * Each token's output equals one causal_conv1d_decode call.  x, w, bias and
+ * out 16-byte aligned. */
+int gdn_prefill(const void *q, const void *k, const void *v, const void *a, const void *b,
+                const float *A_log, const float *dt_bias, gdn_pool *pool, const int32_t *cu_seqlens,
+                const int32_t *read_slot, const int32_t *write_slot, void *out, int nseq, int total_tokens,
+                int keep_in_place, int dtype, void *stream);
+int gdn_verify(const void *q, const void *k, const void *v, const void *a, const void *b,
+               const float *A_log, const float *dt_bias, gdn_pool *pool, const int32_t *cu_seqlens,
+               const int32_t *read_slot, const int32_t *token_slot, void *out, int nseq, int total_tokens,
+               int dtype, void *stream);
+int causal_conv1d_prefill(const void *x, conv_pool *cp, const int32_t *cu_seqlens, const int32_t *read_slot,
+                          const int32_t *write_slot, const int32_t *token_slot, const void *w,
+                          const void *bias, int silu, void *out, int nseq, int total_tokens, int dtype,
+                          void *stream);
+
 /* ---- gdn_layer_decode_commit ------------------------------------------- *
  * gdn_layer_decode in twin mode followed by gdn_commit, in one launch: the
  * same values, then read_slot[r] and write_slot[r] swapped for every row

@@ -207,3 +207,43 @@ def test_small_entry_points_checks(L):
     assert L.gdn_pool_zero_slots(pool, None, 2, None) == EINVAL
     assert L.gdn_pool_zero_slots(None, FAKE, 2, None) == EINVAL
     L.gdn_state_pool_destroy(pool)
+
+
+def test_prefill_argument_checks(L):
+    """gdn_prefill, gdn_verify and causal_conv1d_prefill reject bad arguments
+    on the host and return at once when there is nothing to launch."""
+    rc, pool = _wrap(L, hk=2, hv=2, dk=16, dv=16)
+    assert rc == 0
+    cp = ctypes.c_void_p()
+    assert L.conv_state_pool_wrap(FAKE, 9, 96, 4, 0, ctypes.byref(cp)) == 0
+    P = FAKE
+
+    def prefill(nseq=2, T=5, pool_=pool, ws=P, inplace=0, dtype=0, q=P):
+        return L.gdn_prefill(q, P, P, P, P, P, P, pool_, P, P, ws, P, nseq, T, inplace, dtype, None)
+
+    assert prefill(pool_=None) == EINVAL
+    assert prefill(nseq=-1) == EINVAL
+    assert prefill(T=-1) == EINVAL
+    assert prefill(dtype=3) == EINVAL
+    assert prefill(ws=None) == EINVAL and b"write_slot" in L.gdn_last_error()
+    assert prefill(q=P + 8) == EINVAL and b"aligned" in L.gdn_last_error()
+    assert prefill(nseq=0) == 0
+    assert prefill(nseq=0, ws=None, inplace=1) == 0
+
+    def verify(nseq=2, T=5, ts=P):
+        return L.gdn_verify(P, P, P, P, P, P, P, pool, P, P, ts, P, nseq, T, 0, None)
+
+    assert verify(ts=None) == EINVAL and b"token_slot" in L.gdn_last_error()
+    assert verify(T=0, ts=None) == 0      # no token, no state to keep
+    assert verify(nseq=0) == 0
+
+    def conv(nseq=2, T=5, cpool=cp, x=P, dtype=0):
+        return L.causal_conv1d_prefill(x, cpool, P, P, None, None, P, None, 1, P, nseq, T, dtype, None)
+
+    assert conv(cpool=None) == EINVAL
+    assert conv(dtype=1) == EINVAL and b"dtype" in L.gdn_last_error()
+    assert conv(x=P + 4) == EINVAL
+    assert conv(x=None) == EINVAL
+    assert conv(nseq=0) == 0
+    L.conv_state_pool_destroy(cp)
+    L.gdn_state_pool_destroy(pool)
