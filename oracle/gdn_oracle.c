@@ -497,6 +497,31 @@ int gdn_oracle_conv_prefill(int nseq, int C, int W, int num_slots, const int32_t
     return bad;
 }
 
+/*
+ * Snapshots and forks: slot dst[i] of a pool receives a copy of slot src[i]
+ * ("mstar PR #1139", "What changed": prefix-cache snapshots of the conv window
+ * and the state; "mstar PR #965", "What changed": prefix-cache checkpoints).
+ * pool: [num_slots][slot_elems].  A source outside [0, num_slots) or a
+ * destination outside [1, num_slots) (the null slot is never written) makes
+ * the pair bad: it is skipped.  Destinations must be distinct and no
+ * destination may be a source (then the order of the copies does not
+ * matter).  Returns the number of bad pairs.
+ */
+int gdn_oracle_copy_slots(int num_slots, long slot_elems, double *pool, const int32_t *src,
+                          const int32_t *dst, int n)
+{
+    int bad = 0;
+    for (int i = 0; i < n; ++i) {
+        if (src[i] < 0 || src[i] >= num_slots || dst[i] <= 0 || dst[i] >= num_slots) {
+            ++bad;
+            continue;
+        }
+        for (long e = 0; e < slot_elems; ++e)
+            pool[(size_t)dst[i] * slot_elems + e] = pool[(size_t)src[i] * slot_elems + e];
+    }
+    return bad;
+}
+
 /* Commit of a twin step: the read and write slot of every row trade places. */
 void gdn_oracle_commit(int rows, int32_t *read_slot, int32_t *write_slot)
 {

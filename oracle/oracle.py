@@ -29,7 +29,8 @@ _lib = None
 
 __all__ = [
     "build", "lib", "softplus", "alpha", "beta", "round_bf16", "l2norm", "rule", "head",
-    "conv_row", "step", "conv_step", "layer", "prefill", "conv_prefill", "commit", "max_threads",
+    "conv_row", "step", "conv_step", "layer", "prefill", "conv_prefill", "copy_slots", "commit",
+    "max_threads",
 ]
 
 
@@ -92,6 +93,8 @@ def lib():
             L.gdn_oracle_conv_prefill.restype = _I
             L.gdn_oracle_conv_prefill.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I,
                                                   _P]
+            L.gdn_oracle_copy_slots.restype = _I
+            L.gdn_oracle_copy_slots.argtypes = [_I, ctypes.c_long, _P, _P, _P, _I]
             L.gdn_oracle_commit.restype = None
             L.gdn_oracle_commit.argtypes = [_I, _P, _P]
             L.gdn_oracle_max_threads.restype = _I
@@ -288,6 +291,17 @@ def conv_prefill(cu_seqlens, x, conv_pool, read_slot, write_slot, w, bias, token
     bad = lib().gdn_oracle_conv_prefill(nseq, C, W, num_slots, _ptr(cu), _ptr(x), _ptr(conv_pool), _ptr(rs),
                                         _ptr(ws), _ptr(ts), _ptr(w), _ptr(bias), int(bool(silu)), _ptr(y))
     return y, bad
+
+
+def copy_slots(pool, src, dst) -> int:
+    """Copy slot src[i] to slot dst[i] of an fp64 pool [num_slots][...] in
+    place; returns the number of bad pairs (skipped)."""
+    assert pool.dtype == np.float64 and pool.flags.c_contiguous
+    num_slots = pool.shape[0]
+    slot_elems = int(np.prod(pool.shape[1:]))
+    s, d = _i32(src), _i32(dst)
+    assert s.shape == d.shape
+    return lib().gdn_oracle_copy_slots(num_slots, slot_elems, _ptr(pool), _ptr(s), _ptr(d), int(s.shape[0]))
 
 
 def commit(read_slot: np.ndarray, write_slot: np.ndarray) -> None:

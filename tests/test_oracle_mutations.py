@@ -39,6 +39,9 @@ MUTATIONS = {
     "verify_one_token_slot": ("pool + (size_t)token_slot[t] * slot_elems", "pool + (size_t)token_slot[cu_seqlens[r]] * slot_elems"),
     "prefill_twin_writes_read_slot": ("int ws = write_slot ? write_slot[r] : rs;", "int ws = rs;"),
     "conv_prefill_window_not_carried": ("memcpy(win, new_win, sizeof(double) * slot_elems);", ""),
+    "copy_slots_may_write_null": ("dst[i] <= 0 || dst[i] >= num_slots", "dst[i] < 0 || dst[i] >= num_slots"),
+    "copy_slots_reversed": ("pool[(size_t)dst[i] * slot_elems + e] = pool[(size_t)src[i] * slot_elems + e];",
+                            "pool[(size_t)src[i] * slot_elems + e] = pool[(size_t)dst[i] * slot_elems + e];"),
 }
 PIN_FILES = ["test_oracle_pins.py", "test_oracle_prefill_pins.py"]
 

@@ -191,3 +191,26 @@ def test_conv_prefill_equals_numpy_convolve(orc):
     for t in range(6):
         assert np.array_equal(pool[ts[t]], seq[t + 1:t + W])
     assert np.array_equal(pool[rs[0]], start[rs[0]])
+
+
+def test_copy_slots_snapshot_and_fork(orc):
+    """Snapshots and forks: a copied slot holds exactly the source's values,
+    a copy there and back is the identity, copying the null slot zeroes the
+    destination, slots outside the copies are untouched, bad pairs are
+    skipped and counted."""
+    rng = np.random.default_rng(65)
+    pool = rng.standard_normal((9, 2, 3, 4))
+    pool[0] = 0.0
+    start = pool.copy()
+    bad = orc.copy_slots(pool, [2, 5, 0], [7, 1, 8])
+    assert bad == 0
+    assert np.array_equal(pool[7], start[2]) and np.array_equal(pool[1], start[5])
+    assert np.all(pool[8] == 0.0)
+    for s in (0, 2, 3, 4, 5, 6):
+        assert np.array_equal(pool[s], start[s])
+    orc.copy_slots(pool, [7], [3])
+    orc.copy_slots(pool, [3], [4])
+    assert np.array_equal(pool[4], start[2])
+    before = pool.copy()
+    assert orc.copy_slots(pool, [1, 9, -1, 2], [0, 2, 3, 9]) == 4
+    assert np.array_equal(pool, before)
