@@ -25,7 +25,7 @@ from ._lib import (GDN_BF16, GDN_DEVERR_BAD_SLOT, GDN_DEVERR_NONE, GDN_F32, GDN_
 __all__ = [
     "GDNError", "load", "lib_path", "GDNStatePool", "ConvStatePool", "causal_conv1d_decode",
     "gdn_decode_step", "gdn_layer_decode", "gdn_layer_decode_noalloc", "gdn_commit", "gdn_validate_slots",
-    "gdn_prefill", "gdn_verify", "causal_conv1d_prefill",
+    "gdn_prefill", "gdn_verify", "causal_conv1d_prefill", "gdn_layer_decode_bucket",
     "get_device_error", "probe_traffic", "GDN_F32", "GDN_BF16", "GDN_DEVERR_NONE",
     "GDN_DEVERR_BAD_SLOT", "GDN_PROBE_TWIN", "GDN_PROBE_INPLACE", "GDN_PROBE_READ",
     "GDN_PROBE_WRITE",
@@ -113,6 +113,13 @@ class GDNStatePool:
         _check(_lib.load().gdn_pool_zero_slots(self._h, _ptr(slots, "slots", torch.int32),
                                                slots.numel(), _stream(self.tensor.device)))
 
+    def copy_slots(self, src: torch.Tensor, dst: torch.Tensor):
+        """Slot dst[i] receives a copy of slot src[i] (snapshots, forks)."""
+        _numel(dst, src.numel(), "dst")
+        _check(_lib.load().gdn_pool_copy_slots(self._h, _ptr(src, "src", torch.int32),
+                                               _ptr(dst, "dst", torch.int32), src.numel(),
+                                               _stream(self.tensor.device)))
+
     def __del__(self):
         h = getattr(self, "_h", None)
         if h is not None and h.value:
@@ -148,6 +155,13 @@ class ConvStatePool:
     def zero_slots(self, slots: torch.Tensor):
         _check(_lib.load().conv_pool_zero_slots(self._h, _ptr(slots, "slots", torch.int32),
                                                 slots.numel(), _stream(self.tensor.device)))
+
+    def copy_slots(self, src: torch.Tensor, dst: torch.Tensor):
+        """Slot dst[i] receives a copy of slot src[i] (snapshots, forks)."""
+        _numel(dst, src.numel(), "dst")
+        _check(_lib.load().conv_pool_copy_slots(self._h, _ptr(src, "src", torch.int32),
+                                                _ptr(dst, "dst", torch.int32), src.numel(),
+                                                _stream(self.tensor.device)))
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -369,6 +383,43 @@ def gdn_layer_decode_noalloc(x, conv_pool: ConvStatePool, w, bias, A_log, dt_bia
         pool.handle, _ptr(read_slot, "read_slot", torch.int32, dev),
         _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev), rows,
         int(bool(keep_in_place)), int(scratch_slot), _dtype_code(dt), _stream(dev)))
+    return out
+
+
+def gdn_layer_decode_bucket(x, conv_pool: ConvStatePool, w, bias, A_log, dt_bias, a, b, pool: GDNStatePool,
+                            read_slot, write_slot, n_decode: torch.Tensor, out: Optional[torch.Tensor] = None,
+                            keep_in_place: bool = False, commit: bool = False,
+                            silu: bool = True) -> torch.Tensor:
+    """The decode half of a mixed step: the launch covers the bucket (x's rows);
+    only rows below the device int32 n_decode are decoded, the rest are left
+    alone (outputs zero).  With commit (twin only) the decoded rows' tables are
+    swapped in the same launch."""
+    if commit and (keep_in_place or write_slot is None):
+        raise ValueError("commit needs twin slots (a write_slot table, keep_in_place False)")
+    rows = x.shape[0]
+    dt = x.dtype
+    dev = x.device
+    C = 2 * pool.hk * pool.dk + pool.hv * pool.dv
+    _numel(x, rows * C, "x")
+    _numel(w, C * conv_pool.width, "w")
+    if bias is not None:
+        _numel(bias, C, "bias")
+    for tname, tt, n in (("a", a, rows * pool.hv), ("b", b, rows * pool.hv), ("A_log", A_log, pool.hv),
+                         ("dt_bias", dt_bias, pool.hv), ("read_slot", read_slot, rows), ("n_decode", n_decode, 1)):
+        _numel(tt, n, tname)
+    if write_slot is not None:
+        _numel(write_slot, rows, "write_slot")
+    if out is None:
+        out = torch.empty((rows, pool.hv, pool.dv), dtype=dt, device=dev)
+    _numel(out, rows * pool.hv * pool.dv, "out")
+    _check(_lib.load().gdn_layer_decode_bucket(
+        _ptr(x, "x", dt, dev), conv_pool.handle, _ptr(w, "w", dt, dev), _ptr(bias, "bias", dt, dev),
+        int(bool(silu)), _ptr(A_log, "A_log", torch.float32, dev),
+        _ptr(dt_bias, "dt_bias", torch.float32, dev), _ptr(a, "a", dt, dev), _ptr(b, "b", dt, dev),
+        pool.handle, _ptr(read_slot, "read_slot", torch.int32, dev),
+        _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev), rows,
+        _ptr(n_decode, "n_decode", torch.int32, dev), int(bool(keep_in_place)), int(bool(commit)),
+        _dtype_code(dt), _stream(dev)))
     return out
 
 

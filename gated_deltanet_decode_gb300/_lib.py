@@ -38,11 +38,11 @@ GDN_NOALLOC_SCRATCH_SLOTS = 64
 EXPORTS = [
     "gdn_last_error", "gdn_abi_version",
     "gdn_state_pool_create", "gdn_state_pool_wrap", "gdn_state_pool_destroy", "gdn_pool_data",
-    "gdn_pool_num_slots", "gdn_pool_dims", "gdn_pool_zero_slots",
+    "gdn_pool_num_slots", "gdn_pool_dims", "gdn_pool_zero_slots", "gdn_pool_copy_slots",
     "conv_state_pool_create", "conv_state_pool_wrap", "conv_state_pool_destroy", "conv_pool_data",
-    "conv_pool_num_slots", "conv_pool_zero_slots",
+    "conv_pool_num_slots", "conv_pool_zero_slots", "conv_pool_copy_slots",
     "causal_conv1d_decode", "gdn_decode_step", "gdn_layer_decode", "gdn_layer_decode_commit",
-    "gdn_layer_decode_noalloc", "gdn_prefill", "gdn_verify", "causal_conv1d_prefill",
+    "gdn_layer_decode_noalloc", "gdn_layer_decode_bucket", "gdn_prefill", "gdn_verify", "causal_conv1d_prefill",
     "gdn_commit", "gdn_validate_slots", "gdn_get_device_error", "gdn_probe_traffic",
 ]
 
@@ -65,6 +65,8 @@ _SIGS = {
     "gdn_pool_num_slots": (_I, [_P]),
     "gdn_pool_dims": (gdn_dims, [_P]),
     "gdn_pool_zero_slots": (_I, [_P, _P, _I, _P]),
+    "gdn_pool_copy_slots": (_I, [_P, _P, _P, _I, _P]),
+    "conv_pool_copy_slots": (_I, [_P, _P, _P, _I, _P]),
     "conv_state_pool_create": (_I, [_I, _I, _I, _I, _P, _PP]),
     "conv_state_pool_wrap": (_I, [_P, _I, _I, _I, _I, _PP]),
     "conv_state_pool_destroy": (_I, [_P]),
@@ -77,6 +79,8 @@ _SIGS = {
     "gdn_layer_decode_commit": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P]),
     "gdn_layer_decode_noalloc": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                                       _P]),
+    "gdn_layer_decode_bucket": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I,
+                                     _P]),
     "gdn_prefill": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "gdn_verify": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     "causal_conv1d_prefill": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _P]),

@@ -176,6 +176,28 @@ __global__ void zero_slots_kernel(char *base, size_t slot_bytes, int num_slots, 
     }
 }
 
+// Snapshots and forks: slot dst[k] receives slot src[k] of a pool whose slot
+// is `slot_bytes` bytes (a multiple of 16).  A source outside the pool or a
+// destination outside [1, num_slots) skips the pair and reports it.
+__global__ void copy_slots_kernel(char *base, size_t slot_bytes, int num_slots, const int32_t *src,
+                                  const int32_t *dst, int n, int *err)
+{
+    const size_t vec_per_slot = slot_bytes / 16;
+    const size_t total = vec_per_slot * (size_t)n;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const int k = (int)(i / vec_per_slot);
+        const int s = src[k], d = dst[k];
+        if (s < 0 || s >= num_slots || d <= 0 || d >= num_slots) {
+            if (i % vec_per_slot == 0)
+                gdn::report(err, GDN_DEVERR_BAD_SLOT);
+            continue;
+        }
+        const uint4 v = reinterpret_cast<const uint4 *>(base + (size_t)s * slot_bytes)[i % vec_per_slot];
+        reinterpret_cast<uint4 *>(base + (size_t)d * slot_bytes)[i % vec_per_slot] = v;
+    }
+}
+
 // Traffic probes: the state bytes of a step, no arithmetic.  A block moves
 // 16 KiB (4 vectors a thread), the size of one block of the state kernel at
 // one pass with dk = 128.
@@ -362,6 +384,39 @@ static int zero_slots(void *base, size_t slot_bytes, int num_slots, const int32_
     return ok();
 }
 
+static int copy_slots(void *base, size_t slot_bytes, int num_slots, const int32_t *src, const int32_t *dst,
+                      int n, void *stream)
+{
+    if (n < 0)
+        return fail(GDN_EINVAL, "n=%d < 0", n);
+    if (n == 0)
+        return ok();
+    if (!src || !dst)
+        return fail(GDN_EINVAL, "src and dst must be non-NULL");
+    int *err = nullptr;
+    int rc = device_error_ptr(&err);
+    if (rc)
+        return rc;
+    const size_t total = slot_bytes / 16 * (size_t)n;
+    size_t blocks = (total + 255) / 256;
+    if (blocks > 152 * 16)
+        blocks = 152 * 16;
+    copy_slots_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<char *>(base), slot_bytes, num_slots, src, dst, n, err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "copy_slots launch");
+    return ok();
+}
+
+int gdn_pool_copy_slots(gdn_pool *pool, const int32_t *src, const int32_t *dst, int n, void *stream)
+{
+    if (!pool)
+        return fail(GDN_EINVAL, "pool is NULL");
+    return copy_slots(pool->data, state_slot_floats(pool->dims) * sizeof(float), pool->num_slots, src, dst, n,
+                      stream);
+}
+
 int gdn_pool_zero_slots(gdn_pool *pool, const int32_t *slots, int n, void *stream)
 {
     if (!pool)
@@ -447,6 +502,14 @@ int conv_state_pool_destroy(conv_pool *pool)
 
 void *conv_pool_data(const conv_pool *pool) { return pool ? pool->data : nullptr; }
 int conv_pool_num_slots(const conv_pool *pool) { return pool ? pool->num_slots : 0; }
+
+int conv_pool_copy_slots(conv_pool *pool, const int32_t *src, const int32_t *dst, int n, void *stream)
+{
+    if (!pool)
+        return fail(GDN_EINVAL, "pool is NULL");
+    return copy_slots(pool->data, (size_t)(pool->width - 1) * pool->channels * dtype_size(pool->dtype),
+                      pool->num_slots, src, dst, n, stream);
+}
 
 int conv_pool_zero_slots(conv_pool *pool, const int32_t *slots, int n, void *stream)
 {
@@ -812,6 +875,32 @@ int causal_conv1d_prefill(const void *x, conv_pool *cp, const int32_t *cu_seqlen
     cudaError_t e = gdn::launch_conv_prefill(s, dtype, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "causal_conv1d_prefill launch");
+    return ok();
+}
+
+int gdn_layer_decode_bucket(const void *x, conv_pool *cp, const void *w, const void *bias, int silu,
+                            const float *A_log, const float *dt_bias, const void *a, const void *b,
+                            gdn_pool *pool, int32_t *read_slot, int32_t *write_slot, void *out, int rows,
+                            const int32_t *n_decode, int keep_in_place, int commit, int dtype, void *stream)
+{
+    if (commit && keep_in_place)
+        return fail(GDN_EINVAL, "commit swaps twin slots; it does not apply in place");
+    if (rows > 0 && !n_decode)
+        return fail(GDN_EINVAL, "n_decode is NULL");
+    gdn::StepArgs s;
+    bool none = true;
+    int rc = layer_args(x, cp, w, bias, silu, A_log, dt_bias, a, b, pool, read_slot, write_slot, out, rows,
+                        keep_in_place, dtype, &s, &none);
+    if (rc || none)
+        return rc;
+    rc = work_ptr(pool, &s.work);
+    if (rc)
+        return rc;
+    s.n_live = n_decode;
+    s.commit = commit ? 1 : 0;
+    cudaError_t e = gdn::launch_gdn_layer(s, dtype, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "gdn_layer_decode_bucket launch");
     return ok();
 }
 

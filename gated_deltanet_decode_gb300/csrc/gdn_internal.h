@@ -43,6 +43,7 @@ struct StepArgs {
     int *err;
     unsigned int *work; // the pool's two work counters (claim, producers done), zero between launches
     int commit;         // twin only: swap read_slot and write_slot once every producer has read them
+    const int32_t *n_live; // device count or NULL: rows at or past *n_live are left alone (outputs zero)
     // fused layer only
     const void *x;
     void *conv;        // conv pool data

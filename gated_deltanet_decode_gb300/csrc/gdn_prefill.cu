@@ -12,10 +12,12 @@
 // kernel's geometry) and written once at the end (or once a token when
 // verifying).  The tokens stream through a ring of shared-memory stages: a
 // loader warp computes the gates 32 tokens at a time and bulk-copies each
-// token's raw q, k and v chunk; the 8 consumer warps normalise q and k (one
-// channel a thread, a CTA-wide sum through an mbarrier) and update the state
-// rows exactly as the decode kernel does, with the same operations in the
-// same order, so T tokens of a prefill equal T decode steps bit for bit.
+// token's raw q, k and v chunk; two norm warps, taking alternate tokens,
+// turn q and k into fp32 values and form their norms and k^ . q^; the 8
+// consumer warps then only update their state rows.  Every sum is formed
+// with the decode kernel's operations in its order (the norm warps play the
+// decode kernel's 8 consumer warps lane by lane), so T tokens of a prefill
+// equal T decode steps bit for bit.
 //
 // The rule is sequential in the tokens: a CTA's work is one token after the
 // other, and the launch has nseq * hv * (dv / RB) CTAs.  (The chunked form,
@@ -31,7 +33,9 @@ namespace {
 
 constexpr int kWarps = 8;                    // consumer warps
 constexpr int kConsumerThreads = kWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32; // + the loader warp
+constexpr int kNormWarps = 2;                // warps that normalise q and k, alternate tokens
+constexpr int kLoader = kWarps;              // warp index of the loader
+constexpr int kThreads = (kWarps + 1 + kNormWarps) * 32;
 constexpr int kStages = 8;                   // token ring depth
 constexpr float kL2Eps = 1e-6f;
 
@@ -70,9 +74,9 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_kernel(const PrefillA
     constexpr int E = L::E;
 
     __shared__ __align__(128) unsigned char ring[kStages * L::BYTES];
-    __shared__ __align__(8) unsigned long long bars[2 * kStages + 1]; // full, empty, qk
-    __shared__ __align__(16) float qkbuf[2][2 * DK];                 // a token's q | k values
-    __shared__ float part[2][kWarps][2];
+    __shared__ __align__(8) unsigned long long bars[3 * kStages]; // full, ready, empty
+    __shared__ __align__(16) float qkf[kStages][2 * DK];          // a token's q | k values, fp32
+    __shared__ float norm_q[kStages], norm_k[kStages], kap[kStages];
     __shared__ float gate_a[kStages], gate_b[kStages];
     __shared__ float tab_a[32], tab_b[32];
     __shared__ int s_cls, s_t0, s_t1, s_rs, s_ws;
@@ -88,8 +92,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_kernel(const PrefillA
     const int rows = min(RB, p.dv - chunk * RB);
     const bool verify = p.token_slot != nullptr;
     auto full_bar = [&](int s) { return sm_addr(&bars[s]); };
-    auto empty_bar = [&](int s) { return sm_addr(&bars[kStages + s]); };
-    const uint32_t qk_bar = sm_addr(&bars[2 * kStages]);
+    auto ready_bar = [&](int s) { return sm_addr(&bars[kStages + s]); };
+    auto empty_bar = [&](int s) { return sm_addr(&bars[2 * kStages + s]); };
     auto timeout = [&]() {
         report(p.err, GDN_DEVERR_TIMEOUT);
         atomicExch(&abort_flag, 1);
@@ -98,9 +102,9 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_kernel(const PrefillA
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full_bar(s), 2); // copies + gates
+            mbar_init(ready_bar(s), 1); // the token's norm warp
             mbar_init(empty_bar(s), kWarps);
         }
-        mbar_init(qk_bar, kWarps);
         abort_flag = 0;
         issued_n = 0;
         consumed_n = 0;
@@ -110,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_kernel(const PrefillA
     wait_prior_grid();
 
     // the sequence: its tokens, its slots, and whether it is real
-    if (warp == kWarps) {
+    if (warp == kLoader) {
         const int t0 = p.cu_seqlens[r], t1 = p.cu_seqlens[r + 1];
         const int rs = p.read_slot[r];
         const bool in_place = p.write_slot == nullptr || verify;
@@ -155,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_kernel(const PrefillA
     const int n = t1 - t0;
     const int rs = s_rs, ws = s_ws;
 
-    if (warp == kWarps) {
+    if (warp == kLoader) {
         // ============================ loader ============================
         // Gates 32 tokens at a time, one a lane; then one lane streams the
         // tokens' raw q, k and v chunk into the ring: copies with their byte
@@ -206,6 +210,76 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_kernel(const PrefillA
             stop = __shfl_sync(0xffffffffu, stop, 0);
             __syncwarp();
         }
+    } else if (warp > kLoader) {
+        // ========================== norm warps ==========================
+        // Token k belongs to norm warp k % kNormWarps.  Lane l plays thread
+        // 32w + l of the decode kernel's consumer warp w, for every w: the same
+        // channels, the same fma chains, the same butterflies, the same order
+        // of the per-warp sums, so the norms and k^ . q^ are the decode
+        // kernel's to the bit.
+        for (int k = warp - kLoader - 1; k < n; k += kNormWarps) {
+            const int s = k % kStages;
+            if (!mbar_wait(full_bar(s), (uint32_t)((k / kStages) & 1))) {
+                timeout();
+                break;
+            }
+            const unsigned char *st = ring + (size_t)s * L::BYTES;
+            float *qf = qkf[s];
+            float pq[kWarps], pk[kWarps];
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                float a = 0.f, b = 0.f;
+#pragma unroll
+                for (int c0 = 32 * w; c0 < 2 * DK; c0 += kConsumerThreads) {
+                    const int c = c0 + lane;
+                    const float val = sh_val<T>(st + L::QK, c);
+                    qf[c] = val;
+                    if (c < DK)
+                        a = __fmaf_rn(val, val, a);
+                    else
+                        b = __fmaf_rn(val, val, b);
+                }
+                pq[w] = a;
+                pk[w] = b;
+            }
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                // a warp without q (or k) channels sums exact zeros: skip its butterfly
+                if (32 * w < DK) {
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1)
+                        pq[w] += __shfl_xor_sync(0xffffffffu, pq[w], off);
+                }
+                if ((32 * w < 2 * DK && 32 * w + 31 >= DK) || 32 * w + kConsumerThreads < 2 * DK) {
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1)
+                        pk[w] += __shfl_xor_sync(0xffffffffu, pk[w], off);
+                }
+            }
+            float qq = 0.f, kk2 = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                qq += pq[w];
+                kk2 += pk[w];
+            }
+            const float inv_q = __fdiv_rn(1.0f, sqrtf(qq + kL2Eps)) * rsqrtf((float)DK);
+            const float inv_k = __fdiv_rn(1.0f, sqrtf(kk2 + kL2Eps));
+            __syncwarp();
+            float pqk = 0.f;
+            for (int i = lane; i < DK; i += 32)
+                pqk = __fmaf_rn(qf[i], qf[DK + i], pqk);
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1)
+                pqk += __shfl_xor_sync(0xffffffffu, pqk, off);
+            if (lane == 0) {
+                norm_q[s] = inv_q;
+                norm_k[s] = inv_k;
+                kap[s] = pqk * inv_q * inv_k;
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(ready_bar(s));
+        }
     } else {
         // =========================== consumers ==========================
         const int lrow = lane / G::LPR, lcol = lane % G::LPR;
@@ -222,62 +296,16 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_kernel(const PrefillA
         bool ok = true;
         for (int k = 0; k < n; ++k) {
             const int s = k % kStages;
-            if (!mbar_wait(full_bar(s), (uint32_t)((k / kStages) & 1))) {
+            if (!mbar_wait(ready_bar(s), (uint32_t)((k / kStages) & 1))) {
                 timeout();
                 ok = false;
                 break;
             }
             const unsigned char *st = ring + (size_t)s * L::BYTES;
-            const int qb = k & 1;
-            float *qk = qkbuf[qb];
-            // q and k values, their norms, k^ . q^ (as at a decode chain's start)
-            float psq = 0.f, psk = 0.f;
-            for (int c = t; c < 2 * DK; c += kConsumerThreads) {
-                const float val = sh_val<T>(st + L::QK, c);
-                qk[c] = val;
-                if (c < DK)
-                    psq = __fmaf_rn(val, val, psq);
-                else
-                    psk = __fmaf_rn(val, val, psk);
-            }
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) {
-                psq += __shfl_xor_sync(0xffffffffu, psq, off);
-                psk += __shfl_xor_sync(0xffffffffu, psk, off);
-            }
-            if (lane == 0) {
-                part[qb][warp][0] = psq;
-                part[qb][warp][1] = psk;
-            }
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(qk_bar);
-            if (!mbar_wait(qk_bar, (uint32_t)(k & 1))) {
-                timeout();
-                ok = false;
-                break;
-            }
-            float qq = 0.f, kk2 = 0.f;
-#pragma unroll
-            for (int wi = 0; wi < kWarps; ++wi) {
-                qq += part[qb][wi][0];
-                kk2 += part[qb][wi][1];
-            }
-            const float inv_q = __fdiv_rn(1.0f, sqrtf(qq + kL2Eps)) * rsqrtf((float)DK);
-            const float inv_k = __fdiv_rn(1.0f, sqrtf(kk2 + kL2Eps));
-            float pqk = 0.f;
-            for (int i = lane; i < DK; i += 32)
-                pqk = __fmaf_rn(qk[i], qk[DK + i], pqk);
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1)
-                pqk += __shfl_xor_sync(0xffffffffu, pqk, off);
-            const float kappa = pqk * inv_q * inv_k;
-            const float vi = live_row ? sh_val<T>(st + L::V, row) : 0.f;
+            const float *qk = qkf[s];
+            const float inv_q = norm_q[s], inv_k = norm_k[s], kappa = kap[s];
             const float alpha = gate_a[s], beta = gate_b[s];
-            // the stage is no longer needed: its q/k values are in qkbuf
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(empty_bar(s));
+            const float vi = live_row ? sh_val<T>(st + L::V, row) : 0.f;
             float4 kh[4], qh[4];
 #pragma unroll
             for (int mm = 0; mm < 4; ++mm) {
@@ -285,6 +313,10 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_kernel(const PrefillA
                 qh[mm] = *reinterpret_cast<const float4 *>(&qk[j]);
                 kh[mm] = *reinterpret_cast<const float4 *>(&qk[DK + j]);
             }
+            // everything this warp needs from the stage is in registers
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(empty_bar(s));
             float2 u2 = make_float2(0.f, 0.f), w2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int mm = 0; mm < 4; ++mm) {
@@ -338,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_kernel(const PrefillA
     // A CTA whose waits ran out leaves no copy in flight: the loader waits
     // (bounded) for every stage it filled that was not consumed.
     asm volatile("barrier.sync 0;" ::: "memory");
-    if (abort_flag && tid == kConsumerThreads) {
+    if (abort_flag && tid == kLoader * 32) {
         for (int k = consumed_n; k < issued_n; ++k)
             mbar_wait(full_bar(k % kStages), (uint32_t)((k / kStages) & 1));
     }

@@ -223,6 +223,12 @@ gdn_stream_kernel(const StepArgs p, const Sched sc)
         int lo = sc.first(blockIdx.x, gridDim.x) * sc.per_unit; // items [lo, hi) to do next
         int hi = sc.first(blockIdx.x + 1, gridDim.x) * sc.per_unit;
         const bool claims = sc.n_static < sc.n_units;
+        // a bucket's decode half: rows at or past the device count are not this launch's
+        int live_rows = p.rows;
+        if (p.n_live) {
+            const int nl = *p.n_live;
+            live_rows = nl < 0 ? 0 : (nl < p.rows ? nl : p.rows);
+        }
         const bool counted = claims || p.commit; // producers count themselves done
         int kdone = 0;                // items issued so far
         int prev_r = -1, prev_g = -1; // the item before the batch
@@ -324,8 +330,10 @@ gdn_stream_kernel(const StepArgs p, const Sched sc)
             float av = 0.f, bv = 0.f, al = 0.f, dt = 0.f;
             if (valid) {
                 sc.item_at(lo + lane, q.r, q.h, q.chunk);
-                q.rs = p.read_slot[q.r];
-                q.ws = p.in_place ? q.rs : p.write_slot[q.r];
+                if (q.r < live_rows) {
+                    q.rs = p.read_slot[q.r];
+                    q.ws = p.in_place ? q.rs : p.write_slot[q.r];
+                }
                 av = ld_act<T>(p.a, (size_t)q.r * p.hv + q.h);
                 bv = ld_act<T>(p.b, (size_t)q.r * p.hv + q.h);
                 al = p.A_log[q.h];
@@ -402,12 +410,12 @@ gdn_stream_kernel(const StepArgs p, const Sched sc)
                     // the whole warp swaps the tables, 256 rows a round, loads first
                     int32_t *rs = const_cast<int32_t *>(p.read_slot);
                     int32_t *ws = const_cast<int32_t *>(p.write_slot);
-                    for (int r0 = 0; r0 < p.rows; r0 += 256) {
+                    for (int r0 = 0; r0 < live_rows; r0 += 256) {
                         int32_t vr[8], vw[8];
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const int r = r0 + 32 * j + lane;
-                            if (r < p.rows) {
+                            if (r < live_rows) {
                                 vr[j] = rs[r];
                                 vw[j] = ws[r];
                             }
@@ -415,7 +423,7 @@ gdn_stream_kernel(const StepArgs p, const Sched sc)
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const int r = r0 + 32 * j + lane;
-                            if (r < p.rows) {
+                            if (r < live_rows) {
                                 rs[r] = vw[j];
                                 ws[r] = vr[j];
                             }

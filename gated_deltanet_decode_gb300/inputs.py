@@ -124,15 +124,16 @@ class Gen:
         ws[real] = perm[n_real:2 * n_real] if twin else perm[:n_real]
         return rs, ws
 
-    def seq_tables(self, lens, num_slots: int, n_pad: int = 0):
+    def seq_tables(self, lens, num_slots: int, n_pad: int = 0, token_slots: bool = True):
         """Packed sequences of the given lengths for the many-token calls:
         (cu_seqlens [nseq+1], read_slot [nseq], write_slot [nseq],
         token_slot [T]), int32.
 
         n_pad sequences, at random positions, are padding (slots 0, token
         slots 0).  Real sequences take distinct slots from a random
-        permutation of 1..num_slots-1: reads first, then writes, then one slot
-        a token of the real sequences (for a state a token)."""
+        permutation of 1..num_slots-1: reads first, then writes, then (with
+        token_slots) one slot a token of the real sequences, for a state a
+        token; without, token_slot is all zeros."""
         lens = np.asarray(lens, dtype=np.int64)
         nseq = len(lens)
         cu = np.zeros(nseq + 1, dtype=np.int32)
@@ -141,7 +142,7 @@ class Gen:
         if n_pad:
             pad[self.rng.choice(nseq, size=n_pad, replace=False)] = True
         n_real = int((~pad).sum())
-        n_tok = int(lens[~pad].sum())
+        n_tok = int(lens[~pad].sum()) if token_slots else 0
         need = 2 * n_real + n_tok
         if need > num_slots - 1:
             raise ValueError(f"the sequences need {need} slots, the pool has {num_slots - 1}")
@@ -152,7 +153,7 @@ class Gen:
         ws[~pad] = perm[n_real:2 * n_real]
         ts = np.zeros(int(cu[-1]), dtype=np.int32)
         nxt = 2 * n_real
-        for r in range(nseq):
+        for r in range(nseq if token_slots else 0):
             if not pad[r]:
                 ts[cu[r]:cu[r + 1]] = perm[nxt:nxt + lens[r]]
                 nxt += int(lens[r])

@@ -136,6 +136,18 @@ gdn_dims gdn_pool_dims(const gdn_pool *pool);
  * be 0. */
 int gdn_pool_zero_slots(gdn_pool *pool, const int32_t *slots, int n, void *stream);
 
+/* Snapshots and forks: slot dst[i] receives an exact copy of slot src[i], for
+ * i < n (src, dst: device int32 arrays).  A prefix-cache checkpoint copies a
+ * request's state and conv window into snapshot slots, and a fork copies
+ * them into a new request's slots ("mstar PR #1139", "What changed": prefix
+ * snapshots of the conv window and state; "mstar PR #965", "What changed":
+ * prefix-cache checkpoints).  A source outside [0, num_slots) or a
+ * destination outside [1, num_slots) skips the pair and sets the device
+ * error word (the null slot is never written).  Destinations must be
+ * distinct and must not be sources.  n may be 0.  conv_pool_copy_slots does
+ * the same for a conv pool. */
+int gdn_pool_copy_slots(gdn_pool *pool, const int32_t *src, const int32_t *dst, int n, void *stream);
+
 /* ---- conv window pool ------------------------------------------------- *
  * Layout: [num_slots][width-1][channels] in the activation dtype, channel
  * contiguous, oldest input first.  width is 2..4; channels a multiple of 8.
@@ -149,6 +161,7 @@ int conv_state_pool_destroy(conv_pool *pool);
 void *conv_pool_data(const conv_pool *pool);
 int conv_pool_num_slots(const conv_pool *pool);
 int conv_pool_zero_slots(conv_pool *pool, const int32_t *slots, int n, void *stream);
+int conv_pool_copy_slots(conv_pool *pool, const int32_t *src, const int32_t *dst, int n, void *stream);
 
 /* ---- causal_conv1d_decode --------------------------------------------- *
  * For each row r with s = slot_idx[r] != 0 and each channel c:
@@ -250,6 +263,23 @@ int gdn_layer_decode_commit(const void *x, conv_pool *cp, const void *w, const v
                             const float *A_log, const float *dt_bias, const void *a, const void *b,
                             gdn_pool *pool, int32_t *read_slot, int32_t *write_slot, void *out,
                             int rows, int dtype, void *stream);
+
+/* ---- gdn_layer_decode_bucket ------------------------------------------- *
+ * The decode half of a mixed step ("mstar PR #965", "What changed": decode
+ * rows lead the bucket, the GDN decode kernel runs over the leading run of
+ * one-token rows, sized to the bucket, and the width changes no real row's
+ * result).  The launch covers `rows` (the bucket); only rows below *n_decode
+ * (an int32 on the device, read when the kernel runs, so a captured launch
+ * can serve every decode count) are decoded, exactly as gdn_layer_decode
+ * would decode them.  Rows at or past *n_decode are left alone: their outputs
+ * are zero, and their slots, conv windows and table entries are not touched
+ * even when they name real slots (they belong to the bucket's prefill rows).
+ * With commit != 0 (twin only) the tables of the decoded rows are swapped in
+ * the same launch, as by gdn_layer_decode_commit. */
+int gdn_layer_decode_bucket(const void *x, conv_pool *cp, const void *w, const void *bias, int silu,
+                            const float *A_log, const float *dt_bias, const void *a, const void *b,
+                            gdn_pool *pool, int32_t *read_slot, int32_t *write_slot, void *out, int rows,
+                            const int32_t *n_decode, int keep_in_place, int commit, int dtype, void *stream);
 
 /* ---- gdn_layer_decode_noalloc ------------------------------------------ *
  * gdn_layer_decode for callers that cannot allocate device memory; the pages

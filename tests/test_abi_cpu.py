@@ -174,6 +174,14 @@ def test_layer_and_conv_argument_checks(L):
     assert layer_c(cp, ws=None) == EINVAL
     assert layer_c(bad_cp) == EINVAL and b"channels" in L.gdn_last_error()
     assert layer_c(cp, rows=0) == 0
+    # a bucket's decode half: a device row count, and commit only with twin slots
+    def layer_b(n=P, inplace=0, commit=0, rows=4):
+        return L.gdn_layer_decode_bucket(P, cp, P, None, 1, P, P, P, P, pool, P, P, P, rows, n, inplace,
+                                         commit, 0, None)
+
+    assert layer_b(n=None) == EINVAL and b"n_decode" in L.gdn_last_error()
+    assert layer_b(inplace=1, commit=1) == EINVAL
+    assert layer_b(rows=0) == 0
     # the no-allocation variant: same checks, plus its scratch slot
     from gated_deltanet_decode_gb300._lib import GDN_NOALLOC_SCRATCH_SLOTS
 
@@ -245,5 +253,21 @@ def test_prefill_argument_checks(L):
     assert conv(x=P + 4) == EINVAL
     assert conv(x=None) == EINVAL
     assert conv(nseq=0) == 0
+    L.conv_state_pool_destroy(cp)
+    L.gdn_state_pool_destroy(pool)
+
+
+def test_copy_slots_argument_checks(L):
+    rc, pool = _wrap(L)
+    assert rc == 0
+    cp = ctypes.c_void_p()
+    assert L.conv_state_pool_wrap(FAKE, 9, 96, 4, 0, ctypes.byref(cp)) == 0
+    assert L.gdn_pool_copy_slots(None, FAKE, FAKE, 1, None) == EINVAL
+    assert L.gdn_pool_copy_slots(pool, FAKE, FAKE, -1, None) == EINVAL
+    assert L.gdn_pool_copy_slots(pool, None, FAKE, 1, None) == EINVAL
+    assert L.gdn_pool_copy_slots(pool, None, None, 0, None) == 0
+    assert L.conv_pool_copy_slots(None, FAKE, FAKE, 1, None) == EINVAL
+    assert L.conv_pool_copy_slots(cp, FAKE, None, 2, None) == EINVAL
+    assert L.conv_pool_copy_slots(cp, None, None, 0, None) == 0
     L.conv_state_pool_destroy(cp)
     L.gdn_state_pool_destroy(pool)

@@ -96,3 +96,57 @@ def test_probes_move_the_bytes(gdn):
     assert not pool.tensor[[2, 4, 6]].any()
     assert torch.equal(pool.tensor[[0, 1, 3, 5, 7, 8]], start[[0, 1, 3, 5, 7, 8]])
     assert gdn.get_device_error() == 0
+
+
+def test_copy_slots_snapshot_restore_and_bad_pairs(gdn, orc):
+    """Snapshots and forks: copies are exact (the oracle's copy of the same
+    pool), a snapshot taken before a decode step restores the state, bad
+    pairs are skipped and set the device error word."""
+    import numpy as np
+    import torch
+    from gated_deltanet_decode_gb300 import inputs as I
+    s = I.QWEN_08B.with_(rows=8)
+    gen = I.Gen(90)
+    n_slots = 40
+    pool_np = gen.state_pool(s, n_slots)
+    pool = gdn.GDNStatePool(n_slots, s.hk, s.hv, s.dk, s.dv, device="cuda",
+                            tensor=torch.from_numpy(pool_np.copy()).cuda())
+    cp_np = gen.conv_pool(s, n_slots).astype(np.float32)
+    cp = gdn.ConvStatePool(n_slots, s.channels, s.width, dtype=torch.float32, device="cuda",
+                           tensor=torch.from_numpy(cp_np.copy()).cuda())
+    src = np.array([3, 7, 0, 12], np.int32)
+    dst = np.array([20, 21, 22, 23], np.int32)
+    ts, td = (torch.from_numpy(a).cuda() for a in (src, dst))
+    pool.copy_slots(ts, td)
+    cp.copy_slots(ts, td)
+    torch.cuda.synchronize()
+    ref = pool_np.astype(np.float64)
+    assert orc.copy_slots(ref, src, dst) == 0
+    assert np.array_equal(pool.tensor.cpu().numpy().astype(np.float64), ref)
+    ref_cp = cp_np.astype(np.float64)
+    orc.copy_slots(ref_cp, src, dst)
+    assert np.array_equal(cp.tensor.cpu().numpy().astype(np.float64), ref_cp)
+    # snapshot, one decode step in place, restore: the state is back
+    rows = np.array([3, 7, 12, 5], np.int32)
+    snap = np.array([30, 31, 32, 33], np.int32)
+    tr, tsn = (torch.from_numpy(a).cuda() for a in (rows, snap))
+    before = pool.tensor.clone()
+    pool.copy_slots(tr, tsn)
+    inp = gen.step_inputs(s.with_(rows=4))
+    q, k, v, a, b = (I.to_torch(inp[n], s.dtype, "cuda") for n in ("q", "k", "v", "a", "b"))
+    prm = gen.params(s)
+    gdn.gdn_decode_step(q, k, v, a, b, I.to_torch(prm["A_log"], "f32", "cuda"),
+                        I.to_torch(prm["dt_bias"], "f32", "cuda"), pool, tr, None, keep_in_place=True)
+    torch.cuda.synchronize()
+    assert not torch.equal(pool.tensor[tr.long()], before[tr.long()])
+    pool.copy_slots(tsn, tr)
+    torch.cuda.synchronize()
+    assert torch.equal(pool.tensor[tr.long()], before[tr.long()])
+    assert gdn.get_device_error() == 0
+    # bad pairs: a destination on the null slot, a source past the pool
+    now = pool.tensor.clone()
+    pool.copy_slots(torch.tensor([4, 99], dtype=torch.int32, device="cuda"),
+                    torch.tensor([0, 25], dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert gdn.get_device_error() == 1
+    assert torch.equal(pool.tensor, now)
