@@ -289,7 +289,7 @@ def run_many_tokens(G, I, device, n=20):
         gen = I.Gen(2000 + i)
         lens = [tok] * nseq
         T = nseq * tok
-        cu, rs, ws, _ = gen.seq_tables(lens, 2 * nseq + 1)
+        cu, rs, ws, _ = gen.seq_tables(lens, 2 * nseq + 1, token_slots=False)
         prm = gen.params(s)
         inp = gen.step_inputs(s.with_(rows=T))
         st = {k: I.to_torch(v, s.dtype, device) for k, v in inp.items()}
@@ -766,6 +766,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true",
                     help="omit the sweep, 9B and decode-stack workloads (reported beside the headline)")
+    ap.add_argument("--many-tokens-only", action="store_true",
+                    help="time only the prefill, verification and sequence-conv workloads (one GPU) "
+                         "and print their JSON")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -782,6 +785,13 @@ def main():
     import torch
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if args.many_tokens_only:
+        import gated_deltanet_decode_gb300 as G
+        from gated_deltanet_decode_gb300 import inputs as I
+        G.load()
+        if rank == 0:
+            print(json.dumps(run_many_tokens(G, I, device)), flush=True)
+        return
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
