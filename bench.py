@@ -77,10 +77,19 @@ def hbm_peak():
 
 
 def kernel_source_sha() -> str:
+    """Hash of the layer kernel's code: its sources with comments, blank lines
+    and surrounding whitespace removed, so that editing a comment does not
+    disown a profile taken on the same code."""
+    import re
     h = hashlib.sha256()
     for p in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, p), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, p)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for line in text.splitlines():
+            line = line.split("//", 1)[0].strip()
+            if line:
+                h.update(line.encode() + b"\n")
     return h.hexdigest()
 
 

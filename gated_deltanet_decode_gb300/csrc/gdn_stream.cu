@@ -13,7 +13,13 @@
 //  * Work item = RB consecutive value rows of one (row, value head): 16 KiB of
 //    fp32 state (RB = 4096 / dk), contiguous in the pool.  A persistent grid
 //    (three CTAs per SM for the fused layer, two for the plain step) splits
-//    the items into contiguous ranges, equal to within one item.
+//    the items into contiguous ranges, equal to within one item.  With a
+//    dozen or more items a CTA, only the first half is split that way; the
+//    rest is claimed at run time, a (row, value head) a claim, from a counter
+//    the state pool handle owns, so that CTAs on SMs that stream slower take
+//    less of the tail (SMs' streaming rates differ by about a fifth).  The
+//    last producer to finish resets the counter (and, when asked, commits
+//    the slot tables, or stops at a device-side row count for a bucket).
 //  * Chains: consecutive items of a CTA that share a row and qk head form a
 //    chain.  Only a chain's first item copies q and k (or their conv inputs)
 //    and computes the q/k values, their norms and k^ . q^; the rest of the
@@ -33,8 +39,9 @@
 //    lanes a row, 16-byte vectors interleaved so a warp store covers whole
 //    128-byte lines), forms u = S k and w = S q with packed f32x2 FMAs and one
 //    butterfly, and stores S' = alpha S + c k^ (c = beta (v - alpha u k^))
-//    straight to HBM, with o = alpha w + c (k^ . q^).  Then the warps release
-//    the stage ("empty").
+//    straight to HBM, with o = alpha w + c (k^ . q^).  A warp releases the
+//    stage ("empty") as soon as its state row and v are in registers, before
+//    the math and the stores.
 //  * Every wait is bounded: a wait that runs out reports GDN_DEVERR_TIMEOUT
 //    and its warp leaves the loop (no hardware barrier inside the loop can be
 //    left waiting); the CTA stops after the producer has waited (bounded) for

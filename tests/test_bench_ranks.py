@@ -68,3 +68,22 @@ def test_recorded_traffic_follows_kernel_source(tmp_path, monkeypatch):
     assert bench.recorded_traffic() == 1234
     p.write_text("- traffic_per_launch_bytes: 1234\n- source_sha256: " + "0" * 64 + "\n")
     assert bench.recorded_traffic() is None
+
+
+def test_kernel_hash_follows_code_not_comments(tmp_path, monkeypatch):
+    import shutil
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    for p in bench.KERNEL_SOURCES:
+        dst = tmp_path / p
+        dst.parent.mkdir(parents=True, exist_ok=True)
+        shutil.copy(os.path.join(ROOT, p), dst)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_source_sha()
+    first = tmp_path / bench.KERNEL_SOURCES[0]
+    text = first.read_text()
+    first.write_text("// a new comment\n/* and a block\n   comment */\n\n" + text)
+    assert bench.kernel_source_sha() == h0
+    first.write_text(text.replace("kMaxStages = 8", "kMaxStages = 7"))
+    assert bench.kernel_source_sha() != h0

@@ -250,3 +250,28 @@ def test_prefill_bad_slots_and_ranges(gdn):
     start2 = torch.from_numpy(c2.pool_np).cuda()
     assert torch.equal(c2.pool.tensor[int(c2.ws_np[0])], start2[int(c2.rs_np[0])])
     assert gdn.get_device_error() == 0
+
+
+@pytest.mark.parametrize("dk,dv", [(32, 64), (64, 32), (256, 128), (16, 8), (128, 256)])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_prefill_other_head_sizes(gdn, dk, dv, dtype):
+    """Every head size the kernels are built for: prefill in place and
+    verification equal token-by-token decode steps, bit for bit."""
+    s = I.Shape(rows=1, hk=2, hv=4, dk=dk, dv=dv, width=4, dtype=dtype, num_slots=0)
+    c = Case(gdn, s, [5, 0, 3, 7], seed=76)
+    ref_out, ref_pool, snaps = c.decode_reference(snapshots=True)
+    c.reset()
+    out = c.prefill(keep_in_place=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out)
+    assert torch.equal(c.pool.tensor, ref_pool)
+    c.reset()
+    out = c.verify()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out)
+    for r, n in enumerate(c.lens):
+        if c.rs_np[r] == 0:
+            continue
+        for i in range(n):
+            assert torch.equal(c.pool.tensor[int(c.ts_np[c.cu_np[r] + i])], snaps[i][int(c.rs_np[r])])
+    assert gdn.get_device_error() == 0
