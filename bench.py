@@ -567,16 +567,7 @@ def run_ours(args, rank, world, device):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {
-            "workload": "0.8B-shaped GDN decode layer: fused conv+rule, 64 rows, 16 qk/16 v heads, "
-                        "dk=dv=128, 6144 conv channels width 4, bf16 activations, fp32 state, "
-                        "129-slot pools, twin slots, commit each step (in the layer's launch)",
-            "rows": s.rows, "hk": s.hk, "hv": s.hv, "dk": s.dk, "dv": s.dv, "conv_width": s.width,
-            "activations": s.dtype, "num_slots": s.num_slots, "mode": "twin",
-            "l2": f"inputs larger than L2: {NSETS} layer instances in rotation "
-                  f"({NSETS} x {s.num_slots * s.hv * s.dv * s.dk * 4 / 1e6:.0f} MB of state)",
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-        },
+        "config": workload_config(s, world),
         "us_per_layer": round(layer_mean_ms * 1e3, 3),
         "layer_timing": f"{KL} back-to-back gdn_layer_decode launches over the {NSETS} instances, "
                         "CUDA events at both ends",
@@ -774,6 +765,20 @@ def cpu_baseline(budget_s: float = 12.0):
                       f"median {per * 1e3:.1f} ms per step"}
 
 
+def workload_config(s, world: int) -> dict:
+    """The bench's workload, as both arms report it."""
+    return {
+        "workload": "0.8B-shaped GDN decode layer: fused conv+rule, 64 rows, 16 qk/16 v heads, "
+                    "dk=dv=128, 6144 conv channels width 4, bf16 activations, fp32 state, "
+                    "129-slot pools, twin slots, commit each step (in the layer's launch)",
+        "rows": s.rows, "hk": s.hk, "hv": s.hv, "dk": s.dk, "dv": s.dv, "conv_width": s.width,
+        "activations": s.dtype, "num_slots": s.num_slots, "mode": "twin",
+        "l2": f"inputs larger than L2: {NSETS} layer instances in rotation "
+              f"({NSETS} x {s.num_slots * s.hv * s.dv * s.dk * 4 / 1e6:.0f} MB of state)",
+        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+    }
+
+
 def run_reference(args):
     """--impl reference: the oracle itself; each step is a bounded sample of the
     workload -- one row and 4 of its 16 head pairs -- so that the default
@@ -798,9 +803,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "0.8B-shaped GDN decode layer (fused conv+rule), sampled: one row "
-                               "and 4 head pairs a step",
-                   "rows": 1, "hk": s.hk, "hv": s.hv, "dk": s.dk, "dv": s.dv},
+        "config": workload_config(I.QWEN_08B, 1),
         "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
