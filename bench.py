@@ -480,9 +480,16 @@ def run_ours(args, rank, world, device):
     lb = layer_bytes(s, real_rows)
     step_bytes = lb + commit_bytes(s.rows)
 
+    # twin: the step is the layer with the commit in its launch; in place: the
+    # in-place layer (nothing to commit)
+    twin = args.write_mode == "twin"
+    step_key, layer_key = ("layer_commit", "layer") if twin else ("layer_ip", "layer_ip")
+    if not twin:
+        step_bytes = lb
     for i in range(args.warmup):
         st = sets[i % NSETS]
-        st["layer_commit"]()
+        st[step_key]()
+        st[layer_key]()
         st["layer"]()
         st["commit"]()
     torch.cuda.synchronize(device)
@@ -505,7 +512,7 @@ def run_ours(args, rank, world, device):
     # programmatic-launch overlap
     t0.record(stream)
     for i in range(K):
-        sets[i % NSETS]["layer_commit"]()
+        sets[i % NSETS][step_key]()
     t1.record(stream)
     host_enqueue_s = time.perf_counter() - host0
     torch.cuda.synchronize(device)
@@ -516,7 +523,7 @@ def run_ours(args, rank, world, device):
     l1 = torch.cuda.Event(enable_timing=True)
     l0.record(stream)
     for i in range(KL):
-        sets[i % NSETS]["layer"]()
+        sets[i % NSETS][layer_key]()
     l1.record(stream)
     torch.cuda.synchronize(device)
     # the same step as two launches (gdn_layer_decode, then gdn_commit), for comparison
@@ -567,7 +574,7 @@ def run_ours(args, rank, world, device):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": workload_config(s, world),
+        "config": workload_config(s, world, args.write_mode),
         "us_per_layer": round(layer_mean_ms * 1e3, 3),
         "layer_timing": f"{KL} back-to-back gdn_layer_decode launches over the {NSETS} instances, "
                         "CUDA events at both ends",
@@ -579,13 +586,13 @@ def run_ours(args, rank, world, device):
         "host_enqueue_s": round(host_enqueue_s, 4),
         "roofline": {
             "bound": "hbm",
-            "kernel": "gdn_layer_decode (gdn_stream_kernel, fused layer, twin)",
+            "kernel": f"gdn_layer_decode (gdn_stream_kernel, fused layer, {args.write_mode.replace('_', ' ')})",
             "achieved": round(achieved, 2),
             "peak": peak,
             "peak_kind": peak_kind,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": recorded_traffic(),
+            "traffic": recorded_traffic() if twin else None,
             "algorithmic_bytes_per_launch": lb,
         },
         "e2e": e2e,
@@ -765,14 +772,16 @@ def cpu_baseline(budget_s: float = 12.0):
                       f"median {per * 1e3:.1f} ms per step"}
 
 
-def workload_config(s, world: int) -> dict:
+def workload_config(s, world: int, mode: str = "twin") -> dict:
     """The bench's workload, as both arms report it."""
+    slots = ("twin slots, commit each step (in the layer's launch)" if mode == "twin"
+             else "state updated in place")
     return {
         "workload": "0.8B-shaped GDN decode layer: fused conv+rule, 64 rows, 16 qk/16 v heads, "
                     "dk=dv=128, 6144 conv channels width 4, bf16 activations, fp32 state, "
-                    "129-slot pools, twin slots, commit each step (in the layer's launch)",
+                    f"129-slot pools, {slots}",
         "rows": s.rows, "hk": s.hk, "hv": s.hv, "dk": s.dk, "dv": s.dv, "conv_width": s.width,
-        "activations": s.dtype, "num_slots": s.num_slots, "mode": "twin",
+        "activations": s.dtype, "num_slots": s.num_slots, "mode": mode,
         "l2": f"inputs larger than L2: {NSETS} layer instances in rotation "
               f"({NSETS} x {s.num_slots * s.hv * s.dv * s.dk * 4 / 1e6:.0f} MB of state)",
         "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -820,6 +829,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true",
                     help="omit the sweep, 9B and decode-stack workloads (reported beside the headline)")
+    ap.add_argument("--write-mode", choices=["twin", "in_place"], default="twin",
+                    help="the timed step's state write: twin slots with the commit (default) or in place")
     ap.add_argument("--many-tokens-only", action="store_true",
                     help="time only the prefill, verification and sequence-conv workloads (one GPU) "
                          "and print their JSON")

@@ -26,6 +26,8 @@
 // which the state prefetch keeps flowing.  (The chunked form,
 // which turns runs of tokens into dense products for the tensor cores, is a
 // different kernel; this one is exact with respect to the decode step.)
+#include <atomic>
+
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
 #include "gdn_ptx.cuh"
@@ -485,15 +487,15 @@ cudaError_t launch_dk(const PrefillArgs &a, cudaStream_t s)
     if (items > 0x7fffffffll)
         return cudaErrorInvalidValue;
     auto kern = gdn_prefill_kernel<T, DK>;
-    static unsigned long long configured = 0; // one bit per device
+    static std::atomic<unsigned long long> configured{0}; // one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
     const unsigned long long bit = 1ull << (dev & 63);
-    if (!(configured & bit)) {
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, M::BYTES);
         if (e != cudaSuccess)
             return e;
-        configured |= bit;
+        configured.fetch_or(bit, std::memory_order_release);
     }
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -55,6 +55,8 @@
 // Twin launches write another slot, so the chunk-0 item of the group's first
 // value head writes it.  The arithmetic per row is the same in every
 // schedule, so twin and in place give bit-identical values.
+#include <atomic>
+
 #include "gdn_device.cuh"
 #include "gdn_ptx.cuh"
 #include "gdn_internal.h"
@@ -693,7 +695,7 @@ gdn_stream_kernel(const StepArgs p, const Sched sc)
 // ---------------------------------------------------------------------------
 // launch
 // ---------------------------------------------------------------------------
-int g_num_sms[64] = {};
+std::atomic<int> g_num_sms[64] = {};
 
 int num_sms()
 {
@@ -730,15 +732,15 @@ cudaError_t launch_stream(const StepArgs &a, bool coarse, cudaStream_t s)
     constexpr int kCtas = ctas_per_sm<LAYER>();
     const size_t smem = (size_t)Stages<T, DK, LAYER, W>::value * L::BYTES;
     auto kern = gdn_stream_kernel<T, DK, LAYER, W>;
-    static unsigned long long configured = 0; // one bit per device, per instantiation
+    static std::atomic<unsigned long long> configured{0}; // one bit per device, per instantiation
     int dev = 0;
     cudaGetDevice(&dev);
     const unsigned long long bit = 1ull << (dev & 63);
-    if (!(configured & bit)) {
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess)
             return e;
-        configured |= bit;
+        configured.fetch_or(bit, std::memory_order_release);
     }
     const int slots = kCtas * num_sms();
     const int grid = (int)(sc.n_units < slots ? sc.n_units : slots);
