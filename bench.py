@@ -766,10 +766,15 @@ def cpu_baseline(budget_s: float = 12.0):
     while not times or time.perf_counter() < t_end:
         times.append(time_oracle_step(orc, d, cores))
     per = statistics.median(times)
+    # the same oracle on one thread: one 8-row step (an eighth of the workload)
+    d1 = oracle_layer_sample(s, 8)
+    one = time_oracle_step(orc, d1, 1) * (s.rows / 8)
     return {"value": round(layer_bytes(s, s.rows) / per / 1e9, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle",
             "sample": f"{len(times)} full 64-row steps of the workload (fp64 oracle layer + commit), "
-                      f"median {per * 1e3:.1f} ms per step"}
+                      f"median {per * 1e3:.1f} ms per step",
+            "one_thread": {"value": round(layer_bytes(s, s.rows) / one / 1e9, 4), "unit": "GB/s",
+                           "sample": "one 8-row step on one thread, scaled to 64 rows"}}
 
 
 def workload_config(s, world: int, mode: str = "twin") -> dict:

@@ -124,72 +124,167 @@ __global__ void __launch_bounds__(kThreads) conv_decode_kernel(const ConvArgs p,
 }
 
 // The conv over many tokens a sequence ("mstar PR #1139", section "Why":
-// prefill keeps the state in place): a thread owns 8 channels of one
-// sequence, keeps their window in registers and walks the tokens in order,
-// so each token's output equals one causal_conv1d_decode call.  The window
-// after the last token goes to the write slot (or back in place); with token
-// slots, the window after every token goes to that token's slot.
+// prefill keeps the state in place).  A token's output depends only on it and
+// the W-1 inputs before it, so the tokens run in parallel: a token thread
+// (one per run of kRun tokens and 8 channels) takes the run's tokens that
+// are at least W-1 into their sequence, sliding their window through
+// registers, and reads only the packed inputs; a window thread (one per
+// sequence and 8 channels) takes the first W-1 tokens, which read the stored
+// window, and then writes the new window -- reads before writes in one
+// thread, so in place is safe.  Each output equals one causal_conv1d_decode
+// call.  With token slots, the window after each token goes to that token's
+// slot (the window thread writes those of the first W-1 tokens).
+template <typename T, int W>
+__device__ __forceinline__ void conv8(const float (&win)[W - 1][8], const float (&x)[8], const float *taps,
+                                      const float (&bias)[8], bool silu, float (&y)[8])
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float wi[W], wn[W - 1];
+#pragma unroll
+        for (int j = 0; j < W; ++j)
+            wi[j] = taps[i * W + j];
+#pragma unroll
+        for (int j = 0; j < W - 1; ++j)
+            wn[j] = win[j][i];
+        y[i] = conv_channel<W>(wn, x[i], wi, bias[i], silu);
+    }
+}
+
+constexpr int kRun = 8; // tokens a token thread walks
+
+// The sequence holding token `tok`: the last r with cu_seqlens[r] <= tok.
+__device__ __forceinline__ int seq_of(const int32_t *cu, int nseq, long long tok)
+{
+    int lo = 0, hi = nseq - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (cu[mid] <= tok)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+template <typename T, int W>
+__device__ __forceinline__ void load_taps(const ConvPrefillArgs &p, int c0, float (&taps)[8 * W], float (&bias)[8])
+{
+    const T *wp = reinterpret_cast<const T *>(p.w) + (size_t)c0 * W;
+#pragma unroll
+    for (int t = 0; t < W; ++t) {
+        float tmp[8];
+        Vec8<T>::load(wp + 8 * t, tmp);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            taps[8 * t + i] = tmp[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        bias[i] = 0.f;
+    if (p.bias)
+        Vec8<T>::load(reinterpret_cast<const T *>(p.bias) + c0, bias);
+}
+
 template <typename T, int W>
 __global__ void __launch_bounds__(kThreads) conv_prefill_kernel(const ConvPrefillArgs p, int groups_per_row)
 {
     wait_prior_grid();
     const long long gid = (long long)blockIdx.x * kThreads + threadIdx.x;
-    const int r = (int)(gid / groups_per_row);
-    const int c0 = (int)(gid % groups_per_row) * kVec;
-    if (r >= p.nseq)
-        return;
+    const long long n_window = (long long)p.nseq * groups_per_row;
     const int C = p.channels;
-    const int t0 = p.cu_seqlens[r], t1 = p.cu_seqlens[r + 1];
-    const int rs = p.read_slot[r];
+    T *conv = reinterpret_cast<T *>(p.conv);
+    const T *xs = reinterpret_cast<const T *>(p.x);
     const bool in_place = p.write_slot == nullptr || p.token_slot != nullptr;
-    const int ws = in_place ? rs : p.write_slot[r];
-    const int cls = classify_seq(rs, ws, in_place, p.token_slot, t0, t1, p.total_tokens, p.num_slots);
-    T *out = reinterpret_cast<T *>(p.out) + c0;
-    if (cls != 1) {
-        if (cls < 0 && c0 == 0)
-            report(p.err, GDN_DEVERR_BAD_SLOT);
-        if (t0 >= 0 && t1 >= t0 && t1 <= p.total_tokens) {
-            float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int t = t0; t < t1; ++t)
-                Vec8<T>::store(out + (size_t)t * C, z);
+    const bool silu = p.silu != 0;
+    T *out = nullptr;
+    float taps[8 * W], bias[8];
+    float win[W - 1][8], x[8], y[8];
+
+    if (gid >= n_window) {
+        // ------------------------- token thread -------------------------
+        const long long g2 = gid - n_window;
+        const long long run = g2 / groups_per_row;
+        const int c0 = (int)(g2 % groups_per_row) * kVec;
+        const long long first = run * kRun;
+        if (first >= p.total_tokens)
+            return;
+        const long long last = first + kRun < p.total_tokens ? first + kRun : p.total_tokens;
+        out = reinterpret_cast<T *>(p.out) + c0;
+        load_taps<T, W>(p, c0, taps, bias);
+        int r = -1, t0 = 0, t1 = 0, cls = 0;
+        long long have = -1; // the window holds the W-1 inputs before token `have`
+        for (long long tok = first; tok < last; ++tok) {
+            if (r < 0 || tok >= t1) {
+                r = seq_of(p.cu_seqlens, p.nseq, tok);
+                t0 = p.cu_seqlens[r];
+                t1 = p.cu_seqlens[r + 1];
+                const int rs = p.read_slot[r];
+                const int ws = in_place ? rs : p.write_slot[r];
+                cls = classify_seq(rs, ws, in_place, p.token_slot, t0, t1, p.total_tokens, p.num_slots);
+                have = -1;
+            }
+            if (tok < t0 || tok >= t1 || tok - t0 < W - 1)
+                continue; // not in this sequence's range, or a window thread's token
+            if (cls != 1) {
+                const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                Vec8<T>::store(out + (size_t)tok * C, z);
+                continue;
+            }
+            if (have != tok) {
+#pragma unroll
+                for (int j = 0; j < W - 1; ++j)
+                    Vec8<T>::load(xs + (size_t)(tok - (W - 1) + j) * C + c0, win[j]);
+            }
+            Vec8<T>::load(xs + (size_t)tok * C + c0, x);
+            conv8<T, W>(win, x, taps, bias, silu, y);
+            Vec8<T>::store(out + (size_t)tok * C, y);
+#pragma unroll
+            for (int j = 0; j + 1 < W - 1; ++j)
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    win[j][c] = win[j + 1][c];
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                win[W - 2][c] = x[c];
+            have = tok + 1;
+            if (p.token_slot) {
+                const int ts = p.token_slot[tok];
+#pragma unroll
+                for (int j = 0; j < W - 1; ++j)
+                    Vec8<T>::store(conv + ((size_t)ts * (W - 1) + j) * C + c0, win[j]);
+            }
         }
         return;
     }
-    T *conv = reinterpret_cast<T *>(p.conv);
-    float win[W - 1][8];
+
+    // ------------------------- window thread --------------------------
+    const int r = (int)(gid / groups_per_row);
+    const int c0 = (int)(gid % groups_per_row) * kVec;
+    const int t0 = p.cu_seqlens[r], t1 = p.cu_seqlens[r + 1];
+    const int rs = p.read_slot[r];
+    const int ws = in_place ? rs : p.write_slot[r];
+    const int cls = classify_seq(rs, ws, in_place, p.token_slot, t0, t1, p.total_tokens, p.num_slots);
+    out = reinterpret_cast<T *>(p.out) + c0;
+    if (cls != 1) {
+        const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (cls < 0 && c0 == 0)
+            report(p.err, GDN_DEVERR_BAD_SLOT);
+        if (t0 >= 0 && t1 >= t0 && t1 <= p.total_tokens)
+            for (int t = t0; t < t1 && t < t0 + W - 1; ++t)
+                Vec8<T>::store(out + (size_t)t * C, z);
+        return;
+    }
+    load_taps<T, W>(p, c0, taps, bias);
+    // the first W-1 tokens, then the new window
 #pragma unroll
     for (int j = 0; j < W - 1; ++j)
         Vec8<T>::load(conv + ((size_t)rs * (W - 1) + j) * C + c0, win[j]);
-    float taps[8 * W];
-    {
-        const T *wp = reinterpret_cast<const T *>(p.w) + (size_t)c0 * W;
-#pragma unroll
-        for (int t = 0; t < W; ++t) {
-            float tmp[8];
-            Vec8<T>::load(wp + 8 * t, tmp);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                taps[8 * t + i] = tmp[i];
-        }
-    }
-    float bias[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (p.bias)
-        Vec8<T>::load(reinterpret_cast<const T *>(p.bias) + c0, bias);
-    const T *xp = reinterpret_cast<const T *>(p.x) + c0;
-    for (int t = t0; t < t1; ++t) {
-        float x[8], y[8];
-        Vec8<T>::load(xp + (size_t)t * C, x);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float wi[W], wn[W - 1];
-#pragma unroll
-            for (int j = 0; j < W; ++j)
-                wi[j] = taps[i * W + j];
-#pragma unroll
-            for (int j = 0; j < W - 1; ++j)
-                wn[j] = win[j][i];
-            y[i] = conv_channel<W>(wn, x[i], wi, bias[i], p.silu != 0);
-        }
+    const int n = t1 - t0;
+    const int head = n < W - 1 ? n : W - 1;
+    for (int t = t0; t < t0 + head; ++t) {
+        Vec8<T>::load(xs + (size_t)t * C + c0, x);
+        conv8<T, W>(win, x, taps, bias, silu, y);
         Vec8<T>::store(out + (size_t)t * C, y);
         // the window moves on by one token; values stay in the activation type
 #pragma unroll
@@ -208,6 +303,13 @@ __global__ void __launch_bounds__(kThreads) conv_prefill_kernel(const ConvPrefil
         }
     }
     if (!p.token_slot) {
+        // the window after the last token: the last W-1 inputs (with the old
+        // window's tail when the sequence is shorter than that)
+        if (n > W - 1) {
+#pragma unroll
+            for (int j = 0; j < W - 1; ++j)
+                Vec8<T>::load(xs + (size_t)(t1 - (W - 1) + j) * C + c0, win[j]);
+        }
 #pragma unroll
         for (int j = 0; j < W - 1; ++j)
             Vec8<T>::store(conv + ((size_t)ws * (W - 1) + j) * C + c0, win[j]);
@@ -218,10 +320,13 @@ template <typename T, int W>
 cudaError_t launch_prefill_w(const ConvPrefillArgs &a, cudaStream_t s)
 {
     const int groups = a.channels / kVec;
-    const long long threads = (long long)a.nseq * groups;
-    if (threads == 0)
+    const long long runs = ((long long)a.total_tokens + kRun - 1) / kRun;
+    const long long threads = ((long long)a.nseq + runs) * groups;
+    if (a.nseq == 0 || threads == 0)
         return cudaSuccess;
     const long long blocks = (threads + kThreads - 1) / kThreads;
+    if (blocks > 0x7fffffffll)
+        return cudaErrorInvalidValue;
     return launch_pdl(conv_prefill_kernel<T, W>, dim3((unsigned)blocks), dim3(kThreads), 0, s, a, groups);
 }
 

@@ -202,6 +202,12 @@ def test_conv_prefill_equals_decode_conv_and_oracle(gdn, orc, shape, lens):
                               np.abs(c.bias64), silu=False)
     check_conv_outputs(orc, f64(y), y_exact, mag, shape.dtype)
     assert np.array_equal(f64(c.cp.tensor), cp64)
+    # in place: the same outputs, the new window back in the read slot
+    c.reset()
+    y = g.causal_conv1d_prefill(c.x, c.cp, c.cu, c.rs, c.w, c.bias)
+    torch.cuda.synchronize()
+    assert torch.equal(y, ref)
+    assert torch.equal(c.cp.tensor[rs], ref_cp[rs])
     # verify: the window after each token in its token slot
     c.reset()
     y = g.causal_conv1d_prefill(c.x, c.cp, c.cu, c.rs, c.w, c.bias, token_slot=c.ts)
