@@ -234,3 +234,60 @@ def test_fused_commit_equals_layer_then_commit(gdn, shape):
     assert torch.equal(c.pool.tensor, ref_pool)
     assert torch.equal(c.cp.tensor, ref_cp)
     assert gdn.get_device_error() == 0
+
+
+@pytest.mark.slow
+def test_claim_counters_under_repetition_and_two_streams(gdn):
+    """The claimed tail and its counter reset, over and over: 40 launches of
+    the fused layer with its commit (256 rows, where half of the work is
+    claimed) give identical outputs and states every time; and two pools
+    driven from two streams at once, each with its own counters, give what
+    they give one after the other."""
+    s = I.QWEN_08B.with_(rows=256)
+    cases = [LayerCase(gdn, s, seed=35 + i, num_slots=2 * s.rows + 1, pad_frac=0.1) for i in range(2)]
+    inputs = [c.draw()[0] for c in cases]
+
+    def run(c, xd, stream=None):
+        with torch.cuda.stream(stream or torch.cuda.current_stream()):
+            return gdn.gdn_layer_decode(xd["x"], c.cp, c.w, c.bias, c.A_log, c.dt_bias, xd["a"], xd["b"],
+                                        c.pool, c.rs, c.ws, commit=True)
+
+    # one after the other: the reference
+    refs = []
+    for c, xd in zip(cases, inputs):
+        c.reset()
+        rs0, ws0 = c.rs.clone(), c.ws.clone()
+        o = run(c, xd).clone()
+        torch.cuda.synchronize()
+        refs.append((o, c.pool.tensor.clone(), c.cp.tensor.clone(), c.rs.clone(), c.ws.clone()))
+        c.rs.copy_(rs0)
+        c.ws.copy_(ws0)
+    c0, xd0 = cases[0], inputs[0]
+    rs0, ws0 = c0.rs.clone(), c0.ws.clone()
+    for rep in range(40):
+        c0.reset()
+        c0.rs.copy_(rs0)
+        c0.ws.copy_(ws0)
+        o = run(c0, xd0)
+        torch.cuda.synchronize()
+        assert torch.equal(o, refs[0][0]), f"launch {rep}"
+        assert torch.equal(c0.pool.tensor, refs[0][1]), f"launch {rep}"
+        assert torch.equal(c0.rs, refs[0][3]) and torch.equal(c0.ws, refs[0][4]), f"launch {rep}"
+    # both pools at once, on two streams
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for rep in range(10):
+        for c in cases:
+            c.reset()
+        cases[0].rs.copy_(rs0)
+        cases[0].ws.copy_(ws0)
+        rs1, ws1 = refs[1][4], refs[1][3]  # the second case's tables before its commit
+        cases[1].rs.copy_(rs1)
+        cases[1].ws.copy_(ws1)
+        torch.cuda.synchronize()
+        outs = [run(c, xd, st) for c, xd, st in zip(cases, inputs, streams)]
+        torch.cuda.synchronize()
+        for i, (c, o) in enumerate(zip(cases, outs)):
+            assert torch.equal(o, refs[i][0]), f"pool {i}, round {rep}"
+            assert torch.equal(c.pool.tensor, refs[i][1]), f"pool {i}, round {rep}"
+            assert torch.equal(c.cp.tensor, refs[i][2]), f"pool {i}, round {rep}"
+    assert gdn.get_device_error() == 0

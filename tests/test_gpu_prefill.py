@@ -281,3 +281,25 @@ def test_prefill_other_head_sizes(gdn, dk, dv, dtype):
         for i in range(n):
             assert torch.equal(c.pool.tensor[int(c.ts_np[c.cu_np[r] + i])], snaps[i][int(c.rs_np[r])])
     assert gdn.get_device_error() == 0
+
+
+@pytest.mark.slow
+def test_prefill_256_tokens_matches_oracle(gdn, orc):
+    """A 256-token prefill (0.8B shape, twin) against the fp64 oracle: every
+    output within the bf16 tolerance and every final state within the
+    chained-state tolerance of 256 steps."""
+    s = I.QWEN_08B
+    c = Case(gdn, s, [256, 0, 3], seed=77, n_pad=0)
+    out = c.prefill()
+    torch.cuda.synchronize()
+    pool = c.pool_np.astype(np.float64).copy()
+    o_ref, bad = orc.prefill(c.cu_np, c.ref["q"], c.ref["k"], c.ref["v"], c.ref["a"], c.ref["b"],
+                             c.prm["A_log"], c.prm["dt_bias"], pool, c.rs_np, write_slot=c.ws_np)
+    assert bad == 0
+    assert_out_close(f64(out), o_ref, s.dtype)
+    got = c.pool.tensor.cpu().numpy()
+    for sl in c.ws_np:
+        for h in range(s.hv):
+            err = state_rel_err(got[sl, h], pool[sl, h])
+            assert err <= STATE_TOL_CHAIN, f"slot {sl} head {h}: {err:.3g}"
+    assert gdn.get_device_error() == 0
