@@ -65,11 +65,20 @@ def _stream(dev: torch.device) -> int:
     return torch.cuda.current_stream(dev).cuda_stream
 
 
-def _ptr(t: Optional[torch.Tensor], what: str, dtype=None, device=None, contiguous=True):
+def _ptr(t: Optional[torch.Tensor], what: str, dtype=None, device=None, contiguous=True, host_ok=False):
+    """Device pointer of a tensor.  With host_ok, a page-locked (pinned) host
+    tensor is accepted too: under unified addressing its pointer is valid on
+    the device, and the kernels read or write it across the host link."""
     if t is None:
         return None
     if not t.is_cuda:
-        raise ValueError(f"{what} must be a CUDA tensor")
+        if host_ok and t.is_pinned():
+            if dtype is not None and t.dtype != dtype:
+                raise TypeError(f"{what} must be {dtype}, got {t.dtype}")
+            if contiguous and not t.is_contiguous():
+                raise ValueError(f"{what} must be contiguous")
+            return t.data_ptr()
+        raise ValueError(f"{what} must be a CUDA tensor" + (" or pinned host memory" if host_ok else ""))
     if device is not None and t.device != device:
         raise ValueError(f"{what} is on {t.device}, expected {device}")
     if dtype is not None and t.dtype != dtype:
@@ -180,7 +189,7 @@ def causal_conv1d_decode(x: torch.Tensor, conv_pool: ConvStatePool, slot_idx: to
     """Conv state update for one token a row. x: [rows][C] (row stride allowed)."""
     rows, C = x.shape
     dt = conv_pool.dtype
-    dev = x.device
+    dev = conv_pool.tensor.device
     if x.stride(1) != 1:
         raise ValueError("x rows must be contiguous")
     if out is None:
@@ -195,16 +204,17 @@ def causal_conv1d_decode(x: torch.Tensor, conv_pool: ConvStatePool, slot_idx: to
         _ptr(x, "x", dt, dev, contiguous=False), x.stride(0), conv_pool.handle,
         _ptr(slot_idx, "slot_idx", torch.int32, dev), _ptr(write_slot, "write_slot", torch.int32, dev),
         _ptr(w, "w", dt, dev), _ptr(bias, "bias", dt, dev), int(bool(silu)),
-        _ptr(out, "out", dt, dev), rows, _dtype_code(dt), _stream(dev)))
+        _ptr(out, "out", dt, dev, host_ok=True), rows, _dtype_code(dt), _stream(dev)))
     return out
 
 
 def gdn_decode_step(q, k, v, a, b, A_log, dt_bias, pool: GDNStatePool, read_slot, write_slot=None,
                     out: Optional[torch.Tensor] = None, keep_in_place: bool = False) -> torch.Tensor:
-    """Gated delta rule for one token a row. q,k: [rows][hk][dk]; v: [rows][hv][dv]; a,b: [rows][hv]."""
+    """Gated delta rule for one token a row. q,k: [rows][hk][dk]; v: [rows][hv][dv]; a,b: [rows][hv].
+    q, k, v, a, b and out may be pinned host tensors (read and written across the host link)."""
     rows = q.shape[0]
     dt = q.dtype
-    dev = q.device
+    dev = pool.tensor.device
     _numel(q, rows * pool.hk * pool.dk, "q")
     _numel(k, rows * pool.hk * pool.dk, "k")
     _numel(v, rows * pool.hv * pool.dv, "v")
@@ -219,11 +229,12 @@ def gdn_decode_step(q, k, v, a, b, A_log, dt_bias, pool: GDNStatePool, read_slot
         out = torch.empty((rows, pool.hv, pool.dv), dtype=dt, device=dev)
     _numel(out, rows * pool.hv * pool.dv, "out")
     _check(_lib.load().gdn_decode_step(
-        _ptr(q, "q", dt, dev), _ptr(k, "k", dt, dev), _ptr(v, "v", dt, dev), _ptr(a, "a", dt, dev),
-        _ptr(b, "b", dt, dev), _ptr(A_log, "A_log", torch.float32, dev),
+        _ptr(q, "q", dt, dev, host_ok=True), _ptr(k, "k", dt, dev, host_ok=True),
+        _ptr(v, "v", dt, dev, host_ok=True), _ptr(a, "a", dt, dev, host_ok=True),
+        _ptr(b, "b", dt, dev, host_ok=True), _ptr(A_log, "A_log", torch.float32, dev),
         _ptr(dt_bias, "dt_bias", torch.float32, dev), pool.handle,
         _ptr(read_slot, "read_slot", torch.int32, dev), _ptr(write_slot, "write_slot", torch.int32, dev),
-        _ptr(out, "out", dt, dev), rows, pool.hv, int(bool(keep_in_place)), _dtype_code(dt),
+        _ptr(out, "out", dt, dev, host_ok=True), rows, pool.hv, int(bool(keep_in_place)), _dtype_code(dt),
         _stream(dev)))
     return out
 
@@ -250,18 +261,18 @@ def gdn_prefill(q, k, v, a, b, A_log, dt_bias, pool: GDNStatePool, cu_seqlens, r
     v [T][hv][dv], a,b [T][hv]; sequence r is tokens cu_seqlens[r]..cu_seqlens[r+1]).
     The final state goes to write_slot (twin) or back to read_slot (in place)."""
     T, nseq = _prefill_checks(q, k, v, a, b, A_log, dt_bias, pool, cu_seqlens, read_slot)
-    dt, dev = q.dtype, q.device
+    dt, dev = q.dtype, pool.tensor.device
     if write_slot is not None:
         _numel(write_slot, nseq, "write_slot")
     if out is None:
         out = torch.empty((T, pool.hv, pool.dv), dtype=dt, device=dev)
     _numel(out, T * pool.hv * pool.dv, "out")
     _check(_lib.load().gdn_prefill(
-        _ptr(q, "q", dt, dev), _ptr(k, "k", dt, dev), _ptr(v, "v", dt, dev), _ptr(a, "a", dt, dev),
-        _ptr(b, "b", dt, dev), _ptr(A_log, "A_log", torch.float32, dev),
+        _ptr(q, "q", dt, dev, host_ok=True), _ptr(k, "k", dt, dev, host_ok=True), _ptr(v, "v", dt, dev, host_ok=True), _ptr(a, "a", dt, dev, host_ok=True),
+        _ptr(b, "b", dt, dev, host_ok=True), _ptr(A_log, "A_log", torch.float32, dev),
         _ptr(dt_bias, "dt_bias", torch.float32, dev), pool.handle,
         _ptr(cu_seqlens, "cu_seqlens", torch.int32, dev), _ptr(read_slot, "read_slot", torch.int32, dev),
-        _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev), nseq, T,
+        _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev, host_ok=True), nseq, T,
         int(bool(keep_in_place)), _dtype_code(dt), _stream(dev)))
     return out
 
@@ -271,17 +282,17 @@ def gdn_verify(q, k, v, a, b, A_log, dt_bias, pool: GDNStatePool, cu_seqlens, re
     """As gdn_prefill, but the state after token t goes to token_slot[t] (a
     state a token) and the read slot is left alone."""
     T, nseq = _prefill_checks(q, k, v, a, b, A_log, dt_bias, pool, cu_seqlens, read_slot)
-    dt, dev = q.dtype, q.device
+    dt, dev = q.dtype, pool.tensor.device
     _numel(token_slot, T, "token_slot")
     if out is None:
         out = torch.empty((T, pool.hv, pool.dv), dtype=dt, device=dev)
     _numel(out, T * pool.hv * pool.dv, "out")
     _check(_lib.load().gdn_verify(
-        _ptr(q, "q", dt, dev), _ptr(k, "k", dt, dev), _ptr(v, "v", dt, dev), _ptr(a, "a", dt, dev),
-        _ptr(b, "b", dt, dev), _ptr(A_log, "A_log", torch.float32, dev),
+        _ptr(q, "q", dt, dev, host_ok=True), _ptr(k, "k", dt, dev, host_ok=True), _ptr(v, "v", dt, dev, host_ok=True), _ptr(a, "a", dt, dev, host_ok=True),
+        _ptr(b, "b", dt, dev, host_ok=True), _ptr(A_log, "A_log", torch.float32, dev),
         _ptr(dt_bias, "dt_bias", torch.float32, dev), pool.handle,
         _ptr(cu_seqlens, "cu_seqlens", torch.int32, dev), _ptr(read_slot, "read_slot", torch.int32, dev),
-        _ptr(token_slot, "token_slot", torch.int32, dev), _ptr(out, "out", dt, dev), nseq, T,
+        _ptr(token_slot, "token_slot", torch.int32, dev), _ptr(out, "out", dt, dev, host_ok=True), nseq, T,
         _dtype_code(dt), _stream(dev)))
     return out
 
@@ -294,7 +305,7 @@ def causal_conv1d_prefill(x, conv_pool: ConvStatePool, cu_seqlens, read_slot, w,
     T = x.shape[0]
     C = conv_pool.channels
     nseq = cu_seqlens.numel() - 1
-    dt, dev = x.dtype, x.device
+    dt, dev = x.dtype, conv_pool.tensor.device
     _numel(x, T * C, "x")
     _numel(w, C * conv_pool.width, "w")
     if bias is not None:
@@ -308,10 +319,10 @@ def causal_conv1d_prefill(x, conv_pool: ConvStatePool, cu_seqlens, read_slot, w,
         out = torch.empty((T, C), dtype=dt, device=dev)
     _numel(out, T * C, "out")
     _check(_lib.load().causal_conv1d_prefill(
-        _ptr(x, "x", dt, dev), conv_pool.handle, _ptr(cu_seqlens, "cu_seqlens", torch.int32, dev),
+        _ptr(x, "x", dt, dev, host_ok=True), conv_pool.handle, _ptr(cu_seqlens, "cu_seqlens", torch.int32, dev),
         _ptr(read_slot, "read_slot", torch.int32, dev), _ptr(write_slot, "write_slot", torch.int32, dev),
         _ptr(token_slot, "token_slot", torch.int32, dev), _ptr(w, "w", dt, dev), _ptr(bias, "bias", dt, dev),
-        int(bool(silu)), _ptr(out, "out", dt, dev), nseq, T, _dtype_code(dt), _stream(dev)))
+        int(bool(silu)), _ptr(out, "out", dt, dev, host_ok=True), nseq, T, _dtype_code(dt), _stream(dev)))
     return out
 
 
@@ -325,7 +336,7 @@ def gdn_layer_decode(x, conv_pool: ConvStatePool, w, bias, A_log, dt_bias, a, b,
         raise ValueError("commit needs twin slots (a write_slot table, keep_in_place False)")
     rows = x.shape[0]
     dt = x.dtype
-    dev = x.device
+    dev = pool.tensor.device
     C = 2 * pool.hk * pool.dk + pool.hv * pool.dv
     _numel(x, rows * C, "x")
     _numel(w, C * conv_pool.width, "w")
@@ -341,11 +352,11 @@ def gdn_layer_decode(x, conv_pool: ConvStatePool, w, bias, A_log, dt_bias, a, b,
     if out is None:
         out = torch.empty((rows, pool.hv, pool.dv), dtype=dt, device=dev)
     _numel(out, rows * pool.hv * pool.dv, "out")
-    args = (_ptr(x, "x", dt, dev), conv_pool.handle, _ptr(w, "w", dt, dev), _ptr(bias, "bias", dt, dev),
+    args = (_ptr(x, "x", dt, dev, host_ok=True), conv_pool.handle, _ptr(w, "w", dt, dev), _ptr(bias, "bias", dt, dev),
             int(bool(silu)), _ptr(A_log, "A_log", torch.float32, dev),
-            _ptr(dt_bias, "dt_bias", torch.float32, dev), _ptr(a, "a", dt, dev), _ptr(b, "b", dt, dev),
+            _ptr(dt_bias, "dt_bias", torch.float32, dev), _ptr(a, "a", dt, dev, host_ok=True), _ptr(b, "b", dt, dev, host_ok=True),
             pool.handle, _ptr(read_slot, "read_slot", torch.int32, dev),
-            _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev), rows)
+            _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev, host_ok=True), rows)
     if commit:
         _check(_lib.load().gdn_layer_decode_commit(*args, _dtype_code(dt), _stream(dev)))
     else:
@@ -362,7 +373,7 @@ def gdn_layer_decode_noalloc(x, conv_pool: ConvStatePool, w, bias, A_log, dt_bia
     is required."""
     rows = x.shape[0]
     dt = x.dtype
-    dev = x.device
+    dev = pool.tensor.device
     C = 2 * pool.hk * pool.dk + pool.hv * pool.dv
     _numel(x, rows * C, "x")
     _numel(w, C * conv_pool.width, "w")
@@ -377,11 +388,11 @@ def gdn_layer_decode_noalloc(x, conv_pool: ConvStatePool, w, bias, A_log, dt_bia
         _numel(write_slot, rows, "write_slot")
     _numel(out, rows * pool.hv * pool.dv, "out")
     _check(_lib.load().gdn_layer_decode_noalloc(
-        _ptr(x, "x", dt, dev), conv_pool.handle, _ptr(w, "w", dt, dev), _ptr(bias, "bias", dt, dev),
+        _ptr(x, "x", dt, dev, host_ok=True), conv_pool.handle, _ptr(w, "w", dt, dev), _ptr(bias, "bias", dt, dev),
         int(bool(silu)), _ptr(A_log, "A_log", torch.float32, dev),
-        _ptr(dt_bias, "dt_bias", torch.float32, dev), _ptr(a, "a", dt, dev), _ptr(b, "b", dt, dev),
+        _ptr(dt_bias, "dt_bias", torch.float32, dev), _ptr(a, "a", dt, dev, host_ok=True), _ptr(b, "b", dt, dev, host_ok=True),
         pool.handle, _ptr(read_slot, "read_slot", torch.int32, dev),
-        _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev), rows,
+        _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev, host_ok=True), rows,
         int(bool(keep_in_place)), int(scratch_slot), _dtype_code(dt), _stream(dev)))
     return out
 
@@ -398,7 +409,7 @@ def gdn_layer_decode_bucket(x, conv_pool: ConvStatePool, w, bias, A_log, dt_bias
         raise ValueError("commit needs twin slots (a write_slot table, keep_in_place False)")
     rows = x.shape[0]
     dt = x.dtype
-    dev = x.device
+    dev = pool.tensor.device
     C = 2 * pool.hk * pool.dk + pool.hv * pool.dv
     _numel(x, rows * C, "x")
     _numel(w, C * conv_pool.width, "w")
@@ -413,11 +424,11 @@ def gdn_layer_decode_bucket(x, conv_pool: ConvStatePool, w, bias, A_log, dt_bias
         out = torch.empty((rows, pool.hv, pool.dv), dtype=dt, device=dev)
     _numel(out, rows * pool.hv * pool.dv, "out")
     _check(_lib.load().gdn_layer_decode_bucket(
-        _ptr(x, "x", dt, dev), conv_pool.handle, _ptr(w, "w", dt, dev), _ptr(bias, "bias", dt, dev),
+        _ptr(x, "x", dt, dev, host_ok=True), conv_pool.handle, _ptr(w, "w", dt, dev), _ptr(bias, "bias", dt, dev),
         int(bool(silu)), _ptr(A_log, "A_log", torch.float32, dev),
-        _ptr(dt_bias, "dt_bias", torch.float32, dev), _ptr(a, "a", dt, dev), _ptr(b, "b", dt, dev),
+        _ptr(dt_bias, "dt_bias", torch.float32, dev), _ptr(a, "a", dt, dev, host_ok=True), _ptr(b, "b", dt, dev, host_ok=True),
         pool.handle, _ptr(read_slot, "read_slot", torch.int32, dev),
-        _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev), rows,
+        _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev, host_ok=True), rows,
         _ptr(n_decode, "n_decode", torch.int32, dev), int(bool(keep_in_place)), int(bool(commit)),
         _dtype_code(dt), _stream(dev)))
     return out
@@ -490,7 +501,7 @@ def prepare_layer_decode(x, conv_pool: ConvStatePool, w, bias, A_log, dt_bias, a
         raise ValueError("commit needs twin slots (a write_slot table, keep_in_place False)")
     rows = x.shape[0]
     dt = x.dtype
-    dev = x.device
+    dev = pool.tensor.device
     C = 2 * pool.hk * pool.dk + pool.hv * pool.dv
     _numel(x, rows * C, "x")
     _numel(w, C * conv_pool.width, "w")
@@ -503,11 +514,11 @@ def prepare_layer_decode(x, conv_pool: ConvStatePool, w, bias, A_log, dt_bias, a
     if write_slot is not None:
         _numel(write_slot, rows, "write_slot")
     s = (stream or torch.cuda.current_stream(dev)).cuda_stream
-    args = (_ptr(x, "x", dt, dev), conv_pool.handle, _ptr(w, "w", dt, dev), _ptr(bias, "bias", dt, dev),
+    args = (_ptr(x, "x", dt, dev, host_ok=True), conv_pool.handle, _ptr(w, "w", dt, dev), _ptr(bias, "bias", dt, dev),
             int(bool(silu)), _ptr(A_log, "A_log", torch.float32, dev),
-            _ptr(dt_bias, "dt_bias", torch.float32, dev), _ptr(a, "a", dt, dev), _ptr(b, "b", dt, dev),
+            _ptr(dt_bias, "dt_bias", torch.float32, dev), _ptr(a, "a", dt, dev, host_ok=True), _ptr(b, "b", dt, dev, host_ok=True),
             pool.handle, _ptr(read_slot, "read_slot", torch.int32, dev),
-            _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev), rows)
+            _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev, host_ok=True), rows)
     if commit:
         args += (_dtype_code(dt), s)
     else:

@@ -29,7 +29,12 @@
  *    left in a thread-local buffer read by gdn_last_error().
  *  - Tensor arguments are DEVICE pointers unless stated otherwise; rows are
  *    contiguous and densely packed unless a row stride is given.  The caller
- *    owns every activation buffer.
+ *    owns every activation buffer.  Activation buffers (q, k, v, x, a, b and
+ *    the outputs) may also be page-locked host memory mapped into the
+ *    device's address space (cudaHostAlloc, or pinned memory under unified
+ *    addressing): the kernels then read and write it across the host link,
+ *    with no separate copy.  Pools, slot tables, taps, A_log and dt_bias are
+ *    device memory.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Compute
  *    calls only enqueue work: no host synchronisation and no allocation.  The
  *    first call on a device looks up the library's device error word, so

@@ -271,3 +271,16 @@ def test_copy_slots_argument_checks(L):
     assert L.conv_pool_copy_slots(cp, None, None, 0, None) == 0
     L.conv_state_pool_destroy(cp)
     L.gdn_state_pool_destroy(pool)
+
+
+def test_binding_accepts_only_device_or_pinned_pointers():
+    """The binding hands the library a device pointer, or a page-locked host
+    pointer where the call allows activations in host memory; pageable host
+    memory is refused on the host."""
+    import torch
+    from gated_deltanet_decode_gb300 import _ptr
+    with pytest.raises(ValueError, match="pinned host memory"):
+        _ptr(torch.zeros(4), "x", host_ok=True)
+    with pytest.raises(ValueError, match="must be a CUDA tensor$"):
+        _ptr(torch.zeros(4), "x")
+    assert _ptr(None, "x", host_ok=True) is None

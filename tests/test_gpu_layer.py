@@ -291,3 +291,32 @@ def test_claim_counters_under_repetition_and_two_streams(gdn):
             assert torch.equal(c.pool.tensor, refs[i][1]), f"pool {i}, round {rep}"
             assert torch.equal(c.cp.tensor, refs[i][2]), f"pool {i}, round {rep}"
     assert gdn.get_device_error() == 0
+
+
+def test_activations_in_pinned_host_memory(gdn):
+    """x, a, b and the output may live in pinned host memory: the fused layer
+    (with its commit) reads and writes them across the host link and gives
+    the values it gives with device buffers, bit for bit."""
+    s = I.QWEN_08B
+    c = LayerCase(gdn, s, seed=36, num_slots=2 * s.rows + 1, pad_frac=0.25)
+    xd, _ = c.draw()
+    rs0, ws0 = c.rs.clone(), c.ws.clone()
+    ref = gdn.gdn_layer_decode(xd["x"], c.cp, c.w, c.bias, c.A_log, c.dt_bias, xd["a"], xd["b"], c.pool,
+                               c.rs, c.ws, commit=True).clone()
+    torch.cuda.synchronize()
+    ref_pool, ref_cp, ref_rs = c.pool.tensor.clone(), c.cp.tensor.clone(), c.rs.clone()
+    c.reset()
+    c.rs.copy_(rs0)
+    c.ws.copy_(ws0)
+    hx, ha, hb = (xd[k].cpu().pin_memory() for k in ("x", "a", "b"))
+    hout = torch.full(ref.shape, float("nan"), dtype=ref.dtype).pin_memory()
+    gdn.gdn_layer_decode(hx, c.cp, c.w, c.bias, c.A_log, c.dt_bias, ha, hb, c.pool, c.rs, c.ws, out=hout,
+                         commit=True)
+    torch.cuda.synchronize()
+    assert torch.equal(hout, ref.cpu())
+    assert torch.equal(c.pool.tensor, ref_pool) and torch.equal(c.cp.tensor, ref_cp)
+    assert torch.equal(c.rs, ref_rs)
+    with pytest.raises(ValueError):
+        gdn.gdn_layer_decode(xd["x"].cpu(), c.cp, c.w, c.bias, c.A_log, c.dt_bias, ha, hb, c.pool, c.rs,
+                             c.ws)  # plain (pageable) host memory is refused
+    assert gdn.get_device_error() == 0
