@@ -76,6 +76,27 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def bf16_peak():
+    """Dense bf16 tensor rate, TFLOP/s: the measured burst figure, else the
+    fallback of one earlier GB300 measurement."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def chunked_mma_flops(lens, hv: int) -> float:
+    """Tensor-core flops gdn_prefill_chunked issues (dk = dv = 128, chunks of
+    64, three bf16 products for each split product): per chunk and head, the
+    20 lower 16x16 blocks of K K^T and Q K^T over dk, then per 16 state rows
+    S K^T and S Q^T (16x64 over dk), E T^T and U^T P^T (16x64 over 64) and
+    the state update (16x128 over 64); one m16n8k16 is 4096 flops."""
+    per_chunk = 20 * 8 * 2 * 3 + 8 * (8 * 8 * 6 + 4 * 8 * 3 * 2 + 4 * 16 * 3)
+    chunks = sum((n + 63) // 64 for n in lens)
+    return float(per_chunk * 4096 * chunks * hv)
+
+
 def kernel_source_sha() -> str:
     """Hash of the layer kernel's code: its sources with comments, blank lines
     and surrounding whitespace removed, so that editing a comment does not
@@ -334,6 +355,22 @@ def run_many_tokens(G, I, device, n=20):
                                    "peak": round(peak, 1), "unit": "TFLOP/s",
                                    "frac": round(flops / (us * 1e-6) / 1e12 / peak, 4),
                                    "peak_kind": "fp32 FMA lanes x 2 x max SM clock"}}
+    # the same prefill in chunks on the tensor cores
+    def prefill_chunked(st):
+        G.gdn_prefill_chunked(st["q"], st["k"], st["v"], st["a"], st["b"], st["A_log"], st["dt_bias"],
+                              st["pool"], st["cu"], st["rs"], None, out=st["out"], keep_in_place=True)
+
+    us_c = time_calls([lambda st=st: prefill_chunked(st) for st in sets], n, device)
+    mma = chunked_mma_flops([tok] * nseq, s.hv)
+    tpeak, tkind = bf16_peak()
+    res["prefill_chunked"] = {
+        "workload": f"0.8B-shaped rule, {nseq} sequences x {tok} tokens, in place, chunks of 64 on the tensor cores",
+        "us": round(us_c, 1), "tokens_per_s": round(T / (us_c * 1e-6), 1),
+        "speedup_vs_token_serial": round(us / us_c, 2),
+        "roofline": {"bound": "tensor", "achieved": round(mma / (us_c * 1e-6) / 1e12, 2), "peak": tpeak,
+                     "peak_kind": f"{tkind} dense bf16 (mma.sync issue)", "unit": "TFLOP/s",
+                     "frac": round(mma / (us_c * 1e-6) / 1e12 / tpeak, 4),
+                     "flops_per_launch": mma}}
     cb = 2.0 * T * s.channels * 2 + 2 * nseq * (s.width - 1) * s.channels * 2
     us = time_calls([lambda st=st: conv(st) for st in sets], n, device)
     res["conv_prefill"] = {"workload": f"0.8B-shaped conv, {nseq} sequences x {tok} tokens, in place",
@@ -595,6 +632,7 @@ def run_ours(args, rank, world, device):
             "frac": round(achieved / peak, 4),
             "traffic": recorded_traffic() if twin else None,
             "algorithmic_bytes_per_launch": lb,
+            "frac_of_same_bytes_vendor_copy": round(achieved / probes["vendor_copy_same_bytes"]["GB/s"], 4),
         },
         "e2e": e2e,
         "e2e_zero_copy": e2e_zc,
@@ -636,6 +674,23 @@ def run_probes(G, s, sets, device, K):
         torch.cuda.synchronize(device)
         us = t0.elapsed_time(t1) * 1e3 / K
         res[name] = {"us": round(us, 3), "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1)}
+    # the vendor's device-to-device copy (torch copy_) of the same state bytes,
+    # rotated over as many buffer pairs: what a copy of this size reaches
+    src = [torch.empty(state // 4, dtype=torch.float32, device=device).uniform_() for _ in range(NSETS)]
+    dst = [torch.empty_like(x) for x in src]
+    for i in range(8):
+        dst[i % NSETS].copy_(src[i % NSETS])
+    torch.cuda.synchronize(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(K):
+        dst[i % NSETS].copy_(src[i % NSETS])
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    us = t0.elapsed_time(t1) * 1e3 / K
+    res["vendor_copy_same_bytes"] = {"us": round(us, 3), "GB/s": round(2 * state / (us * 1e-6) / 1e9, 1)}
+    del src, dst
     # the probes wrote the pools; the layer kernel's values are not reused after this
     return res
 

@@ -756,7 +756,8 @@ static int check_tokens(int nseq, int total_tokens, const int32_t *cu_seqlens, c
 static int prefill_launch(const void *q, const void *k, const void *v, const void *a, const void *b,
                           const float *A_log, const float *dt_bias, gdn_pool *pool, const int32_t *cu_seqlens,
                           const int32_t *read_slot, const int32_t *write_slot, const int32_t *token_slot,
-                          void *out, int nseq, int total_tokens, int dtype, void *stream, const char *what)
+                          void *out, int nseq, int total_tokens, int dtype, void *stream, const char *what,
+                          bool chunked = false)
 {
     if (!pool)
         return fail(GDN_EINVAL, "state pool is NULL");
@@ -797,7 +798,8 @@ static int prefill_launch(const void *q, const void *k, const void *v, const voi
     s.dk = pool->dims.dk;
     s.dv = pool->dims.dv;
     s.err = err;
-    cudaError_t e = gdn::launch_gdn_prefill(s, dtype, static_cast<cudaStream_t>(stream));
+    cudaError_t e = chunked ? gdn::launch_gdn_prefill_chunked(s, dtype, static_cast<cudaStream_t>(stream))
+                            : gdn::launch_gdn_prefill(s, dtype, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, what);
     return ok();
@@ -813,6 +815,21 @@ int gdn_prefill(const void *q, const void *k, const void *v, const void *a, cons
     return prefill_launch(q, k, v, a, b, A_log, dt_bias, pool, cu_seqlens, read_slot,
                           keep_in_place ? nullptr : write_slot, nullptr, out, nseq, total_tokens, dtype,
                           stream, "gdn_prefill launch");
+}
+
+int gdn_prefill_chunked(const void *q, const void *k, const void *v, const void *a, const void *b,
+                        const float *A_log, const float *dt_bias, gdn_pool *pool, const int32_t *cu_seqlens,
+                        const int32_t *read_slot, const int32_t *write_slot, void *out, int nseq,
+                        int total_tokens, int keep_in_place, int dtype, void *stream)
+{
+    if (pool && !gdn::chunked_shape_supported(pool->dims.dk, pool->dims.dv))
+        return fail(GDN_EUNSUPPORTED, "gdn_prefill_chunked is built for dk = dv = 128 (pool has %d, %d)",
+                    pool->dims.dk, pool->dims.dv);
+    if (!keep_in_place && nseq > 0 && !write_slot)
+        return fail(GDN_EINVAL, "write_slot is NULL in twin mode");
+    return prefill_launch(q, k, v, a, b, A_log, dt_bias, pool, cu_seqlens, read_slot,
+                          keep_in_place ? nullptr : write_slot, nullptr, out, nseq, total_tokens, dtype,
+                          stream, "gdn_prefill_chunked launch", true);
 }
 
 int gdn_verify(const void *q, const void *k, const void *v, const void *a, const void *b,

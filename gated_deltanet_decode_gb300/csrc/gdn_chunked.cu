@@ -1,0 +1,590 @@
+// The gated delta rule over many tokens a sequence, regrouped over chunks of
+// tokens so that its work runs on the tensor cores (gdn_prefill_chunked).
+//
+// The pages name a chunked GDN path beside the decode kernel ("mstar PR
+// #965", section "Correctness": the mixed wrappers are checked against the
+// chunked GDN path; "mstar PR #1127": one GDN prefill kernel on Blackwell)
+// and print no formula for it.  This kernel computes the recurrence of
+// gdn_prefill,
+//     S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,   o_t = S_t q_t,
+// regrouped exactly over chunks of C = 64 tokens.  Write the step as
+// S_t = alpha_t S_{t-1} + u_t k_t^T with u_t = beta_t (v_t - alpha_t S_{t-1} k_t).
+// Inside a chunk that starts from S_0, let G_t be the running sum of
+// log alpha (so S_t = e^{G_t} S_0 + sum_{s<=t} e^{G_t-G_s} u_s k_s^T).  With
+// Q, K [C][dk] the normalised q and k and V [C][dv]:
+//     A[t][s] = beta_t e^{G_t-G_s} (k_t . k_s)    for s < t, else 0
+//     P[t][s] = e^{G_t-G_s} (q_t . k_s)           for s <= t, else 0
+//     T       = (I + A)^{-1}                       (u's triangular system)
+//     E       = (V^T - (S_0 K^T) diag(e^G)) diag(beta)            [dv][C]
+//     U^T     = E T^T                                               [dv][C]
+//     O^T     = (S_0 Q^T) diag(e^G) + U^T P^T                       [dv][C]
+//     S_C     = e^{G_C} S_0 + (U^T diag(e^{G_C-G})) K
+// Every exponent is G_t - G_s with s <= t, or G_t itself, so no factor
+// exceeds 1 and none overflows.  Tokens past a sequence's end pad the last
+// chunk with zero q, k, v and beta and a zero log-gate, which leaves every
+// real token's result unchanged.
+//
+// Layout of the work: one CTA per (sequence, value head), 8 warps.  Warp w
+// holds state rows 16w..16w+15 (every dk column) in its MMA accumulators for
+// the whole sequence, so the state is read once and written once.  Per chunk
+// the CTA first builds, in shared memory, the normalised Q and K, the gates,
+// A, P and T (T on the CUDA cores in fp32: 16x16 diagonal blocks by forward
+// substitution, then the blocks below them); then each warp forms the
+// products above for its own rows, and writes its outputs.
+//
+// Precision: the products run as mma.sync m16n8k16 bf16 with fp32
+// accumulation, each fp32 operand split into a bf16 head and a bf16 tail
+// (x = hi + lo to about 2^-17 relative); a product sums hi*hi, hi*lo and
+// lo*hi, so it carries about 1e-5 relative error instead of bf16's 4e-3.
+// The result agrees with the token-serial gdn_prefill within the chained
+// state tolerance, not bit for bit.
+//
+// Sequences, slots and errors follow gdn_prefill exactly: padding (read
+// slot 0) and bad sequences zero their outputs and touch no slot, a bad one
+// sets the device error word, an empty real sequence moves its state to the
+// write slot unchanged.
+#include <atomic>
+
+#include "gdn_device.cuh"
+#include "gdn_internal.h"
+
+namespace gdn {
+
+namespace {
+
+typedef __nv_bfloat16 bf16;
+
+constexpr int CK = 64;           // tokens a chunk
+constexpr int CD = 128;          // dk = dv
+constexpr int CWARPS = 8;        // each holds 16 state rows
+constexpr int CTHREADS = CWARPS * 32;
+constexpr int LDK = CD + 8;      // row stride (bf16) of [token][dk] tiles: 8 rows hit distinct banks
+constexpr int LDT = CK + 8;      // row stride (bf16) of [token][token] tiles
+constexpr int LDF = CK + 1;      // row stride (fp32) of the fp32 [token][token] work tiles
+constexpr int LDV = CD + 4;      // row stride (fp32) of the [token][dv] tile
+
+// Shared-memory layout, byte offsets (all 16-byte aligned).
+struct CS {
+    static constexpr int TOK = CK * LDK * 2;     // one bf16 [CK][LDK] tile
+    static constexpr int SQ = CK * LDT * 2;      // one bf16 [CK][LDT] tile
+    static constexpr int QH = 0;                 // q head / tail
+    static constexpr int QL = QH + TOK;
+    static constexpr int KH = QL + TOK;          // k head / tail
+    static constexpr int KL = KH + TOK;
+    static constexpr int PH = KL + TOK;          // P head / tail [t][s]
+    static constexpr int PL = PH + SQ;
+    static constexpr int TH = PL + SQ;           // T head / tail [t][s]
+    static constexpr int TL = TH + SQ;
+    static constexpr int AF = TL + SQ;           // fp32 A [t][s]; its upper blocks hold scratch
+    static constexpr int XF = AF + CK * LDF * 4; // fp32 T [t][s]
+    static constexpr int VO = XF + CK * LDF * 4; // fp32 [t][dv]: V in, then each warp's outputs
+    static constexpr int GG = VO + CK * LDV * 4; // fp32 [CK] running log-gate G
+    static constexpr int BE = GG + CK * 4;       // fp32 [CK] beta
+    static constexpr int EG = BE + CK * 4;       // fp32 [CK] e^{G_t}
+    static constexpr int EC = EG + CK * 4;       // fp32 [CK] e^{G_C - G_t}
+    static constexpr int BYTES = EC + CK * 4;
+};
+static_assert(CS::BYTES <= 227 * 1024, "shared memory");
+static_assert(CS::AF % 16 == 0 && CS::VO % 16 == 0 && (LDV * 4) % 16 == 0, "alignment");
+
+// ---------------------------------------------------------------------------
+// Tensor-core helpers (mma.sync m16n8k16, bf16 in, fp32 accumulate).
+// Fragment layout, g = lane / 4, c = lane % 4:
+//   A 16x16: a0 = (g, 2c..2c+1), a1 = (g+8, 2c..), a2 = (g, 2c+8..), a3 = (g+8, 2c+8..)
+//   B 16x8:  b0 = (k 2c..2c+1, n g), b1 = (k 2c+8..2c+9, n g)
+//   D 16x8:  d0 = (g, 2c), d1 = (g, 2c+1), d2 = (g+8, 2c), d3 = (g+8, 2c+1)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t bits(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t *>(&v); }
+
+// Split (x, y) into bf16 heads and tails: x = hi.x + lo.x to 2^-17 relative.
+__device__ __forceinline__ void split2(float x, float y, uint32_t &hi, uint32_t &lo)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    const float2 hf = __bfloat1622float2(h);
+    hi = bits(h);
+    lo = bits(__floats2bfloat162_rn(x - hf.x, y - hf.y));
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// d += (ah + al)(bh + bl), dropping al*bl (about 2^-34 relative).
+__device__ __forceinline__ void mma3(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4], uint32_t bh0,
+                                     uint32_t bh1, uint32_t bl0, uint32_t bl1)
+{
+    mma16816(d, al[0], al[1], al[2], al[3], bh0, bh1);
+    mma16816(d, ah[0], ah[1], ah[2], ah[3], bl0, bl1);
+    mma16816(d, ah[0], ah[1], ah[2], ah[3], bh0, bh1);
+}
+
+// A fragment of rows m0.., columns k0.. of a row-major bf16 tile X (row stride ld).
+__device__ __forceinline__ void lda(uint32_t (&a)[4], const bf16 *X, int ld, int m0, int k0, int g, int c)
+{
+    const bf16 *p = X + (m0 + g) * ld + k0 + 2 * c;
+    a[0] = *reinterpret_cast<const uint32_t *>(p);
+    a[1] = *reinterpret_cast<const uint32_t *>(p + 8 * ld);
+    a[2] = *reinterpret_cast<const uint32_t *>(p + 8);
+    a[3] = *reinterpret_cast<const uint32_t *>(p + 8 * ld + 8);
+}
+
+// B fragment with B[k][n] = X[n][k]: columns n0.., rows k0.. (X row-major, stride ld).
+__device__ __forceinline__ void ldb(uint32_t &b0, uint32_t &b1, const bf16 *X, int ld, int n0, int k0, int g, int c)
+{
+    const bf16 *p = X + (n0 + g) * ld + k0 + 2 * c;
+    b0 = *reinterpret_cast<const uint32_t *>(p);
+    b1 = *reinterpret_cast<const uint32_t *>(p + 8);
+}
+
+// B fragments of two adjacent 8-column tiles with B[k][n] = X[k][n] (X
+// row-major [k][n], stride ld): rows k0..k0+15, columns n0..n0+15.  One
+// transposing ldmatrix; lane l names row l%8 of 8x8 matrix l/8, matrix m
+// covering rows k0 + 8(m&1), columns n0 + 8(m>>1).
+__device__ __forceinline__ void ldb_trans2(uint32_t (&b)[4], const bf16 *X, int ld, int k0, int n0, int lane)
+{
+    const int m = lane >> 3, r = lane & 7;
+    const bf16 *p = X + (k0 + 8 * (m & 1) + r) * ld + n0 + 8 * (m >> 1);
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3])
+                 : "r"(a));
+}
+
+// Split accumulator tiles c0 (columns 0..7) and c1 (8..15) of one 16x16
+// block into the A fragments of that block (rows the same, k = columns).
+__device__ __forceinline__ void acc_to_a(uint32_t (&ah)[4], uint32_t (&al)[4], const float (&c0)[4],
+                                         const float (&c1)[4])
+{
+    split2(c0[0], c0[1], ah[0], al[0]);
+    split2(c0[2], c0[3], ah[1], al[1]);
+    split2(c1[0], c1[1], ah[2], al[2]);
+    split2(c1[2], c1[3], ah[3], al[3]);
+}
+
+template <typename T> __device__ __forceinline__ void load4(float (&v)[4], const T *p);
+template <> __device__ __forceinline__ void load4<float>(float (&v)[4], const float *p)
+{
+    const float4 x = *reinterpret_cast<const float4 *>(p);
+    v[0] = x.x, v[1] = x.y, v[2] = x.z, v[3] = x.w;
+}
+template <> __device__ __forceinline__ void load4<bf16>(float (&v)[4], const bf16 *p)
+{
+    const uint2 x = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x.y));
+    v[0] = a.x, v[1] = a.y, v[2] = b.x, v[3] = b.y;
+}
+
+template <typename T> __device__ __forceinline__ void store2(T *p, float x, float y);
+template <> __device__ __forceinline__ void store2<float>(float *p, float x, float y)
+{
+    *reinterpret_cast<float2 *>(p) = make_float2(x, y);
+}
+template <> __device__ __forceinline__ void store2<bf16>(bf16 *p, float x, float y)
+{
+    *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(x, y);
+}
+
+constexpr float kEps = 1e-6f; // L2-norm epsilon, as in the decode kernels
+
+template <typename TA>
+__global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillArgs p)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    bf16 *const QH = reinterpret_cast<bf16 *>(smem + CS::QH);
+    bf16 *const QL = reinterpret_cast<bf16 *>(smem + CS::QL);
+    bf16 *const KH = reinterpret_cast<bf16 *>(smem + CS::KH);
+    bf16 *const KL = reinterpret_cast<bf16 *>(smem + CS::KL);
+    bf16 *const PH = reinterpret_cast<bf16 *>(smem + CS::PH);
+    bf16 *const PL = reinterpret_cast<bf16 *>(smem + CS::PL);
+    bf16 *const TH = reinterpret_cast<bf16 *>(smem + CS::TH);
+    bf16 *const TL = reinterpret_cast<bf16 *>(smem + CS::TL);
+    float *const AF = reinterpret_cast<float *>(smem + CS::AF);
+    float *const XF = reinterpret_cast<float *>(smem + CS::XF);
+    float *const VO = reinterpret_cast<float *>(smem + CS::VO);
+    float *const GG = reinterpret_cast<float *>(smem + CS::GG);
+    float *const BE = reinterpret_cast<float *>(smem + CS::BE);
+    float *const EG = reinterpret_cast<float *>(smem + CS::EG);
+    float *const EC = reinterpret_cast<float *>(smem + CS::EC);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
+    const int seq = blockIdx.x / p.hv, h = blockIdx.x - seq * p.hv;
+    const int hq = h / (p.hv / p.hk);
+    wait_prior_grid();
+
+    const int t0 = p.cu_seqlens[seq], t1 = p.cu_seqlens[seq + 1];
+    const bool range_ok = t0 >= 0 && t1 >= t0 && t1 <= p.total_tokens;
+    const int rs = p.read_slot[seq];
+    const bool in_place = p.write_slot == nullptr;
+    const int ws = in_place ? rs : p.write_slot[seq];
+    const int cls = range_ok ? classify_row(rs, ws, p.num_slots, in_place) : -1;
+    TA *const out = reinterpret_cast<TA *>(p.out);
+    const size_t out_tok = (size_t)p.hv * CD;
+    if (cls != 1) {
+        // padding or bad: zero outputs (when the token range is sane), no slot touched
+        if (cls < 0 && h == 0 && tid == 0)
+            report(p.err, GDN_DEVERR_BAD_SLOT);
+        if (range_ok) {
+            const long long n_out = (long long)(t1 - t0) * CD;
+            for (long long e = tid; e < n_out; e += CTHREADS)
+                out[(size_t)(t0 + e / CD) * out_tok + (size_t)h * CD + (size_t)(e % CD)] = from_f<TA>(0.f);
+        }
+        return;
+    }
+
+    // the state: rows 16w + g and 16w + g + 8 of this warp, columns 8j + 2c, +1
+    const size_t slot_floats = (size_t)p.hv * CD * CD;
+    const size_t head_off = (size_t)h * CD * CD;
+    float sacc[16][4];
+    {
+        const float *S0 = p.pool + (size_t)rs * slot_floats + head_off + (size_t)(16 * warp + g) * CD + 2 * c;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float2 x = *reinterpret_cast<const float2 *>(S0 + 8 * j);
+            const float2 y = *reinterpret_cast<const float2 *>(S0 + 8 * CD + 8 * j);
+            sacc[j][0] = x.x, sacc[j][1] = x.y, sacc[j][2] = y.x, sacc[j][3] = y.y;
+        }
+    }
+    // P's blocks above the diagonal are never computed: zero both halves once
+    for (int e = tid; e < 2 * CS::SQ / 4; e += CTHREADS)
+        reinterpret_cast<uint32_t *>(PH)[e] = 0u;
+
+    const float rate = expf(p.A_log[h]);
+    const float dtb = p.dt_bias[h];
+    const float qscale = 1.0f / sqrtf((float)CD);
+    const TA *const qg = reinterpret_cast<const TA *>(p.q);
+    const TA *const kg = reinterpret_cast<const TA *>(p.k);
+    const TA *const vg = reinterpret_cast<const TA *>(p.v);
+    const TA *const ag = reinterpret_cast<const TA *>(p.a);
+    const TA *const bg = reinterpret_cast<const TA *>(p.b);
+    const int L = t1 - t0;
+
+#pragma unroll 1
+    for (int c0 = 0; c0 < L; c0 += CK) {
+        const int n = min(CK, L - c0);
+        __syncthreads(); // every warp is done with the previous chunk's tiles
+
+        // ---- the chunk's gates: log alpha, beta, running sums (warp 0) ----
+        if (warp == 0) {
+            float la[2], bt[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int tt = lane + 32 * i;
+                la[i] = 0.f, bt[i] = 0.f;
+                if (tt < n) {
+                    const size_t idx = (size_t)(t0 + c0 + tt) * p.hv + h;
+                    la[i] = rate == 0.f ? 0.f : -rate * softplus_f(to_f(ag[idx]) + dtb);
+                    bt[i] = gate_beta(to_f(bg[idx]));
+                }
+            }
+            float s0 = la[0], s1 = la[1];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float x0 = __shfl_up_sync(0xffffffffu, s0, o);
+                const float x1 = __shfl_up_sync(0xffffffffu, s1, o);
+                if (lane >= o)
+                    s0 += x0, s1 += x1;
+            }
+            s1 += __shfl_sync(0xffffffffu, s0, 31);
+            const float gc = __shfl_sync(0xffffffffu, s1, 31);
+            GG[lane] = s0, GG[lane + 32] = s1;
+            BE[lane] = bt[0], BE[lane + 32] = bt[1];
+            EG[lane] = expf(s0), EG[lane + 32] = expf(s1);
+            EC[lane] = expf(gc - s0), EC[lane + 32] = expf(gc - s1);
+        }
+
+        // ---- q, k (normalised, split) and v: a token a warp, 4 channels a lane ----
+        for (int tt = warp; tt < CK; tt += CWARPS) {
+            float qv[4] = {0.f, 0.f, 0.f, 0.f}, kv[4] = {0.f, 0.f, 0.f, 0.f}, vv[4] = {0.f, 0.f, 0.f, 0.f};
+            if (tt < n) {
+                const size_t tok = (size_t)(t0 + c0 + tt);
+                load4<TA>(qv, qg + (tok * p.hk + hq) * CD + 4 * lane);
+                load4<TA>(kv, kg + (tok * p.hk + hq) * CD + 4 * lane);
+                load4<TA>(vv, vg + (tok * p.hv + h) * CD + 4 * lane);
+            }
+            float sq = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
+            float sk = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            }
+            const float iq = qscale / sqrtf(sq + kEps), ik = 1.0f / sqrtf(sk + kEps);
+            uint32_t h0, l0, h1, l1;
+            split2(qv[0] * iq, qv[1] * iq, h0, l0);
+            split2(qv[2] * iq, qv[3] * iq, h1, l1);
+            *reinterpret_cast<uint2 *>(QH + tt * LDK + 4 * lane) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2 *>(QL + tt * LDK + 4 * lane) = make_uint2(l0, l1);
+            split2(kv[0] * ik, kv[1] * ik, h0, l0);
+            split2(kv[2] * ik, kv[3] * ik, h1, l1);
+            *reinterpret_cast<uint2 *>(KH + tt * LDK + 4 * lane) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2 *>(KL + tt * LDK + 4 * lane) = make_uint2(l0, l1);
+            *reinterpret_cast<float4 *>(VO + tt * LDV + 4 * lane) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+        }
+        __syncthreads();
+
+        // ---- K K^T -> A and Q K^T -> P, lower 16x16 blocks only (10 each) ----
+        for (int u = warp; u < 20; u += CWARPS) {
+            const bool isq = u >= 10;
+            const int idx = isq ? u - 10 : u;
+            const int mb = idx >= 6 ? 3 : idx >= 3 ? 2 : idx >= 1 ? 1 : 0;
+            const int nb = idx - mb * (mb + 1) / 2;
+            const bf16 *XH = isq ? QH : KH, *XL = isq ? QL : KL;
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int kb = 0; kb < CD / 16; ++kb) {
+                uint32_t ah[4], al[4];
+                lda(ah, XH, LDK, 16 * mb, 16 * kb, g, c);
+                lda(al, XL, LDK, 16 * mb, 16 * kb, g, c);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    uint32_t bh0, bh1, bl0, bl1;
+                    ldb(bh0, bh1, KH, LDK, 16 * nb + 8 * nt, 16 * kb, g, c);
+                    ldb(bl0, bl1, KL, LDK, 16 * nb + 8 * nt, 16 * kb, g, c);
+                    mma3(acc[nt], ah, al, bh0, bh1, bl0, bl1);
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int t = 16 * mb + g + 8 * hr;
+                    const int s = 16 * nb + 8 * nt + 2 * c;
+                    const float x = acc[nt][2 * hr], y = acc[nt][2 * hr + 1];
+                    const float gt = GG[t];
+                    if (!isq) {
+                        const float bt = BE[t];
+                        AF[t * LDF + s] = s < t ? bt * expf(gt - GG[s]) * x : 0.f;
+                        AF[t * LDF + s + 1] = s + 1 < t ? bt * expf(gt - GG[s + 1]) * y : 0.f;
+                    } else {
+                        const float px = s <= t ? expf(gt - GG[s]) * x : 0.f;
+                        const float py = s + 1 <= t ? expf(gt - GG[s + 1]) * y : 0.f;
+                        uint32_t hh, ll;
+                        split2(px, py, hh, ll);
+                        *reinterpret_cast<uint32_t *>(PH + t * LDT + s) = hh;
+                        *reinterpret_cast<uint32_t *>(PL + t * LDT + s) = ll;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- T = (I + A)^{-1}, fp32 ----
+        // diagonal 16x16 blocks: forward substitution on a unit vector, one column a thread
+        if (tid < CK) {
+            const int base = 16 * (tid >> 4), col = tid & 15;
+            float x[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const float *arow = AF + (base + r) * LDF + base;
+                float acc = r == col ? 1.f : 0.f;
+#pragma unroll
+                for (int s = 0; s < r; ++s)
+                    acc = fmaf(-arow[s], x[s], acc);
+                x[r] = acc;
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r)
+                XF[(base + r) * LDF + base + col] = x[r];
+        }
+        __syncthreads();
+        // blocks below the diagonal, by distance d: T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ,
+        // the sum parked in A's unused block (J, I); one element a thread
+        {
+            const int r = tid >> 4, col = tid & 15;
+#pragma unroll 1
+            for (int d = 1; d < CK / 16; ++d) {
+                for (int J = 0; J + d < CK / 16; ++J) {
+                    const int I = J + d;
+                    float acc = 0.f;
+                    for (int K = J; K < I; ++K) {
+                        const float *arow = AF + (16 * I + r) * LDF + 16 * K;
+                        const float *tcol = XF + (16 * K) * LDF + 16 * J + col;
+#pragma unroll
+                        for (int s = 0; s < 16; ++s)
+                            acc = fmaf(arow[s], tcol[s * LDF], acc);
+                    }
+                    AF[(16 * J + r) * LDF + 16 * I + col] = acc;
+                }
+                __syncthreads();
+                for (int J = 0; J + d < CK / 16; ++J) {
+                    const int I = J + d;
+                    const float *trow = XF + (16 * I + r) * LDF + 16 * I;
+                    const float *xcol = AF + (16 * J) * LDF + 16 * I + col;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int s = 0; s < 16; ++s)
+                        acc = fmaf(trow[s], xcol[s * LDF], acc);
+                    XF[(16 * I + r) * LDF + 16 * J + col] = -acc;
+                }
+                __syncthreads();
+            }
+        }
+        // T's lower triangle, split (above it: zero)
+        for (int e = tid; e < CK * CK / 2; e += CTHREADS) {
+            const int t = e / (CK / 2), s = 2 * (e % (CK / 2));
+            const float x = s <= t ? XF[t * LDF + s] : 0.f;
+            const float y = s + 1 <= t ? XF[t * LDF + s + 1] : 0.f;
+            uint32_t hh, ll;
+            split2(x, y, hh, ll);
+            *reinterpret_cast<uint32_t *>(TH + t * LDT + s) = hh;
+            *reinterpret_cast<uint32_t *>(TL + t * LDT + s) = ll;
+        }
+        __syncthreads();
+
+        // ---- this warp's rows: Z = S K^T and Y = S Q^T (16 x 64 each) ----
+        float z[8][4], y[8][4], u[8][4];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                z[nt][e] = 0.f, y[nt][e] = 0.f, u[nt][e] = 0.f;
+#pragma unroll
+        for (int kb = 0; kb < CD / 16; ++kb) {
+            uint32_t ah[4], al[4];
+            acc_to_a(ah, al, sacc[2 * kb], sacc[2 * kb + 1]);
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                uint32_t bh0, bh1, bl0, bl1;
+                ldb(bh0, bh1, KH, LDK, 8 * nt, 16 * kb, g, c);
+                ldb(bl0, bl1, KL, LDK, 8 * nt, 16 * kb, g, c);
+                mma3(z[nt], ah, al, bh0, bh1, bl0, bl1);
+                ldb(bh0, bh1, QH, LDK, 8 * nt, 16 * kb, g, c);
+                ldb(bl0, bl1, QL, LDK, 8 * nt, 16 * kb, g, c);
+                mma3(y[nt], ah, al, bh0, bh1, bl0, bl1);
+            }
+        }
+        // E = (V^T - Z diag(e^G)) diag(beta), in place of Z
+        const int rA = 16 * warp + g;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int t = 8 * nt + 2 * c + (e & 1), r = rA + 8 * (e >> 1);
+                z[nt][e] = BE[t] * (VO[t * LDV + r] - EG[t] * z[nt][e]);
+            }
+        // U^T = E T^T
+#pragma unroll
+        for (int kb = 0; kb < CK / 16; ++kb) {
+            uint32_t ah[4], al[4];
+            acc_to_a(ah, al, z[2 * kb], z[2 * kb + 1]);
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                uint32_t bh0, bh1, bl0, bl1;
+                ldb(bh0, bh1, TH, LDT, 8 * nt, 16 * kb, g, c);
+                ldb(bl0, bl1, TL, LDT, 8 * nt, 16 * kb, g, c);
+                mma3(u[nt], ah, al, bh0, bh1, bl0, bl1);
+            }
+        }
+        // O^T = Y diag(e^G) + U^T P^T
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+            const int t = 8 * nt + 2 * c;
+            const float e0 = EG[t], e1 = EG[t + 1];
+            y[nt][0] *= e0, y[nt][1] *= e1, y[nt][2] *= e0, y[nt][3] *= e1;
+        }
+#pragma unroll
+        for (int kb = 0; kb < CK / 16; ++kb) {
+            uint32_t ah[4], al[4];
+            acc_to_a(ah, al, u[2 * kb], u[2 * kb + 1]);
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                uint32_t bh0, bh1, bl0, bl1;
+                ldb(bh0, bh1, PH, LDT, 8 * nt, 16 * kb, g, c);
+                ldb(bl0, bl1, PL, LDT, 8 * nt, 16 * kb, g, c);
+                mma3(y[nt], ah, al, bh0, bh1, bl0, bl1);
+            }
+        }
+        // outputs into this warp's own columns of the V tile (this lane read exactly these)
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int t = 8 * nt + 2 * c + (e & 1), r = rA + 8 * (e >> 1);
+                VO[t * LDV + r] = y[nt][e];
+            }
+        // S = e^{G_C} S + (U^T diag(e^{G_C - G})) K
+        const float gC = EG[CK - 1];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sacc[j][e] *= gC;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+            const int t = 8 * nt + 2 * c;
+            const float e0 = EC[t], e1 = EC[t + 1];
+            u[nt][0] *= e0, u[nt][1] *= e1, u[nt][2] *= e0, u[nt][3] *= e1;
+        }
+#pragma unroll
+        for (int kb = 0; kb < CK / 16; ++kb) {
+            uint32_t ah[4], al[4];
+            acc_to_a(ah, al, u[2 * kb], u[2 * kb + 1]);
+#pragma unroll
+            for (int np = 0; np < CD / 16; ++np) {
+                uint32_t bh[4], bl[4];
+                ldb_trans2(bh, KH, LDK, 16 * kb, 16 * np, lane);
+                ldb_trans2(bl, KL, LDK, 16 * kb, 16 * np, lane);
+                mma3(sacc[2 * np], ah, al, bh[0], bh[1], bl[0], bl[1]);
+                mma3(sacc[2 * np + 1], ah, al, bh[2], bh[3], bl[2], bl[3]);
+            }
+        }
+        __syncwarp();
+        // this warp's 16 output columns of each real token: 8 lanes a token, two values a lane
+        for (int e = lane; e < n * 8; e += 32) {
+            const int t = e >> 3, r = 16 * warp + 2 * (e & 7);
+            const float2 v2 = *reinterpret_cast<const float2 *>(VO + t * LDV + r);
+            store2<TA>(out + (size_t)(t0 + c0 + t) * out_tok + (size_t)h * CD + r, v2.x, v2.y);
+        }
+    }
+
+    // the final state, to the write slot (the read slot in place)
+    {
+        float *Sd = p.pool + (size_t)ws * slot_floats + head_off + (size_t)(16 * warp + g) * CD + 2 * c;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            *reinterpret_cast<float2 *>(Sd + 8 * j) = make_float2(sacc[j][0], sacc[j][1]);
+            *reinterpret_cast<float2 *>(Sd + 8 * CD + 8 * j) = make_float2(sacc[j][2], sacc[j][3]);
+        }
+    }
+}
+
+template <typename TA>
+cudaError_t launch_chunked_t(const PrefillArgs &a, cudaStream_t s)
+{
+    const long long ctas = (long long)a.nseq * a.hv;
+    if (ctas == 0)
+        return cudaSuccess;
+    if (ctas > 0x7fffffffll)
+        return cudaErrorInvalidValue;
+    auto kern = gdn_chunked_kernel<TA>;
+    static std::atomic<unsigned long long> configured{0}; // one bit per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CS::BYTES);
+        if (e != cudaSuccess)
+            return e;
+        configured.fetch_or(bit, std::memory_order_release);
+    }
+    return launch_pdl(kern, dim3((unsigned)ctas), dim3(CTHREADS), (size_t)CS::BYTES, s, a);
+}
+
+} // namespace
+
+bool chunked_shape_supported(int dk, int dv) { return dk == CD && dv == CD; }
+
+cudaError_t launch_gdn_prefill_chunked(const PrefillArgs &a, int dtype, cudaStream_t s)
+{
+    if (!chunked_shape_supported(a.dk, a.dv))
+        return cudaErrorInvalidValue;
+    return dtype == GDN_BF16 ? launch_chunked_t<bf16>(a, s) : launch_chunked_t<float>(a, s);
+}
+
+} // namespace gdn

@@ -101,9 +101,13 @@ cudaError_t launch_gdn_layer(const StepArgs &a, int dtype, cudaStream_t s);
 cudaError_t launch_conv(const ConvArgs &a, int dtype, cudaStream_t s);
 cudaError_t launch_gdn_prefill(const PrefillArgs &a, int dtype, cudaStream_t s);
 cudaError_t launch_conv_prefill(const ConvPrefillArgs &a, int dtype, cudaStream_t s);
+// The chunked (tensor-core) form of launch_gdn_prefill: in place or twin, no token slots.
+cudaError_t launch_gdn_prefill_chunked(const PrefillArgs &a, int dtype, cudaStream_t s);
 
 // True when the state kernels are built for (dk, dv).
 bool step_shape_supported(int dk, int dv);
+// True when the chunked prefill is built for (dk, dv).
+bool chunked_shape_supported(int dk, int dv);
 // True when the fused layer can run this shape.
 bool layer_shape_supported(int dk, int dv, int group, bool in_place);
 

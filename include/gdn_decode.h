@@ -248,6 +248,18 @@ int gdn_prefill(const void *q, const void *k, const void *v, const void *a, cons
                 const float *A_log, const float *dt_bias, gdn_pool *pool, const int32_t *cu_seqlens,
                 const int32_t *read_slot, const int32_t *write_slot, void *out, int nseq, int total_tokens,
                 int keep_in_place, int dtype, void *stream);
+/* gdn_prefill_chunked: gdn_prefill's operation and contract (same
+ * arguments, slots, padding, bad sequences, in place or twin), computed in
+ * chunks of 64 tokens on the tensor cores: the chunked GDN path that the
+ * pages check the mixed step against ("mstar PR #965", "Correctness") and
+ * run as one GDN prefill kernel ("mstar PR #1127").  Each product splits its
+ * fp32 operands into bf16 heads and tails, so outputs and final states agree
+ * with gdn_prefill to about 1e-5 relative per chunk, not bit for bit.  Built
+ * for dk = dv = 128 (GDN_EUNSUPPORTED otherwise).  q, k, v 16-byte aligned. */
+int gdn_prefill_chunked(const void *q, const void *k, const void *v, const void *a, const void *b,
+                        const float *A_log, const float *dt_bias, gdn_pool *pool, const int32_t *cu_seqlens,
+                        const int32_t *read_slot, const int32_t *write_slot, void *out, int nseq,
+                        int total_tokens, int keep_in_place, int dtype, void *stream);
 int gdn_verify(const void *q, const void *k, const void *v, const void *a, const void *b,
                const float *A_log, const float *dt_bias, gdn_pool *pool, const int32_t *cu_seqlens,
                const int32_t *read_slot, const int32_t *token_slot, void *out, int nseq, int total_tokens,

@@ -257,6 +257,30 @@ def test_prefill_argument_checks(L):
     L.gdn_state_pool_destroy(pool)
 
 
+def test_prefill_chunked_argument_checks(L):
+    """gdn_prefill_chunked: built for dk = dv = 128 only (unsupported shapes
+    are refused before anything else), otherwise gdn_prefill's checks."""
+    P = FAKE
+    rc, small = _wrap(L, hk=2, hv=2, dk=16, dv=16)
+    assert rc == 0
+    rc, pool = _wrap(L, hk=2, hv=4, dk=128, dv=128)
+    assert rc == 0
+
+    def chunked(nseq=2, T=5, pool_=pool, ws=P, inplace=0, dtype=1, q=P):
+        return L.gdn_prefill_chunked(q, P, P, P, P, P, P, pool_, P, P, ws, P, nseq, T, inplace, dtype, None)
+
+    assert chunked(pool_=small) == EUNSUPPORTED and b"128" in L.gdn_last_error()
+    assert chunked(pool_=None) == EINVAL
+    assert chunked(nseq=-1) == EINVAL
+    assert chunked(dtype=3) == EINVAL
+    assert chunked(ws=None) == EINVAL and b"write_slot" in L.gdn_last_error()
+    assert chunked(q=P + 8) == EINVAL and b"aligned" in L.gdn_last_error()
+    assert chunked(nseq=0) == 0
+    assert chunked(nseq=0, ws=None, inplace=1) == 0
+    L.gdn_state_pool_destroy(small)
+    L.gdn_state_pool_destroy(pool)
+
+
 def test_copy_slots_argument_checks(L):
     rc, pool = _wrap(L)
     assert rc == 0

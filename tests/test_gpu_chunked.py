@@ -1,0 +1,166 @@
+"""GPU checks of gdn_prefill_chunked, the tensor-core chunked form of the
+rule over many tokens a sequence ("mstar PR #965", "Correctness": the
+chunked GDN path; "mstar PR #1127": one GDN prefill kernel).
+
+1. Against the fp64 oracle (the rule token after token): every output within
+   the bf16 tolerance, every final state within the chained-state tolerance;
+   sequences of 1, 63, 64, 65, 130 and 512 tokens cover whole chunks, ragged
+   tails and one-token chunks, in place and twin, the 0.8B and 9B (grouped
+   heads) shapes, bf16 and fp32 activations.
+2. Against the exact token-serial gdn_prefill on the GPU: the two agree far
+   inside the tolerances (about 1e-5 relative), so the chunking adds no
+   error the oracle tolerances would hide.
+3. Padding, empty, bad slots and bad token ranges behave as in gdn_prefill,
+   bit for bit: zero outputs, untouched slots, the device error word.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gated_deltanet_decode_gb300 import inputs as I
+from gpu_helpers import STATE_TOL_CHAIN, assert_out_close, f64, state_rel_err, ti
+from test_gpu_prefill import Case
+
+pytestmark = pytest.mark.gpu
+
+
+def chunked(c, keep_in_place=False, out=None):
+    return c.gdn.gdn_prefill_chunked(c.dev["q"], c.dev["k"], c.dev["v"], c.dev["a"], c.dev["b"], c.A_log,
+                                     c.dt_bias, c.pool, c.cu, c.rs, None if keep_in_place else c.ws,
+                                     out=out, keep_in_place=keep_in_place)
+
+
+def oracle(orc, c, keep_in_place):
+    pool = c.pool_np.astype(np.float64).copy()
+    o_ref, bad = orc.prefill(c.cu_np, c.ref["q"], c.ref["k"], c.ref["v"], c.ref["a"], c.ref["b"],
+                             c.prm["A_log"], c.prm["dt_bias"], pool, c.rs_np,
+                             write_slot=None if keep_in_place else c.ws_np)
+    assert bad == 0
+    return o_ref, pool
+
+
+def check_against_oracle(c, out, o_ref, pool, keep_in_place):
+    assert_out_close(f64(out), o_ref, c.s.dtype)
+    got = c.pool.tensor.cpu().numpy()
+    real = c.rs_np > 0
+    slots = c.rs_np[real] if keep_in_place else c.ws_np[real]
+    for sl in slots:
+        for h in range(c.s.hv):
+            err = state_rel_err(got[sl, h], pool[sl, h])
+            assert err <= STATE_TOL_CHAIN, f"slot {sl} head {h}: {err:.3g}"
+    # every slot no real sequence writes is untouched (padding's included)
+    written = set(int(x) for x in slots)
+    for sl in range(c.num_slots):
+        if sl not in written:
+            assert np.array_equal(got[sl], c.pool_np[sl]), f"slot {sl} changed"
+
+
+CASES = [(I.QWEN_08B, [130, 64, 0, 1, 63, 65]), (I.QWEN_9B, [70, 0, 129, 5]),
+         (I.QWEN_08B.with_(dtype="f32"), [65, 3, 128])]
+IDS = ["0.8b", "9b", "0.8b-f32"]
+
+
+@pytest.mark.parametrize("shape,lens", CASES, ids=IDS)
+@pytest.mark.parametrize("keep_in_place", [False, True], ids=["twin", "in_place"])
+def test_chunked_matches_oracle(gdn, orc, shape, lens, keep_in_place):
+    c = Case(gdn, shape, lens, seed=90)
+    out = chunked(c, keep_in_place)
+    torch.cuda.synchronize()
+    o_ref, pool = oracle(orc, c, keep_in_place)
+    check_against_oracle(c, out, o_ref, pool, keep_in_place)
+    assert gdn.get_device_error() == 0
+
+
+@pytest.mark.slow
+def test_chunked_512_tokens_matches_oracle(gdn, orc):
+    """Eight chunks in one sequence (0.8B shape, twin) against the oracle."""
+    c = Case(gdn, I.QWEN_08B, [512, 0, 200], seed=91, n_pad=0)
+    out = chunked(c)
+    torch.cuda.synchronize()
+    o_ref, pool = oracle(orc, c, False)
+    check_against_oracle(c, out, o_ref, pool, False)
+    assert gdn.get_device_error() == 0
+
+
+@pytest.mark.parametrize("shape,lens", [(I.QWEN_08B, [512, 97, 0, 64, 1]), (I.QWEN_9B, [300, 33])],
+                         ids=["0.8b", "9b"])
+def test_chunked_close_to_exact_prefill(gdn, shape, lens):
+    """The chunked and the token-serial kernels on the same inputs: states
+    within 5e-5 of each other (relative to each head's largest entry), fp32
+    outputs of the same kernels likewise."""
+    for dtype in ("bf16", "f32"):
+        s = shape.with_(dtype=dtype)
+        c = Case(gdn, s, lens, seed=92)
+        ref = c.prefill().clone()
+        torch.cuda.synchronize()
+        ref_pool = c.pool.tensor.clone()
+        c.reset()
+        out = chunked(c)
+        torch.cuda.synchronize()
+        got, want = c.pool.tensor.cpu().numpy(), ref_pool.cpu().numpy()
+        for sl in c.ws_np[c.rs_np > 0]:
+            for h in range(s.hv):
+                err = state_rel_err(got[sl, h], want[sl, h].astype(np.float64))
+                assert err <= 5e-5, f"{dtype} slot {sl} head {h}: {err:.3g}"
+        if dtype == "f32":
+            o, r = f64(out), f64(ref)
+            scale = np.abs(r).max()
+            assert np.abs(o - r).max() <= 5e-5 * scale
+        else:
+            assert_out_close(f64(out), f64(ref), "bf16")
+    assert gdn.get_device_error() == 0
+
+
+def test_chunked_padding_bad_slots_and_ranges(gdn):
+    """The same sequence-level contract as gdn_prefill, bit for bit."""
+    s = I.QWEN_08B
+    # a bad write slot (equal to the read slot) spoils that sequence only
+    c = Case(gdn, s, [70, 3, 5], seed=93, n_pad=0)
+    start = torch.from_numpy(c.pool_np).cuda()
+    ws = c.ws_np.copy()
+    ws[1] = c.rs_np[1]
+    c.ws = ti(ws)
+    out = chunked(c)
+    torch.cuda.synchronize()
+    assert gdn.get_device_error() == 1
+    assert not out[c.cu_np[1]:c.cu_np[2]].any()
+    assert out[c.cu_np[0]:c.cu_np[1]].any()
+    assert torch.equal(c.pool.tensor[int(c.rs_np[1])], start[int(c.rs_np[1])])
+    # a token range past total_tokens is bad; the other sequences run
+    c.reset()
+    c.ws = ti(c.ws_np)
+    cu = c.cu_np.copy()
+    cu[3] = c.T + 5
+    c.cu = ti(cu)
+    out = chunked(c)
+    torch.cuda.synchronize()
+    assert gdn.get_device_error() == 1
+    assert torch.equal(c.pool.tensor[int(c.ws_np[2])], start[int(c.ws_np[2])])
+    assert not torch.equal(c.pool.tensor[int(c.ws_np[0])], start[int(c.ws_np[0])])
+    # padding rows (read slot 0) write zeros and touch nothing; an empty twin
+    # sequence moves its state unchanged
+    c2 = Case(gdn, s, [0, 2, 66], seed=94, n_pad=1)
+    start2 = torch.from_numpy(c2.pool_np).cuda()
+    out = torch.full((c2.T, s.hv, s.dv), 7.0, dtype=torch.bfloat16, device="cuda")
+    chunked(c2, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(c2.pool.tensor[int(c2.ws_np[0])], start2[int(c2.rs_np[0])])
+    for r in range(len(c2.lens)):
+        if c2.rs_np[r] == 0:
+            assert not out[c2.cu_np[r]:c2.cu_np[r + 1]].any()
+    assert gdn.get_device_error() == 0
+
+
+def test_chunked_in_place_equals_twin(gdn):
+    """In place and twin run the same arithmetic: identical outputs and states."""
+    c = Case(gdn, I.QWEN_08B, [150, 7, 64], seed=95, n_pad=0)
+    out_t = chunked(c).clone()
+    torch.cuda.synchronize()
+    twin = c.pool.tensor.clone()
+    c.reset()
+    out_i = chunked(c, keep_in_place=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out_t, out_i)
+    for r in range(len(c.lens)):
+        assert torch.equal(c.pool.tensor[int(c.rs_np[r])], twin[int(c.ws_np[r])])
+    assert gdn.get_device_error() == 0

@@ -303,3 +303,36 @@ def test_prefill_256_tokens_matches_oracle(gdn, orc):
             err = state_rel_err(got[sl, h], pool[sl, h])
             assert err <= STATE_TOL_CHAIN, f"slot {sl} head {h}: {err:.3g}"
     assert gdn.get_device_error() == 0
+
+
+def test_step_and_prefill_with_pinned_host_activations(gdn):
+    """gdn_decode_step and gdn_prefill read q, k, v, a, b and write their
+    outputs in pinned host memory too, with the values of device buffers."""
+    s = I.QWEN_08B
+    c = Case(gdn, s, [5, 0, 3, 7], seed=78)
+    c.reset()
+    ref = c.prefill(keep_in_place=True).clone()
+    torch.cuda.synchronize()
+    ref_pool = c.pool.tensor.clone()
+    c.reset()
+    h = {k: c.dev[k].cpu().pin_memory() for k in ("q", "k", "v", "a", "b")}
+    hout = torch.empty(ref.shape, dtype=ref.dtype).pin_memory()
+    gdn.gdn_prefill(h["q"], h["k"], h["v"], h["a"], h["b"], c.A_log, c.dt_bias, c.pool, c.cu, c.rs, None,
+                    out=hout, keep_in_place=True)
+    torch.cuda.synchronize()
+    assert torch.equal(hout, ref.cpu()) and torch.equal(c.pool.tensor, ref_pool)
+    # one decode step over the first token of every sequence
+    c.reset()
+    idx, rs = c.step_rows(0)
+    it = torch.from_numpy(idx).cuda()
+    dev_in = [c.dev[k][it].contiguous() for k in ("q", "k", "v", "a", "b")]
+    o_ref = gdn.gdn_decode_step(*dev_in, c.A_log, c.dt_bias, c.pool, ti(rs), None, keep_in_place=True).clone()
+    torch.cuda.synchronize()
+    p_ref = c.pool.tensor.clone()
+    c.reset()
+    host_in = [t_.cpu().pin_memory() for t_ in dev_in]
+    hout = torch.empty(o_ref.shape, dtype=o_ref.dtype).pin_memory()
+    gdn.gdn_decode_step(*host_in, c.A_log, c.dt_bias, c.pool, ti(rs), None, out=hout, keep_in_place=True)
+    torch.cuda.synchronize()
+    assert torch.equal(hout, o_ref.cpu()) and torch.equal(c.pool.tensor, p_ref)
+    assert gdn.get_device_error() == 0
