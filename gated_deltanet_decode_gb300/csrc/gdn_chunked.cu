@@ -84,7 +84,11 @@ struct CS {
     static constexpr int EC = EG + CK * 4;       // fp32 [CK] e^{G_C - G_t}
     static constexpr int BYTES = EC + CK * 4;
 };
-static_assert(CS::BYTES <= 227 * 1024, "shared memory");
+// bf16 activations add a staging area for the next chunk's raw q, k, v
+// (bulk-copied by cp.async while the current chunk computes).
+constexpr int kStageBytes = 3 * CK * CD * 2;
+template <typename TA> constexpr int smem_bytes() { return CS::BYTES + (sizeof(TA) == 2 ? kStageBytes : 0); }
+static_assert(CS::BYTES + kStageBytes <= 227 * 1024, "shared memory");
 static_assert(CS::AF % 16 == 0 && CS::VO % 16 == 0 && (LDV * 4) % 16 == 0, "alignment");
 
 // ---------------------------------------------------------------------------
@@ -166,19 +170,62 @@ __device__ __forceinline__ void acc_to_a(uint32_t (&ah)[4], uint32_t (&al)[4], c
     split2(c1[2], c1[3], ah[3], al[3]);
 }
 
-template <typename T> __device__ __forceinline__ void load4(float (&v)[4], const T *p);
-template <> __device__ __forceinline__ void load4<float>(float (&v)[4], const float *p)
+// A fragment of a row-major fp32 tile (rows m0.., columns k0..), split.
+__device__ __forceinline__ void lda_f32(uint32_t (&ah)[4], uint32_t (&al)[4], const float *X, int ld, int m0, int k0,
+                                        int g, int c)
 {
-    const float4 x = *reinterpret_cast<const float4 *>(p);
-    v[0] = x.x, v[1] = x.y, v[2] = x.z, v[3] = x.w;
+    const float *p = X + (m0 + g) * ld + k0 + 2 * c;
+    split2(p[0], p[1], ah[0], al[0]);
+    split2(p[8 * ld], p[8 * ld + 1], ah[1], al[1]);
+    split2(p[8], p[9], ah[2], al[2]);
+    split2(p[8 * ld + 8], p[8 * ld + 9], ah[3], al[3]);
 }
-template <> __device__ __forceinline__ void load4<bf16>(float (&v)[4], const bf16 *p)
+
+// B fragment with B[k][n] = X[k][n] of a row-major fp32 tile (rows k0..,
+// columns n0..), split.
+__device__ __forceinline__ void ldb_f32(uint32_t &bh0, uint32_t &bh1, uint32_t &bl0, uint32_t &bl1, const float *X,
+                                        int ld, int k0, int n0, int g, int c)
 {
-    const uint2 x = *reinterpret_cast<const uint2 *>(p);
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x.x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x.y));
+    const float *p = X + (k0 + 2 * c) * ld + n0 + g;
+    split2(p[0], p[ld], bh0, bl0);
+    split2(p[8 * ld], p[9 * ld], bh1, bl1);
+}
+
+// Four activations as loaded (one 16- or 8-byte load), then as fp32.
+template <typename T> struct Raw4;
+template <> struct Raw4<float> { float4 v; };
+template <> struct Raw4<bf16> { uint2 v; };
+template <typename T> __device__ __forceinline__ Raw4<T> ldraw(const T *p);
+template <> __device__ __forceinline__ Raw4<float> ldraw<float>(const float *p)
+{
+    return {*reinterpret_cast<const float4 *>(p)};
+}
+template <> __device__ __forceinline__ Raw4<bf16> ldraw<bf16>(const bf16 *p)
+{
+    return {*reinterpret_cast<const uint2 *>(p)};
+}
+template <typename T> __device__ __forceinline__ Raw4<T> raw_zero();
+template <> __device__ __forceinline__ Raw4<float> raw_zero<float>() { return {make_float4(0.f, 0.f, 0.f, 0.f)}; }
+template <> __device__ __forceinline__ Raw4<bf16> raw_zero<bf16>() { return {make_uint2(0u, 0u)}; }
+__device__ __forceinline__ void unpack(float (&v)[4], const Raw4<float> &r)
+{
+    v[0] = r.v.x, v[1] = r.v.y, v[2] = r.v.z, v[3] = r.v.w;
+}
+__device__ __forceinline__ void unpack(float (&v)[4], const Raw4<bf16> &r)
+{
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.v.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.v.y));
     v[0] = a.x, v[1] = a.y, v[2] = b.x, v[3] = b.y;
 }
+
+// 16-byte asynchronous copy global -> shared; src_bytes 0 writes zeros.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes)
+{
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 template <typename T> __device__ __forceinline__ void store2(T *p, float x, float y);
 template <> __device__ __forceinline__ void store2<float>(float *p, float x, float y)
@@ -264,12 +311,100 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
     const TA *const bg = reinterpret_cast<const TA *>(p.b);
     const int L = t1 - t0;
 
+    // bf16: the raw q, k, v of the chunk starting at token cn (zeros past
+    // the sequence), one 16-byte copy at a time, into the staging area
+    constexpr bool kStaged = sizeof(TA) == 2;
+    TA *const RQ = reinterpret_cast<TA *>(smem + CS::BYTES);
+    TA *const RK = RQ + CK * CD;
+    TA *const RV = RK + CK * CD;
+    auto stage = [&](int cn) {
+        const int nn = min(CK, L - cn);
+        for (int e = tid; e < 3 * CK * (CD / 8); e += CTHREADS) {
+            const int which = e / (CK * (CD / 8)), rem = e - which * (CK * (CD / 8));
+            const int tt = rem / (CD / 8), j = rem - tt * (CD / 8);
+            const bool live = tt < nn;
+            const size_t tok = (size_t)(t0 + cn + (live ? tt : 0));
+            const TA *src = which == 0   ? qg + (tok * p.hk + hq) * CD
+                            : which == 1 ? kg + (tok * p.hk + hq) * CD
+                                         : vg + (tok * p.hv + h) * CD;
+            TA *dst = (which == 0 ? RQ : which == 1 ? RK : RV) + tt * CD;
+            cp_async16(dst + 8 * j, src + 8 * j, live ? 16 : 0);
+        }
+        cp_async_commit();
+    };
+    // the gate inputs of the chunk starting at cn: warp 0, tokens lane and lane + 32
+    TA ra[2], rb[2];
+    auto gates_in = [&](int cn) {
+        const int nn = min(CK, L - cn);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int tt = lane + 32 * i;
+            if (tt < nn) {
+                const size_t idx = (size_t)(t0 + cn + tt) * p.hv + h;
+                ra[i] = ag[idx], rb[i] = bg[idx];
+            }
+        }
+    };
+    if (L > 0) {
+        if (kStaged)
+            stage(0);
+        if (warp == 0)
+            gates_in(0);
+    }
+
 #pragma unroll 1
     for (int c0 = 0; c0 < L; c0 += CK) {
         const int n = min(CK, L - c0);
-        __syncthreads(); // every warp is done with the previous chunk's tiles
+        if (kStaged)
+            cp_async_wait_all();
+        __syncthreads(); // every warp is done with the previous chunk's tiles; the staged inputs landed
 
-        // ---- the chunk's gates: log alpha, beta, running sums (warp 0) ----
+        // ---- the chunk's inputs (staged for bf16; else every load in flight
+        // before any is used): q, k, v: 8 tokens a warp (token warp + 8i), 4
+        // channels a lane ----
+        constexpr int TPW = CK / CWARPS;
+        Raw4<TA> rq[TPW], rk[TPW], rv[TPW];
+#pragma unroll
+        for (int i = 0; i < TPW; ++i) {
+            const int tt = warp + CWARPS * i;
+            if (kStaged) {
+                rq[i] = ldraw<TA>(RQ + tt * CD + 4 * lane);
+                rk[i] = ldraw<TA>(RK + tt * CD + 4 * lane);
+                rv[i] = ldraw<TA>(RV + tt * CD + 4 * lane);
+            } else if (tt < n) {
+                const size_t tok = (size_t)(t0 + c0 + tt);
+                rq[i] = ldraw<TA>(qg + (tok * p.hk + hq) * CD + 4 * lane);
+                rk[i] = ldraw<TA>(kg + (tok * p.hk + hq) * CD + 4 * lane);
+                rv[i] = ldraw<TA>(vg + (tok * p.hv + h) * CD + 4 * lane);
+            } else {
+                rq[i] = raw_zero<TA>(), rk[i] = raw_zero<TA>(), rv[i] = raw_zero<TA>();
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < TPW; ++i) {
+            const int tt = warp + CWARPS * i;
+            float qv[4], kv[4], vv[4];
+            unpack(qv, rq[i]), unpack(kv, rk[i]), unpack(vv, rv[i]);
+            float sq = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
+            float sk = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            }
+            const float iq = qscale * rsqrtf(sq + kEps), ik = rsqrtf(sk + kEps);
+            uint32_t h0, l0, h1, l1;
+            split2(qv[0] * iq, qv[1] * iq, h0, l0);
+            split2(qv[2] * iq, qv[3] * iq, h1, l1);
+            *reinterpret_cast<uint2 *>(QH + tt * LDK + 4 * lane) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2 *>(QL + tt * LDK + 4 * lane) = make_uint2(l0, l1);
+            split2(kv[0] * ik, kv[1] * ik, h0, l0);
+            split2(kv[2] * ik, kv[3] * ik, h1, l1);
+            *reinterpret_cast<uint2 *>(KH + tt * LDK + 4 * lane) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2 *>(KL + tt * LDK + 4 * lane) = make_uint2(l0, l1);
+            *reinterpret_cast<float4 *>(VO + tt * LDV + 4 * lane) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+        }
+        // the gates: log alpha, beta, running sums (zero past the chunk's tokens)
         if (warp == 0) {
             float la[2], bt[2];
 #pragma unroll
@@ -277,9 +412,8 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
                 const int tt = lane + 32 * i;
                 la[i] = 0.f, bt[i] = 0.f;
                 if (tt < n) {
-                    const size_t idx = (size_t)(t0 + c0 + tt) * p.hv + h;
-                    la[i] = rate == 0.f ? 0.f : -rate * softplus_f(to_f(ag[idx]) + dtb);
-                    bt[i] = gate_beta(to_f(bg[idx]));
+                    la[i] = rate == 0.f ? 0.f : -rate * softplus_f(to_f(ra[i]) + dtb);
+                    bt[i] = gate_beta(to_f(rb[i]));
                 }
             }
             float s0 = la[0], s1 = la[1];
@@ -297,67 +431,55 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
             EG[lane] = expf(s0), EG[lane + 32] = expf(s1);
             EC[lane] = expf(gc - s0), EC[lane + 32] = expf(gc - s1);
         }
-
-        // ---- q, k (normalised, split) and v: a token a warp, 4 channels a lane ----
-        for (int tt = warp; tt < CK; tt += CWARPS) {
-            float qv[4] = {0.f, 0.f, 0.f, 0.f}, kv[4] = {0.f, 0.f, 0.f, 0.f}, vv[4] = {0.f, 0.f, 0.f, 0.f};
-            if (tt < n) {
-                const size_t tok = (size_t)(t0 + c0 + tt);
-                load4<TA>(qv, qg + (tok * p.hk + hq) * CD + 4 * lane);
-                load4<TA>(kv, kg + (tok * p.hk + hq) * CD + 4 * lane);
-                load4<TA>(vv, vg + (tok * p.hv + h) * CD + 4 * lane);
-            }
-            float sq = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
-            float sk = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
-#pragma unroll
-            for (int o = 16; o; o >>= 1) {
-                sq += __shfl_xor_sync(0xffffffffu, sq, o);
-                sk += __shfl_xor_sync(0xffffffffu, sk, o);
-            }
-            const float iq = qscale / sqrtf(sq + kEps), ik = 1.0f / sqrtf(sk + kEps);
-            uint32_t h0, l0, h1, l1;
-            split2(qv[0] * iq, qv[1] * iq, h0, l0);
-            split2(qv[2] * iq, qv[3] * iq, h1, l1);
-            *reinterpret_cast<uint2 *>(QH + tt * LDK + 4 * lane) = make_uint2(h0, h1);
-            *reinterpret_cast<uint2 *>(QL + tt * LDK + 4 * lane) = make_uint2(l0, l1);
-            split2(kv[0] * ik, kv[1] * ik, h0, l0);
-            split2(kv[2] * ik, kv[3] * ik, h1, l1);
-            *reinterpret_cast<uint2 *>(KH + tt * LDK + 4 * lane) = make_uint2(h0, h1);
-            *reinterpret_cast<uint2 *>(KL + tt * LDK + 4 * lane) = make_uint2(l0, l1);
-            *reinterpret_cast<float4 *>(VO + tt * LDV + 4 * lane) = make_float4(vv[0], vv[1], vv[2], vv[3]);
-        }
         __syncthreads();
+        // the next chunk's inputs travel while this one computes
+        if (c0 + CK < L) {
+            if (kStaged)
+                stage(c0 + CK);
+            if (warp == 0)
+                gates_in(c0 + CK);
+        }
 
-        // ---- K K^T -> A and Q K^T -> P, lower 16x16 blocks only (10 each) ----
-        for (int u = warp; u < 20; u += CWARPS) {
-            const bool isq = u >= 10;
-            const int idx = isq ? u - 10 : u;
-            const int mb = idx >= 6 ? 3 : idx >= 3 ? 2 : idx >= 1 ? 1 : 0;
-            const int nb = idx - mb * (mb + 1) / 2;
-            const bf16 *XH = isq ? QH : KH, *XL = isq ? QL : KL;
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        // ---- K K^T -> A and Q K^T -> P: the 8-column tiles of their lower
+        // 16x16 blocks (10 blocks x 2 tiles x 2 products = 40), 5 a warp,
+        // their accumulation chains interleaved ----
+        {
+            constexpr int NT = 40 / CWARPS;
+            float acc[NT][4];
+            int mrow[NT], ncol[NT];
+            bool isq[NT];
+#pragma unroll
+            for (int i = 0; i < NT; ++i) {
+                const int tau = warp + CWARPS * i;
+                isq[i] = tau >= 20;
+                const int idx = isq[i] ? tau - 20 : tau;
+                const int blk = idx >> 1;
+                const int mb = blk >= 6 ? 3 : blk >= 3 ? 2 : blk >= 1 ? 1 : 0;
+                mrow[i] = 16 * mb;
+                ncol[i] = 16 * (blk - mb * (mb + 1) / 2) + 8 * (idx & 1);
+                acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+            }
 #pragma unroll
             for (int kb = 0; kb < CD / 16; ++kb) {
-                uint32_t ah[4], al[4];
-                lda(ah, XH, LDK, 16 * mb, 16 * kb, g, c);
-                lda(al, XL, LDK, 16 * mb, 16 * kb, g, c);
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    uint32_t bh0, bh1, bl0, bl1;
-                    ldb(bh0, bh1, KH, LDK, 16 * nb + 8 * nt, 16 * kb, g, c);
-                    ldb(bl0, bl1, KL, LDK, 16 * nb + 8 * nt, 16 * kb, g, c);
-                    mma3(acc[nt], ah, al, bh0, bh1, bl0, bl1);
+                for (int i = 0; i < NT; ++i) {
+                    uint32_t ah[4], al[4], bh0, bh1, bl0, bl1;
+                    lda(ah, isq[i] ? QH : KH, LDK, mrow[i], 16 * kb, g, c);
+                    lda(al, isq[i] ? QL : KL, LDK, mrow[i], 16 * kb, g, c);
+                    ldb(bh0, bh1, KH, LDK, ncol[i], 16 * kb, g, c);
+                    ldb(bl0, bl1, KL, LDK, ncol[i], 16 * kb, g, c);
+                    mma3(acc[i], ah, al, bh0, bh1, bl0, bl1);
                 }
             }
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
+            for (int i = 0; i < NT; ++i) {
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
-                    const int t = 16 * mb + g + 8 * hr;
-                    const int s = 16 * nb + 8 * nt + 2 * c;
-                    const float x = acc[nt][2 * hr], y = acc[nt][2 * hr + 1];
+                    const int t = mrow[i] + g + 8 * hr;
+                    const int s = ncol[i] + 2 * c;
+                    const float x = acc[i][2 * hr], y = acc[i][2 * hr + 1];
                     const float gt = GG[t];
-                    if (!isq) {
+                    if (!isq[i]) {
                         const float bt = BE[t];
                         AF[t * LDF + s] = s < t ? bt * expf(gt - GG[s]) * x : 0.f;
                         AF[t * LDF + s + 1] = s + 1 < t ? bt * expf(gt - GG[s + 1]) * y : 0.f;
@@ -393,37 +515,46 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
                 XF[(base + r) * LDF + base + col] = x[r];
         }
         __syncthreads();
-        // blocks below the diagonal, by distance d: T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ,
-        // the sum parked in A's unused block (J, I); one element a thread
-        {
-            const int r = tid >> 4, col = tid & 15;
+        // blocks below the diagonal, by distance d, one warp a block (J = warp):
+        //   X = sum_{K=J}^{I-1} A_IK T_KJ, parked in A's unused block (J, I);
+        //   T_IJ = -T_II X
 #pragma unroll 1
-            for (int d = 1; d < CK / 16; ++d) {
-                for (int J = 0; J + d < CK / 16; ++J) {
-                    const int I = J + d;
-                    float acc = 0.f;
-                    for (int K = J; K < I; ++K) {
-                        const float *arow = AF + (16 * I + r) * LDF + 16 * K;
-                        const float *tcol = XF + (16 * K) * LDF + 16 * J + col;
+        for (int d = 1; d < CK / 16; ++d) {
+            const int J = warp, I = warp + d;
+            if (I < CK / 16) {
+                float x[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                for (int K = J; K < I; ++K) {
+                    uint32_t ah[4], al[4];
+                    lda_f32(ah, al, AF, LDF, 16 * I, 16 * K, g, c);
 #pragma unroll
-                        for (int s = 0; s < 16; ++s)
-                            acc = fmaf(arow[s], tcol[s * LDF], acc);
+                    for (int nt = 0; nt < 2; ++nt) {
+                        uint32_t bh0, bh1, bl0, bl1;
+                        ldb_f32(bh0, bh1, bl0, bl1, XF, LDF, 16 * K, 16 * J + 8 * nt, g, c);
+                        mma3(x[nt], ah, al, bh0, bh1, bl0, bl1);
                     }
-                    AF[(16 * J + r) * LDF + 16 * I + col] = acc;
                 }
-                __syncthreads();
-                for (int J = 0; J + d < CK / 16; ++J) {
-                    const int I = J + d;
-                    const float *trow = XF + (16 * I + r) * LDF + 16 * I;
-                    const float *xcol = AF + (16 * J) * LDF + 16 * I + col;
-                    float acc = 0.f;
 #pragma unroll
-                    for (int s = 0; s < 16; ++s)
-                        acc = fmaf(trow[s], xcol[s * LDF], acc);
-                    XF[(16 * I + r) * LDF + 16 * J + col] = -acc;
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        AF[(16 * J + g + 8 * (e >> 1)) * LDF + 16 * I + 8 * nt + 2 * c + (e & 1)] = x[nt][e];
+                __syncwarp();
+                float tij[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                uint32_t ah[4], al[4];
+                lda_f32(ah, al, XF, LDF, 16 * I, 16 * I, g, c);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    uint32_t bh0, bh1, bl0, bl1;
+                    ldb_f32(bh0, bh1, bl0, bl1, AF, LDF, 16 * J, 16 * I + 8 * nt, g, c);
+                    mma3(tij[nt], ah, al, bh0, bh1, bl0, bl1);
                 }
-                __syncthreads();
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        XF[(16 * I + g + 8 * (e >> 1)) * LDF + 16 * J + 8 * nt + 2 * c + (e & 1)] = -tij[nt][e];
             }
+            __syncthreads();
         }
         // T's lower triangle, split (above it: zero)
         for (int e = tid; e < CK * CK / 2; e += CTHREADS) {
@@ -568,12 +699,12 @@ cudaError_t launch_chunked_t(const PrefillArgs &a, cudaStream_t s)
     cudaGetDevice(&dev);
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CS::BYTES);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<TA>());
         if (e != cudaSuccess)
             return e;
         configured.fetch_or(bit, std::memory_order_release);
     }
-    return launch_pdl(kern, dim3((unsigned)ctas), dim3(CTHREADS), (size_t)CS::BYTES, s, a);
+    return launch_pdl(kern, dim3((unsigned)ctas), dim3(CTHREADS), (size_t)smem_bytes<TA>(), s, a);
 }
 
 } // namespace
