@@ -86,15 +86,21 @@ def bf16_peak():
         return 1900.0, "fallback"
 
 
-def chunked_mma_flops(lens, hv: int) -> float:
+def chunked_mma_flops(lens, hv: int, bf16_inputs: bool = True) -> float:
     """Tensor-core flops gdn_prefill_chunked issues (dk = dv = 128, chunks of
-    64, three bf16 products for each split product): per chunk and head, the
-    20 lower 16x16 blocks of K K^T and Q K^T over dk, then per 16 state rows
-    S K^T and S Q^T (16x64 over dk), E T^T and U^T P^T (16x64 over 64) and
-    the state update (16x128 over 64); one m16n8k16 is 4096 flops."""
-    per_chunk = 20 * 8 * 2 * 3 + 8 * (8 * 8 * 6 + 4 * 8 * 3 * 2 + 4 * 16 * 3)
+    64; one m16n8k16 is 4096 flops).  A product of two split fp32 operands
+    takes three m16n8k16 (hi*hi, hi*lo, lo*hi); with bf16 inputs q and k
+    are exact and unsplit, so a product with them takes two, and K K^T and
+    Q K^T take one.  Per chunk and head: the 40 8-column tiles of the lower
+    blocks of K K^T and Q K^T over dk (8 k-steps); the 6 blocks of T below
+    the diagonal (96); then per 16 state rows S K^T and S Q^T (2 x 8 tiles x
+    8 k-steps), E T^T and U^T P^T (8 tiles x 4 k-steps, three each) and the
+    state update (16 tiles x 4 k-steps)."""
+    x = 2 if bf16_inputs else 3
+    prep = 40 * 8 * (1 if bf16_inputs else 3) + 96
+    scan = 8 * (2 * 8 * 8 * x + 2 * 8 * 4 * 3 + 16 * 4 * x)
     chunks = sum((n + 63) // 64 for n in lens)
-    return float(per_chunk * 4096 * chunks * hv)
+    return float((prep + scan) * 4096 * chunks * hv)
 
 
 def kernel_source_sha() -> str:

@@ -78,17 +78,19 @@ struct CS {
     static constexpr int AF = TL + SQ;           // fp32 A [t][s]; its upper blocks hold scratch
     static constexpr int XF = AF + CK * LDF * 4; // fp32 T [t][s]
     static constexpr int VO = XF + CK * LDF * 4; // fp32 [t][dv]: V in, then each warp's outputs
-    static constexpr int GG = VO + CK * LDV * 4; // fp32 [CK] running log-gate G
-    static constexpr int BE = GG + CK * 4;       // fp32 [CK] beta
-    static constexpr int EG = BE + CK * 4;       // fp32 [CK] e^{G_t}
-    static constexpr int EC = EG + CK * 4;       // fp32 [CK] e^{G_C - G_t}
-    static constexpr int BYTES = EC + CK * 4;
+    // gates, two sets (a chunk's and the next one's), each fp32
+    // [G (running log-gate) | beta | e^{G_t} | e^{G_C - G_t}] x [CK]
+    static constexpr int GATES = VO + CK * LDV * 4;
+    static constexpr int IQ = GATES + 2 * 4 * CK * 4; // fp32 [CK] q's norm scale (1 when q is stored normalised)
+    static constexpr int IK = IQ + CK * 4;       // fp32 [CK] k's norm scale (likewise)
+    static constexpr int BYTES = IK + CK * 4;
 };
 // bf16 activations add a staging area for the next chunk's raw q, k, v
-// (bulk-copied by cp.async while the current chunk computes).
+// (16-byte asynchronous copies while the current chunk computes).
 constexpr int kStageBytes = 3 * CK * CD * 2;
-template <typename TA> constexpr int smem_bytes() { return CS::BYTES + (sizeof(TA) == 2 ? kStageBytes : 0); }
-static_assert(CS::BYTES + kStageBytes <= 227 * 1024, "shared memory");
+constexpr int kStageOffset = (CS::BYTES + 127) & ~127;
+template <typename TA> constexpr int smem_bytes() { return kStageOffset + (sizeof(TA) == 2 ? kStageBytes : 0); }
+static_assert(kStageOffset + kStageBytes <= 227 * 1024, "shared memory");
 static_assert(CS::AF % 16 == 0 && CS::VO % 16 == 0 && (LDV * 4) % 16 == 0, "alignment");
 
 // ---------------------------------------------------------------------------
@@ -254,10 +256,13 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
     float *const AF = reinterpret_cast<float *>(smem + CS::AF);
     float *const XF = reinterpret_cast<float *>(smem + CS::XF);
     float *const VO = reinterpret_cast<float *>(smem + CS::VO);
-    float *const GG = reinterpret_cast<float *>(smem + CS::GG);
-    float *const BE = reinterpret_cast<float *>(smem + CS::BE);
-    float *const EG = reinterpret_cast<float *>(smem + CS::EG);
-    float *const EC = reinterpret_cast<float *>(smem + CS::EC);
+    float *const GATES = reinterpret_cast<float *>(smem + CS::GATES);
+    float *const IQ = reinterpret_cast<float *>(smem + CS::IQ);
+    float *const IK = reinterpret_cast<float *>(smem + CS::IK);
+    // bf16 q and k are exact in bf16: they are stored raw (no tail) and their
+    // norms applied as per-token scales, so products with them need no
+    // split on their side; fp32 q and k are stored normalised and split
+    constexpr bool kExact = sizeof(TA) == 2;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
     const int seq = blockIdx.x / p.hv, h = blockIdx.x - seq * p.hv;
@@ -312,9 +317,9 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
     const int L = t1 - t0;
 
     // bf16: the raw q, k, v of the chunk starting at token cn (zeros past
-    // the sequence), one 16-byte copy at a time, into the staging area
+    // the sequence), 16 bytes a copy, every thread a share, into the staging area
     constexpr bool kStaged = sizeof(TA) == 2;
-    TA *const RQ = reinterpret_cast<TA *>(smem + CS::BYTES);
+    TA *const RQ = reinterpret_cast<TA *>(smem + kStageOffset);
     TA *const RK = RQ + CK * CD;
     TA *const RV = RK + CK * CD;
     auto stage = [&](int cn) {
@@ -332,7 +337,7 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
         }
         cp_async_commit();
     };
-    // the gate inputs of the chunk starting at cn: warp 0, tokens lane and lane + 32
+    // the gate inputs of the chunk starting at cn: warp 2, tokens lane and lane + 32
     TA ra[2], rb[2];
     auto gates_in = [&](int cn) {
         const int nn = min(CK, L - cn);
@@ -345,16 +350,54 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
             }
         }
     };
+    // the gates of the chunk starting at cn from ra, rb (warp 2): log alpha,
+    // beta, running sums (zero past the chunk's tokens), into set `set`
+    auto gates = [&](int cn, int set) {
+        const int nn = min(CK, L - cn);
+        float *const G = GATES + set * 4 * CK;
+        float la[2], bt[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int tt = lane + 32 * i;
+            la[i] = 0.f, bt[i] = 0.f;
+            if (tt < nn) {
+                la[i] = rate == 0.f ? 0.f : -rate * softplus_f(to_f(ra[i]) + dtb);
+                bt[i] = gate_beta(to_f(rb[i]));
+            }
+        }
+        float s0 = la[0], s1 = la[1];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float x0 = __shfl_up_sync(0xffffffffu, s0, o);
+            const float x1 = __shfl_up_sync(0xffffffffu, s1, o);
+            if (lane >= o)
+                s0 += x0, s1 += x1;
+        }
+        s1 += __shfl_sync(0xffffffffu, s0, 31);
+        const float gc = __shfl_sync(0xffffffffu, s1, 31);
+        G[lane] = s0, G[lane + 32] = s1;
+        G[CK + lane] = bt[0], G[CK + lane + 32] = bt[1];
+        G[2 * CK + lane] = expf(s0), G[2 * CK + lane + 32] = expf(s1);
+        G[3 * CK + lane] = expf(gc - s0), G[3 * CK + lane + 32] = expf(gc - s1);
+    };
     if (L > 0) {
         if (kStaged)
             stage(0);
-        if (warp == 0)
+        if (warp == 2) {
             gates_in(0);
+            gates(0, 0);
+        }
     }
 
 #pragma unroll 1
     for (int c0 = 0; c0 < L; c0 += CK) {
         const int n = min(CK, L - c0);
+        const int set = (c0 / CK) & 1;
+        const float *const GG = GATES + set * 4 * CK; // this chunk's gates
+        const float *const BE = GG + CK;
+        const float *const EG = GG + 2 * CK;
+        const float *const EC = GG + 3 * CK;
+        const bool more = c0 + CK < L;
         if (kStaged)
             cp_async_wait_all();
         __syncthreads(); // every warp is done with the previous chunk's tiles; the staged inputs landed
@@ -367,11 +410,11 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
 #pragma unroll
         for (int i = 0; i < TPW; ++i) {
             const int tt = warp + CWARPS * i;
-            if (kStaged) {
+            if (kStaged) { // zeros past the sequence
                 rq[i] = ldraw<TA>(RQ + tt * CD + 4 * lane);
                 rk[i] = ldraw<TA>(RK + tt * CD + 4 * lane);
                 rv[i] = ldraw<TA>(RV + tt * CD + 4 * lane);
-            } else if (tt < n) {
+            } else if (!kStaged && tt < n) {
                 const size_t tok = (size_t)(t0 + c0 + tt);
                 rq[i] = ldraw<TA>(qg + (tok * p.hk + hq) * CD + 4 * lane);
                 rk[i] = ldraw<TA>(kg + (tok * p.hk + hq) * CD + 4 * lane);
@@ -393,52 +436,30 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
                 sk += __shfl_xor_sync(0xffffffffu, sk, o);
             }
             const float iq = qscale * rsqrtf(sq + kEps), ik = rsqrtf(sk + kEps);
-            uint32_t h0, l0, h1, l1;
-            split2(qv[0] * iq, qv[1] * iq, h0, l0);
-            split2(qv[2] * iq, qv[3] * iq, h1, l1);
-            *reinterpret_cast<uint2 *>(QH + tt * LDK + 4 * lane) = make_uint2(h0, h1);
-            *reinterpret_cast<uint2 *>(QL + tt * LDK + 4 * lane) = make_uint2(l0, l1);
-            split2(kv[0] * ik, kv[1] * ik, h0, l0);
-            split2(kv[2] * ik, kv[3] * ik, h1, l1);
-            *reinterpret_cast<uint2 *>(KH + tt * LDK + 4 * lane) = make_uint2(h0, h1);
-            *reinterpret_cast<uint2 *>(KL + tt * LDK + 4 * lane) = make_uint2(l0, l1);
+            if constexpr (kExact) {
+                *reinterpret_cast<uint2 *>(QH + tt * LDK + 4 * lane) = *reinterpret_cast<const uint2 *>(&rq[i]);
+                *reinterpret_cast<uint2 *>(KH + tt * LDK + 4 * lane) = *reinterpret_cast<const uint2 *>(&rk[i]);
+                if (lane == 0)
+                    IQ[tt] = iq, IK[tt] = ik;
+            } else {
+                uint32_t h0, l0, h1, l1;
+                split2(qv[0] * iq, qv[1] * iq, h0, l0);
+                split2(qv[2] * iq, qv[3] * iq, h1, l1);
+                *reinterpret_cast<uint2 *>(QH + tt * LDK + 4 * lane) = make_uint2(h0, h1);
+                *reinterpret_cast<uint2 *>(QL + tt * LDK + 4 * lane) = make_uint2(l0, l1);
+                split2(kv[0] * ik, kv[1] * ik, h0, l0);
+                split2(kv[2] * ik, kv[3] * ik, h1, l1);
+                *reinterpret_cast<uint2 *>(KH + tt * LDK + 4 * lane) = make_uint2(h0, h1);
+                *reinterpret_cast<uint2 *>(KL + tt * LDK + 4 * lane) = make_uint2(l0, l1);
+                if (lane == 0)
+                    IQ[tt] = 1.f, IK[tt] = 1.f;
+            }
             *reinterpret_cast<float4 *>(VO + tt * LDV + 4 * lane) = make_float4(vv[0], vv[1], vv[2], vv[3]);
         }
-        // the gates: log alpha, beta, running sums (zero past the chunk's tokens)
-        if (warp == 0) {
-            float la[2], bt[2];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int tt = lane + 32 * i;
-                la[i] = 0.f, bt[i] = 0.f;
-                if (tt < n) {
-                    la[i] = rate == 0.f ? 0.f : -rate * softplus_f(to_f(ra[i]) + dtb);
-                    bt[i] = gate_beta(to_f(rb[i]));
-                }
-            }
-            float s0 = la[0], s1 = la[1];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float x0 = __shfl_up_sync(0xffffffffu, s0, o);
-                const float x1 = __shfl_up_sync(0xffffffffu, s1, o);
-                if (lane >= o)
-                    s0 += x0, s1 += x1;
-            }
-            s1 += __shfl_sync(0xffffffffu, s0, 31);
-            const float gc = __shfl_sync(0xffffffffu, s1, 31);
-            GG[lane] = s0, GG[lane + 32] = s1;
-            BE[lane] = bt[0], BE[lane + 32] = bt[1];
-            EG[lane] = expf(s0), EG[lane + 32] = expf(s1);
-            EC[lane] = expf(gc - s0), EC[lane + 32] = expf(gc - s1);
-        }
         __syncthreads();
-        // the next chunk's inputs travel while this one computes
-        if (c0 + CK < L) {
-            if (kStaged)
-                stage(c0 + CK);
-            if (warp == 0)
-                gates_in(c0 + CK);
-        }
+        // the next chunk's gate inputs travel while this one computes
+        if (more && warp == 2)
+            gates_in(c0 + CK);
 
         // ---- K K^T -> A and Q K^T -> P: the 8-column tiles of their lower
         // 16x16 blocks (10 blocks x 2 tiles x 2 products = 40), 5 a warp,
@@ -465,10 +486,14 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
                 for (int i = 0; i < NT; ++i) {
                     uint32_t ah[4], al[4], bh0, bh1, bl0, bl1;
                     lda(ah, isq[i] ? QH : KH, LDK, mrow[i], 16 * kb, g, c);
-                    lda(al, isq[i] ? QL : KL, LDK, mrow[i], 16 * kb, g, c);
                     ldb(bh0, bh1, KH, LDK, ncol[i], 16 * kb, g, c);
-                    ldb(bl0, bl1, KL, LDK, ncol[i], 16 * kb, g, c);
-                    mma3(acc[i], ah, al, bh0, bh1, bl0, bl1);
+                    if constexpr (kExact) {
+                        mma16816(acc[i], ah[0], ah[1], ah[2], ah[3], bh0, bh1); // exact products
+                    } else {
+                        lda(al, isq[i] ? QL : KL, LDK, mrow[i], 16 * kb, g, c);
+                        ldb(bl0, bl1, KL, LDK, ncol[i], 16 * kb, g, c);
+                        mma3(acc[i], ah, al, bh0, bh1, bl0, bl1);
+                    }
                 }
             }
 #pragma unroll
@@ -477,7 +502,8 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
                 for (int hr = 0; hr < 2; ++hr) {
                     const int t = mrow[i] + g + 8 * hr;
                     const int s = ncol[i] + 2 * c;
-                    const float x = acc[i][2 * hr], y = acc[i][2 * hr + 1];
+                    const float nt_ = isq[i] ? IQ[t] : IK[t];
+                    const float x = acc[i][2 * hr] * nt_ * IK[s], y = acc[i][2 * hr + 1] * nt_ * IK[s + 1];
                     const float gt = GG[t];
                     if (!isq[i]) {
                         const float bt = BE[t];
@@ -513,6 +539,8 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
 #pragma unroll
             for (int r = 0; r < 16; ++r)
                 XF[(base + r) * LDF + base + col] = x[r];
+        } else if (more && warp == 2) {
+            gates(c0 + CK, set ^ 1); // meanwhile: the next chunk's gates
         }
         __syncthreads();
         // blocks below the diagonal, by distance d, one warp a block (J = warp):
@@ -568,6 +596,10 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
         }
         __syncthreads();
 
+        // the next chunk's q, k, v travel during this chunk's products (a
+        // warp stalled on issuing them leaves the tensor pipe to the other)
+        if (more && kStaged)
+            stage(c0 + CK);
         // ---- this warp's rows: Z = S K^T and Y = S Q^T (16 x 64 each) ----
         float z[8][4], y[8][4], u[8][4];
 #pragma unroll
@@ -583,11 +615,21 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
             for (int nt = 0; nt < 8; ++nt) {
                 uint32_t bh0, bh1, bl0, bl1;
                 ldb(bh0, bh1, KH, LDK, 8 * nt, 16 * kb, g, c);
-                ldb(bl0, bl1, KL, LDK, 8 * nt, 16 * kb, g, c);
-                mma3(z[nt], ah, al, bh0, bh1, bl0, bl1);
+                if constexpr (kExact) {
+                    mma16816(z[nt], al[0], al[1], al[2], al[3], bh0, bh1);
+                    mma16816(z[nt], ah[0], ah[1], ah[2], ah[3], bh0, bh1);
+                } else {
+                    ldb(bl0, bl1, KL, LDK, 8 * nt, 16 * kb, g, c);
+                    mma3(z[nt], ah, al, bh0, bh1, bl0, bl1);
+                }
                 ldb(bh0, bh1, QH, LDK, 8 * nt, 16 * kb, g, c);
-                ldb(bl0, bl1, QL, LDK, 8 * nt, 16 * kb, g, c);
-                mma3(y[nt], ah, al, bh0, bh1, bl0, bl1);
+                if constexpr (kExact) {
+                    mma16816(y[nt], al[0], al[1], al[2], al[3], bh0, bh1);
+                    mma16816(y[nt], ah[0], ah[1], ah[2], ah[3], bh0, bh1);
+                } else {
+                    ldb(bl0, bl1, QL, LDK, 8 * nt, 16 * kb, g, c);
+                    mma3(y[nt], ah, al, bh0, bh1, bl0, bl1);
+                }
             }
         }
         // E = (V^T - Z diag(e^G)) diag(beta), in place of Z
@@ -597,7 +639,7 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int t = 8 * nt + 2 * c + (e & 1), r = rA + 8 * (e >> 1);
-                z[nt][e] = BE[t] * (VO[t * LDV + r] - EG[t] * z[nt][e]);
+                z[nt][e] = BE[t] * (VO[t * LDV + r] - EG[t] * IK[t] * z[nt][e]);
             }
         // U^T = E T^T
 #pragma unroll
@@ -616,7 +658,7 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
             const int t = 8 * nt + 2 * c;
-            const float e0 = EG[t], e1 = EG[t + 1];
+            const float e0 = EG[t] * IQ[t], e1 = EG[t + 1] * IQ[t + 1];
             y[nt][0] *= e0, y[nt][1] *= e1, y[nt][2] *= e0, y[nt][3] *= e1;
         }
 #pragma unroll
@@ -649,7 +691,7 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
             const int t = 8 * nt + 2 * c;
-            const float e0 = EC[t], e1 = EC[t + 1];
+            const float e0 = EC[t] * IK[t], e1 = EC[t + 1] * IK[t + 1];
             u[nt][0] *= e0, u[nt][1] *= e1, u[nt][2] *= e0, u[nt][3] *= e1;
         }
 #pragma unroll
@@ -660,9 +702,16 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
             for (int np = 0; np < CD / 16; ++np) {
                 uint32_t bh[4], bl[4];
                 ldb_trans2(bh, KH, LDK, 16 * kb, 16 * np, lane);
-                ldb_trans2(bl, KL, LDK, 16 * kb, 16 * np, lane);
-                mma3(sacc[2 * np], ah, al, bh[0], bh[1], bl[0], bl[1]);
-                mma3(sacc[2 * np + 1], ah, al, bh[2], bh[3], bl[2], bl[3]);
+                if constexpr (kExact) {
+                    mma16816(sacc[2 * np], al[0], al[1], al[2], al[3], bh[0], bh[1]);
+                    mma16816(sacc[2 * np], ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
+                    mma16816(sacc[2 * np + 1], al[0], al[1], al[2], al[3], bh[2], bh[3]);
+                    mma16816(sacc[2 * np + 1], ah[0], ah[1], ah[2], ah[3], bh[2], bh[3]);
+                } else {
+                    ldb_trans2(bl, KL, LDK, 16 * kb, 16 * np, lane);
+                    mma3(sacc[2 * np], ah, al, bh[0], bh[1], bl[0], bl[1]);
+                    mma3(sacc[2 * np + 1], ah, al, bh[2], bh[3], bl[2], bl[3]);
+                }
             }
         }
         __syncwarp();
