@@ -277,12 +277,20 @@ def run_extras(G, I, device, n=400):
         nb = layer_bytes(sh, real)
         tw = time_calls([st["layer"] for st in sets], n, device)
         ip = time_calls([st["layer_ip"] for st in sets], n, device)
+        # chained and warm: one instance, each step reading what the one before
+        # wrote (twin with the commit in the launch, or in place), so whatever
+        # of the state L2 still holds is reused
+        tw_w = time_calls([sets[0]["layer_commit"]], n, device)
+        ip_w = time_calls([sets[0]["layer_ip"]], n, device)
         sweep[str(rows)] = {"real_rows": real, "twin_us": round(tw, 2), "in_place_us": round(ip, 2),
-                            "twin_GBs": round(nb / tw / 1e3, 1), "in_place_GBs": round(nb / ip / 1e3, 1)}
+                            "twin_GBs": round(nb / tw / 1e3, 1), "in_place_GBs": round(nb / ip / 1e3, 1),
+                            "twin_chained_warm_us": round(tw_w, 2), "in_place_chained_warm_us": round(ip_w, 2)}
         del sets
         torch.cuda.empty_cache()
     res["sweep_rows_write_mode"] = {"workload": "0.8B-shaped fused layer, 25% padding rows on the null "
-                                                "slot, 513-slot pools, twin vs in place", "rows": sweep}
+                                                "slot, 513-slot pools, twin vs in place; cold = four "
+                                                "instances in rotation, chained warm = one instance "
+                                                "stepping on its own output", "rows": sweep}
     gqa = {}
     for rows in (64, 256):
         sh = I.QWEN_9B.with_(rows=rows, num_slots=2 * rows + 1)

@@ -17,8 +17,31 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kVec = 8; // channels per thread
 
+// Eight activations as loaded (for rows kept in registers before use).
+template <typename T> struct Raw8;
+template <> struct Raw8<float> { float4 a, b; };
+template <> struct Raw8<__nv_bfloat16> { uint4 u; };
+
 template <typename T> struct Vec8;
 template <> struct Vec8<float> {
+    static __device__ __forceinline__ Raw8<float> ldraw(const float *p)
+    {
+        return {*reinterpret_cast<const float4 *>(p), *reinterpret_cast<const float4 *>(p + 4)};
+    }
+    static __device__ __forceinline__ Raw8<float> zero()
+    {
+        return {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    }
+    static __device__ __forceinline__ void unpack(const Raw8<float> &r, float (&v)[8])
+    {
+        v[0] = r.a.x; v[1] = r.a.y; v[2] = r.a.z; v[3] = r.a.w;
+        v[4] = r.b.x; v[5] = r.b.y; v[6] = r.b.z; v[7] = r.b.w;
+    }
+    static __device__ __forceinline__ void straw(float *p, const Raw8<float> &r)
+    {
+        *reinterpret_cast<float4 *>(p) = r.a;
+        *reinterpret_cast<float4 *>(p + 4) = r.b;
+    }
     static __device__ __forceinline__ void load(const float *p, float (&v)[8])
     {
         const float4 a = *reinterpret_cast<const float4 *>(p);
@@ -33,6 +56,25 @@ template <> struct Vec8<float> {
     }
 };
 template <> struct Vec8<__nv_bfloat16> {
+    static __device__ __forceinline__ Raw8<__nv_bfloat16> ldraw(const __nv_bfloat16 *p)
+    {
+        return {*reinterpret_cast<const uint4 *>(p)};
+    }
+    static __device__ __forceinline__ Raw8<__nv_bfloat16> zero() { return {make_uint4(0u, 0u, 0u, 0u)}; }
+    static __device__ __forceinline__ void unpack(const Raw8<__nv_bfloat16> &r, float (&v)[8])
+    {
+        const uint32_t w[4] = {r.u.x, r.u.y, r.u.z, r.u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    }
+    static __device__ __forceinline__ void straw(__nv_bfloat16 *p, const Raw8<__nv_bfloat16> &r)
+    {
+        *reinterpret_cast<uint4 *>(p) = r.u;
+    }
     static __device__ __forceinline__ void load(const __nv_bfloat16 *p, float (&v)[8])
     {
         const uint4 u = *reinterpret_cast<const uint4 *>(p);
@@ -127,8 +169,9 @@ __global__ void __launch_bounds__(kThreads) conv_decode_kernel(const ConvArgs p,
 // prefill keeps the state in place).  A token's output depends only on it and
 // the W-1 inputs before it, so the tokens run in parallel: a token thread
 // (one per run of kRun tokens and 8 channels) takes the run's tokens that
-// are at least W-1 into their sequence, sliding their window through
-// registers, and reads only the packed inputs; a window thread (one per
+// are at least W-1 into their sequence; it loads every input row they need
+// (the run's and the W-1 before it) at once, so many loads are in flight,
+// and reads only the packed inputs; a window thread (one per
 // sequence and 8 channels) takes the first W-1 tokens, which read the stored
 // window, and then writes the new window -- reads before writes in one
 // thread, so in place is safe.  Each output equals one causal_conv1d_decode
@@ -151,7 +194,7 @@ __device__ __forceinline__ void conv8(const float (&win)[W - 1][8], const float 
     }
 }
 
-constexpr int kRun = 8; // tokens a token thread walks
+constexpr int kRun = 4; // tokens a token thread walks
 
 // The sequence holding token `tok`: the last r with cu_seqlens[r] <= tok.
 __device__ __forceinline__ int seq_of(const int32_t *cu, int nseq, long long tok)
@@ -212,9 +255,21 @@ __global__ void __launch_bounds__(kThreads) conv_prefill_kernel(const ConvPrefil
         const long long last = first + kRun < p.total_tokens ? first + kRun : p.total_tokens;
         out = reinterpret_cast<T *>(p.out) + c0;
         load_taps<T, W>(p, c0, taps, bias);
+        // every input row the run needs (its tokens and the W-1 before them),
+        // all loads in flight before any is used; rows outside [0, T) read as zeros
+        constexpr int NR = kRun + W - 1;
+        Raw8<T> raw[NR];
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+            const long long tok = first - (W - 1) + i;
+            raw[i] = tok >= 0 && tok < p.total_tokens ? Vec8<T>::ldraw(xs + (size_t)tok * C + c0) : Vec8<T>::zero();
+        }
         int r = -1, t0 = 0, t1 = 0, cls = 0;
-        long long have = -1; // the window holds the W-1 inputs before token `have`
-        for (long long tok = first; tok < last; ++tok) {
+#pragma unroll
+        for (int i = 0; i < kRun; ++i) {
+            const long long tok = first + i;
+            if (tok >= last)
+                break;
             if (r < 0 || tok >= t1) {
                 r = seq_of(p.cu_seqlens, p.nseq, tok);
                 t0 = p.cu_seqlens[r];
@@ -222,7 +277,6 @@ __global__ void __launch_bounds__(kThreads) conv_prefill_kernel(const ConvPrefil
                 const int rs = p.read_slot[r];
                 const int ws = in_place ? rs : p.write_slot[r];
                 cls = classify_seq(rs, ws, in_place, p.token_slot, t0, t1, p.total_tokens, p.num_slots);
-                have = -1;
             }
             if (tok < t0 || tok >= t1 || tok - t0 < W - 1)
                 continue; // not in this sequence's range, or a window thread's token
@@ -231,28 +285,19 @@ __global__ void __launch_bounds__(kThreads) conv_prefill_kernel(const ConvPrefil
                 Vec8<T>::store(out + (size_t)tok * C, z);
                 continue;
             }
-            if (have != tok) {
+            // the W-1 inputs before tok are rows i..i+W-2 (all in this sequence)
 #pragma unroll
-                for (int j = 0; j < W - 1; ++j)
-                    Vec8<T>::load(xs + (size_t)(tok - (W - 1) + j) * C + c0, win[j]);
-            }
-            Vec8<T>::load(xs + (size_t)tok * C + c0, x);
+            for (int j = 0; j < W - 1; ++j)
+                Vec8<T>::unpack(raw[i + j], win[j]);
+            Vec8<T>::unpack(raw[i + W - 1], x);
             conv8<T, W>(win, x, taps, bias, silu, y);
             Vec8<T>::store(out + (size_t)tok * C, y);
-#pragma unroll
-            for (int j = 0; j + 1 < W - 1; ++j)
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    win[j][c] = win[j + 1][c];
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                win[W - 2][c] = x[c];
-            have = tok + 1;
             if (p.token_slot) {
+                // the window after tok: rows i+1..i+W-1, as they were read
                 const int ts = p.token_slot[tok];
 #pragma unroll
                 for (int j = 0; j < W - 1; ++j)
-                    Vec8<T>::store(conv + ((size_t)ts * (W - 1) + j) * C + c0, win[j]);
+                    Vec8<T>::straw(conv + ((size_t)ts * (W - 1) + j) * C + c0, raw[i + 1 + j]);
             }
         }
         return;
