@@ -15,8 +15,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libgdn_decode.so")
-SOURCES = ["gdn_api.cu", "gdn_stream.cu", "gdn_conv.cu", "gdn_prefill.cu", "gdn_chunked.cu"]
+SOURCES = ["gdn_api.cu", "gdn_stream.cu", "gdn_conv.cu", "gdn_prefill.cu", "gdn_chunked.cu", "gdn_chunked_tc.cu"]
 HEADERS = [os.path.join(CSRC, "gdn_device.cuh"), os.path.join(CSRC, "gdn_ptx.cuh"),
+           os.path.join(CSRC, "gdn_chunk_common.cuh"),
            os.path.join(CSRC, "gdn_internal.h"),
            os.path.join(ROOT, "include", "gdn_decode.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

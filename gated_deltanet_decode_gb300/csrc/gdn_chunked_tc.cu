@@ -1,0 +1,668 @@
+// The chunked gated delta rule with the state in tensor memory: the
+// tcgen05 form of gdn_prefill_chunked for bf16 activations.
+//
+// The operation, the regrouping over chunks of 64 tokens and the split
+// products are those of gdn_chunked.cu (whose header states the algebra):
+// per chunk A, P and T = (I + A)^{-1}, then with S_0 the state before it
+//     Z|Y = S_0 [K|Q]^T,  E = (V^T - Z diag(e^G ik)) diag(beta),  U = E T^T,
+//     O   = Y diag(e^G iq) + U P^T,  S_C = e^{G_C} S_0 + U diag(e^{G_C-G} ik) K
+// (ik, iq: the per-token norm scales of the raw bf16 k and q, which are exact
+// operands).  Here the four products that carry the state's 128 rows run as
+// M = 128 tcgen05.mma with the accumulators in tensor memory:
+//   * the state S lives in TMEM for the whole sequence (fp32, 128 columns);
+//   * its bf16 head and tail, the A operand of Z|Y, are written back into
+//     TMEM from S at the start of each chunk; E, U and U diag(e^{G_C-G} ik)
+//     likewise (tcgen05.mma reads A from TMEM);
+//   * B operands (raw K|Q, raw K transposed, T and P heads and tails) sit in
+//     shared memory in the canonical no-swizzle K-major layout: 8-row x
+//     16-byte core matrices, adjacent along K at 128 bytes (the descriptor's
+//     leading offset), 8-row groups at K/8 x 128 bytes (its stride offset);
+//   * one thread issues the products and commits each group to an mbarrier;
+//     the CTA's threads read and write TMEM one state row a thread (two warps
+//     on each 32-lane quarter, each taking half of the columns).
+// Z|Y is issued as soon as the chunk's K and Q are in shared memory and runs
+// on the tensor cores while all warps form A, P and T (mma.sync tiles and the
+// fp32 blocked inverse shared with gdn_chunked.cu).
+//
+// Tensor memory (512 columns, one CTA an SM): S 0-127; Z 128-191, later the
+// head|tail of U diag(e^{G_C-G} ik) (128-159 | 160-191); Y, then O, 192-255;
+// U 256-319; the head|tail of S 320-383 | 384-447, later those of E
+// (320-351 | 352-383) and of U (384-415 | 416-447).  Every region is reused
+// only after the mbarrier of the products that read it has completed.
+#include <atomic>
+
+#include "gdn_chunk_common.cuh"
+#include "gdn_device.cuh"
+#include "gdn_internal.h"
+#include "gdn_ptx.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int TC_WARPS = 8;
+constexpr int TC_THREADS = TC_WARPS * 32;
+constexpr uint32_t kTmemCols = 512;
+
+// TMEM columns
+constexpr uint32_t C_S = 0, C_Z = 128, C_Y = 192, C_U = 256, C_SH = 320, C_SL = 384;
+constexpr uint32_t C_EH = 320, C_EL = 352, C_UH = 384, C_UL = 416, C_WH = 128, C_WL = 160;
+
+// Byte offset of element (row, k) in a canonical K-major tile with K columns.
+template <int K> __device__ __forceinline__ int cm_off(int row, int k)
+{
+    return ((((row >> 3) * (K / 8)) + (k >> 3)) << 7) + ((row & 7) << 4) + ((k & 7) << 1);
+}
+
+// Shared-memory layout, byte offsets.
+struct TS {
+    static constexpr int KQ = 0;                  // bf16 [128][128]: raw K rows 0-63, raw Q rows 64-127
+    static constexpr int KT = KQ + 128 * CD * 2;  // bf16 [128 = dk][64 = tokens]: raw K transposed
+    static constexpr int PH = KT + CD * CK * 2;   // bf16 [64][64] P head / tail, T head / tail
+    static constexpr int PL = PH + CK * CK * 2;
+    static constexpr int TH = PL + CK * CK * 2;
+    static constexpr int TL = TH + CK * CK * 2;
+    static constexpr int AF = TL + CK * CK * 2;   // fp32 A [t][s] (upper blocks: scratch)
+    static constexpr int XF = AF + CK * LDF * 4;  // fp32 T [t][s]
+    static constexpr int GATES = XF + CK * LDF * 4; // two sets of [G | beta | e^G | e^{G_C-G}] x CK
+    static constexpr int IQ = GATES + 2 * 4 * CK * 4;
+    static constexpr int IK = IQ + CK * 4;
+    static constexpr int BARS = IK + CK * 4;      // mbarriers: Z|Y, U, O and S
+    static constexpr int TADDR = BARS + 32;       // the TMEM base address
+    static constexpr int BYTES = TADDR + 16;
+    static constexpr int STAGE = (BYTES + 127) & ~127; // raw q, k, v of the next chunk, [CK][CD] each
+    static constexpr int TOTAL = STAGE + 3 * CK * CD * 2;
+};
+static_assert(TS::TOTAL <= 227 * 1024, "shared memory");
+static_assert(TS::BARS % 8 == 0 && TS::KT % 1024 == 0 && TS::PH % 128 == 0, "alignment");
+
+// ---- tcgen05 wrappers ----
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo)
+{
+    // start >> 4 | leading offset (K-adjacent core matrices: 128 B) >> 4 | stride offset >> 4 | version 1
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46);
+}
+// D fp32, A and B bf16, both K-major, M = 128, N = n
+__host__ __device__ constexpr uint32_t idesc_bf16(int n)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, bool acc)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+                 "r"(a_tmem), "l"(b), "r"(idesc), "r"((uint32_t)acc)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// shared-memory writes made visible to the tensor cores' reads
+__device__ __forceinline__ void smem_to_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 32 consecutive columns of this thread's lane
+__device__ __forceinline__ void tld32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                   "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+                   "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+                   "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tst32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+                 "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+                 "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+                 "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+                 : "memory");
+}
+__device__ __forceinline__ void tst16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+                 "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+                 : "memory");
+}
+__device__ __forceinline__ void tst_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 32 fp32 values -> their bf16 head and tail as 16 + 16 packed pairs
+__device__ __forceinline__ void split32(const float (&v)[32], uint32_t (&hi)[16], uint32_t (&lo)[16])
+{
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        split2(v[2 * j], v[2 * j + 1], hi[j], lo[j]);
+}
+
+// A fragment (mma.sync) of rows m0.., columns k0.. of a canonical tile with K columns
+template <int K>
+__device__ __forceinline__ void lda_cm(uint32_t (&a)[4], const unsigned char *X, int m0, int k0, int g, int c)
+{
+    a[0] = *reinterpret_cast<const uint32_t *>(X + cm_off<K>(m0 + g, k0 + 2 * c));
+    a[1] = *reinterpret_cast<const uint32_t *>(X + cm_off<K>(m0 + g + 8, k0 + 2 * c));
+    a[2] = *reinterpret_cast<const uint32_t *>(X + cm_off<K>(m0 + g, k0 + 2 * c + 8));
+    a[3] = *reinterpret_cast<const uint32_t *>(X + cm_off<K>(m0 + g + 8, k0 + 2 * c + 8));
+}
+// B fragment with B[k][n] = X[n][k] of a canonical tile with K columns
+template <int K>
+__device__ __forceinline__ void ldb_cm(uint32_t &b0, uint32_t &b1, const unsigned char *X, int n0, int k0, int g,
+                                       int c)
+{
+    b0 = *reinterpret_cast<const uint32_t *>(X + cm_off<K>(n0 + g, k0 + 2 * c));
+    b1 = *reinterpret_cast<const uint32_t *>(X + cm_off<K>(n0 + g, k0 + 2 * c + 8));
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const PrefillArgs p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *const KQ = smem + TS::KQ;
+    unsigned char *const KT = smem + TS::KT;
+    unsigned char *const PH = smem + TS::PH;
+    unsigned char *const PL = smem + TS::PL;
+    unsigned char *const TH = smem + TS::TH;
+    unsigned char *const TL = smem + TS::TL;
+    float *const AF = reinterpret_cast<float *>(smem + TS::AF);
+    float *const XF = reinterpret_cast<float *>(smem + TS::XF);
+    float *const GATES = reinterpret_cast<float *>(smem + TS::GATES);
+    float *const IQ = reinterpret_cast<float *>(smem + TS::IQ);
+    float *const IK = reinterpret_cast<float *>(smem + TS::IK);
+    uint64_t *const bars = reinterpret_cast<uint64_t *>(smem + TS::BARS);
+    uint32_t *const taddr_slot = reinterpret_cast<uint32_t *>(smem + TS::TADDR);
+    bf16 *const RQ = reinterpret_cast<bf16 *>(smem + TS::STAGE);
+    bf16 *const RK = RQ + CK * CD;
+    bf16 *const RV = RK + CK * CD;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = 32 * quarter + lane; // this thread's state row (its TMEM lane)
+    const int seq = blockIdx.x / p.hv, h = blockIdx.x - seq * p.hv;
+    const int hq = h / (p.hv / p.hk);
+    wait_prior_grid();
+
+    const int t0 = p.cu_seqlens[seq], t1 = p.cu_seqlens[seq + 1];
+    const bool range_ok = t0 >= 0 && t1 >= t0 && t1 <= p.total_tokens;
+    const int rs = p.read_slot[seq];
+    const bool in_place = p.write_slot == nullptr;
+    const int ws = in_place ? rs : p.write_slot[seq];
+    const int cls = range_ok ? classify_row(rs, ws, p.num_slots, in_place) : -1;
+    bf16 *const out = reinterpret_cast<bf16 *>(p.out);
+    const size_t out_tok = (size_t)p.hv * CD;
+    if (cls != 1) {
+        // padding or bad: zero outputs (when the token range is sane), no slot touched
+        if (cls < 0 && h == 0 && tid == 0)
+            report(p.err, GDN_DEVERR_BAD_SLOT);
+        if (range_ok) {
+            const long long n_out = (long long)(t1 - t0) * CD;
+            for (long long e = tid; e < n_out; e += TC_THREADS)
+                out[(size_t)(t0 + e / CD) * out_tok + (size_t)h * CD + (size_t)(e % CD)] = from_f<bf16>(0.f);
+        }
+        return;
+    }
+
+    // tensor memory (all 512 columns) and the products' mbarriers
+    const uint32_t bar_zy = sm_addr(&bars[0]), bar_u = sm_addr(&bars[1]), bar_o = sm_addr(&bars[2]);
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sm_addr(taddr_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (tid == 32) {
+        mbar_init(bar_zy, 1);
+        mbar_init(bar_u, 1);
+        mbar_init(bar_o, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // P's blocks above the diagonal are never computed: zero both halves once
+    for (int e = tid; e < 2 * CK * CK * 2 / 16; e += TC_THREADS)
+        reinterpret_cast<uint4 *>(PH)[e] = make_uint4(0u, 0u, 0u, 0u);
+    tc_before_sync();
+    __syncthreads();
+    tc_after_sync();
+    const uint32_t tbase = *taddr_slot;
+    const uint32_t tlane = tbase + ((uint32_t)(32 * quarter) << 16); // this warp's 32 lanes
+
+    // the state in: row `row`, columns 64*half .. 64*half + 63
+    const size_t slot_floats = (size_t)p.hv * CD * CD;
+    const size_t head_off = (size_t)h * CD * CD;
+    {
+        const float *S0 = p.pool + (size_t)rs * slot_floats + head_off + (size_t)row * CD + 64 * half;
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+            uint32_t r[32];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 v = *reinterpret_cast<const float4 *>(S0 + 32 * q2 + 4 * i);
+                r[4 * i] = __float_as_uint(v.x), r[4 * i + 1] = __float_as_uint(v.y);
+                r[4 * i + 2] = __float_as_uint(v.z), r[4 * i + 3] = __float_as_uint(v.w);
+            }
+            tst32(tlane + C_S + 64 * half + 32 * q2, r);
+        }
+        tst_wait();
+    }
+
+    const float rate = expf(p.A_log[h]);
+    const float dtb = p.dt_bias[h];
+    const float qscale = 1.0f / sqrtf((float)CD);
+    const bf16 *const qg = reinterpret_cast<const bf16 *>(p.q);
+    const bf16 *const kg = reinterpret_cast<const bf16 *>(p.k);
+    const bf16 *const vg = reinterpret_cast<const bf16 *>(p.v);
+    const bf16 *const ag = reinterpret_cast<const bf16 *>(p.a);
+    const bf16 *const bg = reinterpret_cast<const bf16 *>(p.b);
+    const int L = t1 - t0;
+
+    // the raw q, k, v of the chunk starting at token cn (zeros past the
+    // sequence), 16 bytes a copy, every thread a share, into the staging area
+    auto stage = [&](int cn) {
+        const int nn = min(CK, L - cn);
+        for (int e = tid; e < 3 * CK * (CD / 8); e += TC_THREADS) {
+            const int which = e / (CK * (CD / 8)), rem = e - which * (CK * (CD / 8));
+            const int tt = rem / (CD / 8), j = rem - tt * (CD / 8);
+            const bool live = tt < nn;
+            const size_t tok = (size_t)(t0 + cn + (live ? tt : 0));
+            const bf16 *src = which == 0   ? qg + (tok * p.hk + hq) * CD
+                              : which == 1 ? kg + (tok * p.hk + hq) * CD
+                                           : vg + (tok * p.hv + h) * CD;
+            bf16 *dst = (which == 0 ? RQ : which == 1 ? RK : RV) + tt * CD;
+            cp_async16(dst + 8 * j, src + 8 * j, live ? 16 : 0);
+        }
+        cp_async_commit();
+    };
+    // the gate inputs of the chunk starting at cn (warp 2, tokens lane and lane + 32)
+    bf16 ra[2], rb[2];
+    auto gates_in = [&](int cn) {
+        const int nn = min(CK, L - cn);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int tt = lane + 32 * i;
+            if (tt < nn) {
+                const size_t idx = (size_t)(t0 + cn + tt) * p.hv + h;
+                ra[i] = ag[idx], rb[i] = bg[idx];
+            }
+        }
+    };
+    // its gates: log alpha, beta, running sums (zero past the chunk's tokens), into gate set `set`
+    auto gates = [&](int cn, int set) {
+        const int nn = min(CK, L - cn);
+        float *const G = GATES + set * 4 * CK;
+        float la[2], bt[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int tt = lane + 32 * i;
+            la[i] = 0.f, bt[i] = 0.f;
+            if (tt < nn) {
+                la[i] = rate == 0.f ? 0.f : -rate * softplus_f(to_f(ra[i]) + dtb);
+                bt[i] = gate_beta(to_f(rb[i]));
+            }
+        }
+        float s0 = la[0], s1 = la[1];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float x0 = __shfl_up_sync(0xffffffffu, s0, o);
+            const float x1 = __shfl_up_sync(0xffffffffu, s1, o);
+            if (lane >= o)
+                s0 += x0, s1 += x1;
+        }
+        s1 += __shfl_sync(0xffffffffu, s0, 31);
+        const float gc = __shfl_sync(0xffffffffu, s1, 31);
+        G[lane] = s0, G[lane + 32] = s1;
+        G[CK + lane] = bt[0], G[CK + lane + 32] = bt[1];
+        G[2 * CK + lane] = expf(s0), G[2 * CK + lane + 32] = expf(s1);
+        G[3 * CK + lane] = expf(gc - s0), G[3 * CK + lane + 32] = expf(gc - s1);
+    };
+    // this thread's outputs of the chunk starting at cbase (nn tokens): row
+    // `row` of O, tokens 32*half .. 32*half + 31
+    auto write_outputs = [&](int cbase, int nn) {
+        float o[32];
+        tld32(tlane + C_Y + 32 * half, o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int t = 32 * half + i;
+            if (t < nn)
+                out[(size_t)(t0 + cbase + t) * out_tok + (size_t)h * CD + row] = from_f<bf16>(o[i]);
+        }
+    };
+    if (L > 0) {
+        stage(0);
+        if (warp == 2) {
+            gates_in(0);
+            gates(0, 0);
+        }
+    }
+
+    bool abort = false;
+    int n_prev = 0;
+#pragma unroll 1
+    for (int c0 = 0; c0 < L; c0 += CK) {
+        const int ci = c0 / CK;
+        const int n = min(CK, L - c0);
+        const int set = ci & 1;
+        const float *const GG = GATES + set * 4 * CK; // this chunk's gates
+        const float *const BE = GG + CK;
+        const float *const EG = GG + 2 * CK;
+        const float *const EC = GG + 3 * CK;
+        const bool more = c0 + CK < L;
+
+        // ---- (0) the previous chunk's products are done; its outputs, S's
+        // head and tail, this chunk's K | Q, K^T and norms ----
+        cp_async_wait_all();
+        bool late = ci > 0 && !mbar_wait(bar_o, (uint32_t)((ci - 1) & 1));
+        if (late)
+            report(p.err, GDN_DEVERR_TIMEOUT);
+        if (__syncthreads_or(late)) {
+            abort = true;
+            break;
+        }
+        tc_after_sync();
+        if (ci > 0)
+            write_outputs(c0 - CK, n_prev);
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+            float sv[32];
+            uint32_t hi[16], lo[16];
+            tld32(tlane + C_S + 64 * half + 32 * q2, sv);
+            split32(sv, hi, lo);
+            tst16(tlane + C_SH + 32 * half + 16 * q2, hi);
+            tst16(tlane + C_SL + 32 * half + 16 * q2, lo);
+        }
+        tst_wait();
+#pragma unroll
+        for (int i = 0; i < CK / TC_WARPS; ++i) {
+            const int tt = warp + TC_WARPS * i;
+            const uint2 qraw = *reinterpret_cast<const uint2 *>(RQ + tt * CD + 4 * lane);
+            const uint2 kraw = *reinterpret_cast<const uint2 *>(RK + tt * CD + 4 * lane);
+            float qv[4], kv[4];
+            unpack(qv, Raw4<bf16>{qraw}), unpack(kv, Raw4<bf16>{kraw});
+            float sq = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
+            float sk = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            }
+            *reinterpret_cast<uint2 *>(KQ + cm_off<CD>(tt, 4 * lane)) = kraw;
+            *reinterpret_cast<uint2 *>(KQ + cm_off<CD>(CK + tt, 4 * lane)) = qraw;
+            if (lane == 0)
+                IQ[tt] = qscale * rsqrtf(sq + kEps), IK[tt] = rsqrtf(sk + kEps);
+        }
+        {
+            // K^T, one 16-byte core-matrix row (dk j, tokens s0..s0+7) at a time
+            const unsigned short *rk = reinterpret_cast<const unsigned short *>(RK);
+            for (int e = tid; e < CD * (CK / 8); e += TC_THREADS) {
+                const int j = e % CD, s0 = 8 * (e / CD);
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    w[i] = (uint32_t)rk[(s0 + 2 * i) * CD + j] | ((uint32_t)rk[(s0 + 2 * i + 1) * CD + j] << 16);
+                *reinterpret_cast<uint4 *>(KT + cm_off<CK>(j, s0)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+        smem_to_async();
+        tc_before_sync();
+        __syncthreads();
+        tc_after_sync();
+
+        // ---- (1) Z|Y = S [K|Q]^T on the tensor cores, while the CTA forms A, P, T ----
+        if (tid == 0) {
+            const uint32_t kq = sm_addr(KQ);
+#pragma unroll
+            for (int ks = 0; ks < CD / 16; ++ks) {
+                const uint64_t b = smem_desc(kq + 256 * ks, (CD / 8) * 128);
+                tc_mma(tbase + C_Z, tbase + C_SL + 8 * ks, b, idesc_bf16(128), ks > 0);
+                tc_mma(tbase + C_Z, tbase + C_SH + 8 * ks, b, idesc_bf16(128), true);
+            }
+            tc_commit(bar_zy);
+        }
+        if (more && warp == 2)
+            gates_in(c0 + CK);
+        {
+            // K K^T -> A and Q K^T -> P: the 8-column tiles of their lower
+            // 16x16 blocks, 5 a warp (bf16 q, k exact: one m16n8k16 a step)
+            constexpr int NT = 40 / TC_WARPS;
+            float acc[NT][4];
+            int mrow[NT], ncol[NT];
+            bool isq[NT];
+#pragma unroll
+            for (int i = 0; i < NT; ++i) {
+                const int tau = warp + TC_WARPS * i;
+                isq[i] = tau >= 20;
+                const int idx = isq[i] ? tau - 20 : tau;
+                const int blk = idx >> 1;
+                const int mb = blk >= 6 ? 3 : blk >= 3 ? 2 : blk >= 1 ? 1 : 0;
+                mrow[i] = 16 * mb;
+                ncol[i] = 16 * (blk - mb * (mb + 1) / 2) + 8 * (idx & 1);
+                acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+            }
+#pragma unroll
+            for (int kb = 0; kb < CD / 16; ++kb) {
+#pragma unroll
+                for (int i = 0; i < NT; ++i) {
+                    uint32_t a[4], b0, b1;
+                    lda_cm<CD>(a, KQ, (isq[i] ? CK : 0) + mrow[i], 16 * kb, g, c);
+                    ldb_cm<CD>(b0, b1, KQ, ncol[i], 16 * kb, g, c);
+                    mma16816(acc[i], a[0], a[1], a[2], a[3], b0, b1);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < NT; ++i) {
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int t = mrow[i] + g + 8 * hr;
+                    const int s = ncol[i] + 2 * c;
+                    const float nt_ = isq[i] ? IQ[t] : IK[t];
+                    const float x = acc[i][2 * hr] * nt_ * IK[s], y = acc[i][2 * hr + 1] * nt_ * IK[s + 1];
+                    const float gt = GG[t];
+                    if (!isq[i]) {
+                        const float bt = BE[t];
+                        AF[t * LDF + s] = s < t ? bt * expf(gt - GG[s]) * x : 0.f;
+                        AF[t * LDF + s + 1] = s + 1 < t ? bt * expf(gt - GG[s + 1]) * y : 0.f;
+                    } else {
+                        const float px = s <= t ? expf(gt - GG[s]) * x : 0.f;
+                        const float py = s + 1 <= t ? expf(gt - GG[s + 1]) * y : 0.f;
+                        uint32_t hh, ll;
+                        split2(px, py, hh, ll);
+                        *reinterpret_cast<uint32_t *>(PH + cm_off<CK>(t, s)) = hh;
+                        *reinterpret_cast<uint32_t *>(PL + cm_off<CK>(t, s)) = ll;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        if (tid < CK)
+            t_diagonal(AF, XF, tid);
+        else if (more && warp == 2)
+            gates(c0 + CK, set ^ 1); // meanwhile: the next chunk's gates
+        __syncthreads();
+        t_below_diagonal(AF, XF, warp, g, c);
+        for (int e = tid; e < CK * CK / 2; e += TC_THREADS) {
+            const int t = e / (CK / 2), s = 2 * (e % (CK / 2));
+            const float x = s <= t ? XF[t * LDF + s] : 0.f;
+            const float y = s + 1 <= t ? XF[t * LDF + s + 1] : 0.f;
+            uint32_t hh, ll;
+            split2(x, y, hh, ll);
+            *reinterpret_cast<uint32_t *>(TH + cm_off<CK>(t, s)) = hh;
+            *reinterpret_cast<uint32_t *>(TL + cm_off<CK>(t, s)) = ll;
+        }
+        smem_to_async();
+
+        // ---- (2) E and Y diag(e^G iq) from Z|Y, one state row a thread ----
+        late = !mbar_wait(bar_zy, (uint32_t)(ci & 1));
+        if (late)
+            report(p.err, GDN_DEVERR_TIMEOUT);
+        if (__syncthreads_or(late)) {
+            abort = true;
+            break;
+        }
+        tc_after_sync();
+        {
+            float z[32], y[32];
+            tld32(tlane + C_Z + 32 * half, z);
+            tld32(tlane + C_Y + 32 * half, y);
+            uint32_t eh[16], el[16], yo[32];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const int t = 32 * half + i;
+                const float v0 = __bfloat162float(RV[t * CD + row]), v1 = __bfloat162float(RV[(t + 1) * CD + row]);
+                const float e0 = BE[t] * (v0 - EG[t] * IK[t] * z[i]);
+                const float e1 = BE[t + 1] * (v1 - EG[t + 1] * IK[t + 1] * z[i + 1]);
+                split2(e0, e1, eh[i / 2], el[i / 2]);
+                yo[i] = __float_as_uint(y[i] * EG[t] * IQ[t]);
+                yo[i + 1] = __float_as_uint(y[i + 1] * EG[t + 1] * IQ[t + 1]);
+            }
+            tst16(tlane + C_EH + 16 * half, eh);
+            tst16(tlane + C_EL + 16 * half, el);
+            tst32(tlane + C_Y + 32 * half, yo);
+            tst_wait();
+        }
+        tc_before_sync();
+        __syncthreads();
+        tc_after_sync();
+        if (more)
+            stage(c0 + CK); // V is consumed: the next chunk's inputs travel now
+
+        // ---- (3) U = E T^T ----
+        if (tid == 0) {
+            const uint32_t th = sm_addr(TH), tl = sm_addr(TL);
+#pragma unroll
+            for (int ks = 0; ks < CK / 16; ++ks) {
+                const uint64_t bh = smem_desc(th + 256 * ks, (CK / 8) * 128);
+                const uint64_t bl = smem_desc(tl + 256 * ks, (CK / 8) * 128);
+                tc_mma(tbase + C_U, tbase + C_EL + 8 * ks, bh, idesc_bf16(CK), ks > 0);
+                tc_mma(tbase + C_U, tbase + C_EH + 8 * ks, bl, idesc_bf16(CK), true);
+                tc_mma(tbase + C_U, tbase + C_EH + 8 * ks, bh, idesc_bf16(CK), true);
+            }
+            tc_commit(bar_u);
+        }
+        late = !mbar_wait(bar_u, (uint32_t)(ci & 1));
+        if (late)
+            report(p.err, GDN_DEVERR_TIMEOUT);
+        if (__syncthreads_or(late)) {
+            abort = true;
+            break;
+        }
+        tc_after_sync();
+        {
+            // U's head and tail (for O), those of U diag(e^{G_C-G} ik) (for S),
+            // and S scaled by e^{G_C}
+            float u[32];
+            tld32(tlane + C_U + 32 * half, u);
+            uint32_t uh[16], ul[16], wh[16], wl[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const int t = 32 * half + i;
+                split2(u[i], u[i + 1], uh[i / 2], ul[i / 2]);
+                split2(u[i] * EC[t] * IK[t], u[i + 1] * EC[t + 1] * IK[t + 1], wh[i / 2], wl[i / 2]);
+            }
+            tst16(tlane + C_UH + 16 * half, uh);
+            tst16(tlane + C_UL + 16 * half, ul);
+            tst16(tlane + C_WH + 16 * half, wh);
+            tst16(tlane + C_WL + 16 * half, wl);
+            const float gC = EG[CK - 1];
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                float sv[32];
+                uint32_t r[32];
+                tld32(tlane + C_S + 64 * half + 32 * q2, sv);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    r[i] = __float_as_uint(sv[i] * gC);
+                tst32(tlane + C_S + 64 * half + 32 * q2, r);
+            }
+            tst_wait();
+        }
+        tc_before_sync();
+        __syncthreads();
+        tc_after_sync();
+
+        // ---- (4) O += U P^T and S += U diag(e^{G_C-G} ik) K ----
+        if (tid == 0) {
+            const uint32_t ph = sm_addr(PH), pl = sm_addr(PL), kt = sm_addr(KT);
+#pragma unroll
+            for (int ks = 0; ks < CK / 16; ++ks) {
+                const uint64_t bh = smem_desc(ph + 256 * ks, (CK / 8) * 128);
+                const uint64_t bl = smem_desc(pl + 256 * ks, (CK / 8) * 128);
+                tc_mma(tbase + C_Y, tbase + C_UL + 8 * ks, bh, idesc_bf16(CK), true);
+                tc_mma(tbase + C_Y, tbase + C_UH + 8 * ks, bl, idesc_bf16(CK), true);
+                tc_mma(tbase + C_Y, tbase + C_UH + 8 * ks, bh, idesc_bf16(CK), true);
+            }
+#pragma unroll
+            for (int ks = 0; ks < CK / 16; ++ks) {
+                const uint64_t b = smem_desc(kt + 256 * ks, (CK / 8) * 128);
+                tc_mma(tbase + C_S, tbase + C_WL + 8 * ks, b, idesc_bf16(CD), true);
+                tc_mma(tbase + C_S, tbase + C_WH + 8 * ks, b, idesc_bf16(CD), true);
+            }
+            tc_commit(bar_o);
+        }
+        n_prev = n;
+    }
+
+    if (!abort && L > 0) {
+        const int last = (L - 1) / CK;
+        const bool late = !mbar_wait(bar_o, (uint32_t)(last & 1));
+        if (late)
+            report(p.err, GDN_DEVERR_TIMEOUT);
+        abort = __syncthreads_or(late);
+        if (!abort) {
+            tc_after_sync();
+            write_outputs(last * CK, n_prev);
+        }
+    }
+    if (!abort) {
+        // the final state, to the write slot (the read slot in place)
+        float *Sd = p.pool + (size_t)ws * slot_floats + head_off + (size_t)row * CD + 64 * half;
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+            float sv[32];
+            tld32(tlane + C_S + 64 * half + 32 * q2, sv);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                *reinterpret_cast<float4 *>(Sd + 32 * q2 + 4 * i) =
+                    make_float4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]);
+        }
+    }
+    tc_before_sync();
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(kTmemCols) : "memory");
+}
+
+} // namespace
+
+cudaError_t launch_gdn_prefill_chunked_tc(const PrefillArgs &a, cudaStream_t s)
+{
+    const long long ctas = (long long)a.nseq * a.hv;
+    if (ctas == 0)
+        return cudaSuccess;
+    if (ctas > 0x7fffffffll)
+        return cudaErrorInvalidValue;
+    static std::atomic<unsigned long long> configured{0}; // one bit per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(gdn_chunked_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             TS::TOTAL);
+        if (e != cudaSuccess)
+            return e;
+        configured.fetch_or(bit, std::memory_order_release);
+    }
+    return launch_pdl(gdn_chunked_tc_kernel, dim3((unsigned)ctas), dim3(TC_THREADS), (size_t)TS::TOTAL, s, a);
+}
+
+} // namespace gdn

@@ -102,7 +102,9 @@ cudaError_t launch_conv(const ConvArgs &a, int dtype, cudaStream_t s);
 cudaError_t launch_gdn_prefill(const PrefillArgs &a, int dtype, cudaStream_t s);
 cudaError_t launch_conv_prefill(const ConvPrefillArgs &a, int dtype, cudaStream_t s);
 // The chunked (tensor-core) form of launch_gdn_prefill: in place or twin, no token slots.
+// bf16 activations run the tcgen05 kernel (gdn_chunked_tc.cu), fp32 the mma.sync one.
 cudaError_t launch_gdn_prefill_chunked(const PrefillArgs &a, int dtype, cudaStream_t s);
+cudaError_t launch_gdn_prefill_chunked_tc(const PrefillArgs &a, cudaStream_t s);
 
 // True when the state kernels are built for (dk, dv).
 bool step_shape_supported(int dk, int dv);
