@@ -21,14 +21,19 @@
 //     the CTA's threads read and write TMEM one state row a thread (two warps
 //     on each 32-lane quarter, each taking half of the columns).
 // Z|Y is issued as soon as the chunk's K and Q are in shared memory and runs
-// on the tensor cores while all warps form A, P and T (mma.sync tiles and the
-// fp32 blocked inverse shared with gdn_chunked.cu).
+// on the tensor cores while the CTA forms A, P and T (the fp32 blocked
+// inverse shared with gdn_chunked.cu).
 //
 // Tensor memory (512 columns, one CTA an SM): S 0-127; Z 128-191, later the
 // head|tail of U diag(e^{G_C-G} ik) (128-159 | 160-191); Y, then O, 192-255;
 // U 256-319; the head|tail of S 320-383 | 384-447, later those of E
-// (320-351 | 352-383) and of U (384-415 | 416-447).  Every region is reused
-// only after the mbarrier of the products that read it has completed.
+// (320-351 | 352-383) and of U (384-415 | 416-447); [K|Q] K^T 448-511.
+// Every region is reused only after the mbarrier of the products that read
+// it has completed.
+//
+// [K|Q] K^T (rows 0-63: K K^T, 64-127: Q K^T) is itself one M = 128 product
+// with both operands in shared memory; one thread a row turns it into A
+// (fp32) and P (head and tail) with the gates, the norms and the masks.
 #include <atomic>
 
 #include "gdn_chunk_common.cuh"
@@ -46,7 +51,7 @@ constexpr uint32_t kTmemCols = 512;
 
 // TMEM columns
 constexpr uint32_t C_S = 0, C_Z = 128, C_Y = 192, C_U = 256, C_SH = 320, C_SL = 384;
-constexpr uint32_t C_EH = 320, C_EL = 352, C_UH = 384, C_UL = 416, C_WH = 128, C_WL = 160;
+constexpr uint32_t C_EH = 320, C_EL = 352, C_UH = 384, C_UL = 416, C_WH = 128, C_WL = 160, C_KK = 448;
 
 // Byte offset of element (row, k) in a canonical K-major tile with K columns.
 template <int K> __device__ __forceinline__ int cm_off(int row, int k)
@@ -67,7 +72,7 @@ struct TS {
     static constexpr int GATES = XF + CK * LDF * 4; // two sets of [G | beta | e^G | e^{G_C-G}] x CK
     static constexpr int IQ = GATES + 2 * 4 * CK * 4;
     static constexpr int IK = IQ + CK * 4;
-    static constexpr int BARS = IK + CK * 4;      // mbarriers: Z|Y, U, O and S
+    static constexpr int BARS = IK + CK * 4;      // mbarriers: Z|Y, U, O and S, [K|Q] K^T
     static constexpr int TADDR = BARS + 32;       // the TMEM base address
     static constexpr int BYTES = TADDR + 16;
     static constexpr int STAGE = (BYTES + 127) & ~127; // raw q, k, v of the next chunk, [CK][CD] each
@@ -88,6 +93,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int n)
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
+// A and B from shared memory
+__device__ __forceinline__ void tc_mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, bool acc)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+                 "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)acc)
+                 : "memory");
+}
+// A from tensor memory, B from shared memory
 __device__ __forceinline__ void tc_mma(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, bool acc)
 {
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -217,6 +231,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
 
     // tensor memory (all 512 columns) and the products' mbarriers
     const uint32_t bar_zy = sm_addr(&bars[0]), bar_u = sm_addr(&bars[1]), bar_o = sm_addr(&bars[2]);
+    const uint32_t bar_kk = sm_addr(&bars[3]);
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sm_addr(taddr_slot)),
                      "r"(kTmemCols)
@@ -227,11 +242,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
         mbar_init(bar_zy, 1);
         mbar_init(bar_u, 1);
         mbar_init(bar_o, 1);
+        mbar_init(bar_kk, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // P's blocks above the diagonal are never computed: zero both halves once
-    for (int e = tid; e < 2 * CK * CK * 2 / 16; e += TC_THREADS)
-        reinterpret_cast<uint4 *>(PH)[e] = make_uint4(0u, 0u, 0u, 0u);
     tc_before_sync();
     __syncthreads();
     tc_after_sync();
@@ -418,9 +431,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
         __syncthreads();
         tc_after_sync();
 
-        // ---- (1) Z|Y = S [K|Q]^T on the tensor cores, while the CTA forms A, P, T ----
+        // ---- (1) [K|Q] K^T, then Z|Y = S [K|Q]^T, on the tensor cores ----
         if (tid == 0) {
             const uint32_t kq = sm_addr(KQ);
+#pragma unroll
+            for (int ks = 0; ks < CD / 16; ++ks) {
+                const uint64_t ab = smem_desc(kq + 256 * ks, (CD / 8) * 128); // [K|Q] and, its first 64 rows, K
+                tc_mma_ss(tbase + C_KK, ab, ab, idesc_bf16(CK), ks > 0);    // exact bf16 products
+            }
+            tc_commit(bar_kk);
 #pragma unroll
             for (int ks = 0; ks < CD / 16; ++ks) {
                 const uint64_t b = smem_desc(kq + 256 * ks, (CD / 8) * 128);
@@ -431,55 +450,45 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
         }
         if (more && warp == 2)
             gates_in(c0 + CK);
+        // meanwhile the decay e^{G_t - G_s} (s <= t) that A and P share, into T's buffer
+        for (int i = 0; i < CK / 4; ++i) {
+            const int t = tid >> 2, s2 = (tid & 3) + 4 * i;
+            if (s2 <= t)
+                XF[t * LDF + s2] = expf(GG[t] - GG[s2]);
+        }
+        late = !mbar_wait(bar_kk, (uint32_t)(ci & 1));
+        if (late)
+            report(p.err, GDN_DEVERR_TIMEOUT);
+        if (__syncthreads_or(late)) {
+            abort = true;
+            break;
+        }
+        tc_after_sync();
         {
-            // K K^T -> A and Q K^T -> P: the 8-column tiles of their lower
-            // 16x16 blocks, 5 a warp (bf16 q, k exact: one m16n8k16 a step)
-            constexpr int NT = 40 / TC_WARPS;
-            float acc[NT][4];
-            int mrow[NT], ncol[NT];
-            bool isq[NT];
+            // row `row` of [K|Q] K^T, columns (tokens s) 32*half .. 32*half + 31:
+            // rows t < 64 give A[t][s] = beta_t e^{G_t-G_s} ik_t ik_s (k_t . k_s), s < t;
+            // rows 64 + t give P[t][s] = e^{G_t-G_s} iq_t ik_s (q_t . k_s), s <= t
+            // (a warp whose columns all lie above its rows writes zeros)
+            const bool isq = row >= CK;
+            const int t = isq ? row - CK : row;
+            const bool any = 32 * half <= 32 * (quarter & 1) + 31;
+            float d[32];
+            tld32(tlane + C_KK + 32 * half, d);
+            const float nt_ = isq ? IQ[t] : IK[t] * BE[t];
 #pragma unroll
-            for (int i = 0; i < NT; ++i) {
-                const int tau = warp + TC_WARPS * i;
-                isq[i] = tau >= 20;
-                const int idx = isq[i] ? tau - 20 : tau;
-                const int blk = idx >> 1;
-                const int mb = blk >= 6 ? 3 : blk >= 3 ? 2 : blk >= 1 ? 1 : 0;
-                mrow[i] = 16 * mb;
-                ncol[i] = 16 * (blk - mb * (mb + 1) / 2) + 8 * (idx & 1);
-                acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-            }
-#pragma unroll
-            for (int kb = 0; kb < CD / 16; ++kb) {
-#pragma unroll
-                for (int i = 0; i < NT; ++i) {
-                    uint32_t a[4], b0, b1;
-                    lda_cm<CD>(a, KQ, (isq[i] ? CK : 0) + mrow[i], 16 * kb, g, c);
-                    ldb_cm<CD>(b0, b1, KQ, ncol[i], 16 * kb, g, c);
-                    mma16816(acc[i], a[0], a[1], a[2], a[3], b0, b1);
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < NT; ++i) {
-#pragma unroll
-                for (int hr = 0; hr < 2; ++hr) {
-                    const int t = mrow[i] + g + 8 * hr;
-                    const int s = ncol[i] + 2 * c;
-                    const float nt_ = isq[i] ? IQ[t] : IK[t];
-                    const float x = acc[i][2 * hr] * nt_ * IK[s], y = acc[i][2 * hr + 1] * nt_ * IK[s + 1];
-                    const float gt = GG[t];
-                    if (!isq[i]) {
-                        const float bt = BE[t];
-                        AF[t * LDF + s] = s < t ? bt * expf(gt - GG[s]) * x : 0.f;
-                        AF[t * LDF + s + 1] = s + 1 < t ? bt * expf(gt - GG[s + 1]) * y : 0.f;
-                    } else {
-                        const float px = s <= t ? expf(gt - GG[s]) * x : 0.f;
-                        const float py = s + 1 <= t ? expf(gt - GG[s + 1]) * y : 0.f;
-                        uint32_t hh, ll;
-                        split2(px, py, hh, ll);
-                        *reinterpret_cast<uint32_t *>(PH + cm_off<CK>(t, s)) = hh;
-                        *reinterpret_cast<uint32_t *>(PL + cm_off<CK>(t, s)) = ll;
-                    }
+            for (int i = 0; i < 32; i += 2) {
+                const int s0 = 32 * half + i;
+                const bool in0 = any && (isq ? s0 <= t : s0 < t), in1 = any && (isq ? s0 + 1 <= t : s0 + 1 < t);
+                const float x = in0 ? XF[t * LDF + s0] * nt_ * IK[s0] * d[i] : 0.f;
+                const float y = in1 ? XF[t * LDF + s0 + 1] * nt_ * IK[s0 + 1] * d[i + 1] : 0.f;
+                if (!isq) {
+                    AF[t * LDF + s0] = x;
+                    AF[t * LDF + s0 + 1] = y;
+                } else {
+                    uint32_t hh, ll;
+                    split2(x, y, hh, ll);
+                    *reinterpret_cast<uint32_t *>(PH + cm_off<CK>(t, s0)) = hh;
+                    *reinterpret_cast<uint32_t *>(PL + cm_off<CK>(t, s0)) = ll;
                 }
             }
         }
@@ -490,8 +499,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
             gates(c0 + CK, set ^ 1); // meanwhile: the next chunk's gates
         __syncthreads();
         t_below_diagonal(AF, XF, warp, g, c);
+        // T's lower triangle, split, into the canonical layout: a warp writes one
+        // 8 x 8 core matrix at a time (lane: row lane & 7, column pair lane >> 3)
         for (int e = tid; e < CK * CK / 2; e += TC_THREADS) {
-            const int t = e / (CK / 2), s = 2 * (e % (CK / 2));
+            const int cmi = e >> 5, l = e & 31;
+            const int t = 8 * (cmi >> 3) + (l & 7), s = 8 * (cmi & 7) + 2 * (l >> 3);
             const float x = s <= t ? XF[t * LDF + s] : 0.f;
             const float y = s + 1 <= t ? XF[t * LDF + s + 1] : 0.f;
             uint32_t hh, ll;
