@@ -24,10 +24,15 @@
 // chunk with zero q, k, v and beta and a zero log-gate, which leaves every
 // real token's result unchanged.
 //
+// This file runs fp32 activations; bf16 activations (exact in bf16, so q
+// and k need no split) run the tcgen05 kernel of gdn_chunked_tc.cu, which
+// keeps the state in tensor memory.
+//
 // Layout of the work: one CTA per (sequence, value head), 8 warps.  Warp w
 // holds state rows 16w..16w+15 (every dk column) in its MMA accumulators for
 // the whole sequence, so the state is read once and written once.  Per chunk
-// the CTA first builds, in shared memory, the normalised Q and K, the gates,
+// the CTA first loads the chunk's inputs (every load in flight before any is
+// used) and builds, in shared memory, the normalised Q and K, the gates,
 // A, P and T (T on the CUDA cores in fp32: 16x16 diagonal blocks by forward
 // substitution, then the blocks below them); then each warp forms the
 // products above for its own rows, and writes its outputs.
@@ -77,16 +82,9 @@ struct CS {
     // gates, two sets (a chunk's and the next one's), each fp32
     // [G (running log-gate) | beta | e^{G_t} | e^{G_C - G_t}] x [CK]
     static constexpr int GATES = VO + CK * LDV * 4;
-    static constexpr int IQ = GATES + 2 * 4 * CK * 4; // fp32 [CK] q's norm scale (1 when q is stored normalised)
-    static constexpr int IK = IQ + CK * 4;       // fp32 [CK] k's norm scale (likewise)
-    static constexpr int BYTES = IK + CK * 4;
+    static constexpr int BYTES = GATES + 2 * 4 * CK * 4;
 };
-// bf16 activations add a staging area for the next chunk's raw q, k, v
-// (16-byte asynchronous copies while the current chunk computes).
-constexpr int kStageBytes = 3 * CK * CD * 2;
-constexpr int kStageOffset = (CS::BYTES + 127) & ~127;
-template <typename TA> constexpr int smem_bytes() { return kStageOffset + (sizeof(TA) == 2 ? kStageBytes : 0); }
-static_assert(kStageOffset + kStageBytes <= 227 * 1024, "shared memory");
+static_assert(CS::BYTES <= 227 * 1024, "shared memory");
 static_assert(CS::AF % 16 == 0 && CS::VO % 16 == 0 && (LDV * 4) % 16 == 0, "alignment");
 
 
@@ -106,12 +104,6 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
     float *const XF = reinterpret_cast<float *>(smem + CS::XF);
     float *const VO = reinterpret_cast<float *>(smem + CS::VO);
     float *const GATES = reinterpret_cast<float *>(smem + CS::GATES);
-    float *const IQ = reinterpret_cast<float *>(smem + CS::IQ);
-    float *const IK = reinterpret_cast<float *>(smem + CS::IK);
-    // bf16 q and k are exact in bf16: they are stored raw (no tail) and their
-    // norms applied as per-token scales, so products with them need no
-    // split on their side; fp32 q and k are stored normalised and split
-    constexpr bool kExact = sizeof(TA) == 2;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
     const int seq = blockIdx.x / p.hv, h = blockIdx.x - seq * p.hv;
@@ -165,27 +157,6 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
     const TA *const bg = reinterpret_cast<const TA *>(p.b);
     const int L = t1 - t0;
 
-    // bf16: the raw q, k, v of the chunk starting at token cn (zeros past
-    // the sequence), 16 bytes a copy, every thread a share, into the staging area
-    constexpr bool kStaged = sizeof(TA) == 2;
-    TA *const RQ = reinterpret_cast<TA *>(smem + kStageOffset);
-    TA *const RK = RQ + CK * CD;
-    TA *const RV = RK + CK * CD;
-    auto stage = [&](int cn) {
-        const int nn = min(CK, L - cn);
-        for (int e = tid; e < 3 * CK * (CD / 8); e += CTHREADS) {
-            const int which = e / (CK * (CD / 8)), rem = e - which * (CK * (CD / 8));
-            const int tt = rem / (CD / 8), j = rem - tt * (CD / 8);
-            const bool live = tt < nn;
-            const size_t tok = (size_t)(t0 + cn + (live ? tt : 0));
-            const TA *src = which == 0   ? qg + (tok * p.hk + hq) * CD
-                            : which == 1 ? kg + (tok * p.hk + hq) * CD
-                                         : vg + (tok * p.hv + h) * CD;
-            TA *dst = (which == 0 ? RQ : which == 1 ? RK : RV) + tt * CD;
-            cp_async16(dst + 8 * j, src + 8 * j, live ? 16 : 0);
-        }
-        cp_async_commit();
-    };
     // the gate inputs of the chunk starting at cn: warp 2, tokens lane and lane + 32
     TA ra[2], rb[2];
     auto gates_in = [&](int cn) {
@@ -230,8 +201,6 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
         G[3 * CK + lane] = expf(gc - s0), G[3 * CK + lane + 32] = expf(gc - s1);
     };
     if (L > 0) {
-        if (kStaged)
-            stage(0);
         if (warp == 2) {
             gates_in(0);
             gates(0, 0);
@@ -247,23 +216,16 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
         const float *const EG = GG + 2 * CK;
         const float *const EC = GG + 3 * CK;
         const bool more = c0 + CK < L;
-        if (kStaged)
-            cp_async_wait_all();
-        __syncthreads(); // every warp is done with the previous chunk's tiles; the staged inputs landed
+        __syncthreads(); // every warp is done with the previous chunk's tiles
 
-        // ---- the chunk's inputs (staged for bf16; else every load in flight
-        // before any is used): q, k, v: 8 tokens a warp (token warp + 8i), 4
-        // channels a lane ----
+        // ---- the chunk's inputs, every load in flight before any is used:
+        // q, k, v: 8 tokens a warp (token warp + 8i), 4 channels a lane ----
         constexpr int TPW = CK / CWARPS;
         Raw4<TA> rq[TPW], rk[TPW], rv[TPW];
 #pragma unroll
         for (int i = 0; i < TPW; ++i) {
             const int tt = warp + CWARPS * i;
-            if (kStaged) { // zeros past the sequence
-                rq[i] = ldraw<TA>(RQ + tt * CD + 4 * lane);
-                rk[i] = ldraw<TA>(RK + tt * CD + 4 * lane);
-                rv[i] = ldraw<TA>(RV + tt * CD + 4 * lane);
-            } else if (!kStaged && tt < n) {
+            if (tt < n) {
                 const size_t tok = (size_t)(t0 + c0 + tt);
                 rq[i] = ldraw<TA>(qg + (tok * p.hk + hq) * CD + 4 * lane);
                 rk[i] = ldraw<TA>(kg + (tok * p.hk + hq) * CD + 4 * lane);
@@ -285,24 +247,15 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
                 sk += __shfl_xor_sync(0xffffffffu, sk, o);
             }
             const float iq = qscale * rsqrtf(sq + kEps), ik = rsqrtf(sk + kEps);
-            if constexpr (kExact) {
-                *reinterpret_cast<uint2 *>(QH + tt * LDK + 4 * lane) = *reinterpret_cast<const uint2 *>(&rq[i]);
-                *reinterpret_cast<uint2 *>(KH + tt * LDK + 4 * lane) = *reinterpret_cast<const uint2 *>(&rk[i]);
-                if (lane == 0)
-                    IQ[tt] = iq, IK[tt] = ik;
-            } else {
-                uint32_t h0, l0, h1, l1;
-                split2(qv[0] * iq, qv[1] * iq, h0, l0);
-                split2(qv[2] * iq, qv[3] * iq, h1, l1);
-                *reinterpret_cast<uint2 *>(QH + tt * LDK + 4 * lane) = make_uint2(h0, h1);
-                *reinterpret_cast<uint2 *>(QL + tt * LDK + 4 * lane) = make_uint2(l0, l1);
-                split2(kv[0] * ik, kv[1] * ik, h0, l0);
-                split2(kv[2] * ik, kv[3] * ik, h1, l1);
-                *reinterpret_cast<uint2 *>(KH + tt * LDK + 4 * lane) = make_uint2(h0, h1);
-                *reinterpret_cast<uint2 *>(KL + tt * LDK + 4 * lane) = make_uint2(l0, l1);
-                if (lane == 0)
-                    IQ[tt] = 1.f, IK[tt] = 1.f;
-            }
+            uint32_t h0, l0, h1, l1;
+            split2(qv[0] * iq, qv[1] * iq, h0, l0);
+            split2(qv[2] * iq, qv[3] * iq, h1, l1);
+            *reinterpret_cast<uint2 *>(QH + tt * LDK + 4 * lane) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2 *>(QL + tt * LDK + 4 * lane) = make_uint2(l0, l1);
+            split2(kv[0] * ik, kv[1] * ik, h0, l0);
+            split2(kv[2] * ik, kv[3] * ik, h1, l1);
+            *reinterpret_cast<uint2 *>(KH + tt * LDK + 4 * lane) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2 *>(KL + tt * LDK + 4 * lane) = make_uint2(l0, l1);
             *reinterpret_cast<float4 *>(VO + tt * LDV + 4 * lane) = make_float4(vv[0], vv[1], vv[2], vv[3]);
         }
         __syncthreads();
@@ -336,13 +289,9 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
                     uint32_t ah[4], al[4], bh0, bh1, bl0, bl1;
                     lda(ah, isq[i] ? QH : KH, LDK, mrow[i], 16 * kb, g, c);
                     ldb(bh0, bh1, KH, LDK, ncol[i], 16 * kb, g, c);
-                    if constexpr (kExact) {
-                        mma16816(acc[i], ah[0], ah[1], ah[2], ah[3], bh0, bh1); // exact products
-                    } else {
-                        lda(al, isq[i] ? QL : KL, LDK, mrow[i], 16 * kb, g, c);
-                        ldb(bl0, bl1, KL, LDK, ncol[i], 16 * kb, g, c);
-                        mma3(acc[i], ah, al, bh0, bh1, bl0, bl1);
-                    }
+                    lda(al, isq[i] ? QL : KL, LDK, mrow[i], 16 * kb, g, c);
+                    ldb(bl0, bl1, KL, LDK, ncol[i], 16 * kb, g, c);
+                    mma3(acc[i], ah, al, bh0, bh1, bl0, bl1);
                 }
             }
 #pragma unroll
@@ -351,8 +300,7 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
                 for (int hr = 0; hr < 2; ++hr) {
                     const int t = mrow[i] + g + 8 * hr;
                     const int s = ncol[i] + 2 * c;
-                    const float nt_ = isq[i] ? IQ[t] : IK[t];
-                    const float x = acc[i][2 * hr] * nt_ * IK[s], y = acc[i][2 * hr + 1] * nt_ * IK[s + 1];
+                    const float x = acc[i][2 * hr], y = acc[i][2 * hr + 1];
                     const float gt = GG[t];
                     if (!isq[i]) {
                         const float bt = BE[t];
@@ -392,8 +340,6 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
 
         // the next chunk's q, k, v travel during this chunk's products (a
         // warp stalled on issuing them leaves the tensor pipe to the other)
-        if (more && kStaged)
-            stage(c0 + CK);
         // ---- this warp's rows: Z = S K^T and Y = S Q^T (16 x 64 each) ----
         float z[8][4], y[8][4], u[8][4];
 #pragma unroll
@@ -409,21 +355,11 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
             for (int nt = 0; nt < 8; ++nt) {
                 uint32_t bh0, bh1, bl0, bl1;
                 ldb(bh0, bh1, KH, LDK, 8 * nt, 16 * kb, g, c);
-                if constexpr (kExact) {
-                    mma16816(z[nt], al[0], al[1], al[2], al[3], bh0, bh1);
-                    mma16816(z[nt], ah[0], ah[1], ah[2], ah[3], bh0, bh1);
-                } else {
-                    ldb(bl0, bl1, KL, LDK, 8 * nt, 16 * kb, g, c);
-                    mma3(z[nt], ah, al, bh0, bh1, bl0, bl1);
-                }
+                ldb(bl0, bl1, KL, LDK, 8 * nt, 16 * kb, g, c);
+                mma3(z[nt], ah, al, bh0, bh1, bl0, bl1);
                 ldb(bh0, bh1, QH, LDK, 8 * nt, 16 * kb, g, c);
-                if constexpr (kExact) {
-                    mma16816(y[nt], al[0], al[1], al[2], al[3], bh0, bh1);
-                    mma16816(y[nt], ah[0], ah[1], ah[2], ah[3], bh0, bh1);
-                } else {
-                    ldb(bl0, bl1, QL, LDK, 8 * nt, 16 * kb, g, c);
-                    mma3(y[nt], ah, al, bh0, bh1, bl0, bl1);
-                }
+                ldb(bl0, bl1, QL, LDK, 8 * nt, 16 * kb, g, c);
+                mma3(y[nt], ah, al, bh0, bh1, bl0, bl1);
             }
         }
         // E = (V^T - Z diag(e^G)) diag(beta), in place of Z
@@ -433,7 +369,7 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int t = 8 * nt + 2 * c + (e & 1), r = rA + 8 * (e >> 1);
-                z[nt][e] = BE[t] * (VO[t * LDV + r] - EG[t] * IK[t] * z[nt][e]);
+                z[nt][e] = BE[t] * (VO[t * LDV + r] - EG[t] * z[nt][e]);
             }
         // U^T = E T^T
 #pragma unroll
@@ -452,7 +388,7 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
             const int t = 8 * nt + 2 * c;
-            const float e0 = EG[t] * IQ[t], e1 = EG[t + 1] * IQ[t + 1];
+            const float e0 = EG[t], e1 = EG[t + 1];
             y[nt][0] *= e0, y[nt][1] *= e1, y[nt][2] *= e0, y[nt][3] *= e1;
         }
 #pragma unroll
@@ -485,7 +421,7 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
             const int t = 8 * nt + 2 * c;
-            const float e0 = EC[t] * IK[t], e1 = EC[t + 1] * IK[t + 1];
+            const float e0 = EC[t], e1 = EC[t + 1];
             u[nt][0] *= e0, u[nt][1] *= e1, u[nt][2] *= e0, u[nt][3] *= e1;
         }
 #pragma unroll
@@ -496,16 +432,9 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
             for (int np = 0; np < CD / 16; ++np) {
                 uint32_t bh[4], bl[4];
                 ldb_trans2(bh, KH, LDK, 16 * kb, 16 * np, lane);
-                if constexpr (kExact) {
-                    mma16816(sacc[2 * np], al[0], al[1], al[2], al[3], bh[0], bh[1]);
-                    mma16816(sacc[2 * np], ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
-                    mma16816(sacc[2 * np + 1], al[0], al[1], al[2], al[3], bh[2], bh[3]);
-                    mma16816(sacc[2 * np + 1], ah[0], ah[1], ah[2], ah[3], bh[2], bh[3]);
-                } else {
-                    ldb_trans2(bl, KL, LDK, 16 * kb, 16 * np, lane);
-                    mma3(sacc[2 * np], ah, al, bh[0], bh[1], bl[0], bl[1]);
-                    mma3(sacc[2 * np + 1], ah, al, bh[2], bh[3], bl[2], bl[3]);
-                }
+                ldb_trans2(bl, KL, LDK, 16 * kb, 16 * np, lane);
+                mma3(sacc[2 * np], ah, al, bh[0], bh[1], bl[0], bl[1]);
+                mma3(sacc[2 * np + 1], ah, al, bh[2], bh[3], bl[2], bl[3]);
             }
         }
         __syncwarp();
@@ -542,12 +471,12 @@ cudaError_t launch_chunked_t(const PrefillArgs &a, cudaStream_t s)
     cudaGetDevice(&dev);
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<TA>());
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CS::BYTES);
         if (e != cudaSuccess)
             return e;
         configured.fetch_or(bit, std::memory_order_release);
     }
-    return launch_pdl(kern, dim3((unsigned)ctas), dim3(CTHREADS), (size_t)smem_bytes<TA>(), s, a);
+    return launch_pdl(kern, dim3((unsigned)ctas), dim3(CTHREADS), (size_t)CS::BYTES, s, a);
 }
 
 } // namespace
