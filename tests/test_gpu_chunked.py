@@ -164,3 +164,25 @@ def test_chunked_in_place_equals_twin(gdn):
     for r in range(len(c.lens)):
         assert torch.equal(c.pool.tensor[int(c.rs_np[r])], twin[int(c.ws_np[r])])
     assert gdn.get_device_error() == 0
+
+
+@pytest.mark.slow
+def test_chunked_long_sequence_close_to_exact(gdn):
+    """32 chunks in one sequence (2048 tokens, 0.8B shape, bf16, twin):
+    the chunked state and outputs stay within 1e-4 of the exact kernel's
+    after every chunk boundary has carried the state on."""
+    s = I.QWEN_08B
+    c = Case(gdn, s, [2048, 77], seed=96, n_pad=0, token_slots=False)
+    ref = c.prefill().clone()
+    torch.cuda.synchronize()
+    want = c.pool.tensor.cpu().numpy()
+    c.reset()
+    out = chunked(c)
+    torch.cuda.synchronize()
+    got = c.pool.tensor.cpu().numpy()
+    for sl in c.ws_np:
+        for h in range(s.hv):
+            err = state_rel_err(got[sl, h], want[sl, h].astype(np.float64))
+            assert err <= 1e-4, f"slot {sl} head {h}: {err:.3g}"
+    assert_out_close(f64(out), f64(ref), "bf16")
+    assert gdn.get_device_error() == 0

@@ -25,18 +25,19 @@ pytestmark = pytest.mark.gpu
 class Case:
     """Packed sequences with their inputs, a state pool and a conv pool."""
 
-    def __init__(self, gdn, s: I.Shape, lens, seed: int, n_pad: int = 1):
+    def __init__(self, gdn, s: I.Shape, lens, seed: int, n_pad: int = 1, token_slots: bool = True):
         self.gdn, self.s, self.lens = gdn, s, list(lens)
         gen = I.Gen(seed)
         T = int(sum(lens))
         self.T = T
-        self.num_slots = 1 + 2 * len(lens) + T
+        self.num_slots = 1 + 2 * len(lens) + (T if token_slots else 0)
         prm = gen.params(s)
         self.prm = prm
         self.w, self.w64 = pair(prm["w"], s.dtype)
         self.bias, self.bias64 = pair(prm["bias"], s.dtype)
         self.A_log, self.dt_bias = t(prm["A_log"]), t(prm["dt_bias"])
-        self.cu_np, self.rs_np, self.ws_np, self.ts_np = gen.seq_tables(lens, self.num_slots, n_pad)
+        self.cu_np, self.rs_np, self.ws_np, self.ts_np = gen.seq_tables(lens, self.num_slots, n_pad,
+                                                                        token_slots=token_slots)
         self.cu, self.rs, self.ws, self.ts = ti(self.cu_np), ti(self.rs_np), ti(self.ws_np), ti(self.ts_np)
         self.pool_np = gen.state_pool(s, self.num_slots)
         cp_dev, self.cp64 = pair(gen.conv_pool(s, self.num_slots), s.dtype)
