@@ -265,6 +265,59 @@ def time_calls(calls, n, device):
     return a.elapsed_time(b) * 1e3 / n
 
 
+def run_unfused(G, I, device, n=400):
+    """The two calls the fused layer replaces, 0.8B shape, 64 rows, twin:
+    causal_conv1d_decode over the packed q|k|v channels, then gdn_decode_step
+    on q, k, v of the same shapes (four instances in rotation)."""
+    import torch
+    s = I.QWEN_08B
+    dt = s.dtype
+    sets = []
+    for i in range(NSETS):
+        gen = I.Gen(4000 + i)
+        prm = gen.params(s)
+        st = {"pool": G.GDNStatePool(s.num_slots, s.hk, s.hv, s.dk, s.dv, device=device,
+                                     tensor=torch.from_numpy(gen.state_pool(s)).to(device)),
+              "cp": G.ConvStatePool(s.num_slots, s.channels, s.width, dtype=I.torch_dtype(dt), device=device,
+                                    tensor=I.to_torch(gen.conv_pool(s), dt, device)),
+              "w": I.to_torch(prm["w"], dt, device), "bias": I.to_torch(prm["bias"], dt, device),
+              "A_log": I.to_torch(prm["A_log"], "f32", device), "dt_bias": I.to_torch(prm["dt_bias"], "f32", device),
+              "x": I.to_torch(gen.layer_inputs(s)["x"], dt, device)}
+        for k, v in gen.step_inputs(s).items():
+            st[k] = I.to_torch(v, dt, device)
+        rs, ws = gen.slot_tables(s.rows, s.num_slots)
+        st["rs"], st["ws"] = torch.from_numpy(rs).to(device), torch.from_numpy(ws).to(device)
+        st["y"] = torch.empty((s.rows, s.channels), dtype=I.torch_dtype(dt), device=device)
+        st["o"] = torch.empty((s.rows, s.hv, s.dv), dtype=I.torch_dtype(dt), device=device)
+        stream = torch.cuda.current_stream(device).cuda_stream
+        code = G.GDN_BF16 if dt == "bf16" else G.GDN_F32
+        st["conv"] = G.PreparedCall("causal_conv1d_decode",
+                                    (st["x"].data_ptr(), s.channels, st["cp"].handle, st["rs"].data_ptr(),
+                                     st["ws"].data_ptr(), st["w"].data_ptr(), st["bias"].data_ptr(), 1,
+                                     st["y"].data_ptr(), s.rows, code, stream), (st,))
+        st["step"] = G.PreparedCall("gdn_decode_step",
+                                    (st["q"].data_ptr(), st["k"].data_ptr(), st["v"].data_ptr(),
+                                     st["a"].data_ptr(), st["b"].data_ptr(), st["A_log"].data_ptr(),
+                                     st["dt_bias"].data_ptr(), st["pool"].handle, st["rs"].data_ptr(),
+                                     st["ws"].data_ptr(), st["o"].data_ptr(), s.rows, s.hv, 0, code, stream), (st,))
+        sets.append(st)
+
+    def both(st):
+        st["conv"]()
+        st["step"]()
+    conv_us = time_calls([st["conv"] for st in sets], n, device)
+    step_us = time_calls([st["step"] for st in sets], n, device)
+    pair_us = time_calls([lambda st=st: both(st) for st in sets], n, device)
+    state = s.rows * s.hv * s.dv * s.dk * 4 * 2
+    res = {"workload": "0.8B-shaped conv then rule as two calls, 64 rows, twin",
+           "conv_us": round(conv_us, 2), "step_us": round(step_us, 2), "pair_us": round(pair_us, 2),
+           "step_GBs": round(state / step_us / 1e3, 1),
+           "pair_GBs_of_layer_bytes": round(layer_bytes(s, s.rows) / pair_us / 1e3, 1)}
+    del sets
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_extras(G, I, device, n=400):
     """The other workloads, timed on the same terms (four instances in rotation,
     back-to-back launches): the rows x write-mode sweep, the 9B-shaped GQA layer
@@ -305,6 +358,7 @@ def run_extras(G, I, device, n=400):
         torch.cuda.empty_cache()
     res["qwen9b_gqa"] = {"workload": "9B-shaped fused layer: 16 qk / 32 v heads, 2R+1 slots, twin",
                          "rows": gqa}
+    res["unfused_calls"] = run_unfused(G, I, device)
     res["decode_stack"] = run_stack(G, I, device)
     res["many_tokens"] = run_many_tokens(G, I, device)
     return res
