@@ -282,7 +282,8 @@ def gdn_prefill_chunked(q, k, v, a, b, A_log, dt_bias, pool: GDNStatePool, cu_se
                         keep_in_place: bool = False) -> torch.Tensor:
     """gdn_prefill's operation in chunks of 64 tokens on the tensor cores
     (dk = dv = 128): the same arguments and slot semantics, results within
-    about 1e-5 relative of gdn_prefill instead of bit-identical."""
+    about 1e-5 relative of gdn_prefill instead of bit-identical.  Its
+    activations must be device memory."""
     T, nseq = _prefill_checks(q, k, v, a, b, A_log, dt_bias, pool, cu_seqlens, read_slot)
     dt, dev = q.dtype, pool.tensor.device
     if write_slot is not None:
@@ -291,12 +292,12 @@ def gdn_prefill_chunked(q, k, v, a, b, A_log, dt_bias, pool: GDNStatePool, cu_se
         out = torch.empty((T, pool.hv, pool.dv), dtype=dt, device=dev)
     _numel(out, T * pool.hv * pool.dv, "out")
     _check(_lib.load().gdn_prefill_chunked(
-        _ptr(q, "q", dt, dev, host_ok=True), _ptr(k, "k", dt, dev, host_ok=True),
-        _ptr(v, "v", dt, dev, host_ok=True), _ptr(a, "a", dt, dev, host_ok=True),
-        _ptr(b, "b", dt, dev, host_ok=True), _ptr(A_log, "A_log", torch.float32, dev),
+        _ptr(q, "q", dt, dev), _ptr(k, "k", dt, dev),
+        _ptr(v, "v", dt, dev), _ptr(a, "a", dt, dev),
+        _ptr(b, "b", dt, dev), _ptr(A_log, "A_log", torch.float32, dev),
         _ptr(dt_bias, "dt_bias", torch.float32, dev), pool.handle,
         _ptr(cu_seqlens, "cu_seqlens", torch.int32, dev), _ptr(read_slot, "read_slot", torch.int32, dev),
-        _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev, host_ok=True), nseq, T,
+        _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev), nseq, T,
         int(bool(keep_in_place)), _dtype_code(dt), _stream(dev)))
     return out
 

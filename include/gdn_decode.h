@@ -34,7 +34,7 @@
  *    device's address space (cudaHostAlloc, or pinned memory under unified
  *    addressing): the kernels then read and write it across the host link,
  *    with no separate copy.  Pools, slot tables, taps, A_log and dt_bias are
- *    device memory.
+ *    device memory, and so are gdn_prefill_chunked's activations.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Compute
  *    calls only enqueue work: no host synchronisation and no allocation.  The
  *    first call on a device looks up the library's device error word, so

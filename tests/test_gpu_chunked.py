@@ -186,3 +186,30 @@ def test_chunked_long_sequence_close_to_exact(gdn):
             assert err <= 1e-4, f"slot {sl} head {h}: {err:.3g}"
     assert_out_close(f64(out), f64(ref), "bf16")
     assert gdn.get_device_error() == 0
+
+
+def test_chunked_graph_replay_equals_eager(gdn):
+    """A captured gdn_prefill_chunked (twin) replays to the eager launch's
+    outputs and states, bit for bit (the call enqueues only device work)."""
+    s = I.QWEN_08B
+    c = Case(gdn, s, [130, 64, 7], seed=97, n_pad=0, token_slots=False)
+    out = torch.empty((c.T, s.hv, s.dv), dtype=torch.bfloat16, device="cuda")
+    chunked(c, out=out)
+    torch.cuda.synchronize()
+    want_out, want_pool = out.clone(), c.pool.tensor.clone()
+    c.reset()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            chunked(c, out=out)
+    torch.cuda.current_stream().wait_stream(side)
+    c.reset()
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, want_out)
+    assert torch.equal(c.pool.tensor, want_pool)
+    assert gdn.get_device_error() == 0
