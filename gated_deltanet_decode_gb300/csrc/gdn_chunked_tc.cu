@@ -34,6 +34,11 @@
 // [K|Q] K^T (rows 0-63: K K^T, 64-127: Q K^T) is itself one M = 128 product
 // with both operands in shared memory; one thread a row turns it into A
 // (fp32) and P (head and tail) with the gates, the norms and the masks.
+//
+// The next chunk's raw q, k, v are copied into a staging area (cp.async)
+// while the current chunk's products run.  Every mbarrier wait is bounded:
+// one that runs out reports GDN_DEVERR_TIMEOUT, and the CTA stops without
+// writing outputs or state, frees its tensor memory and returns.
 #include <atomic>
 
 #include "gdn_chunk_common.cuh"
