@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "gdn_device.cuh"
+
 namespace gdn {
 namespace {
 
@@ -164,6 +166,42 @@ template <> __device__ __forceinline__ void store2<bf16>(bf16 *p, float x, float
 }
 
 constexpr float kEps = 1e-6f; // L2-norm epsilon, as in the decode kernels
+
+// ---------------------------------------------------------------------------
+// A chunk's gates, by one warp (tokens lane and lane + 32 of the nn live
+// ones; zero past them): into G = [running sum of log alpha | beta | e^G |
+// e^{G_C - G}] x CK, with alpha = exp(-rate softplus(a + dt_bias)) taken in
+// log form and beta = sigmoid(b).
+// ---------------------------------------------------------------------------
+template <typename TA>
+__device__ __forceinline__ void chunk_gates(float *G, const TA (&ra)[2], const TA (&rb)[2], int nn, float rate,
+                                            float dtb, int lane)
+{
+    float la[2], bt[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int tt = lane + 32 * i;
+        la[i] = 0.f, bt[i] = 0.f;
+        if (tt < nn) {
+            la[i] = rate == 0.f ? 0.f : -rate * softplus_f(to_f(ra[i]) + dtb);
+            bt[i] = gate_beta(to_f(rb[i]));
+        }
+    }
+    float s0 = la[0], s1 = la[1];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float x0 = __shfl_up_sync(0xffffffffu, s0, o);
+        const float x1 = __shfl_up_sync(0xffffffffu, s1, o);
+        if (lane >= o)
+            s0 += x0, s1 += x1;
+    }
+    s1 += __shfl_sync(0xffffffffu, s0, 31);
+    const float gc = __shfl_sync(0xffffffffu, s1, 31);
+    G[lane] = s0, G[lane + 32] = s1;
+    G[CK + lane] = bt[0], G[CK + lane + 32] = bt[1];
+    G[2 * CK + lane] = expf(s0), G[2 * CK + lane + 32] = expf(s1);
+    G[3 * CK + lane] = expf(gc - s0), G[3 * CK + lane + 32] = expf(gc - s1);
+}
 
 // ---------------------------------------------------------------------------
 // T = (I + A)^{-1} for the chunk's strictly lower A (fp32 [CK][LDF] in AF):

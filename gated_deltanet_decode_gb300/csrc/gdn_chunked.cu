@@ -173,32 +173,7 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
     // the gates of the chunk starting at cn from ra, rb (warp 2): log alpha,
     // beta, running sums (zero past the chunk's tokens), into set `set`
     auto gates = [&](int cn, int set) {
-        const int nn = min(CK, L - cn);
-        float *const G = GATES + set * 4 * CK;
-        float la[2], bt[2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int tt = lane + 32 * i;
-            la[i] = 0.f, bt[i] = 0.f;
-            if (tt < nn) {
-                la[i] = rate == 0.f ? 0.f : -rate * softplus_f(to_f(ra[i]) + dtb);
-                bt[i] = gate_beta(to_f(rb[i]));
-            }
-        }
-        float s0 = la[0], s1 = la[1];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float x0 = __shfl_up_sync(0xffffffffu, s0, o);
-            const float x1 = __shfl_up_sync(0xffffffffu, s1, o);
-            if (lane >= o)
-                s0 += x0, s1 += x1;
-        }
-        s1 += __shfl_sync(0xffffffffu, s0, 31);
-        const float gc = __shfl_sync(0xffffffffu, s1, 31);
-        G[lane] = s0, G[lane + 32] = s1;
-        G[CK + lane] = bt[0], G[CK + lane + 32] = bt[1];
-        G[2 * CK + lane] = expf(s0), G[2 * CK + lane + 32] = expf(s1);
-        G[3 * CK + lane] = expf(gc - s0), G[3 * CK + lane + 32] = expf(gc - s1);
+        chunk_gates(GATES + set * 4 * CK, ra, rb, min(CK, L - cn), rate, dtb, lane);
     };
     if (L > 0) {
         if (warp == 2) {
