@@ -169,24 +169,6 @@ __device__ __forceinline__ void split32(const float (&v)[32], uint32_t (&hi)[16]
         split2(v[2 * j], v[2 * j + 1], hi[j], lo[j]);
 }
 
-// A fragment (mma.sync) of rows m0.., columns k0.. of a canonical tile with K columns
-template <int K>
-__device__ __forceinline__ void lda_cm(uint32_t (&a)[4], const unsigned char *X, int m0, int k0, int g, int c)
-{
-    a[0] = *reinterpret_cast<const uint32_t *>(X + cm_off<K>(m0 + g, k0 + 2 * c));
-    a[1] = *reinterpret_cast<const uint32_t *>(X + cm_off<K>(m0 + g + 8, k0 + 2 * c));
-    a[2] = *reinterpret_cast<const uint32_t *>(X + cm_off<K>(m0 + g, k0 + 2 * c + 8));
-    a[3] = *reinterpret_cast<const uint32_t *>(X + cm_off<K>(m0 + g + 8, k0 + 2 * c + 8));
-}
-// B fragment with B[k][n] = X[n][k] of a canonical tile with K columns
-template <int K>
-__device__ __forceinline__ void ldb_cm(uint32_t &b0, uint32_t &b1, const unsigned char *X, int n0, int k0, int g,
-                                       int c)
-{
-    b0 = *reinterpret_cast<const uint32_t *>(X + cm_off<K>(n0 + g, k0 + 2 * c));
-    b1 = *reinterpret_cast<const uint32_t *>(X + cm_off<K>(n0 + g, k0 + 2 * c + 8));
-}
-
 __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const PrefillArgs p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
