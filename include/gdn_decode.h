@@ -204,7 +204,10 @@ int gdn_decode_step(const void *q, const void *k, const void *v, const void *a, 
 
 /* ---- gdn_layer_decode -------------------------------------------------- *
  * causal_conv1d_decode (SiLU on when silu != 0) followed by gdn_decode_step,
- * in one kernel.  x is [rows][C], C = 2*hk*dk + hv*dv packed [q | k | v],
+ * in one kernel.  The pages run the two as separate kernels ("mstar PR
+ * #1139", "What changed": the decode conv as a kernel of its own beside the
+ * GDN decode wrapper); this fusion is the library's own, with the same
+ * values as the pair.  x is [rows][C], C = 2*hk*dk + hv*dv packed [q | k | v],
  * head-major; the conv pool must have C channels.  Both pools use the same
  * read/write slots.  The conv output is rounded to the activation dtype
  * before the rule, exactly as between the two separate calls, so the result
