@@ -1,5 +1,6 @@
-"""Host logic of the multi-rank benchmark, on CPU with gloo: every rank
-reports the slowest rank's time (world size 2)."""
+"""Host logic of the benchmark on CPU: every rank of a gloo run reports the
+slowest rank's time (world size 2); the byte model; the traffic record's
+source hash; the reference arm's JSON line and its rank handling."""
 import os
 import socket
 
@@ -87,3 +88,36 @@ def test_kernel_hash_follows_code_not_comments(tmp_path, monkeypatch):
     assert bench.kernel_source_sha() == h0
     first.write_text(text.replace("kMaxStages = 8", "kMaxStages = 7"))
     assert bench.kernel_source_sha() != h0
+
+
+def _run_reference(env_extra):
+    import json
+    import subprocess
+    import sys
+    env = dict(os.environ, **env_extra)
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2", "--warmup", "3"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    return [json.loads(ln) for ln in lines]
+
+
+def test_reference_arm_line():
+    """The reference arm (the oracle on the host cores) prints one line with
+    the same metric keys as the CUDA arm, its own CPU baseline and an
+    end-to-end figure with no host-device traffic."""
+    (line,) = _run_reference({"RANK": "0", "WORLD_SIZE": "1"})
+    assert line["impl"] == "reference"
+    assert line["n_gpus"] == 1 and line["steps"] == 2 and line["warmup"] == 3
+    assert line["value"] > 0 and line["unit"] == "GB/s" and line["higher_is_better"] is True
+    assert line["config"]["workload"] and line["dtype"] == "f64" and line["data"] == "synthetic"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == line["value"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_other_ranks_do_no_work():
+    """Under a multi-rank launch only rank 0 runs and prints the oracle."""
+    assert _run_reference({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == []
