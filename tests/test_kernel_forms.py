@@ -1,7 +1,15 @@
-"""The chunked regrouping of the gated delta rule, checked in fp64 against the
-oracle's token-serial rule, on CPU.
+"""The rearranged forms the kernels compute, restated in fp64 and held
+against the oracle's rule, on CPU.
 
-The pages name a chunked GDN path ("mstar PR #965", "Correctness"; "mstar PR
+Decode step ("mstar PR #1139", "Why": the recurrent state update of one
+token).  Each value row i of the state is updated on its own from two dot
+products of the row, u_i = S_i·k̂ and w_i = S_i·q̂, and κ = k̂·q̂:
+
+    c_i = β (v_i - α u_i),   S'_i = α S_i + c_i k̂,   o_i = α w_i + c_i κ
+
+which is S' = α S (I - β k̂ k̂ᵀ) + β v k̂ᵀ and o = S' q̂.
+
+Chunked prefill.  The pages name a chunked GDN path ("mstar PR #965", "Correctness"; "mstar PR
 #1127": one GDN prefill kernel) but print no formula.  The tensor-core
 prefill uses this regrouping, derived from the recurrence
 S_t = α_t S_{t-1} + u_t k̂_tᵀ, u_t = β_t (v_t - α_t S_{t-1} k̂_t).  With G the
@@ -23,6 +31,25 @@ import numpy as np
 import pytest
 
 import oracle
+
+
+def test_decode_row_form_equals_the_rule():
+    """The decode kernels' per-row form against the oracle's literal matrix
+    form, on random heads, including the edge gates α = 1 and β = 0 or 1."""
+    rng = np.random.default_rng(5)
+    dk, dv = 16, 12
+    for al, be in [(0.83, 0.37), (1.0, 0.0), (1.0, 1.0), (0.05, 0.99)]:
+        S = rng.normal(0.0, 0.5, (dv, dk))
+        qh = oracle.l2norm(rng.normal(0.0, 1.0, dk), scale=dk ** -0.5)
+        kh = oracle.l2norm(rng.normal(0.0, 1.0, dk))
+        v = rng.normal(0.0, 1.0, dv)
+        S_ref, o_ref = oracle.rule(S, qh, kh, v, al, be)
+        u, w, kappa = S @ kh, S @ qh, kh @ qh
+        c = be * (v - al * u)
+        S_new = al * S + np.outer(c, kh)
+        o = al * w + c * kappa
+        assert np.abs(S_new - S_ref).max() <= 1e-14 * max(1.0, np.abs(S_ref).max())
+        assert np.abs(o - o_ref).max() <= 1e-14 * max(1.0, np.abs(o_ref).max())
 
 HK, HV, DK, DV = 2, 4, 8, 6          # two value heads a qk head
 LENS = [9, 16, 1, 0, 13]
