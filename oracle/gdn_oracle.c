@@ -57,7 +57,9 @@ double gdn_oracle_softplus(double x)
     return log1p(exp(x));
 }
 
-/* Decay gate: alpha = exp(-exp(A_log) * softplus(a + dt_bias)). */
+/* Decay gate: alpha = exp(-exp(A_log) * softplus(a + dt_bias)).  The pages
+ * name the gates of the rule ("mstar PR #1139", "Why") but print no formula;
+ * this is the standard Gated DeltaNet decay. */
 double gdn_oracle_alpha(double A_log, double a, double dt_bias)
 {
     double decay_rate = exp(A_log);
@@ -68,7 +70,8 @@ double gdn_oracle_alpha(double A_log, double a, double dt_bias)
     return exp(-g);
 }
 
-/* Write strength: beta = sigmoid(b) = 1 / (1 + e^-b). */
+/* Write strength: beta = sigmoid(b) = 1 / (1 + e^-b) (standard Gated
+ * DeltaNet, as for alpha). */
 double gdn_oracle_beta(double b)
 {
     return 1.0 / (1.0 + exp(-b));
@@ -135,7 +138,9 @@ void gdn_oracle_l2norm(const double *x, int n, double eps, double scale, double 
  *   M      = I - beta * khat khat^T             (dk x dk)
  *   S_new  = alpha * (S M) + beta * v khat^T     (dv x dk)
  *   o      = S_new qhat                          (dv)
- * S_new may not alias S.
+ * S_new may not alias S.  The rule the pages name ("mstar PR #1139", "Why":
+ * the recurrent state update of one token), in the standard gated delta
+ * form stated at the top of this file.
  */
 void gdn_oracle_rule(int dk, int dv, const double *S, const double *qhat, const double *khat,
                      const double *v, double alpha, double beta, double *S_new, double *o)
@@ -195,7 +200,10 @@ void gdn_oracle_head(int dk, int dv, const double *S, const double *q, const dou
  * [0, num_slots), a twin write to slot 0, or a twin write slot equal to the
  * read slot (a twin step writes the other slot) makes the row count as bad:
  * its output is zero and nothing is written.  Returns the number of bad rows.
- * Rows must name distinct slots (a precondition of the method).
+ * Rows must name distinct slots (a precondition of the method).  Twin slots
+ * follow "mstar PR #1139", "What changed" (read one slot, write the other);
+ * padding on slot 0 follows "mstar PR #1127" and "mstar PR #965", "What
+ * changed" (padding rows address only the null slot, which stays zero).
  */
 int gdn_oracle_step(int rows, int hk, int hv, int dk, int dv, int num_slots,
                     const double *q, const double *k, const double *v,
@@ -261,6 +269,8 @@ int gdn_oracle_step(int rows, int hk, int hv, int dk, int dv, int num_slots,
  *   pre[c]  = bias[c] + sum_{j<W-1} w[c][j] * win[j][c] + w[c][W-1] * x[c]
  *   y[c]    = silu(pre[c]) = pre / (1 + e^-pre)   (or pre itself when silu == 0)
  *   new_win = [win[1], ..., win[W-2], x]
+ * The conv-state update for one token ("mstar PR #1139", "What changed":
+ * causal_conv1d_decode, with optional bias and activation).
  */
 void gdn_oracle_conv_row(int C, int W, const double *win, const double *x, const double *w,
                          const double *bias, int silu, double *y, double *new_win)
@@ -284,7 +294,8 @@ void gdn_oracle_conv_row(int C, int W, const double *win, const double *x, const
  * x: [rows][C], y: [rows][C].  write_slot == NULL means in place.
  * Padding rows (read slot 0) give y = 0 and touch no slot.  Bad slots as in
  * gdn_oracle_step (with a write slot given, it must differ from the read
- * slot).  Returns the number of bad rows.
+ * slot).  Returns the number of bad rows.  The write slot follows "mstar PR
+ * #1139", "What changed" (the decode conv with a write slot).
  */
 int gdn_oracle_conv_step(int rows, int C, int W, int num_slots, const double *x,
                          double *conv_pool, const int32_t *read_slot, const int32_t *write_slot,
@@ -322,7 +333,9 @@ int gdn_oracle_conv_step(int rows, int C, int W, int num_slots, const double *x,
  * The conv output is rounded to the activation type (act_bf16 = 1: bfloat16,
  * 0: binary32), as it would be when stored between two separate kernels,
  * then split into q, k, v and fed to the decode step.  Both pools use the
- * same read and write slots.  Returns the number of bad rows.
+ * same read and write slots.  Returns the number of bad rows.  The pages run
+ * the conv and the rule as separate kernels ("mstar PR #1139", "What
+ * changed"); this is that composition, step by step.
  */
 int gdn_oracle_layer(int rows, int hk, int hv, int dk, int dv, int W, int num_slots,
                      const double *x, double *conv_pool, const double *w, const double *bias,
@@ -522,7 +535,8 @@ int gdn_oracle_copy_slots(int num_slots, long slot_elems, double *pool, const in
     return bad;
 }
 
-/* Commit of a twin step: the read and write slot of every row trade places. */
+/* Commit of a twin step: the read and write slot of every row trade places
+ * ("mstar PR #1139", "What changed": commit swaps the two slots). */
 void gdn_oracle_commit(int rows, int32_t *read_slot, int32_t *write_slot)
 {
     for (int r = 0; r < rows; ++r) {
