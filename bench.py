@@ -13,6 +13,10 @@ Prints one JSON line: whole-job GB/s of algorithmic bytes, µs per layer,
 the roofline of the layer kernel, an end-to-end figure through host buffers,
 the clocks seen during the timed region and the fp64 oracle timed on the
 host cores.  `--impl reference` times the oracle itself on the same workload.
+
+The traffic probes (the same state reads and writes with no arithmetic,
+read-only and write-only) follow the pages' own roofline measurement of the
+step ("mstar PR #1139", "Numbers").
 """
 from __future__ import annotations
 

@@ -10,6 +10,10 @@ decode path runs in the library's CUDA kernels.  The names follow the C ABI
   gdn_decode_step                gated delta rule per row and value head
   gdn_layer_decode               both in one kernel
   gdn_commit                     twin-slot commit (swap read/write slots)
+
+The operation is the decode step of "mstar PR #1139" ("Why": the GDN rule is
+the recurrent state update of one token a row; "What changed": twin slots,
+the decode-only conv), with padding on the null slot of "mstar PR #1127".
 """
 from __future__ import annotations
 

@@ -1,6 +1,10 @@
 // C ABI of the GDN decode library: argument checks, pools, the sticky device
 // error word, and the small kernels (commit, slot zeroing, traffic probes).
-// The heavy kernels live in gdn_stream.cu and gdn_conv.cu.
+// The heavy kernels live in gdn_stream.cu and gdn_conv.cu.  The pools follow
+// "mstar PR #1139", "What changed" (a request holds two state slots; a decode
+// step reads one and writes the other; commit swaps them; release and
+// rollback zero both, "Tests") and "mstar PR #1127", "What changed" (padding
+// rows sit on slot 0, which stays zero).
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>

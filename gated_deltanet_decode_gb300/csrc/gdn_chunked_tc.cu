@@ -1,5 +1,8 @@
 // The chunked gated delta rule with the state in tensor memory: the
-// tcgen05 form of gdn_prefill_chunked for bf16 activations.
+// tcgen05 form of gdn_prefill_chunked for bf16 activations.  The pages name
+// the chunked GDN path, check the mixed step against it ("mstar PR #965",
+// "Correctness") and run prefill as one GDN kernel ("mstar PR #1127"); they
+// print no formula, so the regrouping below is derived from the recurrence.
 //
 // The operation, the regrouping over chunks of 64 tokens and the split
 // products are those of gdn_chunked.cu (whose header states the algebra):

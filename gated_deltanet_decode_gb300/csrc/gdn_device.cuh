@@ -122,8 +122,10 @@ __device__ __forceinline__ void report(int *err, int code)
 
 // Row classification shared by every slot-indexed kernel.
 //   0 = padding (read slot 0), 1 = real, -1 = bad (reported by the caller).
-// A twin step writes the request's other slot, so a twin write slot equal to
-// the read slot is bad.
+// Padding rows address only the null slot and leave it untouched ("mstar PR
+// #965" and "mstar PR #1127", "What changed").  A twin step writes the
+// request's other slot ("mstar PR #1139", "What changed"), so a twin write
+// slot equal to the read slot is bad.
 __device__ __forceinline__ int classify_row(int rs, int ws, int num_slots, bool in_place)
 {
     if (rs == 0)
