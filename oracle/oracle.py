@@ -7,7 +7,10 @@ path; arrays go in and out as float64 numpy arrays (int32 for slot tables).
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 against closed forms, special cases, a hand-worked example
 (``tests/golden/rule_2x2.json``), an unrolled product of transition matrices
-and brute force on tiny inputs; ``prefill`` and ``conv_prefill`` by
+and brute force on tiny inputs; ``layer``'s composition (the conv output
+rounded to the activation type by construction-known values and hand-worked
+ties, the SiLU forwarded through closed forms, the window written to the slot
+its state goes to) by the layer pins there; ``prefill`` and ``conv_prefill`` by
 ``tests/test_oracle_prefill_pins.py`` (the unrolled product per token, the
 pinned one-token step token by token, numpy's convolution).  Planted mistakes
 in ``tests/test_oracle_mutations.py`` show the pins are sharp.

@@ -40,6 +40,13 @@ MUTATIONS = {
     "prefill_twin_writes_read_slot": ("int ws = write_slot ? write_slot[r] : rs;", "int ws = rs;"),
     "conv_prefill_window_not_carried": ("memcpy(win, new_win, sizeof(double) * slot_elems);", ""),
     "copy_slots_may_write_null": ("dst[i] <= 0 || dst[i] >= num_slots", "dst[i] < 0 || dst[i] >= num_slots"),
+    # the layer's composition: rounding, activation forwarding, in-place window
+    "layer_rounding_dropped": ("y[(size_t)r * C + c] = act_bf16 ? gdn_oracle_round_bf16(t) : gdn_oracle_round_f32(t);",
+                               "y[(size_t)r * C + c] = t;"),
+    "layer_silu_not_forwarded": ("keep_in_place ? NULL : write_slot, w, bias, silu, y);",
+                                 "keep_in_place ? NULL : write_slot, w, bias, 0, y);"),
+    "layer_window_to_twin_in_place": ("keep_in_place ? NULL : write_slot, w, bias, silu, y);",
+                                      "write_slot, w, bias, silu, y);"),
     "copy_slots_reversed": ("pool[(size_t)dst[i] * slot_elems + e] = pool[(size_t)src[i] * slot_elems + e];",
                             "pool[(size_t)src[i] * slot_elems + e] = pool[(size_t)dst[i] * slot_elems + e];"),
 }

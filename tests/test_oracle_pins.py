@@ -443,3 +443,166 @@ def test_layer_identity_conv_reduces_to_step(orc):
     p2 = pool.copy()
     o2, _ = orc.step(q, k, v, a, b, A_log, dt_bias, p2, rs, ws)
     assert np.array_equal(o1, o2) and np.array_equal(p1, p2)
+
+
+# --------------------------------------------------------------------------
+# the layer's composition: conv, rounding to the activation type, split, rule
+# ("mstar PR #1139", "What changed": the decode conv, with its optional
+# activation and its write slot, runs ahead of the GDN decode kernel)
+# --------------------------------------------------------------------------
+
+def _layer_case(rng, rows=3, hk=2, hv=4, dk=8, dv=8, W=4):
+    C = 2 * hk * dk + hv * dv
+    pool, _, _, _, a, b, A_log, dt_bias = _pool_case(rng, rows=rows, hk=hk, hv=hv, dk=dk, dv=dv)
+    cp = rng.standard_normal((pool.shape[0], W - 1, C))
+    cp[0] = 0.0
+    w = np.zeros((C, W))
+    w[:, W - 1] = 1.0                                   # identity taps: y = x before the activation
+    return C, pool, cp, w, a, b, A_log, dt_bias
+
+
+def _split(y, hk, hv, dk, dv):
+    rows = y.shape[0]
+    return (y[:, :hk * dk].reshape(rows, hk, dk), y[:, hk * dk:2 * hk * dk].reshape(rows, hk, dk),
+            y[:, 2 * hk * dk:].reshape(rows, hv, dv))
+
+
+def _bf16_grid_values(rng, shape):
+    """Values with 8 significant bits (m * 2^(e-7), m in 129..255) and offsets of
+    under 0.45 of their spacing: each rounds to the nearest bfloat16 value m * 2^(e-7)
+    by construction, with no rounding routine involved."""
+    m = rng.integers(129, 256, size=shape).astype(np.float64)
+    e = rng.integers(-3, 3, size=shape)
+    sign = np.where(rng.random(shape) < 0.5, -1.0, 1.0)
+    spacing = np.ldexp(1.0, e - 7)
+    exact = sign * m * spacing
+    off = rng.uniform(-0.45, 0.45, size=shape) * spacing
+    off[np.abs(off) < 0.05 * spacing] = 0.25 * spacing[np.abs(off) < 0.05 * spacing]
+    return exact, exact + off
+
+
+def test_layer_rounds_the_conv_output_to_bf16(orc):
+    """act_bf16: the conv output is rounded to bfloat16 before the rule.  With
+    identity taps the layer must equal the step on the bfloat16 values the inputs
+    round to (known by construction, plus hand-worked ties to even), and must
+    differ from the step on the unrounded inputs."""
+    rng = np.random.default_rng(41)
+    hk, hv, dk, dv = 2, 4, 8, 8
+    rows = 3
+    C, pool, cp, w, a, b, A_log, dt_bias = _layer_case(rng, rows=rows, hk=hk, hv=hv, dk=dk, dv=dv)
+    exact, x = _bf16_grid_values(rng, (rows, C))
+    # hand-worked ties (bfloat16 spacing in [1, 2) is 2^-7): 1 + 2^-8 lies halfway
+    # between 1 and 1 + 2^-7 and goes to the even 1; 1 + 3*2^-8 lies halfway between
+    # 1 + 2^-7 and 1 + 2^-6 and goes to the even 1 + 2^-6; 1 + 2^-9 is below halfway
+    x[0, :3] = [1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, 1 + 2.0 ** -9]
+    exact[0, :3] = [1.0, 1 + 2.0 ** -6, 1.0]
+    rs = np.array([1, 0, 2], dtype=np.int32)
+    ws = np.array([3, 0, 4], dtype=np.int32)
+    p1 = pool.copy()
+    o1, bad = orc.layer(x, cp.copy(), w, None, a, b, A_log, dt_bias, p1, rs, ws, hk=hk,
+                        act_bf16=True, silu=False)
+    assert bad == 0
+    q, k, v = _split(exact, hk, hv, dk, dv)
+    p2 = pool.copy()
+    o2, _ = orc.step(q, k, v, a, b, A_log, dt_bias, p2, rs, ws)
+    assert np.array_equal(o1, o2) and np.array_equal(p1, p2)
+    q, k, v = _split(x, hk, hv, dk, dv)
+    p3 = pool.copy()
+    o3, _ = orc.step(q, k, v, a, b, A_log, dt_bias, p3, rs, ws)
+    assert not np.allclose(o1[[0, 2]], o3[[0, 2]], atol=1e-6, rtol=0)
+    assert not np.allclose(p1, p3, atol=1e-7, rtol=0)
+
+
+def test_layer_rounds_the_conv_output_to_f32(orc):
+    """Without act_bf16 the conv output is rounded to binary32 (numpy's cast)."""
+    rng = np.random.default_rng(42)
+    hk, hv, dk, dv = 1, 2, 8, 8
+    rows = 2
+    C, pool, cp, w, a, b, A_log, dt_bias = _layer_case(rng, rows=rows, hk=hk, hv=hv, dk=dk, dv=dv)
+    x = rng.standard_normal((rows, C)) * (1 + 2.0 ** -30)     # not binary32 values
+    x32 = x.astype(np.float32).astype(np.float64)
+    assert not np.array_equal(x, x32)
+    rs = np.array([1, 2], dtype=np.int32)
+    ws = np.array([3, 4], dtype=np.int32)
+    p1 = pool.copy()
+    o1, _ = orc.layer(x, cp.copy(), w, None, a, b, A_log, dt_bias, p1, rs, ws, hk=hk,
+                      act_bf16=False, silu=False)
+    q, k, v = _split(x32, hk, hv, dk, dv)
+    p2 = pool.copy()
+    o2, _ = orc.step(q, k, v, a, b, A_log, dt_bias, p2, rs, ws)
+    assert np.array_equal(o1, o2) and np.array_equal(p1, p2)
+
+
+def test_layer_forwards_silu(orc):
+    """layer(silu=True) applies SiLU before the rounding and the rule.  With
+    identity taps and x = ln m, SiLU gives the closed form ln(m) * m / (m + 1)
+    (silu(ln 3) = 3/4 ln 3); rounded to binary32 (numpy) and to bfloat16 (torch)
+    it must feed the step exactly."""
+    rng = np.random.default_rng(43)
+    hk, hv, dk, dv = 2, 2, 8, 8
+    rows = 2
+    C, pool, cp, w, a, b, A_log, dt_bias = _layer_case(rng, rows=rows, hk=hk, hv=hv, dk=dk, dv=dv)
+    m = rng.uniform(0.05, 20.0, size=(rows, C))
+    m[0, 0] = 3.0
+    x = np.log(m)
+    silu = x * m / (m + 1.0)
+    assert silu[0, 0] == pytest.approx(0.75 * math.log(3.0), abs=1e-15)
+    rs = np.array([1, 2], dtype=np.int32)
+    ws = np.array([3, 4], dtype=np.int32)
+    # binary32 activations
+    p1 = pool.copy()
+    o1, _ = orc.layer(x, cp.copy(), w, None, a, b, A_log, dt_bias, p1, rs, ws, hk=hk,
+                      act_bf16=False, silu=True)
+    y32 = silu.astype(np.float32).astype(np.float64)
+    # the closed form and exp-based SiLU may differ in the last fp64 bits, which can
+    # move a binary32 rounding only when the value sits on a midpoint: none here
+    mid = np.abs(silu - y32) / np.maximum(np.abs(y32), 1e-300)
+    assert np.all(np.abs(mid - 2.0 ** -24) > 1e-12)
+    q, k, v = _split(y32, hk, hv, dk, dv)
+    p2 = pool.copy()
+    o2, _ = orc.step(q, k, v, a, b, A_log, dt_bias, p2, rs, ws)
+    assert np.array_equal(o1, o2) and np.array_equal(p1, p2)
+    # and without the activation the result differs
+    p3 = pool.copy()
+    o3, _ = orc.layer(x, cp.copy(), w, None, a, b, A_log, dt_bias, p3, rs, ws, hk=hk,
+                      act_bf16=False, silu=False)
+    assert not np.allclose(o1, o3, atol=1e-6, rtol=0)
+    # bfloat16 activations (torch's round-to-nearest-even of the binary32 value;
+    # the binary32 value is itself exact to 2^-24, far inside a bfloat16 spacing)
+    torch = pytest.importorskip("torch")
+    ybf = torch.from_numpy(y32).to(torch.bfloat16).to(torch.float64).numpy()
+    p4 = pool.copy()
+    o4, _ = orc.layer(x, cp.copy(), w, None, a, b, A_log, dt_bias, p4, rs, ws, hk=hk,
+                      act_bf16=True, silu=True)
+    q, k, v = _split(ybf, hk, hv, dk, dv)
+    p5 = pool.copy()
+    o5, _ = orc.step(q, k, v, a, b, A_log, dt_bias, p5, rs, ws)
+    assert np.array_equal(o4, o5) and np.array_equal(p4, p5)
+
+
+@pytest.mark.parametrize("keep_in_place", [False, True])
+def test_layer_conv_window_goes_to_the_written_slot(orc, keep_in_place):
+    """The layer's conv window follows its state: twin writes the new window
+    [win[1], win[2], x] to the write slot and leaves the read slot alone; in
+    place writes it back to the read slot and leaves the write slot alone."""
+    rng = np.random.default_rng(44)
+    hk, hv, dk, dv = 1, 2, 8, 8
+    rows = 3
+    C, pool, cp, w, a, b, A_log, dt_bias = _layer_case(rng, rows=rows, hk=hk, hv=hv, dk=dk, dv=dv)
+    w = rng.standard_normal(w.shape) * 0.5              # any taps: the window is a plain copy
+    x = rng.standard_normal((rows, C))
+    rs = np.array([1, 0, 2], dtype=np.int32)
+    ws = np.array([3, 0, 4], dtype=np.int32)
+    c1 = cp.copy()
+    p1 = pool.copy()
+    orc.layer(x, c1, w, None, a, b, A_log, dt_bias, p1, rs, ws, hk=hk,
+              keep_in_place=keep_in_place, act_bf16=False, silu=True)
+    for r in (0, 2):
+        new_win = np.concatenate([cp[rs[r], 1:], x[r][None]], axis=0)
+        dst, other = (rs[r], ws[r]) if keep_in_place else (ws[r], rs[r])
+        assert np.array_equal(c1[dst], new_win)
+        assert np.array_equal(c1[other], cp[other])
+        assert not np.array_equal(p1[dst], pool[dst])
+        assert np.array_equal(p1[other], pool[other])
+    for s in (0, 5, 6):
+        assert np.array_equal(c1[s], cp[s]) and np.array_equal(p1[s], pool[s])
