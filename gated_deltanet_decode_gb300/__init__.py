@@ -23,8 +23,8 @@ from typing import Optional
 import torch
 
 from . import _lib
-from ._lib import (GDN_BF16, GDN_DEVERR_BAD_SLOT, GDN_DEVERR_NONE, GDN_F32, GDN_PROBE_INPLACE,
-                   GDN_PROBE_READ, GDN_PROBE_TWIN, GDN_PROBE_WRITE, gdn_dims)
+from ._lib import (GDN_BF16, GDN_DEVERR_BAD_SLOT, GDN_DEVERR_NONE, GDN_F32, GDN_NOALLOC_SCRATCH_SLOTS,
+                   GDN_PROBE_INPLACE, GDN_PROBE_READ, GDN_PROBE_TWIN, GDN_PROBE_WRITE, gdn_dims)
 
 __all__ = [
     "GDNError", "load", "lib_path", "GDNStatePool", "ConvStatePool", "causal_conv1d_decode",
@@ -32,7 +32,7 @@ __all__ = [
     "gdn_prefill", "gdn_prefill_chunked", "gdn_verify", "causal_conv1d_prefill", "gdn_layer_decode_bucket",
     "get_device_error", "probe_traffic", "GDN_F32", "GDN_BF16", "GDN_DEVERR_NONE",
     "GDN_DEVERR_BAD_SLOT", "GDN_PROBE_TWIN", "GDN_PROBE_INPLACE", "GDN_PROBE_READ",
-    "GDN_PROBE_WRITE",
+    "GDN_PROBE_WRITE", "GDN_NOALLOC_SCRATCH_SLOTS",
 ]
 
 

@@ -304,12 +304,20 @@ int gdn_layer_decode_bucket(const void *x, conv_pool *cp, const void *w, const v
 /* ---- gdn_layer_decode_noalloc ------------------------------------------ *
  * gdn_layer_decode for callers that cannot allocate device memory; the pages
  * have no counterpart (it is an interface matter, not part of the method).
+ * Such callers are, for example, engines that reserve all device memory up
+ * front for their own allocator and forbid cudaMalloc elsewhere, and paths
+ * where cudaMalloc's implicit device-wide synchronisation would stall other
+ * streams.
  * Same arguments, checks and results, bit for bit, as gdn_layer_decode, plus
  * scratch_slot.  The call allocates nothing (no cudaMalloc, no allocating
  * library routine): the kernel's scratch, two 32-bit work counters, is slot
  * `scratch_slot` of a fixed array in the library's device memory of
  * GDN_NOALLOC_SCRATCH_SLOTS slots (8 bytes each, 512 bytes in all), whose
- * device address is looked up once per device.  A slot outside
+ * device address is looked up by the first call on each device (with that
+ * device current; make that first call before any stream capture) and then
+ * cached for the life of the process: it does not survive cudaDeviceReset
+ * or a new primary context on that device, after which the call must not be
+ * used again in the process.  A slot outside
  * [0, GDN_NOALLOC_SCRATCH_SLOTS) is rejected with GDN_EINVAL.  Both counters
  * of the slot must be zero when a launch starts: the array is zero when the
  * library loads and every launch leaves its slot at zero when it ends.

@@ -96,3 +96,57 @@ def check_conv_outputs(orc, y_gpu: np.ndarray, y_exact: np.ndarray, mag: np.ndar
             f"{(~(near & adjacent)).sum()} conv outputs differ from the oracle's rounding "
             "away from a rounding midpoint")
     return flip
+
+
+def bf16_other_neighbour(y_exact: np.ndarray, ref: np.ndarray) -> np.ndarray:
+    """The bfloat16 value next to `ref` on the side of `y_exact` (ref being the
+    oracle's rounding of y_exact): the other correct rounding when y_exact sits
+    on a rounding midpoint.  Formed from the oracle's values alone."""
+    y_exact = np.asarray(y_exact, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    r32 = ref.astype(np.float32)
+    bits = r32.view(np.uint32).astype(np.int64)
+    away = (y_exact > ref) != np.signbit(r32)            # the neighbour is farther from zero
+    out = (bits + np.where(away, 0x10000, -0x10000)).astype(np.uint32).view(np.float32)
+    out = out.astype(np.float64)
+    zero = ref == 0.0
+    out[zero] = np.copysign(2.0 ** -133, y_exact[zero])
+    return out
+
+
+def oracle_layer_on_gpu_roundings(orc, y_gpu, xr, cp_ref, w64, bias64, A_log, dt_bias, pool_ref, rs, ws,
+                                  s, keep_in_place=False, silu=True):
+    """The oracle's layer (conv, rounding to the activation type, split, rule:
+    the composition gdn_oracle_layer performs) on `rows = len(rs)` rows, where
+    each bf16 rounding of the conv output is the oracle's own except at the
+    channels where the GPU's conv (y_gpu, its fp32 evaluation rounded) took the
+    other neighbour of a rounding midpoint and check_conv_outputs accepted it:
+    there the oracle uses that other neighbour, formed from its own exact value.
+    The GPU's value only selects; every input of the rule is the oracle's.
+    Updates cp_ref and pool_ref; returns (o_ref, flips)."""
+    rs = np.asarray(rs, dtype=np.int32)
+    ws = np.asarray(ws, dtype=np.int32)
+    real = rs != 0
+    mag = conv_magnitude(cp_ref[rs], xr["x"], w64, bias64)
+    y_exact, bad = orc.conv_step(xr["x"], cp_ref, rs, None if keep_in_place else ws, w64, bias64, silu=silu)
+    assert bad == 0
+    flips = np.zeros(y_exact.shape, dtype=bool)
+    if s.dtype == "bf16":
+        ref = orc.round_bf16(y_exact)
+        flips[real] = check_conv_outputs(orc, y_gpu[real], y_exact[real], mag[real], "bf16")
+        y_sel = ref.copy()
+        if flips.any():
+            y_sel[flips] = bf16_other_neighbour(y_exact[flips], ref[flips])
+        assert np.array_equal(y_sel[real], y_gpu[real])
+    else:
+        check_conv_outputs(orc, y_gpu[real], y_exact[real], mag[real], "f32")
+        y_sel = y_exact.astype(np.float32).astype(np.float64)
+    rows = y_sel.shape[0]
+    nq = s.hk * s.dk
+    q = y_sel[:, :nq].reshape(rows, s.hk, s.dk)
+    k = y_sel[:, nq:2 * nq].reshape(rows, s.hk, s.dk)
+    v = y_sel[:, 2 * nq:].reshape(rows, s.hv, s.dv)
+    o_ref, bad = orc.step(q, k, v, xr["a"], xr["b"], A_log, dt_bias, pool_ref, rs, ws,
+                          keep_in_place=keep_in_place)
+    assert bad == 0
+    return o_ref, flips
