@@ -23,15 +23,16 @@ from typing import Optional
 import torch
 
 from . import _lib
-from ._lib import (GDN_BF16, GDN_DEVERR_BAD_SLOT, GDN_DEVERR_NONE, GDN_F32, GDN_NOALLOC_SCRATCH_SLOTS,
+from ._lib import (GDN_BF16, GDN_DEVERR_BAD_SLOT, GDN_DEVERR_NONE, GDN_DEVERR_TIMEOUT, GDN_F32,
+                   GDN_NOALLOC_SCRATCH_SLOTS,
                    GDN_PROBE_INPLACE, GDN_PROBE_READ, GDN_PROBE_TWIN, GDN_PROBE_WRITE, gdn_dims)
 
 __all__ = [
     "GDNError", "load", "lib_path", "GDNStatePool", "ConvStatePool", "causal_conv1d_decode",
     "gdn_decode_step", "gdn_layer_decode", "gdn_layer_decode_noalloc", "gdn_commit", "gdn_validate_slots",
     "gdn_prefill", "gdn_prefill_chunked", "gdn_verify", "causal_conv1d_prefill", "gdn_layer_decode_bucket",
-    "get_device_error", "probe_traffic", "GDN_F32", "GDN_BF16", "GDN_DEVERR_NONE",
-    "GDN_DEVERR_BAD_SLOT", "GDN_PROBE_TWIN", "GDN_PROBE_INPLACE", "GDN_PROBE_READ",
+    "get_device_error", "selftest_wait_timeout", "probe_traffic", "GDN_F32", "GDN_BF16", "GDN_DEVERR_NONE",
+    "GDN_DEVERR_BAD_SLOT", "GDN_DEVERR_TIMEOUT", "GDN_PROBE_TWIN", "GDN_PROBE_INPLACE", "GDN_PROBE_READ",
     "GDN_PROBE_WRITE", "GDN_NOALLOC_SCRATCH_SLOTS",
 ]
 
@@ -489,6 +490,15 @@ def get_device_error(device=None) -> int:
     with torch.cuda.device(device):
         _check(_lib.load().gdn_get_device_error(ctypes.byref(code), _stream(device)))
     return code.value
+
+
+def selftest_wait_timeout(rounds: int = 4096, device=None) -> None:
+    """Run a kernel whose bounded wait cannot end (it gives up after `rounds`
+    suspended try_wait rounds); afterwards the device error word reads
+    GDN_DEVERR_TIMEOUT.  Asynchronous."""
+    device = torch.device(device if device is not None else "cuda")
+    with torch.cuda.device(device):
+        _check(_lib.load().gdn_selftest_wait_timeout(int(rounds), _stream(device)))
 
 
 def probe_traffic(pool: GDNStatePool, read_slot: torch.Tensor, write_slot: Optional[torch.Tensor],

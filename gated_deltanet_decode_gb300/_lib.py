@@ -43,7 +43,8 @@ EXPORTS = [
     "conv_pool_num_slots", "conv_pool_zero_slots", "conv_pool_copy_slots",
     "causal_conv1d_decode", "gdn_decode_step", "gdn_layer_decode", "gdn_layer_decode_commit",
     "gdn_layer_decode_noalloc", "gdn_layer_decode_bucket", "gdn_prefill", "gdn_prefill_chunked", "gdn_verify", "causal_conv1d_prefill",
-    "gdn_commit", "gdn_validate_slots", "gdn_get_device_error", "gdn_probe_traffic",
+    "gdn_commit", "gdn_validate_slots", "gdn_get_device_error", "gdn_selftest_wait_timeout",
+    "gdn_probe_traffic",
 ]
 
 
@@ -89,6 +90,7 @@ _SIGS = {
     "gdn_validate_slots": (_I, [_P, _P, _I, _I, _I, _P]),
     "gdn_get_device_error": (_I, [ctypes.POINTER(ctypes.c_int), _P]),
     "gdn_probe_traffic": (_I, [_P, _P, _P, _I, _I, _P, _P]),
+    "gdn_selftest_wait_timeout": (_I, [_I, _P]),
 }
 
 _lock = threading.Lock()

@@ -13,6 +13,7 @@
 
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
+#include "gdn_ptx.cuh"
 
 #define GDN_ABI_VERSION 1
 
@@ -1098,6 +1099,44 @@ int gdn_probe_traffic(gdn_pool *pool, const int32_t *read_slot, const int32_t *w
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return cuda_fail(e, "gdn_probe_traffic launch");
+    return ok();
+}
+
+} // extern "C"
+
+namespace {
+
+// A wait that nothing ends: one thread waits for the first phase of an
+// mbarrier no thread arrives at, through the bounded wait every kernel uses
+// (here with the caller's round limit), and reports the timeout in the device
+// error word.  The failure path runs without anything faulting or hanging:
+// no copy is in flight and the thread leaves normally.
+__global__ void wait_selftest_kernel(int *err, long long rounds)
+{
+    __shared__ __align__(8) unsigned long long bar;
+    const uint32_t b = gdn::sm_addr(&bar);
+    gdn::mbar_init(b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (!gdn::mbar_wait(b, 0, rounds))
+        gdn::report(err, GDN_DEVERR_TIMEOUT);
+}
+
+} // namespace
+
+extern "C" {
+
+int gdn_selftest_wait_timeout(int rounds, void *stream)
+{
+    if (rounds < 1 || (long long)rounds > gdn::kWaitLimit)
+        return fail(GDN_EINVAL, "rounds=%d outside [1, %lld]", rounds, gdn::kWaitLimit);
+    int *err = nullptr;
+    int rc = device_error_ptr(&err);
+    if (rc)
+        return rc;
+    wait_selftest_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(err, (long long)rounds);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "gdn_selftest_wait_timeout launch");
     return ok();
 }
 

@@ -41,10 +41,11 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
                  : "memory");
     return ok != 0;
 }
-// Bounded wait for the phase of `parity` to complete; false when it ran out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+// Bounded wait for the phase of `parity` to complete; false when it ran out
+// (after `limit` suspended try_wait rounds).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit = kWaitLimit)
 {
-    for (long long i = 0; i < kWaitLimit; ++i)
+    for (long long i = 0; i < limit; ++i)
         if (mbar_try(bar, parity))
             return true;
     return false;

@@ -349,6 +349,15 @@ int gdn_validate_slots(const int32_t *read_slot, const int32_t *write_slot, int 
  * clear it. */
 int gdn_get_device_error(int *code, void *stream);
 
+/* Exercise the bounded-wait failure path: one thread waits, through the
+ * same bounded wait the kernels use, on a shared-memory barrier that nothing
+ * arrives at, giving up after `rounds` suspended try_wait rounds (the kernels
+ * use 2^20, about a second at most; a test passes a few thousand, about a
+ * millisecond).  The device error word then reads GDN_DEVERR_TIMEOUT; nothing
+ * faults, no copy is left in flight, and the context serves the next call.
+ * Asynchronous on `stream`.  rounds outside [1, 2^20] -> GDN_EINVAL. */
+int gdn_selftest_wait_timeout(int rounds, void *stream);
+
 /* ---- roofline probes --------------------------------------------------- *
  * Move the state bytes of a step with no arithmetic, over the same pool
  * geometry and slot tables ("mstar PR #1139", "Numbers": the same reads and
