@@ -171,7 +171,16 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
-    def stop(self):
+    def count(self) -> int:
+        return len(self.lines)
+
+    def wait_first(self, timeout_s: float = 3.0) -> None:
+        """Return once the sampler has written a line (nvidia-smi takes a moment to start)."""
+        t_end = time.perf_counter() + timeout_s
+        while self.proc is not None and not self.lines and time.perf_counter() < t_end:
+            time.sleep(0.01)
+
+    def stop(self, since: int = 0):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -182,7 +191,7 @@ class ClockSampler:
         self.t.join(timeout=2)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for line in self.lines[since:]:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -614,6 +623,8 @@ def run_ours(args, rank, world, device):
     K, W = args.steps, args.warmup
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    clocks.wait_first()
+    n_clk = clocks.count() # the clock record starts with the warm-up
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -632,6 +643,16 @@ def run_ours(args, rank, world, device):
         sets[(W + i) % NSETS][step_key]()
     t1.record(stream)
     host_enqueue_s = time.perf_counter() - host0
+    # The same step keeps the GPU under the same load, untimed, until the clock
+    # sampler (one sample per 100 ms) has recorded it three times (at most 1 s):
+    # a short timed region falls between samples, this window surrounds it.
+    t_clk = time.perf_counter() + 1.0
+    i = W + K
+    while clocks.count() < n_clk + 3 and time.perf_counter() < t_clk:
+        for _ in range(50):
+            sets[i % NSETS][step_key]()
+            i += 1
+        torch.cuda.synchronize(device)
     torch.cuda.synchronize(device)
     # second timed region: the layer kernel alone, back to back, for its
     # average launch duration (the roofline's denominator)
@@ -654,7 +675,9 @@ def run_ours(args, rank, world, device):
         st["commit"]()
     s1.record(stream)
     torch.cuda.synchronize(device)
-    clk = clocks.stop()
+    clk = clocks.stop(since=n_clk)
+    clk["window"] = ("nvidia-smi every 100 ms from the warm-up through the timed region and the same "
+                     "step run on untimed until three samples had been taken")
     if world > 1:
         import torch.distributed as dist
         dist.barrier()

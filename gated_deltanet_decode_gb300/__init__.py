@@ -492,13 +492,13 @@ def get_device_error(device=None) -> int:
     return code.value
 
 
-def selftest_wait_timeout(rounds: int = 4096, device=None) -> None:
-    """Run a kernel whose bounded wait cannot end (it gives up after `rounds`
-    suspended try_wait rounds); afterwards the device error word reads
+def selftest_wait_timeout(limit_us: int = 1000, device=None) -> None:
+    """Run a kernel whose bounded wait cannot end (it gives up after
+    `limit_us` microseconds); afterwards the device error word reads
     GDN_DEVERR_TIMEOUT.  Asynchronous."""
     device = torch.device(device if device is not None else "cuda")
     with torch.cuda.device(device):
-        _check(_lib.load().gdn_selftest_wait_timeout(int(rounds), _stream(device)))
+        _check(_lib.load().gdn_selftest_wait_timeout(int(limit_us), _stream(device)))
 
 
 def probe_traffic(pool: GDNStatePool, read_slot: torch.Tensor, write_slot: Optional[torch.Tensor],

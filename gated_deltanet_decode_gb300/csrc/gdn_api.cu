@@ -1108,16 +1108,16 @@ namespace {
 
 // A wait that nothing ends: one thread waits for the first phase of an
 // mbarrier no thread arrives at, through the bounded wait every kernel uses
-// (here with the caller's round limit), and reports the timeout in the device
+// (here with the caller's time limit), and reports the timeout in the device
 // error word.  The failure path runs without anything faulting or hanging:
 // no copy is in flight and the thread leaves normally.
-__global__ void wait_selftest_kernel(int *err, long long rounds)
+__global__ void wait_selftest_kernel(int *err, unsigned long long limit_ns)
 {
     __shared__ __align__(8) unsigned long long bar;
     const uint32_t b = gdn::sm_addr(&bar);
     gdn::mbar_init(b, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    if (!gdn::mbar_wait(b, 0, rounds))
+    if (!gdn::mbar_wait(b, 0, limit_ns))
         gdn::report(err, GDN_DEVERR_TIMEOUT);
 }
 
@@ -1125,15 +1125,15 @@ __global__ void wait_selftest_kernel(int *err, long long rounds)
 
 extern "C" {
 
-int gdn_selftest_wait_timeout(int rounds, void *stream)
+int gdn_selftest_wait_timeout(int limit_us, void *stream)
 {
-    if (rounds < 1 || (long long)rounds > gdn::kWaitLimit)
-        return fail(GDN_EINVAL, "rounds=%d outside [1, %lld]", rounds, gdn::kWaitLimit);
+    if (limit_us < 1 || (unsigned long long)limit_us * 1000ull > gdn::kWaitNs)
+        return fail(GDN_EINVAL, "limit_us=%d outside [1, %llu]", limit_us, gdn::kWaitNs / 1000ull);
     int *err = nullptr;
     int rc = device_error_ptr(&err);
     if (rc)
         return rc;
-    wait_selftest_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(err, (long long)rounds);
+    wait_selftest_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(err, (unsigned long long)limit_us * 1000ull);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return cuda_fail(e, "gdn_selftest_wait_timeout launch");

@@ -7,10 +7,21 @@
 
 namespace gdn {
 
-// Every mbarrier wait is bounded: kWaitLimit suspended try_wait rounds.
-constexpr long long kWaitLimit = 1ll << 20;
+// Every mbarrier wait is bounded in time: it gives up kWaitNs after it began
+// (the %globaltimer clock, nanoseconds), and in any case after kWaitRounds
+// suspended try_wait rounds.  A round suspends for at most about the hint when
+// the barrier is idle, but can take much longer; the clock is the bound that
+// holds in practice.
+constexpr unsigned long long kWaitNs = 1000000000ull; // 1 s
+constexpr long long kWaitRounds = 1ll << 26;
 constexpr uint32_t kSuspendHintNs = 1000;
 
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 __device__ __forceinline__ uint32_t sm_addr(const void *p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -42,12 +53,18 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 // Bounded wait for the phase of `parity` to complete; false when it ran out
-// (after `limit` suspended try_wait rounds).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit = kWaitLimit)
+// (after `limit_ns` nanoseconds, or kWaitRounds rounds).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns = kWaitNs)
 {
-    for (long long i = 0; i < limit; ++i)
+    if (mbar_try(bar, parity))
+        return true;
+    const unsigned long long t0 = global_ns();
+    for (long long i = 0; i < kWaitRounds; ++i) {
         if (mbar_try(bar, parity))
             return true;
+        if (global_ns() - t0 > limit_ns)
+            return false;
+    }
     return false;
 }
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)

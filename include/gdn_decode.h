@@ -351,12 +351,11 @@ int gdn_get_device_error(int *code, void *stream);
 
 /* Exercise the bounded-wait failure path: one thread waits, through the
  * same bounded wait the kernels use, on a shared-memory barrier that nothing
- * arrives at, giving up after `rounds` suspended try_wait rounds (the kernels
- * use 2^20, about a second at most; a test passes a few thousand, about a
- * millisecond).  The device error word then reads GDN_DEVERR_TIMEOUT; nothing
- * faults, no copy is left in flight, and the context serves the next call.
- * Asynchronous on `stream`.  rounds outside [1, 2^20] -> GDN_EINVAL. */
-int gdn_selftest_wait_timeout(int rounds, void *stream);
+ * arrives at, giving up after `limit_us` microseconds (the kernels' waits give
+ * up after one second).  The device error word then reads GDN_DEVERR_TIMEOUT;
+ * nothing faults, no copy is left in flight, and the context serves the next
+ * call.  Asynchronous on `stream`.  limit_us outside [1, 10^6] -> GDN_EINVAL. */
+int gdn_selftest_wait_timeout(int limit_us, void *stream);
 
 /* ---- roofline probes --------------------------------------------------- *
  * Move the state bytes of a step with no arithmetic, over the same pool
