@@ -30,7 +30,7 @@ from ._lib import (GDN_BF16, GDN_DEVERR_BAD_SLOT, GDN_DEVERR_NONE, GDN_DEVERR_TI
 __all__ = [
     "GDNError", "load", "lib_path", "GDNStatePool", "ConvStatePool", "causal_conv1d_decode",
     "gdn_decode_step", "gdn_layer_decode", "gdn_layer_decode_noalloc", "gdn_commit", "gdn_validate_slots",
-    "gdn_prefill", "gdn_prefill_chunked", "gdn_verify", "causal_conv1d_prefill", "gdn_layer_decode_bucket",
+    "gdn_prefill", "gdn_prefill_chunked", "gdn_prefill_chunked_workspace_bytes", "gdn_verify", "causal_conv1d_prefill", "gdn_layer_decode_bucket",
     "get_device_error", "selftest_wait_timeout", "probe_traffic", "GDN_F32", "GDN_BF16", "GDN_DEVERR_NONE",
     "GDN_DEVERR_BAD_SLOT", "GDN_DEVERR_TIMEOUT", "GDN_PROBE_TWIN", "GDN_PROBE_INPLACE", "GDN_PROBE_READ",
     "GDN_PROBE_WRITE", "GDN_NOALLOC_SCRATCH_SLOTS",
@@ -282,13 +282,20 @@ def gdn_prefill(q, k, v, a, b, A_log, dt_bias, pool: GDNStatePool, cu_seqlens, r
     return out
 
 
+def gdn_prefill_chunked_workspace_bytes(nseq: int, total_tokens: int, hv: int) -> int:
+    """Bytes of the device workspace gdn_prefill_chunked needs for bf16 activations."""
+    return int(_lib.load().gdn_prefill_chunked_workspace_bytes(int(nseq), int(total_tokens), int(hv)))
+
+
 def gdn_prefill_chunked(q, k, v, a, b, A_log, dt_bias, pool: GDNStatePool, cu_seqlens, read_slot,
                         write_slot=None, out: Optional[torch.Tensor] = None,
-                        keep_in_place: bool = False) -> torch.Tensor:
+                        keep_in_place: bool = False, workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
     """gdn_prefill's operation in chunks of 64 tokens on the tensor cores
     (dk = dv = 128): the same arguments and slot semantics, results within
     about 1e-5 relative of gdn_prefill instead of bit-identical.  Its
-    activations must be device memory."""
+    activations must be device memory.  bf16 activations use a device
+    workspace (a uint8 tensor of at least gdn_prefill_chunked_workspace_bytes;
+    allocated here when none is given)."""
     T, nseq = _prefill_checks(q, k, v, a, b, A_log, dt_bias, pool, cu_seqlens, read_slot)
     dt, dev = q.dtype, pool.tensor.device
     if write_slot is not None:
@@ -296,6 +303,14 @@ def gdn_prefill_chunked(q, k, v, a, b, A_log, dt_bias, pool: GDNStatePool, cu_se
     if out is None:
         out = torch.empty((T, pool.hv, pool.dv), dtype=dt, device=dev)
     _numel(out, T * pool.hv * pool.dv, "out")
+    need = gdn_prefill_chunked_workspace_bytes(nseq, T, pool.hv) if dt == torch.bfloat16 else 0
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        if workspace.device != dev or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous tensor on the pool's device")
+        ws_ptr, ws_bytes = ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size()
     _check(_lib.load().gdn_prefill_chunked(
         _ptr(q, "q", dt, dev), _ptr(k, "k", dt, dev),
         _ptr(v, "v", dt, dev), _ptr(a, "a", dt, dev),
@@ -303,7 +318,7 @@ def gdn_prefill_chunked(q, k, v, a, b, A_log, dt_bias, pool: GDNStatePool, cu_se
         _ptr(dt_bias, "dt_bias", torch.float32, dev), pool.handle,
         _ptr(cu_seqlens, "cu_seqlens", torch.int32, dev), _ptr(read_slot, "read_slot", torch.int32, dev),
         _ptr(write_slot, "write_slot", torch.int32, dev), _ptr(out, "out", dt, dev), nseq, T,
-        int(bool(keep_in_place)), _dtype_code(dt), _stream(dev)))
+        int(bool(keep_in_place)), ws_ptr, ctypes.c_size_t(ws_bytes), _dtype_code(dt), _stream(dev)))
     return out
 
 

@@ -42,7 +42,7 @@ EXPORTS = [
     "conv_state_pool_create", "conv_state_pool_wrap", "conv_state_pool_destroy", "conv_pool_data",
     "conv_pool_num_slots", "conv_pool_zero_slots", "conv_pool_copy_slots",
     "causal_conv1d_decode", "gdn_decode_step", "gdn_layer_decode", "gdn_layer_decode_commit",
-    "gdn_layer_decode_noalloc", "gdn_layer_decode_bucket", "gdn_prefill", "gdn_prefill_chunked", "gdn_verify", "causal_conv1d_prefill",
+    "gdn_layer_decode_noalloc", "gdn_layer_decode_bucket", "gdn_prefill", "gdn_prefill_chunked", "gdn_prefill_chunked_workspace_bytes", "gdn_verify", "causal_conv1d_prefill",
     "gdn_commit", "gdn_validate_slots", "gdn_get_device_error", "gdn_selftest_wait_timeout",
     "gdn_probe_traffic",
 ]
@@ -83,7 +83,9 @@ _SIGS = {
     "gdn_layer_decode_bucket": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I,
                                      _P]),
     "gdn_prefill": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
-    "gdn_prefill_chunked": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "gdn_prefill_chunked": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, ctypes.c_size_t,
+                                 _I, _P]),
+    "gdn_prefill_chunked_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I]),
     "gdn_verify": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     "causal_conv1d_prefill": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _P]),
     "gdn_commit": (_I, [_P, _P, _I, _P]),

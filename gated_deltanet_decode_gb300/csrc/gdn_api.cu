@@ -762,7 +762,7 @@ static int prefill_launch(const void *q, const void *k, const void *v, const voi
                           const float *A_log, const float *dt_bias, gdn_pool *pool, const int32_t *cu_seqlens,
                           const int32_t *read_slot, const int32_t *write_slot, const int32_t *token_slot,
                           void *out, int nseq, int total_tokens, int dtype, void *stream, const char *what,
-                          bool chunked = false)
+                          bool chunked = false, void *work = nullptr)
 {
     if (!pool)
         return fail(GDN_EINVAL, "state pool is NULL");
@@ -803,6 +803,7 @@ static int prefill_launch(const void *q, const void *k, const void *v, const voi
     s.dk = pool->dims.dk;
     s.dv = pool->dims.dv;
     s.err = err;
+    s.work = work;
     cudaError_t e = chunked ? gdn::launch_gdn_prefill_chunked(s, dtype, static_cast<cudaStream_t>(stream))
                             : gdn::launch_gdn_prefill(s, dtype, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
@@ -822,19 +823,33 @@ int gdn_prefill(const void *q, const void *k, const void *v, const void *a, cons
                           stream, "gdn_prefill launch");
 }
 
+size_t gdn_prefill_chunked_workspace_bytes(int nseq, int total_tokens, int hv)
+{
+    return gdn::prefill_chunked_workspace_bytes(nseq, total_tokens, hv);
+}
+
 int gdn_prefill_chunked(const void *q, const void *k, const void *v, const void *a, const void *b,
                         const float *A_log, const float *dt_bias, gdn_pool *pool, const int32_t *cu_seqlens,
                         const int32_t *read_slot, const int32_t *write_slot, void *out, int nseq,
-                        int total_tokens, int keep_in_place, int dtype, void *stream)
+                        int total_tokens, int keep_in_place, void *workspace, size_t workspace_bytes, int dtype,
+                        void *stream)
 {
     if (pool && !gdn::chunked_shape_supported(pool->dims.dk, pool->dims.dv))
         return fail(GDN_EUNSUPPORTED, "gdn_prefill_chunked is built for dk = dv = 128 (pool has %d, %d)",
                     pool->dims.dk, pool->dims.dv);
     if (!keep_in_place && nseq > 0 && !write_slot)
         return fail(GDN_EINVAL, "write_slot is NULL in twin mode");
+    if (pool && dtype == GDN_BF16 && nseq > 0) {
+        const size_t need = gdn::prefill_chunked_workspace_bytes(nseq, total_tokens, pool->dims.hv);
+        if (!workspace || workspace_bytes < need)
+            return fail(GDN_EINVAL, "workspace of %zu bytes at %p: bf16 activations need %zu bytes", workspace_bytes,
+                        workspace, need);
+        if ((reinterpret_cast<uintptr_t>(workspace) & 127u) != 0)
+            return fail(GDN_EINVAL, "workspace must be 128-byte aligned");
+    }
     return prefill_launch(q, k, v, a, b, A_log, dt_bias, pool, cu_seqlens, read_slot,
                           keep_in_place ? nullptr : write_slot, nullptr, out, nseq, total_tokens, dtype,
-                          stream, "gdn_prefill_chunked launch", true);
+                          stream, "gdn_prefill_chunked launch", true, workspace);
 }
 
 int gdn_verify(const void *q, const void *k, const void *v, const void *a, const void *b,

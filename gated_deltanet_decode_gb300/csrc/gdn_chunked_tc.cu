@@ -59,7 +59,7 @@ constexpr uint32_t kTmemCols = 512;
 
 // TMEM columns
 constexpr uint32_t C_S = 0, C_Z = 128, C_Y = 192, C_U = 256, C_SH = 320, C_SL = 384;
-constexpr uint32_t C_EH = 320, C_EL = 352, C_UH = 384, C_UL = 416, C_WH = 128, C_WL = 160, C_KK = 448;
+constexpr uint32_t C_EH = 320, C_EL = 352, C_UH = 384, C_UL = 416, C_WH = 128, C_WL = 160;
 
 // Byte offset of element (row, k) in a canonical K-major tile with K columns.
 template <int K> __device__ __forceinline__ int cm_off(int row, int k)
@@ -67,27 +67,63 @@ template <int K> __device__ __forceinline__ int cm_off(int row, int k)
     return ((((row >> 3) * (K / 8)) + (k >> 3)) << 7) + ((row & 7) << 4) + ((k & 7) << 1);
 }
 
-// Shared-memory layout, byte offsets.
-struct TS {
-    static constexpr int KQ = 0;                  // bf16 [128][128]: raw K rows 0-63, raw Q rows 64-127
-    static constexpr int KT = KQ + 128 * CD * 2;  // bf16 [128 = dk][64 = tokens]: raw K transposed
-    static constexpr int PH = KT + CD * CK * 2;   // bf16 [64][64] P head / tail, T head / tail
+// One chunk's state-free terms, as the prep kernel writes them to the
+// workspace and as the chunk kernel takes them into shared memory with one
+// bulk copy: P and T = (I + A)^{-1} split into bf16 heads and tails, in the
+// canonical K-major layout the tensor cores read; the gates; the norm scales;
+// a header naming the chunk (sequence, first token in it) the unit holds.
+struct PW {
+    static constexpr int PH = 0;                    // bf16 [64][64] P head, tail, T head, tail
     static constexpr int PL = PH + CK * CK * 2;
     static constexpr int TH = PL + CK * CK * 2;
     static constexpr int TL = TH + CK * CK * 2;
-    static constexpr int AF = TL + CK * CK * 2;   // fp32 A [t][s] (upper blocks: scratch)
-    static constexpr int XF = AF + CK * LDF * 4;  // fp32 T [t][s]
-    static constexpr int GATES = XF + CK * LDF * 4; // two sets of [G | beta | e^G | e^{G_C-G}] x CK
-    static constexpr int IQ = GATES + 2 * 4 * CK * 4;
-    static constexpr int IK = IQ + CK * 4;
-    static constexpr int BARS = IK + CK * 4;      // mbarriers: Z|Y, U, O and S, [K|Q] K^T
-    static constexpr int TADDR = BARS + 32;       // the TMEM base address
+    static constexpr int GATES = TL + CK * CK * 2;  // fp32 [G | beta | e^G | e^{G_C - G}] x CK
+    static constexpr int IQ = GATES + 4 * CK * 4;   // fp32 q norm scales (with 1/sqrt(dk)) [CK]
+    static constexpr int IK = IQ + CK * 4;          // fp32 k norm scales [CK]
+    static constexpr int HDR = IK + CK * 4;         // int32 sequence, first token of the chunk in it
+    static constexpr int BYTES = (HDR + 8 + 127) & ~127;
+};
+static_assert(PW::BYTES % 128 == 0, "prep blocks stay 128-byte aligned");
+
+// Workspace units of one value head: sequence s's chunk j is unit
+// cu_seqlens[s] / CK + s + j.  Distinct for every chunk of nondecreasing
+// cu_seqlens; ceil(total_tokens / CK) + nseq units cover every index.
+__host__ __device__ __forceinline__ long long prep_units(int nseq, int total_tokens)
+{
+    return (long long)(total_tokens + CK - 1) / CK + nseq;
+}
+__device__ __forceinline__ int unit_base(const int32_t *cu, int s) { return cu[s] / CK + s; }
+
+// Shared-memory layout of the chunk kernel, byte offsets.
+struct TS {
+    static constexpr int KQ = 0;                  // bf16 [128][128]: raw K rows 0-63, raw Q rows 64-127
+    static constexpr int KT = KQ + 128 * CD * 2;  // bf16 [128 = dk][64 = tokens]: raw K transposed
+    static constexpr int PB = KT + CD * CK * 2;   // two prep blocks (PW), chunk parity
+    static constexpr int BARS = PB + 2 * PW::BYTES; // mbarriers: Z|Y, U, O and S, prep block 0, 1
+    static constexpr int TADDR = BARS + 48;       // the TMEM base address
     static constexpr int BYTES = TADDR + 16;
     static constexpr int STAGE = (BYTES + 127) & ~127; // raw q, k, v of the next chunk, [CK][CD] each
     static constexpr int TOTAL = STAGE + 3 * CK * CD * 2;
 };
 static_assert(TS::TOTAL <= 227 * 1024, "shared memory");
-static_assert(TS::BARS % 8 == 0 && TS::KT % 1024 == 0 && TS::PH % 128 == 0, "alignment");
+static_assert(TS::BARS % 8 == 0 && TS::KT % 1024 == 0 && TS::PB % 128 == 0, "alignment");
+
+// Shared-memory layout of the prep kernel, byte offsets.
+struct PS {
+    static constexpr int LDQ = CD + 8;            // row stride (bf16) of q and k: rows 272 B apart, so
+                                                  // a fragment's 8 rows fall in distinct banks
+    static constexpr int RQ = 0;                  // bf16 [CK][LDQ] raw q, k (row-major)
+    static constexpr int RK = RQ + CK * LDQ * 2;
+    // once [K|Q] K^T is in registers, q and k are dead: A and the decay / T take their place
+    static constexpr int AF = 0;                  // fp32 A [t][s] (upper blocks: scratch)
+    static constexpr int XF = AF + CK * LDF * 4;  // fp32 decay, then T [t][s]
+    static constexpr int QK_END = RK + CK * LDQ * 2;
+    static constexpr int AX_END = XF + CK * LDF * 4;
+    static constexpr int GATES = QK_END > AX_END ? QK_END : AX_END;
+    static constexpr int IQ = GATES + 4 * CK * 4;
+    static constexpr int IK = IQ + CK * 4;
+    static constexpr int TOTAL = IK + CK * 4;
+};
 
 // ---- tcgen05 wrappers ----
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo)
@@ -100,14 +136,6 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo)
 __host__ __device__ constexpr uint32_t idesc_bf16(int n)
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-}
-// A and B from shared memory
-__device__ __forceinline__ void tc_mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, bool acc)
-{
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-                 "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)acc)
-                 : "memory");
 }
 // A from tensor memory, B from shared memory
 __device__ __forceinline__ void tc_mma(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, bool acc)
@@ -172,32 +200,210 @@ __device__ __forceinline__ void split32(const float (&v)[32], uint32_t (&hi)[16]
         split2(v[2 * j], v[2 * j + 1], hi[j], lo[j]);
 }
 
-__global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const PrefillArgs p)
+// ---------------------------------------------------------------------------
+// The prep kernel: one CTA per (workspace unit, value head).  It finds the
+// chunk its unit holds, then forms the chunk's state-free terms: the gates,
+// the norm scales, [K|Q] K^T on the tensor cores (mma.sync; exact bf16
+// products, fp32 sums), A and P from it, T = (I + A)^{-1} by the blocked
+// inverse, and writes them with a header to the unit.  Units that hold no
+// chunk get a header that names none.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(TC_THREADS, 4) gdn_chunk_prep_kernel(const PrefillArgs p, unsigned char *work,
+                                                                    int units)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    bf16 *const RQ = reinterpret_cast<bf16 *>(smem + PS::RQ);
+    bf16 *const RK = reinterpret_cast<bf16 *>(smem + PS::RK);
+    float *const AF = reinterpret_cast<float *>(smem + PS::AF);
+    float *const XF = reinterpret_cast<float *>(smem + PS::XF);
+    float *const GATES = reinterpret_cast<float *>(smem + PS::GATES);
+    float *const IQ = reinterpret_cast<float *>(smem + PS::IQ);
+    float *const IK = reinterpret_cast<float *>(smem + PS::IK);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
+    const int u = blockIdx.x / p.hv, h = blockIdx.x - (blockIdx.x / p.hv) * p.hv;
+    unsigned char *const blk = work + ((size_t)h * units + u) * PW::BYTES;
+    int32_t *const hdr = reinterpret_cast<int32_t *>(blk + PW::HDR);
+    wait_prior_grid();
+    // The chunk kernel may launch now (every earlier kernel is complete): its
+    // CTAs set up and load their state beside this grid's last CTAs, and wait
+    // for this grid to complete before they read a unit.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    // the sequence whose units start at or before u: the last s with base(s) <= u
+    int lo = 0, hi = p.nseq - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (unit_base(p.cu_seqlens, mid) <= u)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int s = lo;
+    const int t0 = p.cu_seqlens[s], t1 = p.cu_seqlens[s + 1];
+    const int j = u - unit_base(p.cu_seqlens, s);
+    const int c0 = CK * j;
+    if (t0 < 0 || t1 < t0 || t1 > p.total_tokens || j < 0 || c0 >= t1 - t0) {
+        if (tid == 0)
+            hdr[0] = -1, hdr[1] = -1;
+        return;
+    }
+    const int n = min(CK, t1 - t0 - c0);
+    const int hq = h / (p.hv / p.hk);
+    const bf16 *const qg = reinterpret_cast<const bf16 *>(p.q);
+    const bf16 *const kg = reinterpret_cast<const bf16 *>(p.k);
+
+    // the chunk's raw q and k rows (zeros past its tokens), 16 bytes a copy
+    for (int e = tid; e < 2 * CK * (CD / 8); e += TC_THREADS) {
+        const int which = e / (CK * (CD / 8)), rem = e - which * (CK * (CD / 8));
+        const int tt = rem / (CD / 8), jj = rem - tt * (CD / 8);
+        const bool live = tt < n;
+        const size_t tok = (size_t)(t0 + c0 + (live ? tt : 0));
+        const bf16 *src = (which == 0 ? qg : kg) + (tok * p.hk + hq) * CD;
+        bf16 *dst = (which == 0 ? RQ : RK) + tt * PS::LDQ;
+        cp_async16(dst + 8 * jj, src + 8 * jj, live ? 16 : 0);
+    }
+    cp_async_commit();
+    if (warp == 0) {
+        // the gates
+        const bf16 *const ag = reinterpret_cast<const bf16 *>(p.a);
+        const bf16 *const bg = reinterpret_cast<const bf16 *>(p.b);
+        bf16 ra[2], rb[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int tt = lane + 32 * i;
+            ra[i] = rb[i] = from_f<bf16>(0.f);
+            if (tt < n) {
+                const size_t idx = (size_t)(t0 + c0 + tt) * p.hv + h;
+                ra[i] = ag[idx], rb[i] = bg[idx];
+            }
+        }
+        chunk_gates(GATES, ra, rb, n, expf(p.A_log[h]), p.dt_bias[h], lane);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    // norm scales, one token a warp at a time
+    const float qscale = 1.0f / sqrtf((float)CD);
+#pragma unroll
+    for (int i = 0; i < CK / TC_WARPS; ++i) {
+        const int tt = warp + TC_WARPS * i;
+        float qv[4], kv[4];
+        unpack(qv, Raw4<bf16>{*reinterpret_cast<const uint2 *>(RQ + tt * PS::LDQ + 4 * lane)});
+        unpack(kv, Raw4<bf16>{*reinterpret_cast<const uint2 *>(RK + tt * PS::LDQ + 4 * lane)});
+        float sq = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
+        float sk = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            sq += __shfl_xor_sync(0xffffffffu, sq, o);
+            sk += __shfl_xor_sync(0xffffffffu, sk, o);
+        }
+        if (lane == 0)
+            IQ[tt] = qscale * rsqrtf(sq + kEps), IK[tt] = rsqrtf(sk + kEps);
+    }
+    // [K|Q] K^T: warp w takes rows 16 (w & 3) .. + 15 of K (w < 4) or Q (w >= 4)
+    // against all 64 tokens s, over dk
+    float d[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            d[nt][e] = 0.f;
+    const bool isq = warp >= 4;
+    const bf16 *const X = isq ? RQ : RK;
+    const int m0 = 16 * (warp & 3);
+#pragma unroll
+    for (int ks = 0; ks < CD / 16; ++ks) {
+        uint32_t a[4];
+        lda(a, X, PS::LDQ, m0, 16 * ks, g, c);
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+            uint32_t b0, b1;
+            ldb(b0, b1, RK, PS::LDQ, 8 * nt, 16 * ks, g, c);
+            mma16816(d[nt], a[0], a[1], a[2], a[3], b0, b1);
+        }
+    }
+    __syncthreads(); // every warp's products are in registers: q and k are dead
+    // the decay e^{G_t - G_s} (s <= t) that A and P share (over q and k)
+    for (int i = 0; i < CK / 4; ++i) {
+        const int t = tid >> 2, s2 = (tid & 3) + 4 * i;
+        if (s2 <= t)
+            XF[t * LDF + s2] = expf(GATES[t] - GATES[s2]);
+    }
+    __syncthreads();
+
+    // A[t][s] = beta_t e^{G_t-G_s} ik_t ik_s (k_t . k_s), s < t, into AF;
+    // P[t][s] = e^{G_t-G_s} iq_t ik_s (q_t . k_s), s <= t, split, to the unit
+    const float *const BE = GATES + CK;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int t = m0 + g + 8 * hh, s0 = 8 * nt + 2 * c;
+            const float nt_ = isq ? IQ[t] : IK[t] * BE[t];
+            const bool in0 = isq ? s0 <= t : s0 < t, in1 = isq ? s0 + 1 <= t : s0 + 1 < t;
+            const float x = in0 ? XF[t * LDF + s0] * nt_ * IK[s0] * d[nt][2 * hh] : 0.f;
+            const float y = in1 ? XF[t * LDF + s0 + 1] * nt_ * IK[s0 + 1] * d[nt][2 * hh + 1] : 0.f;
+            if (!isq) {
+                AF[t * LDF + s0] = x;
+                AF[t * LDF + s0 + 1] = y;
+            } else {
+                uint32_t ph, pl;
+                split2(x, y, ph, pl);
+                *reinterpret_cast<uint32_t *>(blk + PW::PH + cm_off<CK>(t, s0)) = ph;
+                *reinterpret_cast<uint32_t *>(blk + PW::PL + cm_off<CK>(t, s0)) = pl;
+            }
+        }
+    }
+    __syncthreads();
+    if (tid < CK)
+        t_diagonal(AF, XF, tid);
+    __syncthreads();
+    t_below_diagonal(AF, XF, warp, g, c);
+    // T's lower triangle, split, to the unit: a warp writes one 8 x 8 core
+    // matrix at a time (lane: row lane & 7, column pair lane >> 3)
+    for (int e = tid; e < CK * CK / 2; e += TC_THREADS) {
+        const int cmi = e >> 5, l = e & 31;
+        const int t = 8 * (cmi >> 3) + (l & 7), s2 = 8 * (cmi & 7) + 2 * (l >> 3);
+        const float x = s2 <= t ? XF[t * LDF + s2] : 0.f;
+        const float y = s2 + 1 <= t ? XF[t * LDF + s2 + 1] : 0.f;
+        uint32_t th, tl;
+        split2(x, y, th, tl);
+        *reinterpret_cast<uint32_t *>(blk + PW::TH + cm_off<CK>(t, s2)) = th;
+        *reinterpret_cast<uint32_t *>(blk + PW::TL + cm_off<CK>(t, s2)) = tl;
+    }
+    // the gates and norm scales, then the header
+    float *const og = reinterpret_cast<float *>(blk + PW::GATES);
+    for (int e = tid; e < 4 * CK; e += TC_THREADS)
+        og[e] = GATES[e];
+    if (tid < CK) {
+        reinterpret_cast<float *>(blk + PW::IQ)[tid] = IQ[tid];
+        reinterpret_cast<float *>(blk + PW::IK)[tid] = IK[tid];
+    }
+    if (tid == 0)
+        hdr[0] = s, hdr[1] = c0;
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const PrefillArgs p,
+                                                                     const unsigned char *work, int units)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char *const KQ = smem + TS::KQ;
     unsigned char *const KT = smem + TS::KT;
-    unsigned char *const PH = smem + TS::PH;
-    unsigned char *const PL = smem + TS::PL;
-    unsigned char *const TH = smem + TS::TH;
-    unsigned char *const TL = smem + TS::TL;
-    float *const AF = reinterpret_cast<float *>(smem + TS::AF);
-    float *const XF = reinterpret_cast<float *>(smem + TS::XF);
-    float *const GATES = reinterpret_cast<float *>(smem + TS::GATES);
-    float *const IQ = reinterpret_cast<float *>(smem + TS::IQ);
-    float *const IK = reinterpret_cast<float *>(smem + TS::IK);
     uint64_t *const bars = reinterpret_cast<uint64_t *>(smem + TS::BARS);
     uint32_t *const taddr_slot = reinterpret_cast<uint32_t *>(smem + TS::TADDR);
     bf16 *const RQ = reinterpret_cast<bf16 *>(smem + TS::STAGE);
     bf16 *const RK = RQ + CK * CD;
     bf16 *const RV = RK + CK * CD;
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;
     const int row = 32 * quarter + lane; // this thread's state row (its TMEM lane)
     const int seq = blockIdx.x / p.hv, h = blockIdx.x - seq * p.hv;
     const int hq = h / (p.hv / p.hk);
-    wait_prior_grid();
+    // Everything up to the first chunk's prep block reads only this call's
+    // inputs, which the prep kernel does not write: it runs before
+    // wait_prior_grid, beside the prep kernel's last CTAs (which let this grid
+    // launch only after their own wait, so every earlier kernel is complete).
 
     const int t0 = p.cu_seqlens[seq], t1 = p.cu_seqlens[seq + 1];
     const bool range_ok = t0 >= 0 && t1 >= t0 && t1 <= p.total_tokens;
@@ -219,9 +425,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
         return;
     }
 
+    const int L = t1 - t0;
+    const unsigned char *const hwork = work + (size_t)h * units * PW::BYTES;
+    const int ubase = unit_base(p.cu_seqlens, seq);
+
     // tensor memory (all 512 columns) and the products' mbarriers
     const uint32_t bar_zy = sm_addr(&bars[0]), bar_u = sm_addr(&bars[1]), bar_o = sm_addr(&bars[2]);
-    const uint32_t bar_kk = sm_addr(&bars[3]);
+    const uint32_t bar_pb[2] = {sm_addr(&bars[3]), sm_addr(&bars[4])};
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sm_addr(taddr_slot)),
                      "r"(kTmemCols)
@@ -232,7 +442,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
         mbar_init(bar_zy, 1);
         mbar_init(bar_u, 1);
         mbar_init(bar_o, 1);
-        mbar_init(bar_kk, 1);
+        mbar_init(bar_pb[0], 1);
+        mbar_init(bar_pb[1], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     tc_before_sync();
@@ -260,15 +471,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
         tst_wait();
     }
 
-    const float rate = expf(p.A_log[h]);
-    const float dtb = p.dt_bias[h];
-    const float qscale = 1.0f / sqrtf((float)CD);
     const bf16 *const qg = reinterpret_cast<const bf16 *>(p.q);
     const bf16 *const kg = reinterpret_cast<const bf16 *>(p.k);
     const bf16 *const vg = reinterpret_cast<const bf16 *>(p.v);
-    const bf16 *const ag = reinterpret_cast<const bf16 *>(p.a);
-    const bf16 *const bg = reinterpret_cast<const bf16 *>(p.b);
-    const int L = t1 - t0;
 
     // the raw q, k, v of the chunk starting at token cn (zeros past the
     // sequence), 16 bytes a copy, every thread a share, into the staging area
@@ -287,22 +492,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
         }
         cp_async_commit();
     };
-    // the gate inputs of the chunk starting at cn (warp 2, tokens lane and lane + 32)
-    bf16 ra[2], rb[2];
-    auto gates_in = [&](int cn) {
-        const int nn = min(CK, L - cn);
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int tt = lane + 32 * i;
-            if (tt < nn) {
-                const size_t idx = (size_t)(t0 + cn + tt) * p.hv + h;
-                ra[i] = ag[idx], rb[i] = bg[idx];
-            }
+    // the prep block of chunk cj into the shared prep block of its parity (one
+    // bulk copy; its previous chunk's products, which read it, are done)
+    auto prep_copy = [&](int cj) {
+        if (tid == 0) {
+            smem_to_async();
+            const uint32_t bar = bar_pb[cj & 1];
+            mbar_arrive_tx(bar, (uint32_t)PW::BYTES);
+            bulk_load(sm_addr(smem + TS::PB + (cj & 1) * PW::BYTES), hwork + (size_t)(ubase + cj) * PW::BYTES,
+                      (uint32_t)PW::BYTES, bar);
         }
-    };
-    // its gates: log alpha, beta, running sums (zero past the chunk's tokens), into gate set `set`
-    auto gates = [&](int cn, int set) {
-        chunk_gates(GATES + set * 4 * CK, ra, rb, min(CK, L - cn), rate, dtb, lane);
     };
     // this thread's outputs of the chunk starting at cbase (nn tokens): row
     // `row` of O, tokens 32*half .. 32*half + 31
@@ -316,13 +515,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
                 out[(size_t)(t0 + cbase + t) * out_tok + (size_t)h * CD + row] = from_f<bf16>(o[i]);
         }
     };
-    if (L > 0) {
+    if (L > 0)
         stage(0);
-        if (warp == 2) {
-            gates_in(0);
-            gates(0, 0);
-        }
+    wait_prior_grid(); // the prep kernel's units are complete
+
+    // the prep kernel's units of this sequence must name its chunks (they do
+    // unless cu_seqlens decreases somewhere): otherwise it counts as bad
+    bool named = true;
+    for (int j = tid; CK * j < L; j += TC_THREADS) {
+        const int32_t *hd = reinterpret_cast<const int32_t *>(hwork + (size_t)(ubase + j) * PW::BYTES + PW::HDR);
+        named = named && ubase + j < units && hd[0] == seq && hd[1] == CK * j;
     }
+    if (!__syncthreads_and(named)) {
+        if (h == 0 && tid == 0)
+            report(p.err, GDN_DEVERR_BAD_SLOT);
+        for (long long e = tid; e < (long long)L * CD; e += TC_THREADS)
+            out[(size_t)(t0 + e / CD) * out_tok + (size_t)h * CD + (size_t)(e % CD)] = from_f<bf16>(0.f);
+        cp_async_wait_all();
+        tc_before_sync();
+        __syncthreads();
+        if (warp == 0)
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(kTmemCols) : "memory");
+        return;
+    }
+    if (L > 0)
+        prep_copy(0);
 
     bool abort = false;
     int n_prev = 0;
@@ -330,15 +547,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
     for (int c0 = 0; c0 < L; c0 += CK) {
         const int ci = c0 / CK;
         const int n = min(CK, L - c0);
-        const int set = ci & 1;
-        const float *const GG = GATES + set * 4 * CK; // this chunk's gates
+        unsigned char *const PBc = smem + TS::PB + (ci & 1) * PW::BYTES; // this chunk's prep block
+        unsigned char *const PH = PBc + PW::PH;
+        unsigned char *const PL = PBc + PW::PL;
+        unsigned char *const TH = PBc + PW::TH;
+        unsigned char *const TL = PBc + PW::TL;
+        const float *const GG = reinterpret_cast<const float *>(PBc + PW::GATES); // this chunk's gates
+        const float *const IQ = reinterpret_cast<const float *>(PBc + PW::IQ);
+        const float *const IK = reinterpret_cast<const float *>(PBc + PW::IK);
         const float *const BE = GG + CK;
         const float *const EG = GG + 2 * CK;
         const float *const EC = GG + 3 * CK;
         const bool more = c0 + CK < L;
 
         // ---- (0) the previous chunk's products are done; its outputs, S's
-        // head and tail, this chunk's K | Q, K^T and norms ----
+        // head and tail, this chunk's K | Q and K^T; the next chunk's prep
+        // block on its way ----
         cp_async_wait_all();
         bool late = ci > 0 && !mbar_wait(bar_o, (uint32_t)((ci - 1) & 1));
         if (late)
@@ -348,6 +572,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
             break;
         }
         tc_after_sync();
+        if (more)
+            prep_copy(ci + 1);
         if (ci > 0)
             write_outputs(c0 - CK, n_prev);
 #pragma unroll
@@ -365,19 +591,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
             const int tt = warp + TC_WARPS * i;
             const uint2 qraw = *reinterpret_cast<const uint2 *>(RQ + tt * CD + 4 * lane);
             const uint2 kraw = *reinterpret_cast<const uint2 *>(RK + tt * CD + 4 * lane);
-            float qv[4], kv[4];
-            unpack(qv, Raw4<bf16>{qraw}), unpack(kv, Raw4<bf16>{kraw});
-            float sq = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
-            float sk = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
-#pragma unroll
-            for (int o = 16; o; o >>= 1) {
-                sq += __shfl_xor_sync(0xffffffffu, sq, o);
-                sk += __shfl_xor_sync(0xffffffffu, sk, o);
-            }
             *reinterpret_cast<uint2 *>(KQ + cm_off<CD>(tt, 4 * lane)) = kraw;
             *reinterpret_cast<uint2 *>(KQ + cm_off<CD>(CK + tt, 4 * lane)) = qraw;
-            if (lane == 0)
-                IQ[tt] = qscale * rsqrtf(sq + kEps), IK[tt] = rsqrtf(sk + kEps);
         }
         {
             // K^T, one 16-byte core-matrix row (dk j, tokens s0..s0+7) at a time
@@ -396,15 +611,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
         __syncthreads();
         tc_after_sync();
 
-        // ---- (1) [K|Q] K^T, then Z|Y = S [K|Q]^T, on the tensor cores ----
+        // ---- (1) Z|Y = S [K|Q]^T on the tensor cores ----
         if (tid == 0) {
             const uint32_t kq = sm_addr(KQ);
-#pragma unroll
-            for (int ks = 0; ks < CD / 16; ++ks) {
-                const uint64_t ab = smem_desc(kq + 256 * ks, (CD / 8) * 128); // [K|Q] and, its first 64 rows, K
-                tc_mma_ss(tbase + C_KK, ab, ab, idesc_bf16(CK), ks > 0);    // exact bf16 products
-            }
-            tc_commit(bar_kk);
 #pragma unroll
             for (int ks = 0; ks < CD / 16; ++ks) {
                 const uint64_t b = smem_desc(kq + 256 * ks, (CD / 8) * 128);
@@ -413,73 +622,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
             }
             tc_commit(bar_zy);
         }
-        if (more && warp == 2)
-            gates_in(c0 + CK);
-        // meanwhile the decay e^{G_t - G_s} (s <= t) that A and P share, into T's buffer
-        for (int i = 0; i < CK / 4; ++i) {
-            const int t = tid >> 2, s2 = (tid & 3) + 4 * i;
-            if (s2 <= t)
-                XF[t * LDF + s2] = expf(GG[t] - GG[s2]);
-        }
-        late = !mbar_wait(bar_kk, (uint32_t)(ci & 1));
-        if (late)
-            report(p.err, GDN_DEVERR_TIMEOUT);
-        if (__syncthreads_or(late)) {
-            abort = true;
-            break;
-        }
-        tc_after_sync();
-        {
-            // row `row` of [K|Q] K^T, columns (tokens s) 32*half .. 32*half + 31:
-            // rows t < 64 give A[t][s] = beta_t e^{G_t-G_s} ik_t ik_s (k_t . k_s), s < t;
-            // rows 64 + t give P[t][s] = e^{G_t-G_s} iq_t ik_s (q_t . k_s), s <= t
-            // (a warp whose columns all lie above its rows writes zeros)
-            const bool isq = row >= CK;
-            const int t = isq ? row - CK : row;
-            const bool any = 32 * half <= 32 * (quarter & 1) + 31;
-            float d[32];
-            tld32(tlane + C_KK + 32 * half, d);
-            const float nt_ = isq ? IQ[t] : IK[t] * BE[t];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const int s0 = 32 * half + i;
-                const bool in0 = any && (isq ? s0 <= t : s0 < t), in1 = any && (isq ? s0 + 1 <= t : s0 + 1 < t);
-                const float x = in0 ? XF[t * LDF + s0] * nt_ * IK[s0] * d[i] : 0.f;
-                const float y = in1 ? XF[t * LDF + s0 + 1] * nt_ * IK[s0 + 1] * d[i + 1] : 0.f;
-                if (!isq) {
-                    AF[t * LDF + s0] = x;
-                    AF[t * LDF + s0 + 1] = y;
-                } else {
-                    uint32_t hh, ll;
-                    split2(x, y, hh, ll);
-                    *reinterpret_cast<uint32_t *>(PH + cm_off<CK>(t, s0)) = hh;
-                    *reinterpret_cast<uint32_t *>(PL + cm_off<CK>(t, s0)) = ll;
-                }
-            }
-        }
-        __syncthreads();
-        if (tid < CK)
-            t_diagonal(AF, XF, tid);
-        else if (more && warp == 2)
-            gates(c0 + CK, set ^ 1); // meanwhile: the next chunk's gates
-        __syncthreads();
-        t_below_diagonal(AF, XF, warp, g, c);
-        // T's lower triangle, split, into the canonical layout: a warp writes one
-        // 8 x 8 core matrix at a time (lane: row lane & 7, column pair lane >> 3)
-        for (int e = tid; e < CK * CK / 2; e += TC_THREADS) {
-            const int cmi = e >> 5, l = e & 31;
-            const int t = 8 * (cmi >> 3) + (l & 7), s = 8 * (cmi & 7) + 2 * (l >> 3);
-            const float x = s <= t ? XF[t * LDF + s] : 0.f;
-            const float y = s + 1 <= t ? XF[t * LDF + s + 1] : 0.f;
-            uint32_t hh, ll;
-            split2(x, y, hh, ll);
-            *reinterpret_cast<uint32_t *>(TH + cm_off<CK>(t, s)) = hh;
-            *reinterpret_cast<uint32_t *>(TL + cm_off<CK>(t, s)) = ll;
-        }
-        smem_to_async();
 
         // ---- (2) E and Y diag(e^G iq) from Z|Y, one state row a thread ----
-        late = !mbar_wait(bar_zy, (uint32_t)(ci & 1));
+        late = !mbar_wait(bar_pb[ci & 1], (uint32_t)((ci >> 1) & 1)) || !mbar_wait(bar_zy, (uint32_t)(ci & 1));
         if (late)
             report(p.err, GDN_DEVERR_TIMEOUT);
         if (__syncthreads_or(late)) {
@@ -621,12 +766,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
 
 } // namespace
 
+size_t prefill_chunked_workspace_bytes(int nseq, int total_tokens, int hv)
+{
+    if (nseq <= 0 || total_tokens < 0 || hv <= 0)
+        return 0;
+    return (size_t)prep_units(nseq, total_tokens) * (size_t)hv * (size_t)PW::BYTES;
+}
+
 cudaError_t launch_gdn_prefill_chunked_tc(const PrefillArgs &a, cudaStream_t s)
 {
     const long long ctas = (long long)a.nseq * a.hv;
     if (ctas == 0)
         return cudaSuccess;
-    if (ctas > 0x7fffffffll)
+    const long long units = prep_units(a.nseq, a.total_tokens);
+    if (ctas > 0x7fffffffll || units * a.hv > 0x7fffffffll)
         return cudaErrorInvalidValue;
     static std::atomic<unsigned long long> configured{0}; // one bit per device
     int dev = 0;
@@ -635,11 +788,19 @@ cudaError_t launch_gdn_prefill_chunked_tc(const PrefillArgs &a, cudaStream_t s)
     if (!(configured.load(std::memory_order_acquire) & bit)) {
         cudaError_t e = cudaFuncSetAttribute(gdn_chunked_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              TS::TOTAL);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gdn_chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PS::TOTAL);
         if (e != cudaSuccess)
             return e;
         configured.fetch_or(bit, std::memory_order_release);
     }
-    return launch_pdl(gdn_chunked_tc_kernel, dim3((unsigned)ctas), dim3(TC_THREADS), (size_t)TS::TOTAL, s, a);
+    unsigned char *work = static_cast<unsigned char *>(a.work);
+    cudaError_t e = launch_pdl(gdn_chunk_prep_kernel, dim3((unsigned)(units * a.hv)), dim3(TC_THREADS),
+                               (size_t)PS::TOTAL, s, a, work, (int)units);
+    if (e != cudaSuccess)
+        return e;
+    return launch_pdl(gdn_chunked_tc_kernel, dim3((unsigned)ctas), dim3(TC_THREADS), (size_t)TS::TOTAL, s, a,
+                      static_cast<const unsigned char *>(work), (int)units);
 }
 
 } // namespace gdn

@@ -80,6 +80,7 @@ struct PrefillArgs {
     void *out;
     int nseq, total_tokens, hk, hv, dk, dv;
     int *err;
+    void *work;                // gdn_prefill_chunked, bf16: the chunk prep workspace
 };
 
 struct ConvPrefillArgs {
@@ -105,6 +106,8 @@ cudaError_t launch_conv_prefill(const ConvPrefillArgs &a, int dtype, cudaStream_
 // bf16 activations run the tcgen05 kernel (gdn_chunked_tc.cu), fp32 the mma.sync one.
 cudaError_t launch_gdn_prefill_chunked(const PrefillArgs &a, int dtype, cudaStream_t s);
 cudaError_t launch_gdn_prefill_chunked_tc(const PrefillArgs &a, cudaStream_t s);
+// Bytes of the workspace the bf16 chunked prefill needs (0 for no sequence).
+size_t prefill_chunked_workspace_bytes(int nseq, int total_tokens, int hv);
 
 // True when the state kernels are built for (dk, dv).
 bool step_shape_supported(int dk, int dv);

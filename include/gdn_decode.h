@@ -258,11 +258,22 @@ int gdn_prefill(const void *q, const void *k, const void *v, const void *a, cons
  * run as one GDN prefill kernel ("mstar PR #1127").  Each product splits its
  * fp32 operands into bf16 heads and tails, so outputs and final states agree
  * with gdn_prefill to about 1e-5 relative per chunk, not bit for bit.  Built
- * for dk = dv = 128 (GDN_EUNSUPPORTED otherwise).  q, k, v 16-byte aligned. */
+ * for dk = dv = 128 (GDN_EUNSUPPORTED otherwise).  q, k, v 16-byte aligned.
+ * bf16 activations run two kernels: every chunk's state-free terms (gates,
+ * norms, P, T) in parallel into `workspace`, then the chunks of each
+ * sequence in order.  The caller owns the workspace: device memory, 128-byte
+ * aligned, at least gdn_prefill_chunked_workspace_bytes(nseq, total_tokens,
+ * hv) bytes (GDN_EINVAL otherwise); its contents need no initialisation and
+ * are garbage afterwards; calls that overlap on the GPU need their own.
+ * fp32 activations ignore it (NULL allowed).  cu_seqlens must be
+ * nondecreasing: a sequence whose chunks the prep kernel could not place
+ * counts as bad (zero outputs, GDN_DEVERR_BAD_SLOT, no state written). */
+size_t gdn_prefill_chunked_workspace_bytes(int nseq, int total_tokens, int hv);
 int gdn_prefill_chunked(const void *q, const void *k, const void *v, const void *a, const void *b,
                         const float *A_log, const float *dt_bias, gdn_pool *pool, const int32_t *cu_seqlens,
                         const int32_t *read_slot, const int32_t *write_slot, void *out, int nseq,
-                        int total_tokens, int keep_in_place, int dtype, void *stream);
+                        int total_tokens, int keep_in_place, void *workspace, size_t workspace_bytes,
+                        int dtype, void *stream);
 int gdn_verify(const void *q, const void *k, const void *v, const void *a, const void *b,
                const float *A_log, const float *dt_bias, gdn_pool *pool, const int32_t *cu_seqlens,
                const int32_t *read_slot, const int32_t *token_slot, void *out, int nseq, int total_tokens,

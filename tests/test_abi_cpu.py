@@ -259,24 +259,37 @@ def test_prefill_argument_checks(L):
 
 def test_prefill_chunked_argument_checks(L):
     """gdn_prefill_chunked: built for dk = dv = 128 only (unsupported shapes
-    are refused before anything else), otherwise gdn_prefill's checks."""
+    are refused before anything else); bf16 activations need a 128-byte
+    aligned workspace of gdn_prefill_chunked_workspace_bytes; otherwise
+    gdn_prefill's checks."""
+    import ctypes
     P = FAKE
     rc, small = _wrap(L, hk=2, hv=2, dk=16, dv=16)
     assert rc == 0
     rc, pool = _wrap(L, hk=2, hv=4, dk=128, dv=128)
     assert rc == 0
+    need = L.gdn_prefill_chunked_workspace_bytes(2, 5, 4)
+    # one unit per chunk start, ceil(T / 64) + nseq units a value head, whole 128-byte blocks
+    assert need > 0 and need % (3 * 4) == 0 and (need // 12) % 128 == 0
+    assert L.gdn_prefill_chunked_workspace_bytes(2, 640, 4) == need // 3 * (10 + 2)
+    assert L.gdn_prefill_chunked_workspace_bytes(0, 5, 4) == 0
 
-    def chunked(nseq=2, T=5, pool_=pool, ws=P, inplace=0, dtype=1, q=P):
-        return L.gdn_prefill_chunked(q, P, P, P, P, P, P, pool_, P, P, ws, P, nseq, T, inplace, dtype, None)
+    def chunked(nseq=2, T=5, pool_=pool, ws=P, inplace=0, dtype=1, q=P, work=P, work_bytes=None):
+        wb = need if work_bytes is None else work_bytes
+        return L.gdn_prefill_chunked(q, P, P, P, P, P, P, pool_, P, P, ws, P, nseq, T, inplace, work,
+                                     ctypes.c_size_t(wb), dtype, None)
 
     assert chunked(pool_=small) == EUNSUPPORTED and b"128" in L.gdn_last_error()
     assert chunked(pool_=None) == EINVAL
     assert chunked(nseq=-1) == EINVAL
     assert chunked(dtype=3) == EINVAL
     assert chunked(ws=None) == EINVAL and b"write_slot" in L.gdn_last_error()
+    assert chunked(work=None) == EINVAL and b"workspace" in L.gdn_last_error()
+    assert chunked(work_bytes=need - 16) == EINVAL and b"workspace" in L.gdn_last_error()
+    assert chunked(work=P + 64) == EINVAL and b"128-byte" in L.gdn_last_error()
     assert chunked(q=P + 8) == EINVAL and b"aligned" in L.gdn_last_error()
     assert chunked(nseq=0) == 0
-    assert chunked(nseq=0, ws=None, inplace=1) == 0
+    assert chunked(nseq=0, ws=None, inplace=1, work=None, work_bytes=0) == 0
     L.gdn_state_pool_destroy(small)
     L.gdn_state_pool_destroy(pool)
 
