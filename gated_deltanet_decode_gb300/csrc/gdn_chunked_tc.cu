@@ -323,16 +323,10 @@ __global__ void __launch_bounds__(TC_THREADS, 4) gdn_chunk_prep_kernel(const Pre
         }
     }
     __syncthreads(); // every warp's products are in registers: q and k are dead
-    // the decay e^{G_t - G_s} (s <= t) that A and P share (over q and k)
-    for (int i = 0; i < CK / 4; ++i) {
-        const int t = tid >> 2, s2 = (tid & 3) + 4 * i;
-        if (s2 <= t)
-            XF[t * LDF + s2] = expf(GATES[t] - GATES[s2]);
-    }
-    __syncthreads();
 
-    // A[t][s] = beta_t e^{G_t-G_s} ik_t ik_s (k_t . k_s), s < t, into AF;
-    // P[t][s] = e^{G_t-G_s} iq_t ik_s (q_t . k_s), s <= t, split, to the unit
+    // A[t][s] = beta_t e^{G_t-G_s} ik_t ik_s (k_t . k_s), s < t, into AF (over
+    // q and k); P[t][s] = e^{G_t-G_s} iq_t ik_s (q_t . k_s), s <= t, split, to
+    // the unit; the decay formed where it is used
     const float *const BE = GATES + CK;
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
@@ -341,8 +335,8 @@ __global__ void __launch_bounds__(TC_THREADS, 4) gdn_chunk_prep_kernel(const Pre
             const int t = m0 + g + 8 * hh, s0 = 8 * nt + 2 * c;
             const float nt_ = isq ? IQ[t] : IK[t] * BE[t];
             const bool in0 = isq ? s0 <= t : s0 < t, in1 = isq ? s0 + 1 <= t : s0 + 1 < t;
-            const float x = in0 ? XF[t * LDF + s0] * nt_ * IK[s0] * d[nt][2 * hh] : 0.f;
-            const float y = in1 ? XF[t * LDF + s0 + 1] * nt_ * IK[s0 + 1] * d[nt][2 * hh + 1] : 0.f;
+            const float x = in0 ? expf(GATES[t] - GATES[s0]) * nt_ * IK[s0] * d[nt][2 * hh] : 0.f;
+            const float y = in1 ? expf(GATES[t] - GATES[s0 + 1]) * nt_ * IK[s0 + 1] * d[nt][2 * hh + 1] : 0.f;
             if (!isq) {
                 AF[t * LDF + s0] = x;
                 AF[t * LDF + s0 + 1] = y;
@@ -355,8 +349,19 @@ __global__ void __launch_bounds__(TC_THREADS, 4) gdn_chunk_prep_kernel(const Pre
         }
     }
     __syncthreads();
-    if (tid < CK)
+    if (tid < CK) {
         t_diagonal(AF, XF, tid);
+    } else {
+        // meanwhile the gates and norm scales go to the unit
+        float *const og = reinterpret_cast<float *>(blk + PW::GATES);
+        for (int e = tid - CK; e < 4 * CK; e += TC_THREADS - CK)
+            og[e] = GATES[e];
+        if (tid >= TC_THREADS - CK) {
+            const int t = tid - (TC_THREADS - CK);
+            reinterpret_cast<float *>(blk + PW::IQ)[t] = IQ[t];
+            reinterpret_cast<float *>(blk + PW::IK)[t] = IK[t];
+        }
+    }
     __syncthreads();
     t_below_diagonal(AF, XF, warp, g, c);
     // T's lower triangle, split, to the unit: a warp writes one 8 x 8 core
@@ -370,14 +375,6 @@ __global__ void __launch_bounds__(TC_THREADS, 4) gdn_chunk_prep_kernel(const Pre
         split2(x, y, th, tl);
         *reinterpret_cast<uint32_t *>(blk + PW::TH + cm_off<CK>(t, s2)) = th;
         *reinterpret_cast<uint32_t *>(blk + PW::TL + cm_off<CK>(t, s2)) = tl;
-    }
-    // the gates and norm scales, then the header
-    float *const og = reinterpret_cast<float *>(blk + PW::GATES);
-    for (int e = tid; e < 4 * CK; e += TC_THREADS)
-        og[e] = GATES[e];
-    if (tid < CK) {
-        reinterpret_cast<float *>(blk + PW::IQ)[tid] = IQ[tid];
-        reinterpret_cast<float *>(blk + PW::IK)[tid] = IK[tid];
     }
     if (tid == 0)
         hdr[0] = s, hdr[1] = c0;

@@ -213,3 +213,33 @@ def test_chunked_graph_replay_equals_eager(gdn):
     assert torch.equal(out, want_out)
     assert torch.equal(c.pool.tensor, want_pool)
     assert gdn.get_device_error() == 0
+
+
+def test_chunked_decreasing_cu_seqlens_is_refused_per_sequence(gdn):
+    """cu_seqlens that decreases (overlapping token ranges) cannot place every
+    chunk in the prep workspace: cu = [0, 300, 0, 200] gives sequence 1 a
+    negative range (bad) and sequence 2 the workspace units of sequence 0's
+    chunks 2-4.  Sequence 0 still computes (its state and its tokens that no
+    other sequence names match the exact kernel); sequence 2 is refused as a
+    bad sequence: its state is untouched and the device error word is set."""
+    s = I.QWEN_08B
+    c = Case(gdn, s, [300, 0, 200], seed=98, n_pad=0, token_slots=False)
+    cu = np.array([0, 300, 0, 200], dtype=np.int32)
+    c.cu = ti(cu)
+    ref_out = c.prefill().clone()   # the exact kernel on the same tables
+    torch.cuda.synchronize()
+    assert gdn.get_device_error() == 1  # sequence 1's range
+    ref_pool = c.pool.tensor.clone()
+    c.reset()
+    start = c.pool.tensor.clone()
+    out = chunked(c)
+    torch.cuda.synchronize()
+    assert gdn.get_device_error() == 1
+    ws0, ws2 = int(c.ws_np[0]), int(c.ws_np[2])
+    got = c.pool.tensor.cpu().numpy()
+    want = ref_pool.cpu().numpy()
+    for h in range(s.hv):
+        err = state_rel_err(got[ws0, h], want[ws0, h].astype(np.float64))
+        assert err <= 5e-5, f"sequence 0 head {h}: {err:.3g}"
+    assert torch.equal(c.pool.tensor[ws2], start[ws2])
+    assert_out_close(f64(out[200:300]), f64(ref_out[200:300]), "bf16")
