@@ -321,3 +321,28 @@ def test_binding_accepts_only_device_or_pinned_pointers():
     with pytest.raises(ValueError, match="must be a CUDA tensor$"):
         _ptr(torch.zeros(4), "x")
     assert _ptr(None, "x", host_ok=True) is None
+
+
+def test_prefill_chunked_workspace_holds_every_chunk(L):
+    """The chunked prefill's workspace: sequence s's chunk j (64 tokens a
+    chunk) lives in unit cu_seqlens[s] // 64 + s + j of each value head.  For
+    random nondecreasing cu_seqlens the units of all chunks are distinct and
+    lie inside the size gdn_prefill_chunked_workspace_bytes reports."""
+    import numpy as np
+    block = L.gdn_prefill_chunked_workspace_bytes(1, 1, 1) // 2  # one sequence of one token: 2 units
+    assert block > 0 and block % 128 == 0
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        nseq = int(rng.integers(1, 12))
+        lens = rng.integers(0, 300, size=nseq)
+        lens[rng.random(nseq) < 0.2] = 0
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+        T = int(cu[-1])
+        hv = int(rng.integers(1, 5))
+        units = L.gdn_prefill_chunked_workspace_bytes(nseq, T, hv) // (hv * block)
+        seen = set()
+        for s in range(nseq):
+            for j in range((int(lens[s]) + 63) // 64):
+                u = int(cu[s]) // 64 + s + j
+                assert u not in seen and 0 <= u < units, (cu.tolist(), s, j, u, units)
+                seen.add(u)
