@@ -52,8 +52,12 @@
  *    [0, num_slots), a real row whose write slot is 0, or a twin row whose
  *    write slot equals its read slot) skip that row, zero its outputs and set
  *    a sticky per-device error word, read and cleared by
- *    gdn_get_device_error().  Kernels never trap or assert; their waits on
- *    shared-memory barriers are bounded and report GDN_DEVERR_TIMEOUT.
+ *    gdn_get_device_error().  Kernels never trap or assert; every wait on a
+ *    shared-memory barrier gives up one second after it began (the GPU's
+ *    global timer) and reports GDN_DEVERR_TIMEOUT.
+ *  - Scratch: the state kernels' two work counters live in the library's
+ *    device memory (one pair a pool handle); gdn_prefill_chunked's
+ *    workspace for bf16 activations is caller-owned device memory.
  *  - Preconditions not checked on the fast path: real rows name distinct
  *    write slots, and no row writes a slot another row reads.
  *    gdn_validate_slots() checks them (it synchronises).
