@@ -102,10 +102,14 @@ class GDNStatePool:
     """Recurrent state pool [num_slots][hv][dv][dk] fp32 in torch-owned memory.
 
     The library wraps the tensor (it never frees it).  Slot 0 is the null slot.
+    The pool also holds its in-place counters (`inplace_counters`, zeroed
+    int32 device memory the library's in-place layer launches schedule with);
+    `inplace_counters=False` leaves them out, and in-place launches then give
+    each CTA whole qk heads.
     """
 
     def __init__(self, num_slots: int, hk: int, hv: int, dk: int, dv: int, device=None,
-                 tensor: Optional[torch.Tensor] = None):
+                 tensor: Optional[torch.Tensor] = None, inplace_counters: bool = True):
         L = _lib.load()
         device = torch.device(device if device is not None else "cuda")
         if tensor is None:
@@ -118,6 +122,12 @@ class GDNStatePool:
         _check(L.gdn_state_pool_wrap(_ptr(tensor, "state"), num_slots, gdn_dims(hk, hv, dk, dv),
                                      ctypes.byref(h)))
         self._h = h
+        self.counters = None
+        if inplace_counters:
+            nbytes = L.gdn_pool_inplace_counter_bytes(num_slots, gdn_dims(hk, hv, dk, dv))
+            self.counters = torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device=tensor.device)
+            _check(L.gdn_pool_attach_inplace_counters(h, _ptr(self.counters, "in-place counters"),
+                                                      self.counters.numel() * 4))
 
     @property
     def handle(self):

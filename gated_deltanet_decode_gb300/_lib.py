@@ -38,6 +38,7 @@ GDN_NOALLOC_SCRATCH_SLOTS = 64
 EXPORTS = [
     "gdn_last_error", "gdn_abi_version",
     "gdn_state_pool_create", "gdn_state_pool_wrap", "gdn_state_pool_destroy", "gdn_pool_data",
+    "gdn_pool_inplace_counter_bytes", "gdn_pool_attach_inplace_counters",
     "gdn_pool_num_slots", "gdn_pool_dims", "gdn_pool_zero_slots", "gdn_pool_copy_slots",
     "conv_state_pool_create", "conv_state_pool_wrap", "conv_state_pool_destroy", "conv_pool_data",
     "conv_pool_num_slots", "conv_pool_zero_slots", "conv_pool_copy_slots",
@@ -63,6 +64,8 @@ _SIGS = {
     "gdn_state_pool_wrap": (_I, [_P, _I, gdn_dims, _PP]),
     "gdn_state_pool_destroy": (_I, [_P]),
     "gdn_pool_data": (_P, [_P]),
+    "gdn_pool_inplace_counter_bytes": (ctypes.c_size_t, [_I, gdn_dims]),
+    "gdn_pool_attach_inplace_counters": (_I, [_P, _P, ctypes.c_size_t]),
     "gdn_pool_num_slots": (_I, [_P]),
     "gdn_pool_dims": (gdn_dims, [_P]),
     "gdn_pool_zero_slots": (_I, [_P, _P, _I, _P]),

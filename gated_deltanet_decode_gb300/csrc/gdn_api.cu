@@ -283,6 +283,14 @@ static int check_dims(gdn_dims d)
 
 static size_t state_slot_floats(gdn_dims d) { return (size_t)d.hv * d.dv * d.dk; }
 
+// in-place counters: one 32-bit counter per (slot, qk head), a slot's row
+// padded to 16 bytes so that zero_slots can clear it
+static int qk_stride_of(gdn_dims d) { return (d.hk + 3) & ~3; }
+static size_t qk_count_bytes(int num_slots, gdn_dims d)
+{
+    return (size_t)num_slots * (size_t)qk_stride_of(d) * sizeof(unsigned int);
+}
+
 int gdn_state_pool_create(int num_slots, gdn_dims dims, void *stream, gdn_pool **out)
 {
     if (!out)
@@ -302,21 +310,37 @@ int gdn_state_pool_create(int num_slots, gdn_dims dims, void *stream, gdn_pool *
     }
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaMalloc(state pool)");
+    const size_t cbytes = qk_count_bytes(num_slots, dims);
+    void *cnt = nullptr;
+    e = cudaMalloc(&cnt, cbytes);
+    if (e != cudaSuccess) {
+        cudaFree(p);
+        if (e == cudaErrorMemoryAllocation) {
+            cudaGetLastError();
+            return fail(GDN_ENOMEM, "cudaMalloc(%zu bytes) for the in-place counters failed", cbytes);
+        }
+        return cuda_fail(e, "cudaMalloc(in-place counters)");
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     e = cudaMemsetAsync(p, 0, bytes, s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(cnt, 0, cbytes, s);
     if (e == cudaSuccess)
         e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) {
         cudaFree(p);
+        cudaFree(cnt);
         return cuda_fail(e, "zero-filling the state pool");
     }
     int wi = 0;
     rc = work_index_take(&wi);
     if (rc) {
         cudaFree(p);
+        cudaFree(cnt);
         return rc;
     }
-    *out = new gdn_pool{static_cast<float *>(p), num_slots, dims, true, wi};
+    *out = new gdn_pool{static_cast<float *>(p), num_slots, dims, true, wi,
+                        static_cast<unsigned int *>(cnt), qk_stride_of(dims), true};
     return ok();
 }
 
@@ -338,7 +362,34 @@ int gdn_state_pool_wrap(void *dev_ptr, int num_slots, gdn_dims dims, gdn_pool **
     rc = work_index_take(&wi);
     if (rc)
         return rc;
-    *out = new gdn_pool{static_cast<float *>(dev_ptr), num_slots, dims, false, wi};
+    *out = new gdn_pool{static_cast<float *>(dev_ptr), num_slots, dims, false, wi, nullptr, qk_stride_of(dims),
+                        false};
+    return ok();
+}
+
+size_t gdn_pool_inplace_counter_bytes(int num_slots, gdn_dims dims)
+{
+    if (num_slots < 1 || check_dims(dims) != GDN_OK)
+        return 0;
+    return qk_count_bytes(num_slots, dims);
+}
+
+int gdn_pool_attach_inplace_counters(gdn_pool *pool, void *dev_counters, size_t bytes)
+{
+    if (!pool)
+        return fail(GDN_EINVAL, "pool is NULL");
+    if (pool->owns_qk_count)
+        return fail(GDN_EINVAL, "the pool was created with its own in-place counters");
+    if (!dev_counters) {
+        pool->qk_count = nullptr;
+        return ok();
+    }
+    if (!aligned16(dev_counters))
+        return fail(GDN_EINVAL, "in-place counters must be 16-byte aligned");
+    const size_t need = qk_count_bytes(pool->num_slots, pool->dims);
+    if (bytes < need)
+        return fail(GDN_EINVAL, "in-place counters of %zu bytes: the pool needs %zu", bytes, need);
+    pool->qk_count = static_cast<unsigned int *>(dev_counters);
     return ok();
 }
 
@@ -349,6 +400,11 @@ int gdn_state_pool_destroy(gdn_pool *pool)
     cudaError_t e = cudaSuccess;
     if (pool->owned)
         e = cudaFree(pool->data);
+    if (pool->owns_qk_count) {
+        const cudaError_t e2 = cudaFree(pool->qk_count);
+        if (e == cudaSuccess)
+            e = e2;
+    }
     work_index_give(pool->work_index);
     delete pool;
     if (e != cudaSuccess)
@@ -426,8 +482,13 @@ int gdn_pool_zero_slots(gdn_pool *pool, const int32_t *slots, int n, void *strea
 {
     if (!pool)
         return fail(GDN_EINVAL, "pool is NULL");
-    return zero_slots(pool->data, state_slot_floats(pool->dims) * sizeof(float), pool->num_slots, slots,
-                      n, stream);
+    int rc = zero_slots(pool->data, state_slot_floats(pool->dims) * sizeof(float), pool->num_slots, slots, n,
+                        stream);
+    if (rc || !pool->qk_count)
+        return rc;
+    // the slots' in-place counters too (a launch that stopped early can leave them set)
+    return zero_slots(pool->qk_count, (size_t)pool->qk_stride * sizeof(unsigned int), pool->num_slots, slots, n,
+                      stream);
 }
 
 // ---- conv pool -------------------------------------------------------------
@@ -685,6 +746,8 @@ static int layer_args(const void *x, conv_pool *cp, const void *w, const void *b
     s->read_slot = read_slot;
     s->write_slot = write_slot;
     s->in_place = keep_in_place ? 1 : 0;
+    s->qk_count = keep_in_place ? pool->qk_count : nullptr;
+    s->qk_stride = pool->qk_stride;
     s->out = out;
     s->rows = rows;
     s->hk = d.hk;

@@ -13,6 +13,9 @@ struct gdn_pool {
     gdn_dims dims;
     bool owned;
     int work_index; // this pool's pair of work counters in the library's table
+    unsigned int *qk_count; // in-place counters [num_slots][qk_stride], or NULL
+    int qk_stride;          // counters a slot: hk rounded up to a multiple of 4
+    bool owns_qk_count;     // allocated with the pool (create), else caller memory
 };
 
 struct conv_pool {
@@ -44,6 +47,8 @@ struct StepArgs {
     unsigned int *work; // the pool's two work counters (claim, producers done), zero between launches
     int commit;         // twin only: swap read_slot and write_slot once every producer has read them
     const int32_t *n_live; // device count or NULL: rows at or past *n_live are left alone (outputs zero)
+    unsigned int *qk_count; // fused layer, in place: the pool's counters [slot][qk_stride], or NULL
+    int qk_stride;
     // fused layer only
     const void *x;
     void *conv;        // conv pool data

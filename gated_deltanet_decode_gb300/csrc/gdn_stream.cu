@@ -48,13 +48,20 @@
 //    its copies still in flight.
 //
 // Fused layer, in place: the q/k conv window of a qk group must be written
-// once, after every reader has read it.  In-place launches split the items
-// into ranges of whole groups (all value heads and row chunks sharing the qk
-// head), so a group's items run in order on one CTA and only the first of
-// them copies and reads the window; it writes the new window right after.
-// Twin launches write another slot, so the chunk-0 item of the group's first
-// value head writes it.  The arithmetic per row is the same in every
-// schedule, so twin and in place give bit-identical values.
+// once, after every reader has read it.  With the pool's in-place counters
+// (one per slot and qk head, zero between launches) the items are spread
+// over the CTAs as in a twin launch, and the v warp counts every item of a
+// (slot, qk head) on that pair's counter once the item's copies have landed;
+// the item that brings the count to group * chunks comes after every read of
+// the old window, so its v warp writes the new window (kept from its chain's
+// first item, beside the ring) and sets the counter back to zero.  Without
+// the counters (or where that copy does not fit beside the ring) in-place
+// launches split the items into ranges of whole groups (all value heads and
+// row chunks sharing the qk head), so a group's items run in order on one CTA
+// and only the first of them copies and reads the window; it writes the new
+// window right after.  Twin launches write another slot, so the chunk-0 item
+// of the group's first value head writes it.  The arithmetic per row is the
+// same in every schedule, so twin and in place give bit-identical values.
 #include <atomic>
 
 #include "gdn_device.cuh"
@@ -125,18 +132,19 @@ struct Meta {
     float alpha, beta;
 };
 
-// Work units, in (row, value head, chunk) order.  Fine: a unit is an item.
-// Coarse: a unit is a whole qk group (group value heads x row chunks), its
-// items in order.  The first n_static units are split into contiguous ranges,
-// CTA b of g taking [first(b), first(b + 1)) (equal to within one unit); the
-// rest are claimed `claim` units at a time from the pool's work counter by
-// whichever CTA runs out first, so that CTAs that stream slower take less of
-// the tail.
+// Items in (row, value head, chunk) order, which is also (row, qk head,
+// value head of the group, chunk): a qk group's items are consecutive.  A
+// unit is per_unit consecutive items (per_unit divides hv * chunks); coarse
+// launches (in place without counters) take a whole qk group a unit.  The
+// first n_static units are split into contiguous ranges, CTA b of g taking
+// [first(b), first(b + 1)) (equal to within one unit); the rest are claimed
+// `claim` units at a time from the pool's work counter by whichever CTA runs
+// out first, so that CTAs that stream slower take less of the tail.
 struct Sched {
     int hv, group, chunks;
     int n_units;
-    int per_unit;    // 1 (fine) or group * chunks (coarse)
-    int coarse;
+    int per_unit;    // items a unit
+    int coarse;      // in place, whole qk groups a CTA, the group's first item writes its window
     int n_static;    // units split statically (n_units: no claims)
     int claim;       // units per claim
 
@@ -147,27 +155,26 @@ struct Sched {
     // item i of the whole launch
     __device__ __forceinline__ void item_at(int i, int &r, int &h, int &chunk) const
     {
-        const int unit = i / per_unit;
-        if (!coarse) {
-            chunk = unit % chunks;
-            const int rh = unit / chunks;
-            h = rh % hv;
-            r = rh / hv;
-        } else {
-            const int j = i % per_unit;
-            const int hk = hv / group;
-            r = unit / hk;
-            h = (unit % hk) * group + j / chunks;
-            chunk = j % chunks;
-        }
+        chunk = i % chunks;
+        const int rh = i / chunks;
+        h = rh % hv;
+        r = rh / hv;
     }
 };
 
-// Stages a CTA holds: as many as fit beside the other CTAs of its SM.
+// Stages a CTA holds: as many as fit beside the other CTAs of its SM.  An
+// in-place launch with counters also keeps its current chain's new q/k
+// window ([W-1][2 DK] activations) after the ring, where the space left over
+// holds it (in-place launches of the shapes where it does not fit take whole
+// qk groups a CTA).
 template <typename T, int DK, bool LAYER, int W> struct Stages {
-    static constexpr int fit = ((227 * 1024) / ctas_per_sm<LAYER>() - 4096) / Stage<T, DK, LAYER, W>::BYTES;
+    static constexpr int avail = (227 * 1024) / ctas_per_sm<LAYER>() - 4096;
+    static constexpr int fit = avail / Stage<T, DK, LAYER, W>::BYTES;
     static constexpr int value = fit > kMaxStages ? kMaxStages : fit;
     static_assert(value >= 2, "a stage ring needs two stages");
+    static constexpr int RING = value * Stage<T, DK, LAYER, W>::BYTES;
+    static constexpr int QKW = LAYER ? (2 * DK * (W - 1) * (int)sizeof(T) + 127) & ~127 : 0;
+    static constexpr bool counted_in_place = LAYER && RING + QKW <= avail;
 };
 
 template <typename T, int DK, bool LAYER, int W>
@@ -465,6 +472,35 @@ gdn_stream_kernel(const StepArgs p, const Sched sc)
     } else if (LAYER && warp == kConsumerWarps + 1) {
         // =========================== v warp =============================
         if constexpr (LAYER) {
+            // In place with counters: the count of item k goes out after its
+            // stage is released and is looked at (settled) one item later, or
+            // before a new chain overwrites the kept window, so its latency hides
+            // behind the next item's wait.  A lane keeps the channels c = lane +
+            // 32 i of the window, written and read by that lane alone.
+            const bool counted_ip = p.in_place && !sc.coarse;
+            const unsigned per_pair = (unsigned)(group * sc.chunks);
+            T *qkw = reinterpret_cast<T *>(smem + Stages<T, DK, LAYER, W>::RING); // [W-1][2 DK]
+            unsigned *pend = nullptr; // the counter whose count is in flight
+            unsigned pend_old = 0;    // lane 0: the value before that count
+            int pend_slot = 0, pend_g = 0;
+            auto settle = [&]() {
+                if (!pend)
+                    return;
+                const unsigned old = __shfl_sync(0xffffffffu, pend_old, 0);
+                if (old == per_pair - 1) {
+                    // every item of the pair has counted, so every read of the old window is done
+                    T *wout = reinterpret_cast<T *>(p.conv) + (size_t)pend_slot * (W - 1) * C;
+                    for (int c = lane; c < 2 * DK; c += 32) {
+                        const int gc = c < DK ? pend_g * DK + c : p.hk * DK + pend_g * DK + (c - DK);
+#pragma unroll
+                        for (int j = 0; j < W - 1; ++j)
+                            wout[(size_t)j * C + gc] = qkw[j * 2 * DK + c];
+                    }
+                    if (lane == 0)
+                        atomicExch(pend, 0u); // zero for the pool's next launch
+                }
+                pend = nullptr;
+            };
             for (int k = 0;; ++k) {
                 const int s = k % nst;
                 if (!mbar_wait(full_bar(s), (uint32_t)((k / nst) & 1))) {
@@ -473,8 +509,22 @@ gdn_stream_kernel(const StepArgs p, const Sched sc)
                 }
                 unsigned char *st = stage(s);
                 const Meta m = *reinterpret_cast<const Meta *>(st + L::META);
-                if (m.live < 0)
+                if (m.live < 0) {
+                    settle();
                     break; // end of the stream
+                }
+                if (counted_ip && m.live && !m.reuse) {
+                    // a chain starts: keep its new q/k window (old positions 1..W-2, then x)
+                    settle();
+                    const T *win = reinterpret_cast<const T *>(st + L::WIN);
+                    const T *xs = reinterpret_cast<const T *>(st + L::XS);
+                    for (int c = lane; c < 2 * DK; c += 32) {
+#pragma unroll
+                        for (int j = 0; j + 1 < W - 1; ++j)
+                            qkw[j * 2 * DK + c] = win[(j + 1) * L::NCH + c];
+                        qkw[(W - 2) * 2 * DK + c] = xs[c];
+                    }
+                }
                 if (m.live) {
                     float *vn = reinterpret_cast<float *>(st + L::VN);
                     T *wout = reinterpret_cast<T *>(p.conv) + (size_t)m.ws * (W - 1) * C;
@@ -501,6 +551,15 @@ gdn_stream_kernel(const StepArgs p, const Sched sc)
                 if (lane == 0) {
                     mbar_arrive(vready_bar(s));
                     mbar_arrive(empty_bar(s));
+                }
+                if (counted_ip && m.live) {
+                    settle();
+                    const int g = m.h / group;
+                    pend = p.qk_count + (size_t)m.rs * p.qk_stride + g;
+                    pend_slot = m.rs;
+                    pend_g = g;
+                    if (lane == 0)
+                        pend_old = atomicAdd(pend, 1u);
                 }
             }
         }
@@ -547,10 +606,12 @@ gdn_stream_kernel(const StepArgs p, const Sched sc)
                             val = round_act<T>(conv_channel<W>(winq, xq, wq, bq, p.silu != 0));
                             // The q/k window is written once per group.  Twin: by the chunk-0
                             // item of the group's first value head (it writes another slot).
-                            // In place: a group lies within one CTA and only its first item
-                            // copies the window (the rest reuse its q/k), so that item writes
-                            // the window as soon as its own copy has landed.
-                            const bool writer = p.in_place ? true : (m.h % group == 0 && m.chunk == 0);
+                            // In place, whole groups a CTA: a group's only window reader is
+                            // its first item, which writes the window as soon as its own
+                            // copy has landed.  In place with counters: by the v warp of the group's
+                            // last item (above), never here.
+                            const bool writer =
+                                p.in_place ? sc.coarse != 0 : (m.h % group == 0 && m.chunk == 0);
                             if (writer) {
                                 T *wout = reinterpret_cast<T *>(p.conv) + (size_t)m.ws * (W - 1) * C;
                                 const int gc = isq ? g * DK + c : p.hk * DK + g * DK + (c - DK);
@@ -711,6 +772,55 @@ int num_sms()
     return g_num_sms[dev];
 }
 
+// A launch's split: units of per_unit items, the first n_static of them in
+// static ranges over `grid` CTAs, the rest claimed `claim` units at a time.
+struct Split {
+    int per_unit, n_units, grid, n_static, claim;
+};
+
+Split make_split(long long items, int per_unit, int chunks, int slots, bool can_claim)
+{
+    Split p;
+    p.per_unit = per_unit;
+    p.n_units = (int)(items / per_unit);
+    p.grid = p.n_units < slots ? p.n_units : slots;
+    // With a dozen or more items a CTA, half of the units are claimed at run
+    // time, about a (row, value head) a claim; with fewer, the claims' latency
+    // costs more than the balance they buy (measured on the 0.8B and 9B layer
+    // shapes at 16 to 256 rows).
+    p.claim = (chunks < 4 ? chunks : 4) / per_unit;
+    if (p.claim < 1)
+        p.claim = 1;
+    p.n_static = p.n_units;
+    if (can_claim && items >= (long long)kClaimMinItemsPerCta * p.grid)
+        p.n_static = p.n_units / 2 / p.claim * p.claim;
+    return p;
+}
+
+// The longest share of a CTA under a split, in item times: the largest
+// static range plus one claim, each chain start (q/k conv, norms and their
+// CTA-wide sum, once per row and qk head a CTA meets) counted as 1.5 items.
+// A static range of single items that cuts chains meets up to one chain more
+// than whole chains would.  Fitted on the fused layer (0.8B and 9B shapes,
+// 1 to 256 rows, twin and in place): single items at 1-8, 32 and 64 rows of
+// the 0.8B shape and at every size of the 9B one (whose chains are 8 items),
+// whole chains at 16, 24, 48 and 96 rows of the 0.8B shape (10 % faster at
+// 16 and 24 rows); where it picks the slower of the two, by under 0.25 us.
+double share_cost(const Split &p, int chain)
+{
+    if (p.grid <= 0)
+        return 0.0;
+    const long long m = ((long long)p.n_static + p.grid - 1) / p.grid; // units in the largest range
+    const long long it = m * p.per_unit;
+    long long starts = p.per_unit >= chain ? m : (it > 0 ? 1 + (it - 1 + chain - 1) / chain : 0);
+    if (starts > it)
+        starts = it;
+    double cost = (double)it + 1.5 * (double)starts;
+    if (p.n_static < p.n_units)
+        cost += (double)p.claim * p.per_unit + 1.5;
+    return cost;
+}
+
 template <typename T, int DK, bool LAYER, int W>
 cudaError_t launch_stream(const StepArgs &a, bool coarse, cudaStream_t s)
 {
@@ -720,39 +830,47 @@ cudaError_t launch_stream(const StepArgs &a, bool coarse, cudaStream_t s)
     sc.hv = a.hv;
     sc.group = a.hv / a.hk;
     sc.chunks = (a.dv + RB - 1) / RB;
+    // in place without room for the kept window: whole groups a CTA
+    if (LAYER && a.in_place && !Stages<T, DK, LAYER, W>::counted_in_place)
+        coarse = true;
     sc.coarse = coarse ? 1 : 0;
-    sc.per_unit = coarse ? sc.group * sc.chunks : 1;
     const long long items = (long long)a.rows * a.hv * sc.chunks;
     if (items > (1ll << 30))
         return cudaErrorInvalidValue;
-    sc.n_units = (int)(items / sc.per_unit);
-    if (sc.n_units == 0)
+    if (items == 0)
         return cudaSuccess;
     // ctas_per_sm CTAs per SM, each with as many stages as fit
     constexpr int kCtas = ctas_per_sm<LAYER>();
-    const size_t smem = (size_t)Stages<T, DK, LAYER, W>::value * L::BYTES;
+    const int slots = kCtas * num_sms();
+    // a unit: one item, or a whole chain (a row's qk group: group value heads
+    // x chunks), whichever gives the shorter longest share; coarse launches
+    // take whole chains
+    const int chain = sc.group * sc.chunks;
+    Split sp = make_split(items, coarse ? chain : 1, sc.chunks, slots, a.work != nullptr);
+    if (!coarse) {
+        const Split whole = make_split(items, chain, sc.chunks, slots, a.work != nullptr);
+        if (share_cost(whole, chain) < share_cost(sp, chain))
+            sp = whole;
+    }
+    sc.per_unit = sp.per_unit;
+    sc.n_units = sp.n_units;
+    sc.n_static = sp.n_static;
+    sc.claim = sp.claim;
+    using ST = Stages<T, DK, LAYER, W>;
+    const size_t smem_max = (size_t)ST::RING + (ST::counted_in_place ? ST::QKW : 0);
+    const size_t smem = (size_t)ST::RING + (LAYER && a.in_place && !coarse ? ST::QKW : 0);
     auto kern = gdn_stream_kernel<T, DK, LAYER, W>;
     static std::atomic<unsigned long long> configured{0}; // one bit per device, per instantiation
     int dev = 0;
     cudaGetDevice(&dev);
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
         if (e != cudaSuccess)
             return e;
         configured.fetch_or(bit, std::memory_order_release);
     }
-    const int slots = kCtas * num_sms();
-    const int grid = (int)(sc.n_units < slots ? sc.n_units : slots);
-    // With a dozen or more items a CTA, half of the units are claimed at run
-    // time, a (row, value head) of fine items (or one coarse unit) a claim;
-    // with fewer, the claims' latency costs more than the balance they buy
-    // (measured on the 0.8B and 9B layer shapes at 16 to 256 rows).
-    sc.claim = coarse ? 1 : (sc.chunks < 4 ? sc.chunks : 4);
-    sc.n_static = sc.n_units;
-    if (items >= (long long)kClaimMinItemsPerCta * grid && a.work)
-        sc.n_static = sc.n_units / 2 / sc.claim * sc.claim;
-    return launch_pdl(kern, dim3(grid), dim3(threads_for<LAYER>()), smem, s, a, sc);
+    return launch_pdl(kern, dim3(sp.grid), dim3(threads_for<LAYER>()), smem, s, a, sc);
 }
 
 template <typename T, bool LAYER, int W>
@@ -791,7 +909,7 @@ cudaError_t launch_gdn_step(const StepArgs &a, int dtype, cudaStream_t s)
 
 cudaError_t launch_gdn_layer(const StepArgs &a, int dtype, cudaStream_t s)
 {
-    const bool coarse = a.in_place != 0;
+    const bool coarse = a.in_place != 0 && a.qk_count == nullptr;
     switch (a.width) {
     case 2: return dtype == GDN_BF16 ? dispatch_dk<__nv_bfloat16, true, 2>(a, coarse, s) : dispatch_dk<float, true, 2>(a, coarse, s);
     case 3: return dtype == GDN_BF16 ? dispatch_dk<__nv_bfloat16, true, 3>(a, coarse, s) : dispatch_dk<float, true, 3>(a, coarse, s);

@@ -131,18 +131,44 @@ int gdn_abi_version(void);
  * takes one pair of work counters from a fixed table in the library's device
  * memory (GDN_MAX_POOLS pairs; GDN_ENOMEM once all are taken) and returns it
  * in gdn_state_pool_destroy, which must come after the pool's last launch has
- * finished. */
+ * finished.  gdn_state_pool_create also allocates the pool's in-place
+ * counters (below); a wrapped pool has none until some are attached. */
 int gdn_state_pool_create(int num_slots, gdn_dims dims, void *stream, gdn_pool **out);
 int gdn_state_pool_wrap(void *dev_ptr, int num_slots, gdn_dims dims, gdn_pool **out);
 int gdn_state_pool_destroy(gdn_pool *pool);
+
+/* In-place counters: scheduling scratch of the fused layer in place
+ * (gdn_layer_decode and its variants with keep_in_place), one 32-bit counter
+ * per (slot, qk head), zero between launches.  A qk head's conv window is
+ * read by the items of all its value heads and, in place ("mstar PR #1139",
+ * "What changed": keep_in_place updates the slot a row reads), rewritten in
+ * the same slot, so it must be written after its last read.  With the counters, a
+ * launch spreads those items over all CTAs (as twin launches do) and the
+ * item that counts last writes the window; without them each CTA takes
+ * whole qk heads, which leaves most of the GPU idle below about 30 rows
+ * (so do two shapes whose kept window does not fit beside the kernel's
+ * ring: dk = 256 with width 3 in bf16 and with width 4 in fp32).  Results
+ * are bit-identical either way.
+ * gdn_pool_inplace_counter_bytes gives the size for a pool (0 for bad
+ * arguments).  gdn_pool_attach_inplace_counters gives a wrapped pool
+ * caller-owned device memory of at least that size, 16-byte aligned and
+ * zero-filled, which must stay allocated while launches may use it; NULL
+ * detaches them.  It makes no CUDA call; GDN_EINVAL for a pool made by
+ * gdn_state_pool_create (it has its own), a NULL pool, a misaligned or short
+ * buffer.  Counters are left set only by a launch that stopped on
+ * GDN_DEVERR_TIMEOUT or by an in-place launch whose live rows name one slot
+ * twice (a caller error: their states race); gdn_pool_zero_slots clears the
+ * listed slots' counters with their states. */
+size_t gdn_pool_inplace_counter_bytes(int num_slots, gdn_dims dims);
+int gdn_pool_attach_inplace_counters(gdn_pool *pool, void *dev_counters, size_t bytes);
 void *gdn_pool_data(const gdn_pool *pool);
 int gdn_pool_num_slots(const gdn_pool *pool);
 gdn_dims gdn_pool_dims(const gdn_pool *pool);
 
 /* Zero the n slots listed in the device array `slots` (a request's release
- * or rollback zeroes both of its slots: "mstar PR #1139", "Tests").  Slots
- * outside [0, num_slots) are skipped and set the device error word.  n may
- * be 0. */
+ * or rollback zeroes both of its slots: "mstar PR #1139", "Tests"), and
+ * their in-place counters if the pool has them.  Slots outside
+ * [0, num_slots) are skipped and set the device error word.  n may be 0. */
 int gdn_pool_zero_slots(gdn_pool *pool, const int32_t *slots, int n, void *stream);
 
 /* Snapshots and forks: slot dst[i] receives an exact copy of slot src[i], for

@@ -71,6 +71,29 @@ def test_state_pool_wrap_validation(L):
     assert L.gdn_state_pool_destroy(None) == 0
 
 
+def test_inplace_counters_size_and_attach(L):
+    """One 32-bit counter per (slot, qk head), a slot's row padded to 16 bytes;
+    attaching checks the pool, the alignment and the size and makes no CUDA
+    call (a fake, never dereferenced address is accepted)."""
+    n = L.gdn_pool_inplace_counter_bytes
+    assert n(9, _dims(hk=2, hv=2)) == 9 * 4 * 4           # hk 2 -> 4 counters a slot
+    assert n(129, _dims(hk=16, hv=16, dk=128, dv=128)) == 129 * 16 * 4
+    assert n(3, _dims(hk=5, hv=10)) == 3 * 8 * 4           # hk 5 -> 8
+    assert n(0, _dims()) == 0 and n(9, _dims(dk=48)) == 0  # bad arguments
+    rc, h = _wrap(L, num_slots=9, hk=2, hv=2)
+    assert rc == 0
+    need = n(9, _dims(hk=2, hv=2))
+    a = L.gdn_pool_attach_inplace_counters
+    assert a(None, FAKE, need) == EINVAL
+    assert a(h, FAKE + 4, need) == EINVAL                    # misaligned
+    assert b"aligned" in L.gdn_last_error()
+    assert a(h, FAKE, need - 1) == EINVAL                    # short
+    assert a(h, FAKE, need) == 0
+    assert a(h, FAKE + 4096, need + 64) == 0                 # replaced
+    assert a(h, None, 0) == 0                                # detached
+    assert L.gdn_state_pool_destroy(h) == 0
+
+
 def test_state_pool_handle_limit(L):
     """Every state pool handle holds one pair of work counters from a fixed
     table; handles beyond GDN_MAX_POOLS fail with GDN_ENOMEM and destroyed
