@@ -57,7 +57,7 @@ constexpr int TC_WARPS = 8;
 constexpr int TC_THREADS = TC_WARPS * 32;
 constexpr uint32_t kTmemCols = 512;
 
-// TMEM columns
+// TMEM columns (O accumulates into U's columns once U is split)
 constexpr uint32_t C_S = 0, C_Z = 128, C_Y = 192, C_U = 256, C_SH = 320, C_SL = 384;
 constexpr uint32_t C_EH = 320, C_EL = 352, C_UH = 384, C_UL = 416, C_WH = 128, C_WL = 160;
 
@@ -97,13 +97,15 @@ __device__ __forceinline__ int unit_base(const int32_t *cu, int s) { return cu[s
 // Shared-memory layout of the chunk kernel, byte offsets.
 struct TS {
     static constexpr int KQ = 0;                  // bf16 [128][128]: raw K rows 0-63, raw Q rows 64-127
-    static constexpr int KT = KQ + 128 * CD * 2;  // bf16 [128 = dk][64 = tokens]: raw K transposed
-    static constexpr int PB = KT + CD * CK * 2;   // two prep blocks (PW), chunk parity
+    static constexpr int KT_BYTES = CD * CK * 2;  // bf16 [128 = dk][64 = tokens]: raw K transposed
+    static constexpr int KT = KQ + 128 * CD * 2;  // two of them, chunk parity
+    static constexpr int PB = KT + 2 * KT_BYTES;  // two prep blocks (PW), chunk parity
     static constexpr int BARS = PB + 2 * PW::BYTES; // mbarriers: Z|Y, U, O and S, prep block 0, 1
     static constexpr int TADDR = BARS + 48;       // the TMEM base address
     static constexpr int BYTES = TADDR + 16;
-    static constexpr int STAGE = (BYTES + 127) & ~127; // raw q, k, v of the next chunk, [CK][CD] each
-    static constexpr int TOTAL = STAGE + 3 * CK * CD * 2;
+    static constexpr int STAGE = (BYTES + 127) & ~127; // raw v of the next chunk, [CK][CD]
+    static constexpr int OUTS = STAGE + CK * CD * 2;   // bf16 outputs of a chunk, [CK][CD]
+    static constexpr int TOTAL = OUTS + CK * CD * 2;
 };
 static_assert(TS::TOTAL <= 227 * 1024, "shared memory");
 static_assert(TS::BARS % 8 == 0 && TS::KT % 1024 == 0 && TS::PB % 128 == 0, "alignment");
@@ -388,9 +390,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
     unsigned char *const KT = smem + TS::KT;
     uint64_t *const bars = reinterpret_cast<uint64_t *>(smem + TS::BARS);
     uint32_t *const taddr_slot = reinterpret_cast<uint32_t *>(smem + TS::TADDR);
-    bf16 *const RQ = reinterpret_cast<bf16 *>(smem + TS::STAGE);
-    bf16 *const RK = RQ + CK * CD;
-    bf16 *const RV = RK + CK * CD;
+    bf16 *const RV = reinterpret_cast<bf16 *>(smem + TS::STAGE);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;
@@ -473,21 +473,51 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
     const bf16 *const vg = reinterpret_cast<const bf16 *>(p.v);
 
     // the raw q, k, v of the chunk starting at token cn (zeros past the
-    // sequence), 16 bytes a copy, every thread a share, into the staging area
+    // sequence), 16 bytes a copy, every thread a share: k and q straight into
+    // the K | Q tile (a 16-byte piece of a row is a core-matrix row), v into
+    // the staging area
     auto stage = [&](int cn) {
         const int nn = min(CK, L - cn);
         for (int e = tid; e < 3 * CK * (CD / 8); e += TC_THREADS) {
             const int which = e / (CK * (CD / 8)), rem = e - which * (CK * (CD / 8));
-            const int tt = rem / (CD / 8), j = rem - tt * (CD / 8);
+            // k and q: consecutive threads take consecutive 16-byte rows of the
+            // tile (a core matrix's 8 rows, then the next core matrix), so the
+            // shared-memory writes do not collide in the banks; v: row-major
+            const int cmi = rem >> 3;
+            const int tt = which < 2 ? ((cmi / (CD / 8)) << 3) + (rem & 7) : rem / (CD / 8);
+            const int j = which < 2 ? cmi % (CD / 8) : rem % (CD / 8);
             const bool live = tt < nn;
             const size_t tok = (size_t)(t0 + cn + (live ? tt : 0));
             const bf16 *src = which == 0   ? qg + (tok * p.hk + hq) * CD
                               : which == 1 ? kg + (tok * p.hk + hq) * CD
                                            : vg + (tok * p.hv + h) * CD;
-            bf16 *dst = (which == 0 ? RQ : which == 1 ? RK : RV) + tt * CD;
-            cp_async16(dst + 8 * j, src + 8 * j, live ? 16 : 0);
+            void *dst = which == 0   ? (void *)(KQ + cm_off<CD>(CK + tt, 8 * j))
+                        : which == 1 ? (void *)(KQ + cm_off<CD>(tt, 8 * j))
+                                     : (void *)(RV + tt * CD + 8 * j);
+            cp_async16(dst, src + 8 * j, live ? 16 : 0);
         }
         cp_async_commit();
+    };
+    // K^T of the chunk whose K rows are in the K | Q tile, into K^T buffer
+    // `buf`: a warp transposes four 8x8 core matrices a step (ldmatrix .trans:
+    // lane l gets tokens 2 (l % 4) and 2 (l % 4) + 1 of dk row l / 4) and
+    // stores each as one word of the transposed core-matrix row
+    auto build_kt = [&](int buf) {
+        unsigned char *const kt = KT + buf * TS::KT_BYTES;
+        for (int g = warp; g < (CK / 8) * (CD / 8) / 4; g += TC_WARPS) {
+            const int m = 4 * g + (lane >> 3);
+            const uint32_t src = sm_addr(KQ + cm_off<CD>(8 * (m / (CD / 8)) + (lane & 7), 8 * (m % (CD / 8))));
+            uint32_t r[4];
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                         : "r"(src)
+                         : "memory");
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int mi = 4 * g + i, tb = mi / (CD / 8), jb = mi % (CD / 8);
+                *reinterpret_cast<uint32_t *>(kt + cm_off<CK>(8 * jb + (lane >> 2), 8 * tb + 2 * (lane & 3))) = r[i];
+            }
+        }
     };
     // the prep block of chunk cj into the shared prep block of its parity (one
     // bulk copy; its previous chunk's products, which read it, are done)
@@ -500,16 +530,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
                       (uint32_t)PW::BYTES, bar);
         }
     };
-    // this thread's outputs of the chunk starting at cbase (nn tokens): row
-    // `row` of O, tokens 32*half .. 32*half + 31
-    auto write_outputs = [&](int cbase, int nn) {
+    // The outputs of a chunk leave in two steps: each thread puts its row
+    // `row` of O (in U's columns), tokens 32*half .. 32*half + 31, into the
+    // shared output tile (put_outputs); after a CTA barrier every thread
+    // stores 16-byte pieces of the tile's token rows (store_outputs).
+    bf16 *const OS = reinterpret_cast<bf16 *>(smem + TS::OUTS);
+    auto put_outputs = [&]() {
         float o[32];
-        tld32(tlane + C_Y + 32 * half, o);
+        tld32(tlane + C_U + 32 * half, o);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int t = 32 * half + i;
-            if (t < nn)
-                out[(size_t)(t0 + cbase + t) * out_tok + (size_t)h * CD + row] = from_f<bf16>(o[i]);
+        for (int i = 0; i < 32; ++i)
+            OS[(32 * half + i) * CD + row] = from_f<bf16>(o[i]);
+    };
+    // (16-byte stores when `out` is 16-byte aligned, as its rows then are;
+    // the call does not require it, so 2-byte stores otherwise)
+    const bool out16 = (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+    auto store_outputs = [&](int cbase, int nn) {
+        if (out16) {
+            for (int e = tid; e < nn * (CD / 8); e += TC_THREADS) {
+                const int t = e / (CD / 8), j = e % (CD / 8);
+                *reinterpret_cast<uint4 *>(out + (size_t)(t0 + cbase + t) * out_tok + (size_t)h * CD + 8 * j) =
+                    *reinterpret_cast<const uint4 *>(OS + t * CD + 8 * j);
+            }
+        } else {
+            for (int e = tid; e < nn * CD; e += TC_THREADS)
+                out[(size_t)(t0 + cbase + e / CD) * out_tok + (size_t)h * CD + (e % CD)] = OS[e];
         }
     };
     if (L > 0)
@@ -535,8 +580,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
             asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(kTmemCols) : "memory");
         return;
     }
-    if (L > 0)
+    if (L > 0) {
         prep_copy(0);
+        cp_async_wait_all();
+        __syncthreads(); // the first chunk's K rows are in place
+        build_kt(0);
+    }
 
     bool abort = false;
     int n_prev = 0;
@@ -557,10 +606,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
         const float *const EC = GG + 3 * CK;
         const bool more = c0 + CK < L;
 
-        // ---- (0) the previous chunk's products are done; its outputs, S's
-        // head and tail, this chunk's K | Q and K^T; the next chunk's prep
+        // ---- (0) the previous chunk's products are done; S's head and tail
+        // (this chunk's K | Q and K^T are in place); the next chunk's prep
         // block on its way ----
-        cp_async_wait_all();
         bool late = ci > 0 && !mbar_wait(bar_o, (uint32_t)((ci - 1) & 1));
         if (late)
             report(p.err, GDN_DEVERR_TIMEOUT);
@@ -571,8 +619,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
         tc_after_sync();
         if (more)
             prep_copy(ci + 1);
-        if (ci > 0)
-            write_outputs(c0 - CK, n_prev);
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2) {
             float sv[32];
@@ -583,27 +629,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
             tst16(tlane + C_SL + 32 * half + 16 * q2, lo);
         }
         tst_wait();
-#pragma unroll
-        for (int i = 0; i < CK / TC_WARPS; ++i) {
-            const int tt = warp + TC_WARPS * i;
-            const uint2 qraw = *reinterpret_cast<const uint2 *>(RQ + tt * CD + 4 * lane);
-            const uint2 kraw = *reinterpret_cast<const uint2 *>(RK + tt * CD + 4 * lane);
-            *reinterpret_cast<uint2 *>(KQ + cm_off<CD>(tt, 4 * lane)) = kraw;
-            *reinterpret_cast<uint2 *>(KQ + cm_off<CD>(CK + tt, 4 * lane)) = qraw;
-        }
-        {
-            // K^T, one 16-byte core-matrix row (dk j, tokens s0..s0+7) at a time
-            const unsigned short *rk = reinterpret_cast<const unsigned short *>(RK);
-            for (int e = tid; e < CD * (CK / 8); e += TC_THREADS) {
-                const int j = e % CD, s0 = 8 * (e / CD);
-                uint32_t w[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    w[i] = (uint32_t)rk[(s0 + 2 * i) * CD + j] | ((uint32_t)rk[(s0 + 2 * i + 1) * CD + j] << 16);
-                *reinterpret_cast<uint4 *>(KT + cm_off<CK>(j, s0)) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-        }
-        smem_to_async();
+        smem_to_async(); // K | Q and K^T, written through the generic proxy
         tc_before_sync();
         __syncthreads();
         tc_after_sync();
@@ -620,7 +646,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
             tc_commit(bar_zy);
         }
 
-        // ---- (2) E and Y diag(e^G iq) from Z|Y, one state row a thread ----
+        // ---- (2) the previous chunk's outputs, while Z|Y runs; then E and
+        // Y diag(e^G iq) from Z|Y, one state row a thread ----
+        if (ci > 0)
+            put_outputs();
         late = !mbar_wait(bar_pb[ci & 1], (uint32_t)((ci >> 1) & 1)) || !mbar_wait(bar_zy, (uint32_t)(ci & 1));
         if (late)
             report(p.err, GDN_DEVERR_TIMEOUT);
@@ -629,6 +658,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
             break;
         }
         tc_after_sync();
+        if (ci > 0)
+            store_outputs(c0 - CK, n_prev);
         {
             float z[32], y[32];
             tld32(tlane + C_Z + 32 * half, z);
@@ -653,7 +684,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
         __syncthreads();
         tc_after_sync();
         if (more)
-            stage(c0 + CK); // V is consumed: the next chunk's inputs travel now
+            stage(c0 + CK); // K | Q and V are consumed: the next chunk's inputs travel now
 
         // ---- (3) U = E T^T ----
         if (tid == 0) {
@@ -692,6 +723,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
             tst16(tlane + C_UL + 16 * half, ul);
             tst16(tlane + C_WH + 16 * half, wh);
             tst16(tlane + C_WL + 16 * half, wl);
+            {
+                // Y diag(e^G iq) into U's columns, where O accumulates
+                float yv[32];
+                uint32_t yr[32];
+                tld32(tlane + C_Y + 32 * half, yv);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    yr[i] = __float_as_uint(yv[i]);
+                tst32(tlane + C_U + 32 * half, yr);
+            }
             const float gC = EG[CK - 1];
 #pragma unroll
             for (int q2 = 0; q2 < 2; ++q2) {
@@ -711,14 +752,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
 
         // ---- (4) O += U P^T and S += U diag(e^{G_C-G} ik) K ----
         if (tid == 0) {
-            const uint32_t ph = sm_addr(PH), pl = sm_addr(PL), kt = sm_addr(KT);
+            const uint32_t ph = sm_addr(PH), pl = sm_addr(PL), kt = sm_addr(KT + (ci & 1) * TS::KT_BYTES);
 #pragma unroll
             for (int ks = 0; ks < CK / 16; ++ks) {
                 const uint64_t bh = smem_desc(ph + 256 * ks, (CK / 8) * 128);
                 const uint64_t bl = smem_desc(pl + 256 * ks, (CK / 8) * 128);
-                tc_mma(tbase + C_Y, tbase + C_UL + 8 * ks, bh, idesc_bf16(CK), true);
-                tc_mma(tbase + C_Y, tbase + C_UH + 8 * ks, bl, idesc_bf16(CK), true);
-                tc_mma(tbase + C_Y, tbase + C_UH + 8 * ks, bh, idesc_bf16(CK), true);
+                tc_mma(tbase + C_U, tbase + C_UL + 8 * ks, bh, idesc_bf16(CK), true);
+                tc_mma(tbase + C_U, tbase + C_UH + 8 * ks, bl, idesc_bf16(CK), true);
+                tc_mma(tbase + C_U, tbase + C_UH + 8 * ks, bh, idesc_bf16(CK), true);
             }
 #pragma unroll
             for (int ks = 0; ks < CK / 16; ++ks) {
@@ -729,6 +770,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
             tc_commit(bar_o);
         }
         n_prev = n;
+        if (more) {
+            // the next chunk's K^T, beside these products (its K rows landed
+            // during them; they read the other K^T buffer)
+            cp_async_wait_all();
+            __syncthreads();
+            build_kt((ci + 1) & 1);
+        }
     }
 
     if (!abort && L > 0) {
@@ -739,7 +787,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
         abort = __syncthreads_or(late);
         if (!abort) {
             tc_after_sync();
-            write_outputs(last * CK, n_prev);
+            put_outputs();
+            __syncthreads();
+            store_outputs(last * CK, n_prev);
         }
     }
     if (!abort) {

@@ -243,3 +243,26 @@ def test_chunked_decreasing_cu_seqlens_is_refused_per_sequence(gdn):
         assert err <= 5e-5, f"sequence 0 head {h}: {err:.3g}"
     assert torch.equal(c.pool.tensor[ws2], start[ws2])
     assert_out_close(f64(out[200:300]), f64(ref_out[200:300]), "bf16")
+
+
+def test_chunked_output_not_16_byte_aligned(gdn):
+    """The call does not require `out` to be 16-byte aligned: an output view
+    2 bytes past an aligned buffer gets the same values as an aligned one
+    (the kernel then stores its output rows 2 bytes at a time)."""
+    c = Case(gdn, I.QWEN_08B, [130, 64, 1], seed=95, n_pad=0)
+    T = int(c.cu_np[-1])
+    n = T * c.s.hv * c.s.dv
+    before = c.pool.tensor.clone()
+    out_a = chunked(c, keep_in_place=False)
+    torch.cuda.synchronize()
+    after = c.pool.tensor.clone()
+    c.pool.tensor.copy_(before)
+    buf = torch.zeros(n + 8, dtype=torch.bfloat16, device="cuda")
+    view = buf[1:1 + n].view(T, c.s.hv, c.s.dv)
+    assert view.data_ptr() % 16 == 2
+    chunked(c, keep_in_place=False, out=view)
+    torch.cuda.synchronize()
+    assert torch.equal(view, out_a)
+    assert torch.equal(c.pool.tensor, after)
+    assert buf[0].item() == 0 and not buf[1 + n:].any()
+    assert gdn.get_device_error() == 0
