@@ -55,11 +55,17 @@ namespace {
 
 constexpr int TC_WARPS = 8;
 constexpr int TC_THREADS = TC_WARPS * 32;
+// the chunk kernel: the eight warps above, one a (TMEM lane quarter, column
+// half), plus a warp that issues the tensor-core products
+constexpr int TCW_THREADS = TC_THREADS + 32;
 constexpr uint32_t kTmemCols = 512;
 
-// TMEM columns (O accumulates into U's columns once U is split)
+// TMEM columns.  O accumulates into U's columns once U is split; E's and
+// then U's heads and tails share 448-511 (S's split is read by the Z and Y
+// products while E is formed, and written again while O's product still
+// reads U's split); W's take Z's columns.
 constexpr uint32_t C_S = 0, C_Z = 128, C_Y = 192, C_U = 256, C_SH = 320, C_SL = 384;
-constexpr uint32_t C_EH = 320, C_EL = 352, C_UH = 384, C_UL = 416, C_WH = 128, C_WL = 160;
+constexpr uint32_t C_EH = 448, C_EL = 480, C_UH = 448, C_UL = 480, C_WH = 128, C_WL = 160;
 
 // Byte offset of element (row, k) in a canonical K-major tile with K columns.
 template <int K> __device__ __forceinline__ int cm_off(int row, int k)
@@ -96,15 +102,17 @@ __device__ __forceinline__ int unit_base(const int32_t *cu, int s) { return cu[s
 
 // Shared-memory layout of the chunk kernel, byte offsets.
 struct TS {
-    static constexpr int KQ = 0;                  // bf16 [128][128]: raw K rows 0-63, raw Q rows 64-127
+    static constexpr int KQ_BYTES = 128 * CD * 2; // bf16 [128][128]: raw K rows 0-63, raw Q rows 64-127
+    static constexpr int KQ = 0;                  // two of them, chunk parity
     static constexpr int KT_BYTES = CD * CK * 2;  // bf16 [128 = dk][64 = tokens]: raw K transposed
-    static constexpr int KT = KQ + 128 * CD * 2;  // two of them, chunk parity
+    static constexpr int KT = KQ + 2 * KQ_BYTES;  // two of them, chunk parity
     static constexpr int PB = KT + 2 * KT_BYTES;  // two prep blocks (PW), chunk parity
-    static constexpr int BARS = PB + 2 * PW::BYTES; // mbarriers: Z|Y, U, O and S, prep block 0, 1
-    static constexpr int TADDR = BARS + 48;       // the TMEM base address
+    static constexpr int BARS = PB + 2 * PW::BYTES; // mbarriers: Z, U, O, prep block 0, 1, S, and
+                                                    // S's split, E, U's split ready
+    static constexpr int TADDR = BARS + 80;       // the TMEM base address
     static constexpr int BYTES = TADDR + 16;
-    static constexpr int STAGE = (BYTES + 127) & ~127; // raw v of the next chunk, [CK][CD]
-    static constexpr int OUTS = STAGE + CK * CD * 2;   // bf16 outputs of a chunk, [CK][CD]
+    static constexpr int STAGE = (BYTES + 127) & ~127; // raw v, [CK][CD], two of them, chunk parity
+    static constexpr int OUTS = STAGE + 2 * CK * CD * 2; // bf16 outputs of a chunk, [CK][CD]
     static constexpr int TOTAL = OUTS + CK * CD * 2;
 };
 static_assert(TS::TOTAL <= 227 * 1024, "shared memory");
@@ -382,7 +390,21 @@ __global__ void __launch_bounds__(TC_THREADS, 4) gdn_chunk_prep_kernel(const Pre
         hdr[0] = s, hdr[1] = c0;
 }
 
-__global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const PrefillArgs p,
+// the eight compute warps (256 threads) meet at named barrier 1; the _or
+// form also returns whether any of them passed true
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ bool compute_sync_or(bool v)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 256, p;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)v)
+                 : "memory");
+    return r != 0;
+}
+
+__global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const PrefillArgs p,
                                                                      const unsigned char *work, int units)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -416,7 +438,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
             report(p.err, GDN_DEVERR_BAD_SLOT);
         if (range_ok) {
             const long long n_out = (long long)(t1 - t0) * CD;
-            for (long long e = tid; e < n_out; e += TC_THREADS)
+            for (long long e = tid; e < n_out; e += TCW_THREADS)
                 out[(size_t)(t0 + e / CD) * out_tok + (size_t)h * CD + (size_t)(e % CD)] = from_f<bf16>(0.f);
         }
         return;
@@ -427,8 +449,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
     const int ubase = unit_base(p.cu_seqlens, seq);
 
     // tensor memory (all 512 columns) and the products' mbarriers
-    const uint32_t bar_zy = sm_addr(&bars[0]), bar_u = sm_addr(&bars[1]), bar_o = sm_addr(&bars[2]);
+    const uint32_t bar_z = sm_addr(&bars[0]), bar_u = sm_addr(&bars[1]), bar_o = sm_addr(&bars[2]);
     const uint32_t bar_pb[2] = {sm_addr(&bars[3]), sm_addr(&bars[4])};
+    const uint32_t bar_s = sm_addr(&bars[5]);
+    // compute warps -> product warp: S's split, E's split, U's and W's splits are in TMEM
+    const uint32_t bar_sready = sm_addr(&bars[6]), bar_eready = sm_addr(&bars[7]);
+    const uint32_t bar_wready = sm_addr(&bars[8]);
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sm_addr(taddr_slot)),
                      "r"(kTmemCols)
@@ -436,9 +462,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 32) {
-        mbar_init(bar_zy, 1);
+        mbar_init(bar_z, 1);
         mbar_init(bar_u, 1);
         mbar_init(bar_o, 1);
+        mbar_init(bar_s, 1);
+        mbar_init(bar_sready, TC_WARPS);
+        mbar_init(bar_eready, TC_WARPS);
+        mbar_init(bar_wready, TC_WARPS);
         mbar_init(bar_pb[0], 1);
         mbar_init(bar_pb[1], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -449,10 +479,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
     const uint32_t tbase = *taddr_slot;
     const uint32_t tlane = tbase + ((uint32_t)(32 * quarter) << 16); // this warp's 32 lanes
 
-    // the state in: row `row`, columns 64*half .. 64*half + 63
+    // the state in: row `row`, columns 64*half .. 64*half + 63 (compute warps)
     const size_t slot_floats = (size_t)p.hv * CD * CD;
     const size_t head_off = (size_t)h * CD * CD;
-    {
+    if (warp < TC_WARPS) {
         const float *S0 = p.pool + (size_t)rs * slot_floats + head_off + (size_t)row * CD + 64 * half;
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2) {
@@ -476,9 +506,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
     // sequence), 16 bytes a copy, every thread a share: k and q straight into
     // the K | Q tile (a 16-byte piece of a row is a core-matrix row), v into
     // the staging area
-    auto stage = [&](int cn) {
+    // (which: 0 q, 1 k, 2 v; -1 all three), as one cp.async group
+    auto stage = [&](int cn, int buf, int part) {
+        unsigned char *const kq = KQ + buf * TS::KQ_BYTES;
+        bf16 *const rv = RV + buf * CK * CD;
         const int nn = min(CK, L - cn);
-        for (int e = tid; e < 3 * CK * (CD / 8); e += TC_THREADS) {
+        const int e0 = part < 0 ? 0 : part * CK * (CD / 8);
+        const int e1 = part < 0 ? 3 * CK * (CD / 8) : e0 + CK * (CD / 8);
+#pragma unroll 4
+        for (int e = e0 + tid; e < e1; e += TC_THREADS) {
             const int which = e / (CK * (CD / 8)), rem = e - which * (CK * (CD / 8));
             // k and q: consecutive threads take consecutive 16-byte rows of the
             // tile (a core matrix's 8 rows, then the next core matrix), so the
@@ -491,22 +527,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
             const bf16 *src = which == 0   ? qg + (tok * p.hk + hq) * CD
                               : which == 1 ? kg + (tok * p.hk + hq) * CD
                                            : vg + (tok * p.hv + h) * CD;
-            void *dst = which == 0   ? (void *)(KQ + cm_off<CD>(CK + tt, 8 * j))
-                        : which == 1 ? (void *)(KQ + cm_off<CD>(tt, 8 * j))
-                                     : (void *)(RV + tt * CD + 8 * j);
+            void *dst = which == 0   ? (void *)(kq + cm_off<CD>(CK + tt, 8 * j))
+                        : which == 1 ? (void *)(kq + cm_off<CD>(tt, 8 * j))
+                                     : (void *)(rv + tt * CD + 8 * j);
             cp_async16(dst, src + 8 * j, live ? 16 : 0);
         }
         cp_async_commit();
     };
-    // K^T of the chunk whose K rows are in the K | Q tile, into K^T buffer
+    // K^T of the chunk whose K rows are in K | Q tile `buf`, into K^T buffer
     // `buf`: a warp transposes four 8x8 core matrices a step (ldmatrix .trans:
     // lane l gets tokens 2 (l % 4) and 2 (l % 4) + 1 of dk row l / 4) and
     // stores each as one word of the transposed core-matrix row
     auto build_kt = [&](int buf) {
         unsigned char *const kt = KT + buf * TS::KT_BYTES;
+        const unsigned char *const kq = KQ + buf * TS::KQ_BYTES;
         for (int g = warp; g < (CK / 8) * (CD / 8) / 4; g += TC_WARPS) {
             const int m = 4 * g + (lane >> 3);
-            const uint32_t src = sm_addr(KQ + cm_off<CD>(8 * (m / (CD / 8)) + (lane & 7), 8 * (m % (CD / 8))));
+            const uint32_t src = sm_addr(kq + cm_off<CD>(8 * (m / (CD / 8)) + (lane & 7), 8 * (m % (CD / 8))));
             uint32_t r[4];
             asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                          : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -557,21 +594,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
                 out[(size_t)(t0 + cbase + e / CD) * out_tok + (size_t)h * CD + (e % CD)] = OS[e];
         }
     };
-    if (L > 0)
-        stage(0);
+    if (L > 0 && warp < TC_WARPS)
+        stage(0, 0, -1);
     wait_prior_grid(); // the prep kernel's units are complete
 
     // the prep kernel's units of this sequence must name its chunks (they do
     // unless cu_seqlens decreases somewhere): otherwise it counts as bad
     bool named = true;
-    for (int j = tid; CK * j < L; j += TC_THREADS) {
+    for (int j = tid; CK * j < L; j += TCW_THREADS) {
         const int32_t *hd = reinterpret_cast<const int32_t *>(hwork + (size_t)(ubase + j) * PW::BYTES + PW::HDR);
         named = named && ubase + j < units && hd[0] == seq && hd[1] == CK * j;
     }
     if (!__syncthreads_and(named)) {
         if (h == 0 && tid == 0)
             report(p.err, GDN_DEVERR_BAD_SLOT);
-        for (long long e = tid; e < (long long)L * CD; e += TC_THREADS)
+        for (long long e = tid; e < (long long)L * CD; e += TCW_THREADS)
             out[(size_t)(t0 + e / CD) * out_tok + (size_t)h * CD + (size_t)(e % CD)] = from_f<bf16>(0.f);
         cp_async_wait_all();
         tc_before_sync();
@@ -584,111 +621,237 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
         prep_copy(0);
         cp_async_wait_all();
         __syncthreads(); // the first chunk's K rows are in place
-        build_kt(0);
+        if (warp < TC_WARPS)
+            build_kt(0);
     }
 
-    bool abort = false;
-    int n_prev = 0;
+    // this chunk's prep block, by chunk parity
+    auto pblock = [&](int ci) { return smem + TS::PB + (ci & 1) * PW::BYTES; };
+
+    if (warp < TC_WARPS) {
+        // ======================= compute warps =======================
+        bool abort = false;
+        int n_prev = 0;
 #pragma unroll 1
-    for (int c0 = 0; c0 < L; c0 += CK) {
-        const int ci = c0 / CK;
-        const int n = min(CK, L - c0);
-        unsigned char *const PBc = smem + TS::PB + (ci & 1) * PW::BYTES; // this chunk's prep block
-        unsigned char *const PH = PBc + PW::PH;
-        unsigned char *const PL = PBc + PW::PL;
-        unsigned char *const TH = PBc + PW::TH;
-        unsigned char *const TL = PBc + PW::TL;
-        const float *const GG = reinterpret_cast<const float *>(PBc + PW::GATES); // this chunk's gates
-        const float *const IQ = reinterpret_cast<const float *>(PBc + PW::IQ);
-        const float *const IK = reinterpret_cast<const float *>(PBc + PW::IK);
-        const float *const BE = GG + CK;
-        const float *const EG = GG + 2 * CK;
-        const float *const EC = GG + 3 * CK;
-        const bool more = c0 + CK < L;
+        for (int c0 = 0; c0 < L; c0 += CK) {
+            const int ci = c0 / CK;
+            const int n = min(CK, L - c0);
+            unsigned char *const PBc = pblock(ci);
+            const float *const GG = reinterpret_cast<const float *>(PBc + PW::GATES); // this chunk's gates
+            const float *const IQ = reinterpret_cast<const float *>(PBc + PW::IQ);
+            const float *const IK = reinterpret_cast<const float *>(PBc + PW::IK);
+            const float *const BE = GG + CK;
+            const float *const EG = GG + 2 * CK;
+            const float *const EC = GG + 3 * CK;
+            const bool more = c0 + CK < L;
 
-        // ---- (0) the previous chunk's products are done; S's head and tail
-        // (this chunk's K | Q and K^T are in place); the next chunk's prep
-        // block on its way ----
-        bool late = ci > 0 && !mbar_wait(bar_o, (uint32_t)((ci - 1) & 1));
-        if (late)
-            report(p.err, GDN_DEVERR_TIMEOUT);
-        if (__syncthreads_or(late)) {
-            abort = true;
-            break;
-        }
-        tc_after_sync();
-        if (more)
-            prep_copy(ci + 1);
+            // ---- (0) the previous chunk's state update is done: S's head
+            // and tail for the product warp (this chunk's K | Q and K^T are
+            // in place) ----
+            bool late = ci > 0 && !mbar_wait(bar_s, (uint32_t)((ci - 1) & 1));
+            if (late)
+                report(p.err, GDN_DEVERR_TIMEOUT);
+            if (compute_sync_or(late)) {
+                abort = true;
+                break;
+            }
+            tc_after_sync();
 #pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
-            float sv[32];
-            uint32_t hi[16], lo[16];
-            tld32(tlane + C_S + 64 * half + 32 * q2, sv);
-            split32(sv, hi, lo);
-            tst16(tlane + C_SH + 32 * half + 16 * q2, hi);
-            tst16(tlane + C_SL + 32 * half + 16 * q2, lo);
-        }
-        tst_wait();
-        smem_to_async(); // K | Q and K^T, written through the generic proxy
-        tc_before_sync();
-        __syncthreads();
-        tc_after_sync();
+            for (int q2 = 0; q2 < 2; ++q2) {
+                float sv[32];
+                uint32_t hi[16], lo[16];
+                tld32(tlane + C_S + 64 * half + 32 * q2, sv);
+                split32(sv, hi, lo);
+                tst16(tlane + C_SH + 32 * half + 16 * q2, hi);
+                tst16(tlane + C_SL + 32 * half + 16 * q2, lo);
+            }
+            tst_wait();
+            cp_async_wait_group<1>(); // this chunk's q (its v may still travel)
+            smem_to_async();          // K | Q and K^T, written through the generic proxy
+            tc_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar_sready);
 
-        // ---- (1) Z|Y = S [K|Q]^T on the tensor cores ----
-        if (tid == 0) {
-            const uint32_t kq = sm_addr(KQ);
+            // ---- (2) the previous chunk's outputs, while Z runs; this
+            // chunk's prep block; then E from Z, one state row a thread ----
+            late = __any_sync(0xffffffffu, ci > 0 && !mbar_wait(bar_o, (uint32_t)((ci - 1) & 1)));
+            if (ci > 0 && !late)
+                put_outputs(); // warp-wide TMEM loads: the warp agrees on `late`
+            // The next chunk's inputs travel in thirds while this chunk's
+            // products run: k now, q during U's product, v after the next K^T
+            // is built.  A buffer's last readers were the previous chunk's
+            // products.
+            if (more) {
+                stage(c0 + CK, (ci + 1) & 1, 1);
+                cp_async_wait_group<1>(); // this chunk's v
+            } else {
+                cp_async_wait_group<0>();
+            }
+            late = late || !mbar_wait(bar_pb[ci & 1], (uint32_t)((ci >> 1) & 1)) ||
+                   !mbar_wait(bar_z, (uint32_t)(ci & 1));
+            if (late)
+                report(p.err, GDN_DEVERR_TIMEOUT);
+            if (compute_sync_or(late)) {
+                abort = true;
+                break;
+            }
+            tc_after_sync();
+            if (ci > 0)
+                store_outputs(c0 - CK, n_prev);
+            if (more)
+                prep_copy(ci + 1); // its block's last readers, the previous chunk's products, are done
+            {
+                const bf16 *const rv = RV + (ci & 1) * CK * CD;
+                float z[32];
+                tld32(tlane + C_Z + 32 * half, z);
+                uint32_t eh[16], el[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const int t = 32 * half + i;
+                    const float v0 = __bfloat162float(rv[t * CD + row]), v1 = __bfloat162float(rv[(t + 1) * CD + row]);
+                    const float e0 = BE[t] * (v0 - EG[t] * IK[t] * z[i]);
+                    const float e1 = BE[t + 1] * (v1 - EG[t + 1] * IK[t + 1] * z[i + 1]);
+                    split2(e0, e1, eh[i / 2], el[i / 2]);
+                }
+                tst16(tlane + C_EH + 16 * half, eh);
+                tst16(tlane + C_EL + 16 * half, el);
+                tst_wait();
+            }
+            tc_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar_eready);
+
+            // ---- (3) U's head and tail (for O), those of U diag(e^{G_C-G}
+            // ik) (for S), Y diag(e^G iq) into U's columns (where O
+            // accumulates), and S scaled by e^{G_C} ----
+            if (more)
+                stage(c0 + CK, (ci + 1) & 1, 0);
+            late = !mbar_wait(bar_u, (uint32_t)(ci & 1)); // Y's products came before U's
+            if (late)
+                report(p.err, GDN_DEVERR_TIMEOUT);
+            if (compute_sync_or(late)) {
+                abort = true;
+                break;
+            }
+            tc_after_sync();
+            {
+                float u[32];
+                tld32(tlane + C_U + 32 * half, u);
+                uint32_t uh[16], ul[16], wh[16], wl[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const int t = 32 * half + i;
+                    split2(u[i], u[i + 1], uh[i / 2], ul[i / 2]);
+                    split2(u[i] * EC[t] * IK[t], u[i + 1] * EC[t + 1] * IK[t + 1], wh[i / 2], wl[i / 2]);
+                }
+                tst16(tlane + C_UH + 16 * half, uh);
+                tst16(tlane + C_UL + 16 * half, ul);
+                tst16(tlane + C_WH + 16 * half, wh);
+                tst16(tlane + C_WL + 16 * half, wl);
+                {
+                    float y[32];
+                    uint32_t yo[32];
+                    tld32(tlane + C_Y + 32 * half, y);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int t = 32 * half + i;
+                        yo[i] = __float_as_uint(y[i] * EG[t] * IQ[t]);
+                    }
+                    tst32(tlane + C_U + 32 * half, yo);
+                }
+                const float gC = EG[CK - 1];
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    float sv[32];
+                    uint32_t r[32];
+                    tld32(tlane + C_S + 64 * half + 32 * q2, sv);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        r[i] = __float_as_uint(sv[i] * gC);
+                    tst32(tlane + C_S + 64 * half + 32 * q2, r);
+                }
+                tst_wait();
+            }
+            if (more)
+                cp_async_wait_group<1>(); // the next chunk's k (its q may still travel)
+            tc_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar_wready);
+            n_prev = n;
+            if (more) {
+                // the next chunk's K^T, beside the products (they read the
+                // other K^T buffer), then its v
+                compute_sync(); // every thread's share of its k rows landed
+                build_kt((ci + 1) & 1);
+                stage(c0 + CK, (ci + 1) & 1, 2);
+            }
+        }
+
+        if (!abort && L > 0) {
+            const int last = (L - 1) / CK;
+            const bool late = !mbar_wait(bar_o, (uint32_t)(last & 1)); // after S's product
+            if (late)
+                report(p.err, GDN_DEVERR_TIMEOUT);
+            abort = compute_sync_or(late);
+            if (!abort) {
+                tc_after_sync();
+                put_outputs();
+                compute_sync();
+                store_outputs(last * CK, n_prev);
+            }
+        }
+        if (!abort) {
+            // the final state, to the write slot (the read slot in place)
+            float *Sd = p.pool + (size_t)ws * slot_floats + head_off + (size_t)row * CD + 64 * half;
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                float sv[32];
+                tld32(tlane + C_S + 64 * half + 32 * q2, sv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    *reinterpret_cast<float4 *>(Sd + 32 * q2 + 4 * i) =
+                        make_float4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]);
+            }
+        }
+    } else {
+        // ======================= product warp ========================
+        // Per chunk: Z = S K^T (committed alone, E needs it first), Y = S
+        // Q^T; U = E T^T (its commit covers Y's products too); S += W K,
+        // then O += U P^T.  Each group waits for the compute warps' inputs.
+#pragma unroll 1
+        for (int c0 = 0; lane == 0 && c0 < L; c0 += CK) {
+            const int ci = c0 / CK;
+            unsigned char *const PBc = pblock(ci);
+            if (!mbar_wait(bar_sready, (uint32_t)(ci & 1))) {
+                report(p.err, GDN_DEVERR_TIMEOUT);
+                break;
+            }
+            tc_after_sync();
+            const uint32_t kq = sm_addr(KQ + (ci & 1) * TS::KQ_BYTES);
 #pragma unroll
             for (int ks = 0; ks < CD / 16; ++ks) {
                 const uint64_t b = smem_desc(kq + 256 * ks, (CD / 8) * 128);
-                tc_mma(tbase + C_Z, tbase + C_SL + 8 * ks, b, idesc_bf16(128), ks > 0);
-                tc_mma(tbase + C_Z, tbase + C_SH + 8 * ks, b, idesc_bf16(128), true);
+                tc_mma(tbase + C_Z, tbase + C_SL + 8 * ks, b, idesc_bf16(CK), ks > 0);
+                tc_mma(tbase + C_Z, tbase + C_SH + 8 * ks, b, idesc_bf16(CK), true);
             }
-            tc_commit(bar_zy);
-        }
-
-        // ---- (2) the previous chunk's outputs, while Z|Y runs; then E and
-        // Y diag(e^G iq) from Z|Y, one state row a thread ----
-        if (ci > 0)
-            put_outputs();
-        late = !mbar_wait(bar_pb[ci & 1], (uint32_t)((ci >> 1) & 1)) || !mbar_wait(bar_zy, (uint32_t)(ci & 1));
-        if (late)
-            report(p.err, GDN_DEVERR_TIMEOUT);
-        if (__syncthreads_or(late)) {
-            abort = true;
-            break;
-        }
-        tc_after_sync();
-        if (ci > 0)
-            store_outputs(c0 - CK, n_prev);
-        {
-            float z[32], y[32];
-            tld32(tlane + C_Z + 32 * half, z);
-            tld32(tlane + C_Y + 32 * half, y);
-            uint32_t eh[16], el[16], yo[32];
+            tc_commit(bar_z);
+            const uint32_t qrows = kq + (CK / 8) * (CD / 8) * 128; // Q's rows
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const int t = 32 * half + i;
-                const float v0 = __bfloat162float(RV[t * CD + row]), v1 = __bfloat162float(RV[(t + 1) * CD + row]);
-                const float e0 = BE[t] * (v0 - EG[t] * IK[t] * z[i]);
-                const float e1 = BE[t + 1] * (v1 - EG[t + 1] * IK[t + 1] * z[i + 1]);
-                split2(e0, e1, eh[i / 2], el[i / 2]);
-                yo[i] = __float_as_uint(y[i] * EG[t] * IQ[t]);
-                yo[i + 1] = __float_as_uint(y[i + 1] * EG[t + 1] * IQ[t + 1]);
+            for (int ks = 0; ks < CD / 16; ++ks) {
+                const uint64_t b = smem_desc(qrows + 256 * ks, (CD / 8) * 128);
+                tc_mma(tbase + C_Y, tbase + C_SL + 8 * ks, b, idesc_bf16(CK), ks > 0);
+                tc_mma(tbase + C_Y, tbase + C_SH + 8 * ks, b, idesc_bf16(CK), true);
             }
-            tst16(tlane + C_EH + 16 * half, eh);
-            tst16(tlane + C_EL + 16 * half, el);
-            tst32(tlane + C_Y + 32 * half, yo);
-            tst_wait();
-        }
-        tc_before_sync();
-        __syncthreads();
-        tc_after_sync();
-        if (more)
-            stage(c0 + CK); // K | Q and V are consumed: the next chunk's inputs travel now
 
-        // ---- (3) U = E T^T ----
-        if (tid == 0) {
-            const uint32_t th = sm_addr(TH), tl = sm_addr(TL);
+            if (!mbar_wait(bar_eready, (uint32_t)(ci & 1))) {
+                report(p.err, GDN_DEVERR_TIMEOUT);
+                break;
+            }
+            tc_after_sync();
+            const uint32_t th = sm_addr(PBc + PW::TH), tl = sm_addr(PBc + PW::TL);
 #pragma unroll
             for (int ks = 0; ks < CK / 16; ++ks) {
                 const uint64_t bh = smem_desc(th + 256 * ks, (CK / 8) * 128);
@@ -698,61 +861,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
                 tc_mma(tbase + C_U, tbase + C_EH + 8 * ks, bh, idesc_bf16(CK), true);
             }
             tc_commit(bar_u);
-        }
-        late = !mbar_wait(bar_u, (uint32_t)(ci & 1));
-        if (late)
-            report(p.err, GDN_DEVERR_TIMEOUT);
-        if (__syncthreads_or(late)) {
-            abort = true;
-            break;
-        }
-        tc_after_sync();
-        {
-            // U's head and tail (for O), those of U diag(e^{G_C-G} ik) (for S),
-            // and S scaled by e^{G_C}
-            float u[32];
-            tld32(tlane + C_U + 32 * half, u);
-            uint32_t uh[16], ul[16], wh[16], wl[16];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const int t = 32 * half + i;
-                split2(u[i], u[i + 1], uh[i / 2], ul[i / 2]);
-                split2(u[i] * EC[t] * IK[t], u[i + 1] * EC[t + 1] * IK[t + 1], wh[i / 2], wl[i / 2]);
-            }
-            tst16(tlane + C_UH + 16 * half, uh);
-            tst16(tlane + C_UL + 16 * half, ul);
-            tst16(tlane + C_WH + 16 * half, wh);
-            tst16(tlane + C_WL + 16 * half, wl);
-            {
-                // Y diag(e^G iq) into U's columns, where O accumulates
-                float yv[32];
-                uint32_t yr[32];
-                tld32(tlane + C_Y + 32 * half, yv);
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    yr[i] = __float_as_uint(yv[i]);
-                tst32(tlane + C_U + 32 * half, yr);
-            }
-            const float gC = EG[CK - 1];
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                float sv[32];
-                uint32_t r[32];
-                tld32(tlane + C_S + 64 * half + 32 * q2, sv);
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    r[i] = __float_as_uint(sv[i] * gC);
-                tst32(tlane + C_S + 64 * half + 32 * q2, r);
-            }
-            tst_wait();
-        }
-        tc_before_sync();
-        __syncthreads();
-        tc_after_sync();
 
-        // ---- (4) O += U P^T and S += U diag(e^{G_C-G} ik) K ----
-        if (tid == 0) {
-            const uint32_t ph = sm_addr(PH), pl = sm_addr(PL), kt = sm_addr(KT + (ci & 1) * TS::KT_BYTES);
+            if (!mbar_wait(bar_wready, (uint32_t)(ci & 1))) {
+                report(p.err, GDN_DEVERR_TIMEOUT);
+                break;
+            }
+            tc_after_sync();
+            const uint32_t ph = sm_addr(PBc + PW::PH), pl = sm_addr(PBc + PW::PL);
+            const uint32_t kt = sm_addr(KT + (ci & 1) * TS::KT_BYTES);
+#pragma unroll
+            for (int ks = 0; ks < CK / 16; ++ks) {
+                const uint64_t b = smem_desc(kt + 256 * ks, (CK / 8) * 128);
+                tc_mma(tbase + C_S, tbase + C_WL + 8 * ks, b, idesc_bf16(CD), true);
+                tc_mma(tbase + C_S, tbase + C_WH + 8 * ks, b, idesc_bf16(CD), true);
+            }
+            tc_commit(bar_s);
 #pragma unroll
             for (int ks = 0; ks < CK / 16; ++ks) {
                 const uint64_t bh = smem_desc(ph + 256 * ks, (CK / 8) * 128);
@@ -761,50 +884,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gdn_chunked_tc_kernel(const Pre
                 tc_mma(tbase + C_U, tbase + C_UH + 8 * ks, bl, idesc_bf16(CK), true);
                 tc_mma(tbase + C_U, tbase + C_UH + 8 * ks, bh, idesc_bf16(CK), true);
             }
-#pragma unroll
-            for (int ks = 0; ks < CK / 16; ++ks) {
-                const uint64_t b = smem_desc(kt + 256 * ks, (CK / 8) * 128);
-                tc_mma(tbase + C_S, tbase + C_WL + 8 * ks, b, idesc_bf16(CD), true);
-                tc_mma(tbase + C_S, tbase + C_WH + 8 * ks, b, idesc_bf16(CD), true);
-            }
             tc_commit(bar_o);
         }
-        n_prev = n;
-        if (more) {
-            // the next chunk's K^T, beside these products (its K rows landed
-            // during them; they read the other K^T buffer)
-            cp_async_wait_all();
-            __syncthreads();
-            build_kt((ci + 1) & 1);
-        }
+        __syncwarp(); // lanes 1-31 waited here for lane 0's products
     }
-
-    if (!abort && L > 0) {
-        const int last = (L - 1) / CK;
-        const bool late = !mbar_wait(bar_o, (uint32_t)(last & 1));
-        if (late)
-            report(p.err, GDN_DEVERR_TIMEOUT);
-        abort = __syncthreads_or(late);
-        if (!abort) {
-            tc_after_sync();
-            put_outputs();
-            __syncthreads();
-            store_outputs(last * CK, n_prev);
-        }
-    }
-    if (!abort) {
-        // the final state, to the write slot (the read slot in place)
-        float *Sd = p.pool + (size_t)ws * slot_floats + head_off + (size_t)row * CD + 64 * half;
-#pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
-            float sv[32];
-            tld32(tlane + C_S + 64 * half + 32 * q2, sv);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                *reinterpret_cast<float4 *>(Sd + 32 * q2 + 4 * i) =
-                    make_float4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]);
-        }
-    }
+    cp_async_wait_all(); // a chain that stopped early may have the next chunk's inputs in flight
     tc_before_sync();
     __syncthreads();
     if (warp == 0)
@@ -846,7 +930,7 @@ cudaError_t launch_gdn_prefill_chunked_tc(const PrefillArgs &a, cudaStream_t s)
                                (size_t)PS::TOTAL, s, a, work, (int)units);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(gdn_chunked_tc_kernel, dim3((unsigned)ctas), dim3(TC_THREADS), (size_t)TS::TOTAL, s, a,
+    return launch_pdl(gdn_chunked_tc_kernel, dim3((unsigned)ctas), dim3(TCW_THREADS), (size_t)TS::TOTAL, s, a,
                       static_cast<const unsigned char *>(work), (int)units);
 }
 
