@@ -43,6 +43,11 @@
 // one that runs out reports GDN_DEVERR_TIMEOUT, and the CTA stops without
 // writing outputs or state, frees its tensor memory and returns.
 #include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "gdn_chunk_common.cuh"
 #include "gdn_device.cuh"
@@ -56,8 +61,9 @@ namespace {
 constexpr int TC_WARPS = 8;
 constexpr int TC_THREADS = TC_WARPS * 32;
 // the chunk kernel: the eight warps above, one a (TMEM lane quarter, column
-// half), plus a warp that issues the tensor-core products
-constexpr int TCW_THREADS = TC_THREADS + 32;
+// half), a warp that issues the tensor-core products and a warp that copies
+// the next chunk's q, k and v into shared memory
+constexpr int TCW_THREADS = TC_THREADS + 64;
 constexpr uint32_t kTmemCols = 512;
 
 // TMEM columns.  O accumulates into U's columns once U is split; E's and
@@ -102,20 +108,27 @@ __device__ __forceinline__ int unit_base(const int32_t *cu, int s) { return cu[s
 
 // Shared-memory layout of the chunk kernel, byte offsets.
 struct TS {
-    static constexpr int KQ_BYTES = 128 * CD * 2; // bf16 [128][128]: raw K rows 0-63, raw Q rows 64-127
+    // raw K then raw Q of a chunk, each as two 64-token x 64-dk halves of
+    // 128-byte rows in the 128-byte-swizzled K-major layout (what a tensor
+    // copy with that swizzle writes, 1024-byte aligned)
+    static constexpr int HALF = CK * 64 * 2;      // 8 KiB
+    static constexpr int KQ_BYTES = 4 * HALF;     // K dk 0-63 | K dk 64-127 | Q dk 0-63 | Q dk 64-127
     static constexpr int KQ = 0;                  // two of them, chunk parity
     static constexpr int KT_BYTES = CD * CK * 2;  // bf16 [128 = dk][64 = tokens]: raw K transposed
     static constexpr int KT = KQ + 2 * KQ_BYTES;  // two of them, chunk parity
     static constexpr int PB = KT + 2 * KT_BYTES;  // two prep blocks (PW), chunk parity
-    static constexpr int BARS = PB + 2 * PW::BYTES; // mbarriers: Z, U, O, prep block 0, 1, S, and
-                                                    // S's split, E, U's split ready
-    static constexpr int TADDR = BARS + 80;       // the TMEM base address
+    static constexpr int BARS = PB + 2 * PW::BYTES; // mbarriers: Z, U, O, prep block 0, 1, S;
+                                                    // S's split, E, U's split ready; inputs 0, 1
+    static constexpr int TADDR = BARS + 96;       // the TMEM base address
     static constexpr int BYTES = TADDR + 16;
     static constexpr int STAGE = (BYTES + 127) & ~127; // raw v, [CK][CD], two of them, chunk parity
     static constexpr int OUTS = STAGE + 2 * CK * CD * 2; // bf16 outputs of a chunk, [CK][CD]
-    static constexpr int TOTAL = OUTS + CK * CD * 2;
+    static constexpr int USED = OUTS + CK * CD * 2;
+    static constexpr int TOTAL = USED + 1024;     // the base rounded up to 1024 bytes
 };
 static_assert(TS::TOTAL <= 227 * 1024, "shared memory");
+static_assert(TS::KQ % 1024 == 0 && TS::KQ_BYTES % 1024 == 0 && TS::HALF % 1024 == 0, "swizzled tiles");
+static_assert(TS::STAGE % 128 == 0 && TS::OUTS % 16 == 0, "copy destinations");
 static_assert(TS::BARS % 8 == 0 && TS::KT % 1024 == 0 && TS::PB % 128 == 0, "alignment");
 
 // Shared-memory layout of the prep kernel, byte offsets.
@@ -142,6 +155,26 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo)
     return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46);
 }
+// the same for a K-major operand in the 128-byte-swizzled layout: 8-row
+// groups 1024 bytes apart (stride offset); the leading offset is unused
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr)
+{
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+           (2ull << 61);
+}
+// one box of a 3-D tensor map into shared memory, counted on `bar`
+__device__ __forceinline__ void tma_load3(uint32_t dst, const CUtensorMap *map, int x, int y, int z, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+                 "%3, %4}], [%5];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+                 : "memory");
+}
+// The tensor maps of a call: q and k [tokens][hk][dk], boxes of 64 dk x 1
+// head x 64 tokens, 128-byte swizzle; v [tokens][hv][dv], 128 x 1 x 64.
+struct ChunkMaps {
+    CUtensorMap q, k, v;
+};
 // D fp32, A and B bf16, both K-major, M = 128, N = n
 __host__ __device__ constexpr uint32_t idesc_bf16(int n)
 {
@@ -405,9 +438,11 @@ __device__ __forceinline__ bool compute_sync_or(bool v)
 }
 
 __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const PrefillArgs p,
-                                                                     const unsigned char *work, int units)
+                                                                      const unsigned char *work, int units,
+                                                                      const __grid_constant__ ChunkMaps maps)
 {
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *const smem = smem_raw + ((1024u - (sm_addr(smem_raw) & 1023u)) & 1023u);
     unsigned char *const KQ = smem + TS::KQ;
     unsigned char *const KT = smem + TS::KT;
     uint64_t *const bars = reinterpret_cast<uint64_t *>(smem + TS::BARS);
@@ -455,6 +490,8 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
     // compute warps -> product warp: S's split, E's split, U's and W's splits are in TMEM
     const uint32_t bar_sready = sm_addr(&bars[6]), bar_eready = sm_addr(&bars[7]);
     const uint32_t bar_wready = sm_addr(&bars[8]);
+    // loader warp -> compute warps: a chunk's q, k and v are in shared memory (chunk parity)
+    const uint32_t bar_in[2] = {sm_addr(&bars[9]), sm_addr(&bars[10])};
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sm_addr(taddr_slot)),
                      "r"(kTmemCols)
@@ -469,6 +506,8 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
         mbar_init(bar_sready, TC_WARPS);
         mbar_init(bar_eready, TC_WARPS);
         mbar_init(bar_wready, TC_WARPS);
+        mbar_init(bar_in[0], 1);
+        mbar_init(bar_in[1], 1);
         mbar_init(bar_pb[0], 1);
         mbar_init(bar_pb[1], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -502,57 +541,50 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
     const bf16 *const kg = reinterpret_cast<const bf16 *>(p.k);
     const bf16 *const vg = reinterpret_cast<const bf16 *>(p.v);
 
-    // the raw q, k, v of the chunk starting at token cn (zeros past the
-    // sequence), 16 bytes a copy, every thread a share: k and q straight into
-    // the K | Q tile (a 16-byte piece of a row is a core-matrix row), v into
-    // the staging area
-    // (which: 0 q, 1 k, 2 v; -1 all three), as one cp.async group
-    auto stage = [&](int cn, int buf, int part) {
-        unsigned char *const kq = KQ + buf * TS::KQ_BYTES;
-        bf16 *const rv = RV + buf * CK * CD;
-        const int nn = min(CK, L - cn);
-        const int e0 = part < 0 ? 0 : part * CK * (CD / 8);
-        const int e1 = part < 0 ? 3 * CK * (CD / 8) : e0 + CK * (CD / 8);
-#pragma unroll 4
-        for (int e = e0 + tid; e < e1; e += TC_THREADS) {
-            const int which = e / (CK * (CD / 8)), rem = e - which * (CK * (CD / 8));
-            // k and q: consecutive threads take consecutive 16-byte rows of the
-            // tile (a core matrix's 8 rows, then the next core matrix), so the
-            // shared-memory writes do not collide in the banks; v: row-major
-            const int cmi = rem >> 3;
-            const int tt = which < 2 ? ((cmi / (CD / 8)) << 3) + (rem & 7) : rem / (CD / 8);
-            const int j = which < 2 ? cmi % (CD / 8) : rem % (CD / 8);
-            const bool live = tt < nn;
-            const size_t tok = (size_t)(t0 + cn + (live ? tt : 0));
-            const bf16 *src = which == 0   ? qg + (tok * p.hk + hq) * CD
-                              : which == 1 ? kg + (tok * p.hk + hq) * CD
-                                           : vg + (tok * p.hv + h) * CD;
-            void *dst = which == 0   ? (void *)(kq + cm_off<CD>(CK + tt, 8 * j))
-                        : which == 1 ? (void *)(kq + cm_off<CD>(tt, 8 * j))
-                                     : (void *)(rv + tt * CD + 8 * j);
-            cp_async16(dst, src + 8 * j, live ? 16 : 0);
-        }
-        cp_async_commit();
+    // The raw q, k, v of the chunk starting at token cn into the buffers of
+    // parity `buf`, by five tensor copies counted on bar_in[buf] (one
+    // thread): k and q as two 128-byte-swizzled dk halves each, v row-major.
+    // A box reads past the sequence into the next one's tokens (zeros past the
+    // last token): those rows are neutralised where they are used (E is zero
+    // and K^T has zeros for tokens past the chunk's end).
+    auto load_chunk = [&](int cn, int buf) {
+        const uint32_t bar = bar_in[buf];
+        const uint32_t kq = sm_addr(KQ + buf * TS::KQ_BYTES);
+        mbar_arrive_tx(bar, (uint32_t)(TS::KQ_BYTES + CK * CD * 2));
+        const int tok = t0 + cn;
+        tma_load3(kq, &maps.k, 0, hq, tok, bar);
+        tma_load3(kq + TS::HALF, &maps.k, 64, hq, tok, bar);
+        tma_load3(kq + 2 * TS::HALF, &maps.q, 0, hq, tok, bar);
+        tma_load3(kq + 3 * TS::HALF, &maps.q, 64, hq, tok, bar);
+        tma_load3(sm_addr(RV + buf * CK * CD), &maps.v, 0, h, tok, bar);
     };
-    // K^T of the chunk whose K rows are in K | Q tile `buf`, into K^T buffer
-    // `buf`: a warp transposes four 8x8 core matrices a step (ldmatrix .trans:
-    // lane l gets tokens 2 (l % 4) and 2 (l % 4) + 1 of dk row l / 4) and
-    // stores each as one word of the transposed core-matrix row
-    auto build_kt = [&](int buf) {
+    // K^T of the chunk (nn tokens) whose K rows are in K | Q tile `buf`, into
+    // K^T buffer `buf`: a warp transposes four 8x8 blocks a step (ldmatrix
+    // .trans from the swizzled rows: lane l gets tokens 2 (l % 4) and
+    // 2 (l % 4) + 1 of dk row l / 4), zeroes tokens past nn, and stores each
+    // block as one word of a canonical core-matrix row
+    auto build_kt = [&](int buf, int nn) {
         unsigned char *const kt = KT + buf * TS::KT_BYTES;
         const unsigned char *const kq = KQ + buf * TS::KQ_BYTES;
         for (int g = warp; g < (CK / 8) * (CD / 8) / 4; g += TC_WARPS) {
             const int m = 4 * g + (lane >> 3);
-            const uint32_t src = sm_addr(kq + cm_off<CD>(8 * (m / (CD / 8)) + (lane & 7), 8 * (m % (CD / 8))));
-            uint32_t r[4];
+            const int r = 8 * (m / (CD / 8)) + (lane & 7), jb = m % (CD / 8); // token row, 16-byte piece
+            const uint32_t src = sm_addr(kq + (jb >> 3) * TS::HALF + r * 128 + (((jb & 7) ^ (r & 7)) << 4));
+            uint32_t w[4];
             asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
                          : "r"(src)
                          : "memory");
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int mi = 4 * g + i, tb = mi / (CD / 8), jb = mi % (CD / 8);
-                *reinterpret_cast<uint32_t *>(kt + cm_off<CK>(8 * jb + (lane >> 2), 8 * tb + 2 * (lane & 3))) = r[i];
+                const int mi = 4 * g + i, tb = mi / (CD / 8), jbi = mi % (CD / 8);
+                const int s0 = 8 * tb + 2 * (lane & 3); // tokens s0, s0 + 1
+                uint32_t v = w[i];
+                if (s0 >= nn)
+                    v = 0;
+                else if (s0 + 1 >= nn)
+                    v &= 0xFFFFu;
+                *reinterpret_cast<uint32_t *>(kt + cm_off<CK>(8 * jbi + (lane >> 2), s0)) = v;
             }
         }
     };
@@ -594,8 +626,8 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
                 out[(size_t)(t0 + cbase + e / CD) * out_tok + (size_t)h * CD + (e % CD)] = OS[e];
         }
     };
-    if (L > 0 && warp < TC_WARPS)
-        stage(0, 0, -1);
+    if (L > 0 && warp == TC_WARPS + 1 && lane == 0)
+        load_chunk(0, 0); // q, k and v are this call's inputs: no earlier kernel writes them
     wait_prior_grid(); // the prep kernel's units are complete
 
     // the prep kernel's units of this sequence must name its chunks (they do
@@ -606,6 +638,8 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
         named = named && ubase + j < units && hd[0] == seq && hd[1] == CK * j;
     }
     if (!__syncthreads_and(named)) {
+        if (L > 0 && warp == TC_WARPS + 1 && lane == 0)
+            mbar_wait(bar_in[0], 0u); // the first chunk's copies land before the CTA ends
         if (h == 0 && tid == 0)
             report(p.err, GDN_DEVERR_BAD_SLOT);
         for (long long e = tid; e < (long long)L * CD; e += TCW_THREADS)
@@ -617,12 +651,15 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
             asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(kTmemCols) : "memory");
         return;
     }
+    bool in_late = false; // a wait for the loader's copies ran out
     if (L > 0) {
         prep_copy(0);
-        cp_async_wait_all();
-        __syncthreads(); // the first chunk's K rows are in place
-        if (warp < TC_WARPS)
-            build_kt(0);
+        // chunk c's inputs complete phase c / 2 of bar_in[c % 2]
+        if (warp < TC_WARPS) {
+            in_late = !__all_sync(0xffffffffu, mbar_wait(bar_in[0], 0u));
+            if (!in_late)
+                build_kt(0, min(CK, L));
+        }
     }
 
     // this chunk's prep block, by chunk parity
@@ -648,7 +685,7 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
             // ---- (0) the previous chunk's state update is done: S's head
             // and tail for the product warp (this chunk's K | Q and K^T are
             // in place) ----
-            bool late = ci > 0 && !mbar_wait(bar_s, (uint32_t)((ci - 1) & 1));
+            bool late = in_late || (ci > 0 && !mbar_wait(bar_s, (uint32_t)((ci - 1) & 1)));
             if (late)
                 report(p.err, GDN_DEVERR_TIMEOUT);
             if (compute_sync_or(late)) {
@@ -666,8 +703,7 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
                 tst16(tlane + C_SL + 32 * half + 16 * q2, lo);
             }
             tst_wait();
-            cp_async_wait_group<1>(); // this chunk's q (its v may still travel)
-            smem_to_async();          // K | Q and K^T, written through the generic proxy
+            smem_to_async(); // K^T, written through the generic proxy
             tc_before_sync();
             __syncwarp();
             if (lane == 0)
@@ -678,16 +714,6 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
             late = __any_sync(0xffffffffu, ci > 0 && !mbar_wait(bar_o, (uint32_t)((ci - 1) & 1)));
             if (ci > 0 && !late)
                 put_outputs(); // warp-wide TMEM loads: the warp agrees on `late`
-            // The next chunk's inputs travel in thirds while this chunk's
-            // products run: k now, q during U's product, v after the next K^T
-            // is built.  A buffer's last readers were the previous chunk's
-            // products.
-            if (more) {
-                stage(c0 + CK, (ci + 1) & 1, 1);
-                cp_async_wait_group<1>(); // this chunk's v
-            } else {
-                cp_async_wait_group<0>();
-            }
             late = late || !mbar_wait(bar_pb[ci & 1], (uint32_t)((ci >> 1) & 1)) ||
                    !mbar_wait(bar_z, (uint32_t)(ci & 1));
             if (late)
@@ -710,14 +736,17 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
                 for (int i = 0; i < 32; i += 2) {
                     const int t = 32 * half + i;
                     const float v0 = __bfloat162float(rv[t * CD + row]), v1 = __bfloat162float(rv[(t + 1) * CD + row]);
-                    const float e0 = BE[t] * (v0 - EG[t] * IK[t] * z[i]);
-                    const float e1 = BE[t + 1] * (v1 - EG[t + 1] * IK[t + 1] * z[i + 1]);
+                    // tokens past the chunk's end: E is zero (their v and Z may
+                    // be the next sequence's)
+                    const float e0 = t < n ? BE[t] * (v0 - EG[t] * IK[t] * z[i]) : 0.f;
+                    const float e1 = t + 1 < n ? BE[t + 1] * (v1 - EG[t + 1] * IK[t + 1] * z[i + 1]) : 0.f;
                     split2(e0, e1, eh[i / 2], el[i / 2]);
                 }
                 tst16(tlane + C_EH + 16 * half, eh);
                 tst16(tlane + C_EL + 16 * half, el);
                 tst_wait();
             }
+            smem_to_async(); // v read here, before the loader's next copy into its buffer
             tc_before_sync();
             __syncwarp();
             if (lane == 0)
@@ -726,8 +755,6 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
             // ---- (3) U's head and tail (for O), those of U diag(e^{G_C-G}
             // ik) (for S), Y diag(e^G iq) into U's columns (where O
             // accumulates), and S scaled by e^{G_C} ----
-            if (more)
-                stage(c0 + CK, (ci + 1) & 1, 0);
             late = !mbar_wait(bar_u, (uint32_t)(ci & 1)); // Y's products came before U's
             if (late)
                 report(p.err, GDN_DEVERR_TIMEOUT);
@@ -774,8 +801,6 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
                 }
                 tst_wait();
             }
-            if (more)
-                cp_async_wait_group<1>(); // the next chunk's k (its q may still travel)
             tc_before_sync();
             __syncwarp();
             if (lane == 0)
@@ -783,10 +808,12 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
             n_prev = n;
             if (more) {
                 // the next chunk's K^T, beside the products (they read the
-                // other K^T buffer), then its v
-                compute_sync(); // every thread's share of its k rows landed
-                build_kt((ci + 1) & 1);
-                stage(c0 + CK, (ci + 1) & 1, 2);
+                // other K^T buffer), once the loader warp has its rows in
+                // (a failed wait leaves it unbuilt and ends the loop at the
+                // next chunk's top; the warp agrees, its loads are warp-wide)
+                in_late = !__all_sync(0xffffffffu, mbar_wait(bar_in[(ci + 1) & 1], (uint32_t)(((ci + 1) >> 1) & 1)));
+                if (!in_late)
+                    build_kt((ci + 1) & 1, min(CK, L - c0 - CK));
             }
         }
 
@@ -816,7 +843,7 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
                         make_float4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]);
             }
         }
-    } else {
+    } else if (warp == TC_WARPS) {
         // ======================= product warp ========================
         // Per chunk: Z = S K^T (committed alone, E needs it first), Y = S
         // Q^T; U = E T^T (its commit covers Y's products too); S += W K,
@@ -830,18 +857,19 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
                 break;
             }
             tc_after_sync();
+            // K's and Q's swizzled halves: 16 dk (32 bytes) a step inside a half
             const uint32_t kq = sm_addr(KQ + (ci & 1) * TS::KQ_BYTES);
 #pragma unroll
             for (int ks = 0; ks < CD / 16; ++ks) {
-                const uint64_t b = smem_desc(kq + 256 * ks, (CD / 8) * 128);
+                const uint64_t b = smem_desc_sw128(kq + (ks >> 2) * TS::HALF + 32 * (ks & 3));
                 tc_mma(tbase + C_Z, tbase + C_SL + 8 * ks, b, idesc_bf16(CK), ks > 0);
                 tc_mma(tbase + C_Z, tbase + C_SH + 8 * ks, b, idesc_bf16(CK), true);
             }
             tc_commit(bar_z);
-            const uint32_t qrows = kq + (CK / 8) * (CD / 8) * 128; // Q's rows
+            const uint32_t qh = kq + 2 * TS::HALF;
 #pragma unroll
             for (int ks = 0; ks < CD / 16; ++ks) {
-                const uint64_t b = smem_desc(qrows + 256 * ks, (CD / 8) * 128);
+                const uint64_t b = smem_desc_sw128(qh + (ks >> 2) * TS::HALF + 32 * (ks & 3));
                 tc_mma(tbase + C_Y, tbase + C_SL + 8 * ks, b, idesc_bf16(CK), ks > 0);
                 tc_mma(tbase + C_Y, tbase + C_SH + 8 * ks, b, idesc_bf16(CK), true);
             }
@@ -887,7 +915,30 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
             tc_commit(bar_o);
         }
         __syncwarp(); // lanes 1-31 waited here for lane 0's products
+    } else {
+        // ======================== loader warp ========================
+        // Chunk ci + 1's q, k and v into the buffers of its parity, as soon as
+        // their last readers are done: chunk ci - 1's Z and Y products (K | Q)
+        // and its E (v), both before its U product's commit (chunk 0's were
+        // issued before the wait for the prep kernel).
+        int issued = 0; // chunks whose copies went out (chunk 0's before the loop)
+#pragma unroll 1
+        for (int c0 = 0; lane == 0 && c0 + CK < L; c0 += CK) {
+            const int ci = c0 / CK;
+            if (ci > 0 && !mbar_wait(bar_u, (uint32_t)((ci - 1) & 1))) {
+                report(p.err, GDN_DEVERR_TIMEOUT);
+                break;
+            }
+            load_chunk(c0 + CK, (ci + 1) & 1);
+            issued = ci + 1;
+        }
+        // no copy may still be landing when the CTA ends (the compute warps
+        // waited for every one unless they stopped early)
+        if (lane == 0 && L > 0)
+            mbar_wait(bar_in[issued & 1], (uint32_t)((issued >> 1) & 1));
+        __syncwarp();
     }
+
     cp_async_wait_all(); // a chain that stopped early may have the next chunk's inputs in flight
     tc_before_sync();
     __syncthreads();
@@ -903,6 +954,42 @@ size_t prefill_chunked_workspace_bytes(int nseq, int total_tokens, int hv)
         return 0;
     return (size_t)prep_units(nseq, total_tokens) * (size_t)hv * (size_t)PW::BYTES;
 }
+
+namespace {
+
+// cuTensorMapEncodeTiled, found once through the runtime (no link to the
+// driver library)
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// a bf16 [tokens][heads][CD] tensor, boxes of box_inner x 1 head x CK tokens
+bool encode_map(CUtensorMap *m, const void *base, int heads, int tokens, int box_inner, bool swizzle128)
+{
+    const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)CD, (cuuint64_t)heads, (cuuint64_t)tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)CD * 2, (cuuint64_t)heads * CD * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)box_inner, 1u, (cuuint32_t)CK};
+    const cuuint32_t step[3] = {1u, 1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, step,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+} // namespace
 
 cudaError_t launch_gdn_prefill_chunked_tc(const PrefillArgs &a, cudaStream_t s)
 {
@@ -930,8 +1017,16 @@ cudaError_t launch_gdn_prefill_chunked_tc(const PrefillArgs &a, cudaStream_t s)
                                (size_t)PS::TOTAL, s, a, work, (int)units);
     if (e != cudaSuccess)
         return e;
+    // the tensor maps of q, k and v (unused, and left zero, without tokens)
+    ChunkMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (a.total_tokens > 0 &&
+        (!encode_map(&maps.q, a.q, a.hk, a.total_tokens, 64, true) ||
+         !encode_map(&maps.k, a.k, a.hk, a.total_tokens, 64, true) ||
+         !encode_map(&maps.v, a.v, a.hv, a.total_tokens, CD, false)))
+        return cudaErrorInvalidValue;
     return launch_pdl(gdn_chunked_tc_kernel, dim3((unsigned)ctas), dim3(TCW_THREADS), (size_t)TS::TOTAL, s, a,
-                      static_cast<const unsigned char *>(work), (int)units);
+                      static_cast<const unsigned char *>(work), (int)units, maps);
 }
 
 } // namespace gdn
