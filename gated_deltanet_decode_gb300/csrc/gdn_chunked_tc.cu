@@ -734,12 +734,15 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
                 uint32_t eh[16], el[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
-                    const int t = 32 * half + i;
+                    const int t = 32 * half + i; // even: the pairs below are 8-byte loads
                     const float v0 = __bfloat162float(rv[t * CD + row]), v1 = __bfloat162float(rv[(t + 1) * CD + row]);
+                    const float2 be = *reinterpret_cast<const float2 *>(BE + t);
+                    const float2 eg = *reinterpret_cast<const float2 *>(EG + t);
+                    const float2 ik = *reinterpret_cast<const float2 *>(IK + t);
                     // tokens past the chunk's end: E is zero (their v and Z may
                     // be the next sequence's)
-                    const float e0 = t < n ? BE[t] * (v0 - EG[t] * IK[t] * z[i]) : 0.f;
-                    const float e1 = t + 1 < n ? BE[t + 1] * (v1 - EG[t + 1] * IK[t + 1] * z[i + 1]) : 0.f;
+                    const float e0 = t < n ? be.x * (v0 - eg.x * ik.x * z[i]) : 0.f;
+                    const float e1 = t + 1 < n ? be.y * (v1 - eg.y * ik.y * z[i + 1]) : 0.f;
                     split2(e0, e1, eh[i / 2], el[i / 2]);
                 }
                 tst16(tlane + C_EH + 16 * half, eh);
@@ -770,8 +773,10 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
                     const int t = 32 * half + i;
+                    const float2 ec = *reinterpret_cast<const float2 *>(EC + t);
+                    const float2 ik = *reinterpret_cast<const float2 *>(IK + t);
                     split2(u[i], u[i + 1], uh[i / 2], ul[i / 2]);
-                    split2(u[i] * EC[t] * IK[t], u[i + 1] * EC[t + 1] * IK[t + 1], wh[i / 2], wl[i / 2]);
+                    split2(u[i] * ec.x * ik.x, u[i + 1] * ec.y * ik.y, wh[i / 2], wl[i / 2]);
                 }
                 tst16(tlane + C_UH + 16 * half, uh);
                 tst16(tlane + C_UL + 16 * half, ul);
@@ -782,9 +787,12 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
                     uint32_t yo[32];
                     tld32(tlane + C_Y + 32 * half, y);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
+                    for (int i = 0; i < 32; i += 2) {
                         const int t = 32 * half + i;
-                        yo[i] = __float_as_uint(y[i] * EG[t] * IQ[t]);
+                        const float2 eg = *reinterpret_cast<const float2 *>(EG + t);
+                        const float2 iq = *reinterpret_cast<const float2 *>(IQ + t);
+                        yo[i] = __float_as_uint(y[i] * eg.x * iq.x);
+                        yo[i + 1] = __float_as_uint(y[i + 1] * eg.y * iq.y);
                     }
                     tst32(tlane + C_U + 32 * half, yo);
                 }
