@@ -7,41 +7,39 @@
 // The operation, the regrouping over chunks of 64 tokens and the split
 // products are those of gdn_chunked.cu (whose header states the algebra):
 // per chunk A, P and T = (I + A)^{-1}, then with S_0 the state before it
-//     Z|Y = S_0 [K|Q]^T,  E = (V^T - Z diag(e^G ik)) diag(beta),  U = E T^T,
-//     O   = Y diag(e^G iq) + U P^T,  S_C = e^{G_C} S_0 + U diag(e^{G_C-G} ik) K
+//     Z = S_0 K^T, Y = S_0 Q^T,  E = (V^T - Z diag(e^G ik)) diag(beta),
+//     U = E T^T,  O = Y diag(e^G iq) + U P^T,
+//     S_C = e^{G_C} S_0 + U diag(e^{G_C-G} ik) K
 // (ik, iq: the per-token norm scales of the raw bf16 k and q, which are exact
-// operands).  Here the four products that carry the state's 128 rows run as
-// M = 128 tcgen05.mma with the accumulators in tensor memory:
+// operands).
+//
+// Two kernels.  The prep kernel (one CTA per workspace unit and value head)
+// forms every chunk's state-free terms at once -- the gates, the norm scales,
+// P and T split into bf16 heads and tails -- into a caller-owned workspace.
+// The chunk kernel (one CTA per sequence and value head) then carries the
+// state through the chunks in order:
 //   * the state S lives in TMEM for the whole sequence (fp32, 128 columns);
-//   * its bf16 head and tail, the A operand of Z|Y, are written back into
-//     TMEM from S at the start of each chunk; E, U and U diag(e^{G_C-G} ik)
-//     likewise (tcgen05.mma reads A from TMEM);
-//   * B operands (raw K|Q, raw K transposed, T and P heads and tails) sit in
-//     shared memory in the canonical no-swizzle K-major layout: 8-row x
-//     16-byte core matrices, adjacent along K at 128 bytes (the descriptor's
-//     leading offset), 8-row groups at K/8 x 128 bytes (its stride offset);
-//   * one thread issues the products and commits each group to an mbarrier;
-//     the CTA's threads read and write TMEM one state row a thread (two warps
-//     on each 32-lane quarter, each taking half of the columns).
-// Z|Y is issued as soon as the chunk's K and Q are in shared memory and runs
-// on the tensor cores while the CTA forms A, P and T (the fp32 blocked
-// inverse shared with gdn_chunked.cu).
+//     the products are M = 128 tcgen05.mma with their A operands in TMEM
+//     (the bf16 head and tail of S, E, U and U diag(e^{G_C-G} ik)) and their
+//     B operands in shared memory: raw K and Q in the 128-byte-swizzled
+//     K-major layout a tensor copy writes, raw K^T, T and P in the canonical
+//     no-swizzle K-major layout (8-row x 16-byte core matrices);
+//   * eight compute warps, one per (TMEM lane quarter, column half), do the
+//     TMEM round trips and the elementwise work; a product warp issues every
+//     product and commits each group to an mbarrier (Z alone first, then Y,
+//     U, the state update, O); a loader warp brings each chunk's q, k, v
+//     with tensor copies a chunk ahead into double buffers;
+//   * the prep block of a chunk comes by one bulk copy, a chunk ahead.
 //
 // Tensor memory (512 columns, one CTA an SM): S 0-127; Z 128-191, later the
-// head|tail of U diag(e^{G_C-G} ik) (128-159 | 160-191); Y, then O, 192-255;
-// U 256-319; the head|tail of S 320-383 | 384-447, later those of E
-// (320-351 | 352-383) and of U (384-415 | 416-447); [K|Q] K^T 448-511.
-// Every region is reused only after the mbarrier of the products that read
-// it has completed.
+// head|tail of U diag(e^{G_C-G} ik) (128-159 | 160-191); Y 192-255; U
+// 256-319, later O; the head|tail of S 320-383 | 384-447; those of E and
+// later of U 448-479 | 480-511.  Every region is rewritten only after the
+// products that read it have completed.
 //
-// [K|Q] K^T (rows 0-63: K K^T, 64-127: Q K^T) is itself one M = 128 product
-// with both operands in shared memory; one thread a row turns it into A
-// (fp32) and P (head and tail) with the gates, the norms and the masks.
-//
-// The next chunk's raw q, k, v are copied into a staging area (cp.async)
-// while the current chunk's products run.  Every mbarrier wait is bounded:
-// one that runs out reports GDN_DEVERR_TIMEOUT, and the CTA stops without
-// writing outputs or state, frees its tensor memory and returns.
+// Every mbarrier wait is bounded: one that runs out reports
+// GDN_DEVERR_TIMEOUT, and the CTA stops without writing outputs or state,
+// frees its tensor memory and returns.
 #include <atomic>
 #include <cstring>
 #include <mutex>
