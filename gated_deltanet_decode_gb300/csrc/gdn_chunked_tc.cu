@@ -116,7 +116,8 @@ struct TS {
     static constexpr int KT = KQ + 2 * KQ_BYTES;  // two of them, chunk parity
     static constexpr int PB = KT + 2 * KT_BYTES;  // two prep blocks (PW), chunk parity
     static constexpr int BARS = PB + 2 * PW::BYTES; // mbarriers: Z, U, O, prep block 0, 1, S;
-                                                    // S's split, E, U's split ready; inputs 0, 1
+                                                    // S's split, E, U's split ready; inputs 0, 1;
+                                                    // output tile free
     static constexpr int TADDR = BARS + 96;       // the TMEM base address
     static constexpr int BYTES = TADDR + 16;
     static constexpr int STAGE = (BYTES + 127) & ~127; // raw v, [CK][CD], two of them, chunk parity
@@ -490,6 +491,8 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
     const uint32_t bar_wready = sm_addr(&bars[8]);
     // loader warp -> compute warps: a chunk's q, k and v are in shared memory (chunk parity)
     const uint32_t bar_in[2] = {sm_addr(&bars[9]), sm_addr(&bars[10])};
+    // loader warp -> compute warps: it has stored the output tile (one completion a chunk but the last)
+    const uint32_t bar_osfree = sm_addr(&bars[11]);
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sm_addr(taddr_slot)),
                      "r"(kTmemCols)
@@ -506,6 +509,7 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
         mbar_init(bar_wready, TC_WARPS);
         mbar_init(bar_in[0], 1);
         mbar_init(bar_in[1], 1);
+        mbar_init(bar_osfree, 1);
         mbar_init(bar_pb[0], 1);
         mbar_init(bar_pb[1], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -612,15 +616,15 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
     // (16-byte stores when `out` is 16-byte aligned, as its rows then are;
     // the call does not require it, so 2-byte stores otherwise)
     const bool out16 = (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
-    auto store_outputs = [&](int cbase, int nn) {
+    auto store_outputs = [&](int cbase, int nn, int me, int nthr) {
         if (out16) {
-            for (int e = tid; e < nn * (CD / 8); e += TC_THREADS) {
+            for (int e = me; e < nn * (CD / 8); e += nthr) {
                 const int t = e / (CD / 8), j = e % (CD / 8);
                 *reinterpret_cast<uint4 *>(out + (size_t)(t0 + cbase + t) * out_tok + (size_t)h * CD + 8 * j) =
                     *reinterpret_cast<const uint4 *>(OS + t * CD + 8 * j);
             }
         } else {
-            for (int e = tid; e < nn * CD; e += TC_THREADS)
+            for (int e = me; e < nn * CD; e += nthr)
                 out[(size_t)(t0 + cbase + e / CD) * out_tok + (size_t)h * CD + (e % CD)] = OS[e];
         }
     };
@@ -709,7 +713,10 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
 
             // ---- (2) the previous chunk's outputs, while Z runs; this
             // chunk's prep block; then E from Z, one state row a thread ----
-            late = __any_sync(0xffffffffu, ci > 0 && !mbar_wait(bar_o, (uint32_t)((ci - 1) & 1)));
+            // the previous chunk's O is done, and the loader warp has stored
+            // the output tile of the chunk before it
+            late = __any_sync(0xffffffffu, (ci > 0 && !mbar_wait(bar_o, (uint32_t)((ci - 1) & 1))) ||
+                                               (ci > 1 && !mbar_wait(bar_osfree, (uint32_t)((ci - 2) & 1))));
             if (ci > 0 && !late)
                 put_outputs(); // warp-wide TMEM loads: the warp agrees on `late`
             late = late || !mbar_wait(bar_pb[ci & 1], (uint32_t)((ci >> 1) & 1)) ||
@@ -721,8 +728,6 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
                 break;
             }
             tc_after_sync();
-            if (ci > 0)
-                store_outputs(c0 - CK, n_prev);
             if (more)
                 prep_copy(ci + 1); // its block's last readers, the previous chunk's products, are done
             {
@@ -831,9 +836,16 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
             abort = compute_sync_or(late);
             if (!abort) {
                 tc_after_sync();
-                put_outputs();
+                // the loader warp's store of the tile before (none with one chunk)
+                const bool tile_late =
+                    __any_sync(0xffffffffu, last > 0 && !mbar_wait(bar_osfree, (uint32_t)((last - 1) & 1)));
+                if (tile_late)
+                    report(p.err, GDN_DEVERR_TIMEOUT);
+                if (!tile_late)
+                    put_outputs();
                 compute_sync();
-                store_outputs(last * CK, n_prev);
+                if (!tile_late)
+                    store_outputs(last * CK, n_prev, tid, TC_THREADS);
             }
         }
         if (!abort) {
@@ -927,16 +939,39 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
         // their last readers are done: chunk ci - 1's Z and Y products (K | Q)
         // and its E (v), both before its U product's commit (chunk 0's were
         // issued before the wait for the prep kernel).
+        // It also stores each chunk's outputs but the last: the compute warps
+        // put chunk ci - 1's into the shared tile before they signal chunk
+        // ci's E, and wait for this warp's "tile free" before the next fill.
         int issued = 0; // chunks whose copies went out (chunk 0's before the loop)
 #pragma unroll 1
-        for (int c0 = 0; lane == 0 && c0 + CK < L; c0 += CK) {
+        for (int c0 = 0; c0 < L; c0 += CK) {
             const int ci = c0 / CK;
-            if (ci > 0 && !mbar_wait(bar_u, (uint32_t)((ci - 1) & 1))) {
-                report(p.err, GDN_DEVERR_TIMEOUT);
+            bool late = false;
+            if (c0 + CK < L) {
+                if (lane == 0) {
+                    late = ci > 0 && !mbar_wait(bar_u, (uint32_t)((ci - 1) & 1));
+                    if (!late) {
+                        load_chunk(c0 + CK, (ci + 1) & 1);
+                        issued = ci + 1;
+                    }
+                }
+                late = __shfl_sync(0xffffffffu, late, 0);
+            }
+            // every phase of E's barrier, chunk 0's too: a parity wait passes
+            // at once on a barrier still a phase behind
+            if (!late)
+                late = !__all_sync(0xffffffffu, mbar_wait(bar_eready, (uint32_t)(ci & 1)));
+            if (late) {
+                if (lane == 0)
+                    report(p.err, GDN_DEVERR_TIMEOUT);
                 break;
             }
-            load_chunk(c0 + CK, (ci + 1) & 1);
-            issued = ci + 1;
+            if (ci > 0) {
+                store_outputs(c0 - CK, CK, lane, 32); // a chunk before the last is whole
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar_osfree);
+            }
         }
         // no copy may still be landing when the CTA ends (the compute warps
         // waited for every one unless they stopped early)
