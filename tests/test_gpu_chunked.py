@@ -266,3 +266,26 @@ def test_chunked_output_not_16_byte_aligned(gdn):
     assert torch.equal(c.pool.tensor, after)
     assert buf[0].item() == 0 and not buf[1 + n:].any()
     assert gdn.get_device_error() == 0
+
+
+def test_chunked_ragged_tail_ignores_the_next_sequence(gdn):
+    """A sequence's last, partial chunk is read by the tensor copies as a
+    whole 64-token box, so its rows past the sequence hold the next
+    sequence's tokens.  Those rows reach no result: with the next sequence's
+    q, k and v all NaN, the first sequence's outputs and state are bit-equal
+    to a run where they are ordinary values."""
+    c = Case(gdn, I.QWEN_08B, [100, 80], seed=96, n_pad=0)
+    a, b = int(c.cu_np[0]), int(c.cu_np[1])
+    assert b - a == 100 and c.rs_np[0] > 0 and c.rs_np[1] > 0
+    out_ok = chunked(c).clone()
+    torch.cuda.synchronize()
+    state_ok = c.pool.tensor[int(c.ws_np[0])].clone()
+    c.reset()
+    for k in ("q", "k", "v"):
+        c.dev[k][b:] = float("nan")
+    out_nan = chunked(c)
+    torch.cuda.synchronize()
+    assert torch.equal(out_nan[a:b], out_ok[a:b])
+    assert torch.equal(c.pool.tensor[int(c.ws_np[0])], state_ok)
+    assert torch.isnan(out_nan[b:].float()).any()  # the poisoned sequence itself is NaN
+    assert gdn.get_device_error() == 0
