@@ -1053,12 +1053,8 @@ cudaError_t launch_gdn_prefill_chunked_tc(const PrefillArgs &a, cudaStream_t s)
             return e;
         configured.fetch_or(bit, std::memory_order_release);
     }
-    unsigned char *work = static_cast<unsigned char *>(a.work);
-    cudaError_t e = launch_pdl(gdn_chunk_prep_kernel, dim3((unsigned)(units * a.hv)), dim3(TC_THREADS),
-                               (size_t)PS::TOTAL, s, a, work, (int)units);
-    if (e != cudaSuccess)
-        return e;
-    // the tensor maps of q, k and v (unused, and left zero, without tokens)
+    // the tensor maps of q, k and v (unused, and left zero, without tokens),
+    // before either kernel goes out
     ChunkMaps maps;
     memset(&maps, 0, sizeof(maps));
     if (a.total_tokens > 0 &&
@@ -1066,6 +1062,11 @@ cudaError_t launch_gdn_prefill_chunked_tc(const PrefillArgs &a, cudaStream_t s)
          !encode_map(&maps.k, a.k, a.hk, a.total_tokens, 64, true) ||
          !encode_map(&maps.v, a.v, a.hv, a.total_tokens, CD, false)))
         return cudaErrorInvalidValue;
+    unsigned char *work = static_cast<unsigned char *>(a.work);
+    cudaError_t e = launch_pdl(gdn_chunk_prep_kernel, dim3((unsigned)(units * a.hv)), dim3(TC_THREADS),
+                               (size_t)PS::TOTAL, s, a, work, (int)units);
+    if (e != cudaSuccess)
+        return e;
     return launch_pdl(gdn_chunked_tc_kernel, dim3((unsigned)ctas), dim3(TCW_THREADS), (size_t)TS::TOTAL, s, a,
                       static_cast<const unsigned char *>(work), (int)units, maps);
 }

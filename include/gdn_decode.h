@@ -295,9 +295,13 @@ int gdn_prefill(const void *q, const void *k, const void *v, const void *a, cons
  * aligned, at least gdn_prefill_chunked_workspace_bytes(nseq, total_tokens,
  * hv) bytes (GDN_EINVAL otherwise); its contents need no initialisation and
  * are garbage afterwards; calls that overlap on the GPU need their own.
- * fp32 activations ignore it (NULL allowed).  cu_seqlens must be
- * nondecreasing: a sequence whose chunks the prep kernel could not place
- * counts as bad (zero outputs, GDN_DEVERR_BAD_SLOT, no state written). */
+ * fp32 activations ignore it (NULL allowed).  The bf16 call also encodes
+ * three tensor maps (q, k, v) on the host for the chunk kernel's tensor
+ * copies; should the driver refuse one, the call returns GDN_ECUDA and
+ * launches nothing.  `out` needs no alignment beyond its element.
+ * cu_seqlens must be nondecreasing: a sequence whose chunks the prep kernel
+ * could not place counts as bad (zero outputs, GDN_DEVERR_BAD_SLOT, no
+ * state written). */
 size_t gdn_prefill_chunked_workspace_bytes(int nseq, int total_tokens, int hv);
 int gdn_prefill_chunked(const void *q, const void *k, const void *v, const void *a, const void *b,
                         const float *A_log, const float *dt_bias, gdn_pool *pool, const int32_t *cu_seqlens,
