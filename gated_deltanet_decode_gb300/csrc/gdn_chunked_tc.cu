@@ -24,7 +24,7 @@
 //     B operands in shared memory: raw K and Q in the 128-byte-swizzled
 //     K-major layout a tensor copy writes, raw K^T, T and P in the canonical
 //     no-swizzle K-major layout (8-row x 16-byte core matrices);
-//   * eight compute warps, one per (TMEM lane quarter, column half), do the
+//   * sixteen compute warps, one per (TMEM lane quarter, column quarter), do the
 //     TMEM round trips and the elementwise work; a product warp issues every
 //     product and commits each group to an mbarrier (Z alone first, then Y,
 //     U, the state update, O); a loader warp brings each chunk's q, k, v
@@ -58,10 +58,12 @@ namespace {
 
 constexpr int TC_WARPS = 8;
 constexpr int TC_THREADS = TC_WARPS * 32;
-// the chunk kernel: the eight warps above, one a (TMEM lane quarter, column
-// half), a warp that issues the tensor-core products and a warp that copies
-// the next chunk's q, k and v into shared memory
-constexpr int TCW_THREADS = TC_THREADS + 64;
+// the chunk kernel: sixteen compute warps, one a (TMEM lane quarter, column
+// quarter), a warp that issues the tensor-core products and a warp that
+// copies the next chunk's q, k and v into shared memory
+constexpr int TCC_WARPS = 16;
+constexpr int TCC_THREADS = TCC_WARPS * 32;
+constexpr int TCW_THREADS = TCC_THREADS + 64;
 constexpr uint32_t kTmemCols = 512;
 
 // TMEM columns.  O accumulates into U's columns once U is split; E's and
@@ -213,6 +215,27 @@ __device__ __forceinline__ void tld32(uint32_t taddr, float (&v)[32])
 #pragma unroll
     for (int i = 0; i < 32; ++i)
         v[i] = __uint_as_float(r[i]);
+}
+// 16 consecutive columns of this thread's lane
+__device__ __forceinline__ void tld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+                 "[%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                   "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tst8(uint32_t taddr, const uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
 }
 __device__ __forceinline__ void tst32(uint32_t taddr, const uint32_t (&r)[32])
 {
@@ -422,13 +445,14 @@ __global__ void __launch_bounds__(TC_THREADS, 4) gdn_chunk_prep_kernel(const Pre
         hdr[0] = s, hdr[1] = c0;
 }
 
-// the eight compute warps (256 threads) meet at named barrier 1; the _or
-// form also returns whether any of them passed true
-__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// the sixteen compute warps (TCC_THREADS = 512 threads) meet at named
+// barrier 1; the _or form also returns whether any of them passed true
+static_assert(TCC_THREADS == 512, "the named barriers below count 512 threads");
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 __device__ __forceinline__ bool compute_sync_or(bool v)
 {
     uint32_t r;
-    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 256, p;\n\t"
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 512, p;\n\t"
                  "selp.u32 %0, 1, 0, q;\n\t}"
                  : "=r"(r)
                  : "r"((uint32_t)v)
@@ -449,7 +473,7 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
     bf16 *const RV = reinterpret_cast<bf16 *>(smem + TS::STAGE);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
+    const int quarter = warp & 3, cq = warp >> 2; // compute warps: TMEM lane quarter, column quarter
     const int row = 32 * quarter + lane; // this thread's state row (its TMEM lane)
     const int seq = blockIdx.x / p.hv, h = blockIdx.x - seq * p.hv;
     const int hq = h / (p.hv / p.hk);
@@ -504,9 +528,9 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
         mbar_init(bar_u, 1);
         mbar_init(bar_o, 1);
         mbar_init(bar_s, 1);
-        mbar_init(bar_sready, TC_WARPS);
-        mbar_init(bar_eready, TC_WARPS);
-        mbar_init(bar_wready, TC_WARPS);
+        mbar_init(bar_sready, TCC_WARPS);
+        mbar_init(bar_eready, TCC_WARPS);
+        mbar_init(bar_wready, TCC_WARPS);
         mbar_init(bar_in[0], 1);
         mbar_init(bar_in[1], 1);
         mbar_init(bar_osfree, 1);
@@ -520,28 +544,22 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
     const uint32_t tbase = *taddr_slot;
     const uint32_t tlane = tbase + ((uint32_t)(32 * quarter) << 16); // this warp's 32 lanes
 
-    // the state in: row `row`, columns 64*half .. 64*half + 63 (compute warps)
+    // the state in: row `row`, columns 32*cq .. 32*cq + 31 (compute warps)
     const size_t slot_floats = (size_t)p.hv * CD * CD;
     const size_t head_off = (size_t)h * CD * CD;
-    if (warp < TC_WARPS) {
-        const float *S0 = p.pool + (size_t)rs * slot_floats + head_off + (size_t)row * CD + 64 * half;
+    if (warp < TCC_WARPS) {
+        const float *S0 = p.pool + (size_t)rs * slot_floats + head_off + (size_t)row * CD + 32 * cq;
+        uint32_t r[32];
 #pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
-            uint32_t r[32];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 v = *reinterpret_cast<const float4 *>(S0 + 32 * q2 + 4 * i);
-                r[4 * i] = __float_as_uint(v.x), r[4 * i + 1] = __float_as_uint(v.y);
-                r[4 * i + 2] = __float_as_uint(v.z), r[4 * i + 3] = __float_as_uint(v.w);
-            }
-            tst32(tlane + C_S + 64 * half + 32 * q2, r);
+        for (int i = 0; i < 8; ++i) {
+            const float4 v = *reinterpret_cast<const float4 *>(S0 + 4 * i);
+            r[4 * i] = __float_as_uint(v.x), r[4 * i + 1] = __float_as_uint(v.y);
+            r[4 * i + 2] = __float_as_uint(v.z), r[4 * i + 3] = __float_as_uint(v.w);
         }
+        tst32(tlane + C_S + 32 * cq, r);
         tst_wait();
     }
 
-    const bf16 *const qg = reinterpret_cast<const bf16 *>(p.q);
-    const bf16 *const kg = reinterpret_cast<const bf16 *>(p.k);
-    const bf16 *const vg = reinterpret_cast<const bf16 *>(p.v);
 
     // The raw q, k, v of the chunk starting at token cn into the buffers of
     // parity `buf`, by five tensor copies counted on bar_in[buf] (one
@@ -568,7 +586,7 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
     auto build_kt = [&](int buf, int nn) {
         unsigned char *const kt = KT + buf * TS::KT_BYTES;
         const unsigned char *const kq = KQ + buf * TS::KQ_BYTES;
-        for (int g = warp; g < (CK / 8) * (CD / 8) / 4; g += TC_WARPS) {
+        for (int g = warp; g < (CK / 8) * (CD / 8) / 4; g += TCC_WARPS) {
             const int m = 4 * g + (lane >> 3);
             const int r = 8 * (m / (CD / 8)) + (lane & 7), jb = m % (CD / 8); // token row, 16-byte piece
             const uint32_t src = sm_addr(kq + (jb >> 3) * TS::HALF + r * 128 + (((jb & 7) ^ (r & 7)) << 4));
@@ -601,17 +619,17 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
                       (uint32_t)PW::BYTES, bar);
         }
     };
-    // The outputs of a chunk leave in two steps: each thread puts its row
-    // `row` of O (in U's columns), tokens 32*half .. 32*half + 31, into the
-    // shared output tile (put_outputs); after a CTA barrier every thread
-    // stores 16-byte pieces of the tile's token rows (store_outputs).
+    // The outputs of a chunk leave in two steps: each compute thread puts
+    // its row `row` of O (in U's columns), tokens 16*cq .. 16*cq + 15, into
+    // the shared output tile (put_outputs); then threads store 16-byte pieces
+    // of the tile's token rows (store_outputs).
     bf16 *const OS = reinterpret_cast<bf16 *>(smem + TS::OUTS);
     auto put_outputs = [&]() {
-        float o[32];
-        tld32(tlane + C_U + 32 * half, o);
+        float o[16];
+        tld16(tlane + C_U + 16 * cq, o);
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            OS[(32 * half + i) * CD + row] = from_f<bf16>(o[i]);
+        for (int i = 0; i < 16; ++i)
+            OS[(16 * cq + i) * CD + row] = from_f<bf16>(o[i]);
     };
     // (16-byte stores when `out` is 16-byte aligned, as its rows then are;
     // the call does not require it, so 2-byte stores otherwise)
@@ -628,7 +646,7 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
                 out[(size_t)(t0 + cbase + e / CD) * out_tok + (size_t)h * CD + (e % CD)] = OS[e];
         }
     };
-    if (L > 0 && warp == TC_WARPS + 1 && lane == 0)
+    if (L > 0 && warp == TCC_WARPS + 1 && lane == 0)
         load_chunk(0, 0); // q, k and v are this call's inputs: no earlier kernel writes them
     wait_prior_grid(); // the prep kernel's units are complete
 
@@ -640,7 +658,7 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
         named = named && ubase + j < units && hd[0] == seq && hd[1] == CK * j;
     }
     if (!__syncthreads_and(named)) {
-        if (L > 0 && warp == TC_WARPS + 1 && lane == 0)
+        if (L > 0 && warp == TCC_WARPS + 1 && lane == 0)
             mbar_wait(bar_in[0], 0u); // the first chunk's copies land before the CTA ends
         if (h == 0 && tid == 0)
             report(p.err, GDN_DEVERR_BAD_SLOT);
@@ -657,7 +675,7 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
     if (L > 0) {
         prep_copy(0);
         // chunk c's inputs complete phase c / 2 of bar_in[c % 2]
-        if (warp < TC_WARPS) {
+        if (warp < TCC_WARPS) {
             in_late = !__all_sync(0xffffffffu, mbar_wait(bar_in[0], 0u));
             if (!in_late)
                 build_kt(0, min(CK, L));
@@ -667,7 +685,7 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
     // this chunk's prep block, by chunk parity
     auto pblock = [&](int ci) { return smem + TS::PB + (ci & 1) * PW::BYTES; };
 
-    if (warp < TC_WARPS) {
+    if (warp < TCC_WARPS) {
         // ======================= compute warps =======================
         bool abort = false;
         int n_prev = 0;
@@ -695,14 +713,13 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
                 break;
             }
             tc_after_sync();
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
+            {
                 float sv[32];
                 uint32_t hi[16], lo[16];
-                tld32(tlane + C_S + 64 * half + 32 * q2, sv);
+                tld32(tlane + C_S + 32 * cq, sv);
                 split32(sv, hi, lo);
-                tst16(tlane + C_SH + 32 * half + 16 * q2, hi);
-                tst16(tlane + C_SL + 32 * half + 16 * q2, lo);
+                tst16(tlane + C_SH + 16 * cq, hi);
+                tst16(tlane + C_SL + 16 * cq, lo);
             }
             tst_wait();
             smem_to_async(); // K^T, written through the generic proxy
@@ -732,12 +749,12 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
                 prep_copy(ci + 1); // its block's last readers, the previous chunk's products, are done
             {
                 const bf16 *const rv = RV + (ci & 1) * CK * CD;
-                float z[32];
-                tld32(tlane + C_Z + 32 * half, z);
-                uint32_t eh[16], el[16];
+                float z[16];
+                tld16(tlane + C_Z + 16 * cq, z);
+                uint32_t eh[8], el[8];
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const int t = 32 * half + i; // even: the pairs below are 8-byte loads
+                for (int i = 0; i < 16; i += 2) {
+                    const int t = 16 * cq + i; // even: the pairs below are 8-byte loads
                     const float v0 = __bfloat162float(rv[t * CD + row]), v1 = __bfloat162float(rv[(t + 1) * CD + row]);
                     const float2 be = *reinterpret_cast<const float2 *>(BE + t);
                     const float2 eg = *reinterpret_cast<const float2 *>(EG + t);
@@ -748,8 +765,8 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
                     const float e1 = t + 1 < n ? be.y * (v1 - eg.y * ik.y * z[i + 1]) : 0.f;
                     split2(e0, e1, eh[i / 2], el[i / 2]);
                 }
-                tst16(tlane + C_EH + 16 * half, eh);
-                tst16(tlane + C_EL + 16 * half, el);
+                tst8(tlane + C_EH + 8 * cq, eh);
+                tst8(tlane + C_EL + 8 * cq, el);
                 tst_wait();
             }
             smem_to_async(); // v read here, before the loader's next copy into its buffer
@@ -770,45 +787,44 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
             }
             tc_after_sync();
             {
-                float u[32];
-                tld32(tlane + C_U + 32 * half, u);
-                uint32_t uh[16], ul[16], wh[16], wl[16];
+                float u[16];
+                tld16(tlane + C_U + 16 * cq, u);
+                uint32_t uh[8], ul[8], wh[8], wl[8];
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const int t = 32 * half + i;
+                for (int i = 0; i < 16; i += 2) {
+                    const int t = 16 * cq + i;
                     const float2 ec = *reinterpret_cast<const float2 *>(EC + t);
                     const float2 ik = *reinterpret_cast<const float2 *>(IK + t);
                     split2(u[i], u[i + 1], uh[i / 2], ul[i / 2]);
                     split2(u[i] * ec.x * ik.x, u[i + 1] * ec.y * ik.y, wh[i / 2], wl[i / 2]);
                 }
-                tst16(tlane + C_UH + 16 * half, uh);
-                tst16(tlane + C_UL + 16 * half, ul);
-                tst16(tlane + C_WH + 16 * half, wh);
-                tst16(tlane + C_WL + 16 * half, wl);
+                tst8(tlane + C_UH + 8 * cq, uh);
+                tst8(tlane + C_UL + 8 * cq, ul);
+                tst8(tlane + C_WH + 8 * cq, wh);
+                tst8(tlane + C_WL + 8 * cq, wl);
                 {
-                    float y[32];
-                    uint32_t yo[32];
-                    tld32(tlane + C_Y + 32 * half, y);
+                    float y[16];
+                    uint32_t yo[16];
+                    tld16(tlane + C_Y + 16 * cq, y);
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const int t = 32 * half + i;
+                    for (int i = 0; i < 16; i += 2) {
+                        const int t = 16 * cq + i;
                         const float2 eg = *reinterpret_cast<const float2 *>(EG + t);
                         const float2 iq = *reinterpret_cast<const float2 *>(IQ + t);
                         yo[i] = __float_as_uint(y[i] * eg.x * iq.x);
                         yo[i + 1] = __float_as_uint(y[i + 1] * eg.y * iq.y);
                     }
-                    tst32(tlane + C_U + 32 * half, yo);
+                    tst16(tlane + C_U + 16 * cq, yo);
                 }
                 const float gC = EG[CK - 1];
-#pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) {
+                {
                     float sv[32];
                     uint32_t r[32];
-                    tld32(tlane + C_S + 64 * half + 32 * q2, sv);
+                    tld32(tlane + C_S + 32 * cq, sv);
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         r[i] = __float_as_uint(sv[i] * gC);
-                    tst32(tlane + C_S + 64 * half + 32 * q2, r);
+                    tst32(tlane + C_S + 32 * cq, r);
                 }
                 tst_wait();
             }
@@ -845,23 +861,20 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
                     put_outputs();
                 compute_sync();
                 if (!tile_late)
-                    store_outputs(last * CK, n_prev, tid, TC_THREADS);
+                    store_outputs(last * CK, n_prev, tid, TCC_THREADS);
             }
         }
         if (!abort) {
             // the final state, to the write slot (the read slot in place)
-            float *Sd = p.pool + (size_t)ws * slot_floats + head_off + (size_t)row * CD + 64 * half;
+            float *Sd = p.pool + (size_t)ws * slot_floats + head_off + (size_t)row * CD + 32 * cq;
+            float sv[32];
+            tld32(tlane + C_S + 32 * cq, sv);
 #pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                float sv[32];
-                tld32(tlane + C_S + 64 * half + 32 * q2, sv);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    *reinterpret_cast<float4 *>(Sd + 32 * q2 + 4 * i) =
-                        make_float4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]);
-            }
+            for (int i = 0; i < 8; ++i)
+                *reinterpret_cast<float4 *>(Sd + 4 * i) =
+                    make_float4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]);
         }
-    } else if (warp == TC_WARPS) {
+    } else if (warp == TCC_WARPS) {
         // ======================= product warp ========================
         // Per chunk: Z = S K^T (committed alone, E needs it first), Y = S
         // Q^T; U = E T^T (its commit covers Y's products too); S += W K,
