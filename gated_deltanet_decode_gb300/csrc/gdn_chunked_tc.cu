@@ -560,7 +560,6 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
         tst_wait();
     }
 
-
     // The raw q, k, v of the chunk starting at token cn into the buffers of
     // parity `buf`, by five tensor copies counted on bar_in[buf] (one
     // thread): k and q as two 128-byte-swizzled dk halves each, v row-major.
