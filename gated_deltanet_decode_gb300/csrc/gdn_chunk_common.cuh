@@ -17,7 +17,10 @@ typedef __nv_bfloat16 bf16;
 
 constexpr int CK = 64;      // tokens a chunk
 constexpr int CD = 128;     // dk = dv
-constexpr int LDF = CK + 1; // row stride (fp32) of the fp32 [token][token] work tiles
+// Row stride (fp32) of the fp32 [token][token] work tiles: 288-byte rows, so
+// the 8-byte (row g, columns 2c, 2c+1) accesses of an mma fragment put each
+// half-warp's four rows on distinct groups of eight banks.
+constexpr int LDF = CK + 8;
 
 // ---------------------------------------------------------------------------
 // Tensor-core helpers (mma.sync m16n8k16, bf16 in, fp32 accumulate).
@@ -102,11 +105,15 @@ __device__ __forceinline__ void acc_to_a(uint32_t (&ah)[4], uint32_t (&al)[4], c
 __device__ __forceinline__ void lda_f32(uint32_t (&ah)[4], uint32_t (&al)[4], const float *X, int ld, int m0, int k0,
                                         int g, int c)
 {
-    const float *p = X + (m0 + g) * ld + k0 + 2 * c;
-    split2(p[0], p[1], ah[0], al[0]);
-    split2(p[8 * ld], p[8 * ld + 1], ah[1], al[1]);
-    split2(p[8], p[9], ah[2], al[2]);
-    split2(p[8 * ld + 8], p[8 * ld + 9], ah[3], al[3]);
+    const float *p = X + (m0 + g) * ld + k0 + 2 * c; // 8-byte aligned: ld and k0 even
+    float2 v = *reinterpret_cast<const float2 *>(p);
+    split2(v.x, v.y, ah[0], al[0]);
+    v = *reinterpret_cast<const float2 *>(p + 8 * ld);
+    split2(v.x, v.y, ah[1], al[1]);
+    v = *reinterpret_cast<const float2 *>(p + 8);
+    split2(v.x, v.y, ah[2], al[2]);
+    v = *reinterpret_cast<const float2 *>(p + 8 * ld + 8);
+    split2(v.x, v.y, ah[3], al[3]);
 }
 
 // B fragment with B[k][n] = X[k][n] of a row-major fp32 tile (rows k0..,
@@ -255,8 +262,9 @@ __device__ __forceinline__ void t_below_diagonal(float *AF, float *XF, int warp,
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    AF[(16 * J + g + 8 * (e >> 1)) * LDF + 16 * I + 8 * nt + 2 * c + (e & 1)] = x[nt][e];
+                for (int hr = 0; hr < 2; ++hr)
+                    *reinterpret_cast<float2 *>(AF + (16 * J + g + 8 * hr) * LDF + 16 * I + 8 * nt + 2 * c) =
+                        make_float2(x[nt][2 * hr], x[nt][2 * hr + 1]);
             __syncwarp();
             float tij[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             uint32_t ah[4], al[4];
@@ -270,8 +278,9 @@ __device__ __forceinline__ void t_below_diagonal(float *AF, float *XF, int warp,
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    XF[(16 * I + g + 8 * (e >> 1)) * LDF + 16 * J + 8 * nt + 2 * c + (e & 1)] = -tij[nt][e];
+                for (int hr = 0; hr < 2; ++hr)
+                    *reinterpret_cast<float2 *>(XF + (16 * I + g + 8 * hr) * LDF + 16 * J + 8 * nt + 2 * c) =
+                        make_float2(-tij[nt][2 * hr], -tij[nt][2 * hr + 1]);
         }
         __syncthreads();
     }

@@ -279,8 +279,9 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
                     const float gt = GG[t];
                     if (!isq[i]) {
                         const float bt = BE[t];
-                        AF[t * LDF + s] = s < t ? bt * expf(gt - GG[s]) * x : 0.f;
-                        AF[t * LDF + s + 1] = s + 1 < t ? bt * expf(gt - GG[s + 1]) * y : 0.f;
+                        *reinterpret_cast<float2 *>(AF + t * LDF + s) =
+                            make_float2(s < t ? bt * expf(gt - GG[s]) * x : 0.f,
+                                        s + 1 < t ? bt * expf(gt - GG[s + 1]) * y : 0.f);
                     } else {
                         const float px = s <= t ? expf(gt - GG[s]) * x : 0.f;
                         const float py = s + 1 <= t ? expf(gt - GG[s + 1]) * y : 0.f;
@@ -304,8 +305,9 @@ __global__ void __launch_bounds__(CTHREADS, 1) gdn_chunked_kernel(const PrefillA
         // T's lower triangle, split (above it: zero)
         for (int e = tid; e < CK * CK / 2; e += CTHREADS) {
             const int t = e / (CK / 2), s = 2 * (e % (CK / 2));
-            const float x = s <= t ? XF[t * LDF + s] : 0.f;
-            const float y = s + 1 <= t ? XF[t * LDF + s + 1] : 0.f;
+            const float2 v = *reinterpret_cast<const float2 *>(XF + t * LDF + s);
+            const float x = s <= t ? v.x : 0.f;
+            const float y = s + 1 <= t ? v.y : 0.f;
             uint32_t hh, ll;
             split2(x, y, hh, ll);
             *reinterpret_cast<uint32_t *>(TH + t * LDT + s) = hh;

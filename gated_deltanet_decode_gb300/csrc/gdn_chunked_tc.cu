@@ -403,8 +403,7 @@ __global__ void __launch_bounds__(TC_THREADS, 4) gdn_chunk_prep_kernel(const Pre
             const float x = in0 ? expf(GATES[t] - GATES[s0]) * nt_ * IK[s0] * d[nt][2 * hh] : 0.f;
             const float y = in1 ? expf(GATES[t] - GATES[s0 + 1]) * nt_ * IK[s0 + 1] * d[nt][2 * hh + 1] : 0.f;
             if (!isq) {
-                AF[t * LDF + s0] = x;
-                AF[t * LDF + s0 + 1] = y;
+                *reinterpret_cast<float2 *>(AF + t * LDF + s0) = make_float2(x, y);
             } else {
                 uint32_t ph, pl;
                 split2(x, y, ph, pl);
@@ -434,8 +433,9 @@ __global__ void __launch_bounds__(TC_THREADS, 4) gdn_chunk_prep_kernel(const Pre
     for (int e = tid; e < CK * CK / 2; e += TC_THREADS) {
         const int cmi = e >> 5, l = e & 31;
         const int t = 8 * (cmi >> 3) + (l & 7), s2 = 8 * (cmi & 7) + 2 * (l >> 3);
-        const float x = s2 <= t ? XF[t * LDF + s2] : 0.f;
-        const float y = s2 + 1 <= t ? XF[t * LDF + s2 + 1] : 0.f;
+        const float2 v = *reinterpret_cast<const float2 *>(XF + t * LDF + s2);
+        const float x = s2 <= t ? v.x : 0.f;
+        const float y = s2 + 1 <= t ? v.y : 0.f;
         uint32_t th, tl;
         split2(x, y, th, tl);
         *reinterpret_cast<uint32_t *>(blk + PW::TH + cm_off<CK>(t, s2)) = th;
