@@ -392,16 +392,28 @@ __global__ void __launch_bounds__(TC_THREADS, 4) gdn_chunk_prep_kernel(const Pre
     // A[t][s] = beta_t e^{G_t-G_s} ik_t ik_s (k_t . k_s), s < t, into AF (over
     // q and k); P[t][s] = e^{G_t-G_s} iq_t ik_s (q_t . k_s), s <= t, split, to
     // the unit; the decay formed where it is used
+    // (a row's gate and scale, and a column pair's, loaded once: the stores
+    // into AF may alias them for the compiler)
     const float *const BE = GATES + CK;
+    float gt[2], sc[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const int t = m0 + g + 8 * hh;
+        gt[hh] = GATES[t];
+        sc[hh] = isq ? IQ[t] : IK[t] * BE[t];
+    }
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
+        const int s0 = 8 * nt + 2 * c;
+        const float2 gs = *reinterpret_cast<const float2 *>(GATES + s0);
+        const float2 ks = *reinterpret_cast<const float2 *>(IK + s0);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-            const int t = m0 + g + 8 * hh, s0 = 8 * nt + 2 * c;
-            const float nt_ = isq ? IQ[t] : IK[t] * BE[t];
+            const int t = m0 + g + 8 * hh;
+            const float nt_ = sc[hh];
             const bool in0 = isq ? s0 <= t : s0 < t, in1 = isq ? s0 + 1 <= t : s0 + 1 < t;
-            const float x = in0 ? expf(GATES[t] - GATES[s0]) * nt_ * IK[s0] * d[nt][2 * hh] : 0.f;
-            const float y = in1 ? expf(GATES[t] - GATES[s0 + 1]) * nt_ * IK[s0 + 1] * d[nt][2 * hh + 1] : 0.f;
+            const float x = in0 ? expf(gt[hh] - gs.x) * nt_ * ks.x * d[nt][2 * hh] : 0.f;
+            const float y = in1 ? expf(gt[hh] - gs.y) * nt_ * ks.y * d[nt][2 * hh + 1] : 0.f;
             if (!isq) {
                 *reinterpret_cast<float2 *>(AF + t * LDF + s0) = make_float2(x, y);
             } else {
