@@ -365,55 +365,71 @@ __global__ void __launch_bounds__(TC_THREADS, 4) gdn_chunk_prep_kernel(const Pre
         if (lane == 0)
             IQ[tt] = qscale * rsqrtf(sq + kEps), IK[tt] = rsqrtf(sk + kEps);
     }
-    // [K|Q] K^T: warp w takes rows 16 (w & 3) .. + 15 of K (w < 4) or Q (w >= 4)
-    // against all 64 tokens s, over dk
-    float d[8][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            d[nt][e] = 0.f;
+    // [K|Q] K^T over the tiles at or below the diagonal only: row block R
+    // (rows 16R .. 16R + 15) has the 16 x 8 tiles nt = 0 .. 2R + 1 there, 20
+    // of K's 32 and 20 of Q's.  Warp role r = warp & 3 (K's rows for warps
+    // 0-3, Q's for 4-7) takes five: two of block bA from column tile nA and
+    // three of block bB from nB,
+    //   r 0: block 0 tiles 0-1, block 3 tiles 0-2;  r 1: block 1 tiles 0-1, block 3 tiles 3-5;
+    //   r 2: block 1 tiles 2-3, block 2 tiles 0-2;  r 3: block 3 tiles 6-7, block 2 tiles 3-5.
     const bool isq = warp >= 4;
     const bf16 *const X = isq ? RQ : RK;
-    const int m0 = 16 * (warp & 3);
+    const int r = warp & 3;
+    const int bA = r == 0 ? 0 : r == 3 ? 3 : 1, nA = r == 2 ? 2 : r == 3 ? 6 : 0;
+    const int bB = r < 2 ? 3 : 2, nB = (r & 1) ? 3 : 0;
+    float d[5][4];
+#pragma unroll
+    for (int i = 0; i < 5; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            d[i][e] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < CD / 16; ++ks) {
-        uint32_t a[4];
-        lda(a, X, PS::LDQ, m0, 16 * ks, g, c);
+        uint32_t aa[4], ab[4];
+        lda(aa, X, PS::LDQ, 16 * bA, 16 * ks, g, c);
+        lda(ab, X, PS::LDQ, 16 * bB, 16 * ks, g, c);
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
+        for (int i = 0; i < 5; ++i) {
             uint32_t b0, b1;
-            ldb(b0, b1, RK, PS::LDQ, 8 * nt, 16 * ks, g, c);
-            mma16816(d[nt], a[0], a[1], a[2], a[3], b0, b1);
+            ldb(b0, b1, RK, PS::LDQ, 8 * (i < 2 ? nA + i : nB + i - 2), 16 * ks, g, c);
+            if (i < 2)
+                mma16816(d[i], aa[0], aa[1], aa[2], aa[3], b0, b1);
+            else
+                mma16816(d[i], ab[0], ab[1], ab[2], ab[3], b0, b1);
         }
     }
     __syncthreads(); // every warp's products are in registers: q and k are dead
 
     // A[t][s] = beta_t e^{G_t-G_s} ik_t ik_s (k_t . k_s), s < t, into AF (over
     // q and k); P[t][s] = e^{G_t-G_s} iq_t ik_s (q_t . k_s), s <= t, split, to
-    // the unit; the decay formed where it is used
-    // (a row's gate and scale, and a column pair's, loaded once: the stores
-    // into AF may alias them for the compiler)
+    // the unit; the decay formed where it is used.  A row's gate and scale,
+    // and a column pair's, are loaded once (the stores into AF may alias them
+    // for the compiler).  A's tiles above the diagonal are never read; P's
+    // are zero, written below.
     const float *const BE = GATES + CK;
-    float gt[2], sc[2];
+    float gt[2][2], sc[2][2]; // [block A or B][row g or g + 8]
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        const int t = m0 + g + 8 * hh;
-        gt[hh] = GATES[t];
-        sc[hh] = isq ? IQ[t] : IK[t] * BE[t];
-    }
+    for (int w = 0; w < 2; ++w)
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-        const int s0 = 8 * nt + 2 * c;
+        for (int hh = 0; hh < 2; ++hh) {
+            const int t = 16 * (w == 0 ? bA : bB) + g + 8 * hh;
+            gt[w][hh] = GATES[t];
+            sc[w][hh] = isq ? IQ[t] : IK[t] * BE[t];
+        }
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+        const int w = i < 2 ? 0 : 1;
+        const int m0 = 16 * (w == 0 ? bA : bB);
+        const int s0 = 8 * (i < 2 ? nA + i : nB + i - 2) + 2 * c;
         const float2 gs = *reinterpret_cast<const float2 *>(GATES + s0);
         const float2 ks = *reinterpret_cast<const float2 *>(IK + s0);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const int t = m0 + g + 8 * hh;
-            const float nt_ = sc[hh];
+            const float nt_ = sc[w][hh];
             const bool in0 = isq ? s0 <= t : s0 < t, in1 = isq ? s0 + 1 <= t : s0 + 1 < t;
-            const float x = in0 ? expf(gt[hh] - gs.x) * nt_ * ks.x * d[nt][2 * hh] : 0.f;
-            const float y = in1 ? expf(gt[hh] - gs.y) * nt_ * ks.y * d[nt][2 * hh + 1] : 0.f;
+            const float x = in0 ? expf(gt[w][hh] - gs.x) * nt_ * ks.x * d[i][2 * hh] : 0.f;
+            const float y = in1 ? expf(gt[w][hh] - gs.y) * nt_ * ks.y * d[i][2 * hh + 1] : 0.f;
             if (!isq) {
                 *reinterpret_cast<float2 *>(AF + t * LDF + s0) = make_float2(x, y);
             } else {
@@ -421,6 +437,21 @@ __global__ void __launch_bounds__(TC_THREADS, 4) gdn_chunk_prep_kernel(const Pre
                 split2(x, y, ph, pl);
                 *reinterpret_cast<uint32_t *>(blk + PW::PH + cm_off<CK>(t, s0)) = ph;
                 *reinterpret_cast<uint32_t *>(blk + PW::PL + cm_off<CK>(t, s0)) = pl;
+            }
+        }
+    }
+    if (isq) {
+        // P's 12 tiles wholly above the diagonal, three a Q warp: in order
+        // block 0 tiles 2-7, block 1 tiles 4-7, block 2 tiles 6-7
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            const int k = 3 * r + j;
+            const int R = k < 6 ? 0 : k < 10 ? 1 : 2, nt = k < 6 ? k + 2 : k < 10 ? k - 2 : k - 4;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int t = 16 * R + g + 8 * hh, s0 = 8 * nt + 2 * c;
+                *reinterpret_cast<uint32_t *>(blk + PW::PH + cm_off<CK>(t, s0)) = 0u;
+                *reinterpret_cast<uint32_t *>(blk + PW::PL + cm_off<CK>(t, s0)) = 0u;
             }
         }
     }
