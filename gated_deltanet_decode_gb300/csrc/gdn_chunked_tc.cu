@@ -347,23 +347,38 @@ __global__ void __launch_bounds__(TC_THREADS, 4) gdn_chunk_prep_kernel(const Pre
     cp_async_wait_all();
     __syncthreads();
 
-    // norm scales, one token a warp at a time
-    const float qscale = 1.0f / sqrtf((float)CD);
+    // norm scales, four tokens a warp at a time: lanes 8j .. 8j + 7 take
+    // token j's dk 8p .. 8p + 7 and 64 + 8p .. 64 + 8p + 7 (p = lane & 7),
+    // 16 bytes a load, and sum over the eight
+    {
+        const float qscale = 1.0f / sqrtf((float)CD);
+        const int p8 = lane & 7;
 #pragma unroll
-    for (int i = 0; i < CK / TC_WARPS; ++i) {
-        const int tt = warp + TC_WARPS * i;
-        float qv[4], kv[4];
-        unpack(qv, Raw4<bf16>{*reinterpret_cast<const uint2 *>(RQ + tt * PS::LDQ + 4 * lane)});
-        unpack(kv, Raw4<bf16>{*reinterpret_cast<const uint2 *>(RK + tt * PS::LDQ + 4 * lane)});
-        float sq = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
-        float sk = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
+        for (int i = 0; i < CK / (4 * TC_WARPS); ++i) {
+            const int tt = 4 * (TC_WARPS * i + warp) + (lane >> 3);
+            float sq = 0.f, sk = 0.f;
 #pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            sq += __shfl_xor_sync(0xffffffffu, sq, o);
-            sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            for (int hlf = 0; hlf < 2; ++hlf) {
+                const uint4 qv = *reinterpret_cast<const uint4 *>(RQ + tt * PS::LDQ + 64 * hlf + 8 * p8);
+                const uint4 kv = *reinterpret_cast<const uint4 *>(RK + tt * PS::LDQ + 64 * hlf + 8 * p8);
+                const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    // a bf16 pair to fp32 exactly: the low half shifted up, the high half masked
+                    const float q0 = __uint_as_float(qw[e] << 16), q1 = __uint_as_float(qw[e] & 0xffff0000u);
+                    const float k0 = __uint_as_float(kw[e] << 16), k1 = __uint_as_float(kw[e] & 0xffff0000u);
+                    sq = fmaf(q1, q1, fmaf(q0, q0, sq));
+                    sk = fmaf(k1, k1, fmaf(k0, k0, sk));
+                }
+            }
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            }
+            if (p8 == 0)
+                IQ[tt] = qscale * rsqrtf(sq + kEps), IK[tt] = rsqrtf(sk + kEps);
         }
-        if (lane == 0)
-            IQ[tt] = qscale * rsqrtf(sq + kEps), IK[tt] = rsqrtf(sk + kEps);
     }
     // [K|Q] K^T over the tiles at or below the diagonal only: row block R
     // (rows 16R .. 16R + 15) has the 16 x 8 tiles nt = 0 .. 2R + 1 there, 20
@@ -471,18 +486,29 @@ __global__ void __launch_bounds__(TC_THREADS, 4) gdn_chunk_prep_kernel(const Pre
     }
     __syncthreads();
     t_below_diagonal(AF, XF, warp, g, c);
-    // T's lower triangle, split, to the unit: a warp writes one 8 x 8 core
-    // matrix at a time (lane: row lane & 7, column pair lane >> 3)
-    for (int e = tid; e < CK * CK / 2; e += TC_THREADS) {
-        const int cmi = e >> 5, l = e & 31;
-        const int t = 8 * (cmi >> 3) + (l & 7), s2 = 8 * (cmi & 7) + 2 * (l >> 3);
-        const float2 v = *reinterpret_cast<const float2 *>(XF + t * LDF + s2);
-        const float x = s2 <= t ? v.x : 0.f;
-        const float y = s2 + 1 <= t ? v.y : 0.f;
-        uint32_t th, tl;
-        split2(x, y, th, tl);
-        *reinterpret_cast<uint32_t *>(blk + PW::TH + cm_off<CK>(t, s2)) = th;
-        *reinterpret_cast<uint32_t *>(blk + PW::TL + cm_off<CK>(t, s2)) = tl;
+    // T's lower triangle, split, to the unit, one 16-byte row of a core
+    // matrix a thread: a warp writes four adjacent core matrices (512
+    // contiguous bytes); piece p = row group 8 rg, core columns 4 (q & 1) ..
+    // + 3 with q = p / 32, lane: row lane & 7, core column (lane >> 3)
+#pragma unroll
+    for (int i = 0; i < CK * CK / 8 / TC_THREADS; ++i) {
+        const int pc = tid + TC_THREADS * i, q = pc >> 5;
+        const int t = 8 * (q >> 1) + (lane & 7), k8 = 4 * (q & 1) + (lane >> 3);
+        uint4 th = make_uint4(0u, 0u, 0u, 0u), tl = th;
+        if (8 * k8 <= t) {
+            const float4 v0 = *reinterpret_cast<const float4 *>(XF + t * LDF + 8 * k8);
+            const float4 v1 = *reinterpret_cast<const float4 *>(XF + t * LDF + 8 * k8 + 4);
+            const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            uint32_t h[4], l[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                split2(8 * k8 + 2 * e <= t ? v[2 * e] : 0.f, 8 * k8 + 2 * e + 1 <= t ? v[2 * e + 1] : 0.f, h[e],
+                       l[e]);
+            th = make_uint4(h[0], h[1], h[2], h[3]);
+            tl = make_uint4(l[0], l[1], l[2], l[3]);
+        }
+        *reinterpret_cast<uint4 *>(blk + PW::TH + cm_off<CK>(t, 8 * k8)) = th;
+        *reinterpret_cast<uint4 *>(blk + PW::TL + cm_off<CK>(t, 8 * k8)) = tl;
     }
     if (tid == 0)
         hdr[0] = s, hdr[1] = c0;
