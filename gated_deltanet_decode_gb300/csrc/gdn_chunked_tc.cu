@@ -273,7 +273,7 @@ __device__ __forceinline__ void split32(const float (&v)[32], uint32_t (&hi)[16]
 // inverse, and writes them with a header to the unit.  Units that hold no
 // chunk get a header that names none.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(TC_THREADS, 4) gdn_chunk_prep_kernel(const PrefillArgs p, unsigned char *work,
+__global__ void __launch_bounds__(TC_THREADS, 5) gdn_chunk_prep_kernel(const PrefillArgs p, unsigned char *work,
                                                                     int units)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -1130,6 +1130,10 @@ cudaError_t launch_gdn_prefill_chunked_tc(const PrefillArgs &a, cudaStream_t s)
                                              TS::TOTAL);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(gdn_chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PS::TOTAL);
+        // five prep CTAs an SM take more shared memory than the default split leaves
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gdn_chunk_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess)
             return e;
         configured.fetch_or(bit, std::memory_order_release);
