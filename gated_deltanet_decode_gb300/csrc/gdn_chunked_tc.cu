@@ -842,10 +842,23 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(bar_eready);
+            {
+                // S scaled by e^{G_C} while U's product runs: no product reads
+                // or writes S's own columns between its split above and the
+                // state update, which waits for wready (after the wait below)
+                const float gC = EG[CK - 1];
+                float sv[32];
+                uint32_t r[32];
+                tld32(tlane + C_S + 32 * cq, sv);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    r[i] = __float_as_uint(sv[i] * gC);
+                tst32(tlane + C_S + 32 * cq, r);
+            }
 
             // ---- (3) U's head and tail (for O), those of U diag(e^{G_C-G}
             // ik) (for S), Y diag(e^G iq) into U's columns (where O
-            // accumulates), and S scaled by e^{G_C} ----
+            // accumulates) ----
             late = !mbar_wait(bar_u, (uint32_t)(ci & 1)); // Y's products came before U's
             if (late)
                 report(p.err, GDN_DEVERR_TIMEOUT);
@@ -884,17 +897,8 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
                     }
                     tst16(tlane + C_U + 16 * cq, yo);
                 }
-                const float gC = EG[CK - 1];
-                {
-                    float sv[32];
-                    uint32_t r[32];
-                    tld32(tlane + C_S + 32 * cq, sv);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        r[i] = __float_as_uint(sv[i] * gC);
-                    tst32(tlane + C_S + 32 * cq, r);
-                }
-                tst_wait();
+                tst_wait(); // and S's scaled rows, stored during the U product
+
             }
             tc_before_sync();
             __syncwarp();
@@ -1062,6 +1066,8 @@ __global__ void __launch_bounds__(TCW_THREADS, 1) gdn_chunked_tc_kernel(const Pr
     }
 
     cp_async_wait_all(); // a chain that stopped early may have the next chunk's inputs in flight
+    if (warp < TCC_WARPS)
+        tst_wait(); // and S's scaled rows, if it stopped in the wait for U's product
     tc_before_sync();
     __syncthreads();
     if (warp == 0)
