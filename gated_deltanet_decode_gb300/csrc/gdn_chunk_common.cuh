@@ -161,11 +161,6 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_b
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-// until at most N of this thread's most recent cp.async groups are pending
-template <int N> __device__ __forceinline__ void cp_async_wait_group()
-{
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
 template <typename T> __device__ __forceinline__ void store2(T *p, float x, float y);
 template <> __device__ __forceinline__ void store2<float>(float *p, float x, float y)
