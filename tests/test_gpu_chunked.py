@@ -5,8 +5,9 @@ chunked GDN path; "mstar PR #1127": one GDN prefill kernel).
 1. Against the fp64 oracle (the rule token after token): every output within
    the bf16 tolerance, every final state within the chained-state tolerance;
    sequences of 1, 63, 64, 65, 130 and 512 tokens cover whole chunks, ragged
-   tails and one-token chunks, in place and twin, the 0.8B and 9B (grouped
-   heads) shapes, bf16 and fp32 activations.
+   tails and one-token chunks, and last chunks of 17, 31, 48 and 49 tokens
+   end inside or at the edge of a 16-token row block; in place and twin,
+   the 0.8B and 9B (grouped heads) shapes, bf16 and fp32 activations.
 2. Against the exact token-serial gdn_prefill on the GPU: the two agree far
    inside the tolerances (about 1e-5 relative), so the chunking adds no
    error the oracle tolerances would hide.
@@ -56,8 +57,11 @@ def check_against_oracle(c, out, o_ref, pool, keep_in_place):
 
 
 CASES = [(I.QWEN_08B, [130, 64, 0, 1, 63, 65]), (I.QWEN_9B, [70, 0, 129, 5]),
-         (I.QWEN_08B.with_(dtype="f32"), [65, 3, 128])]
-IDS = ["0.8b", "9b", "0.8b-f32"]
+         (I.QWEN_08B.with_(dtype="f32"), [65, 3, 128]),
+         # last chunks ending inside or at the edge of a chunk's 16-token row
+         # blocks (17, 48, 31 and 49 tokens)
+         (I.QWEN_08B, [17, 112, 95, 49])]
+IDS = ["0.8b", "9b", "0.8b-f32", "0.8b-row-block-tails"]
 
 
 @pytest.mark.parametrize("shape,lens", CASES, ids=IDS)
